@@ -1,0 +1,184 @@
+/*
+ * kt_mlp.h -- C ABI of the fused transformer MLP library for one GB300 (sm_103a).
+ *
+ *   Y = act(X . W_up [+ b_up]) . W_down [+ b_down]
+ *
+ * The operation is the transformer feed-forward block in the two forms the pages
+ * work on:
+ *   - the plain GELU MLP: up projection, GELU, down projection -- the F16 SigLIP
+ *     MLP [1,729,1152] -> [1,729,4304] -> [1,729,1152] without biases
+ *     ("MLP layout sweep and remaining representation limits", opening paragraph;
+ *     its "ISA review" section computes GELU through tanh);
+ *   - SDXL's GEGLU FeedForward: one projection to 2F, split along the last axis
+ *     into value (first half) and gate (SECOND half), value * gelu_erf(gate),
+ *     then the projection back ("SDXL as a requirements inventory",
+ *     section 1.3 FeedForward; section 9.3 for the erf form and the half order).
+ *
+ * Numerics: operands in the 16-bit I/O dtype, products accumulated in fp32 in
+ * tensor memory, bias added to the fp32 accumulator, the activation evaluated
+ * in fp32, and exactly ONE rounding (to nearest even) of H to the I/O dtype
+ * before the down projection reads it ("The software stack", section 2.3: the
+ * accumulator is a resident format, never a memory word).  Y is rounded once.
+ *
+ * Layouts (all row-major, contiguous, 16-byte aligned device pointers, dtype dt):
+ *   X[M][D], W_up[D][F_up], W_down[F][D], b_up[F_up], b_down[D], Y[M][D],
+ *   H[M][F];  F_up = F for GELU, 2F for GEGLU.  Weights are [in][out]; a PyTorch
+ *   nn.Linear weight ([out][in]) is passed as weight.t().contiguous().
+ *
+ * Requirements: M >= 1; D >= 8 and F >= 8, both multiples of 8 (16-byte row
+ * pitch for the tensor-memory-accelerator copies).  Anything else returns
+ * KT_ERR_UNSUPPORTED or KT_ERR_INVALID and launches nothing.
+ *
+ * Errors: every call returns a kt_status; kt_last_error() gives a message for
+ * the calling thread's last non-OK status.  Device-side waits are bounded: a
+ * wait that runs out sets the plan's error word, the kernel returns, and
+ * kt_mlp_status() reports KT_ERR_TIMEOUT.  There is no CPU fallback: without a
+ * usable sm_103a device kt_mlp_plan() fails.
+ */
+#ifndef KT_MLP_H
+#define KT_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KT_MLP_ABI_VERSION 1
+
+typedef enum {
+    KT_ACT_GELU_ERF = 0,  /* gelu(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2))                 */
+    KT_ACT_GELU_TANH = 1, /* 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))                   */
+    KT_ACT_GEGLU = 2,     /* P[:, :F] * gelu_erf(P[:, F:]), F_up = 2F                          */
+    KT_ACT_NONE = 3       /* no activation (two chained linear layers); checks the GEMMs alone */
+} kt_act;
+
+typedef enum { KT_F16 = 0, KT_BF16 = 1 } kt_dtype;
+
+typedef enum {
+    KT_OK = 0,
+    KT_ERR_INVALID = 1,     /* bad argument: null pointer, negative size, unknown enum  */
+    KT_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels support          */
+    KT_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed (message says which)  */
+    KT_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (see kt_mlp_status)    */
+    KT_ERR_NOMEM = 5        /* device or host allocation failed                          */
+} kt_status;
+
+typedef struct kt_mlp_plan_s* kt_mlp_plan_t;
+
+/* What the planner chose for one of the two GEMMs (host-side description). */
+typedef struct {
+    int32_t BM, BN, BK;        /* CTA tile: BM x BN output, BK-deep k-blocks              */
+    int32_t stages;            /* shared-memory pipeline depth                            */
+    int32_t split_k;           /* SK: CTAs sharing one output tile along K                */
+    int32_t tiles_m, tiles_n;  /* output tiles: ceil(M/BM) x ceil(N/BN)                   */
+    int32_t kblocks;           /* ceil(K/BK)                                              */
+    int32_t grid;              /* persistent CTAs launched (<= SM count)                  */
+    int32_t waves;             /* ceil(tiles_m * tiles_n * split_k / SMs)                 */
+    int32_t smem_bytes;        /* dynamic shared memory per CTA                           */
+    int32_t tmem_cols;         /* tensor-memory columns allocated per CTA                 */
+    int64_t M, N, K;           /* the GEMM: [M,K] x [K,N]                                 */
+    double useful_over_padded; /* M*N*K / (padded M * padded N * padded K)                */
+    double est_us;             /* the planner's modelled time (a model, not a measurement) */
+} kt_gemm_plan_info;
+
+typedef struct {
+    int64_t M, D, F;
+    int32_t act, dtype, bias;
+    int32_t num_sms;
+    kt_gemm_plan_info up;      /* X[M,D] . W_up[D,F_up] with the fused epilogue -> H[M,F] */
+    kt_gemm_plan_info down;    /* H[M,F] . W_down[F,D] (+ b_down) -> Y[M,D]               */
+    int64_t workspace_bytes;   /* device bytes the plan owns (H, split-K partials, flags) */
+} kt_plan_info;
+
+/*
+ * kt_mlp_plan -- validate the problem, choose tiles / pipeline depth / split-K
+ * with the padding-aware planner, and allocate the plan's device workspace on the
+ * CURRENT device (H[M][F], fp32 split-K partials, tile counters, error word).
+ *   M, D, F  : rows (tokens), model dim, hidden dim.
+ *   act      : kt_act.     dtype: kt_dtype.     bias: 0 = no biases, 1 = b_up and b_down.
+ *   out      : receives the plan handle (owned by the caller; free with kt_mlp_destroy).
+ * Errors: INVALID (null out, non-positive size, bad enum), UNSUPPORTED (D or F not a
+ * multiple of 8, device not sm_103, sizes past the 32-bit tile index range),
+ * CUDA / NOMEM (device query or allocation failed).  On error *out is NULL.
+ */
+kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtype, int bias,
+                      kt_mlp_plan_t* out);
+
+/*
+ * kt_mlp_run -- enqueue the MLP on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  Two kernel launches: the up GEMM with the fused bias/activation/rounding
+ * epilogue writing H into the plan's workspace, then the down GEMM (programmatic
+ * dependent launch) writing Y.  All pointers are device pointers owned by the
+ * caller, 16-byte aligned, laid out as described at the top of this file.  b_up /
+ * b_down must be non-NULL iff the plan has bias = 1.  Asynchronous: returns after
+ * enqueueing.  A plan must not run concurrently on two streams (one workspace).
+ * Errors: INVALID (null / misaligned pointer, bias mismatch), CUDA (launch failed).
+ */
+kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                     const void* b_up, const void* b_down, void* Y, void* stream);
+
+/*
+ * kt_mlp_run_with_h -- as kt_mlp_run, but the rounded intermediate H[M][F] is
+ * written to the caller's device buffer H_out (16-byte aligned) instead of the
+ * plan's workspace, so that it can be inspected.  Same kernels, same results.
+ */
+kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                            const void* b_up, const void* b_down, void* Y, void* H_out, void* stream);
+
+/*
+ * kt_mlp_run_host -- end-to-end call with HOST activations: copies X_host[M][D] to
+ * the device (plan-owned staging), runs the MLP, copies Y back into Y_host[M][D]
+ * and synchronises `stream`.  Weights and biases stay device pointers (resident
+ * model parameters).  Pinned host memory gives asynchronous copies; pageable memory
+ * works but is slower.  Returns after Y_host is filled.
+ */
+kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_up,
+                          const void* W_down, const void* b_up, const void* b_down,
+                          void* Y_host, void* stream);
+
+/*
+ * kt_mlp_status -- synchronise the plan's last stream and read its device error
+ * word.  KT_OK, or KT_ERR_TIMEOUT when a bounded wait ran out in an earlier run
+ * (the word is then cleared), or KT_ERR_CUDA if the stream reported an error.
+ */
+kt_status kt_mlp_status(kt_mlp_plan_t plan);
+
+/* kt_mlp_destroy -- free the plan's workspace (after synchronising its device). */
+kt_status kt_mlp_destroy(kt_mlp_plan_t plan);
+
+/* kt_mlp_describe -- write a one-line text description of the plan into buf. */
+kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len);
+
+/* kt_mlp_get_info -- copy the plan's chosen configuration into *out. */
+kt_status kt_mlp_get_info(kt_mlp_plan_t plan, kt_plan_info* out);
+
+/*
+ * kt_mlp_plan_info -- run the planner alone, on the host, for a device with
+ * `num_sms` SMs.  Touches no GPU; used to inspect and test tile choices.
+ * Same validation and errors as kt_mlp_plan (except CUDA / NOMEM).
+ */
+kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtype, int bias,
+                           int num_sms, kt_plan_info* out);
+
+/*
+ * kt_mlp_debug_stall -- failure-injection hook for tests.  With enable = 1 the next
+ * runs of this plan make the up kernel's producer wait on a barrier nobody
+ * signals, bounded by `limit_us` microseconds; the wait runs out, the kernel
+ * records KT_ERR_TIMEOUT in the plan's error word and returns without computing.
+ * enable = 0 restores normal runs.  No GPU fault is involved.
+ */
+kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us);
+
+/* Thread-local message for the calling thread's last non-OK status ("" if none). */
+const char* kt_last_error(void);
+
+/* KT_MLP_ABI_VERSION of the loaded library. */
+int kt_mlp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KT_MLP_H */

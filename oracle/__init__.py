@@ -32,7 +32,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkt_mlp_oracle.so")
 
 F16, BF16 = 0, 1
-GELU_ERF, GELU_TANH, GEGLU = 0, 1, 2
+GELU_ERF, GELU_TANH, GEGLU, NONE = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None
@@ -148,7 +148,7 @@ def linear(A, B, bias=None) -> np.ndarray:
 
 
 def activation(P, F: int, act: int) -> np.ndarray:
-    """H~ from P: gelu (P is [M,F]) or GEGLU (P is [M,2F], gate = second half)."""
+    """H~ from P: gelu / none (P is [M,F]) or GEGLU (P is [M,2F], gate = second half)."""
     P = np.ascontiguousarray(P, dtype=np.float64)
     M = P.shape[0]
     want = 2 * F if act == GEGLU else F

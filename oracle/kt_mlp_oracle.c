@@ -11,6 +11,7 @@
  *
  *   P[m,j]  = sum_k X[m,k] * W_up[k,j]  (+ b_up[j])                      j < F_up
  *   gelu    : H~[m,j] = gelu(P[m,j])                                     F_up = F
+ *   none    : H~[m,j] = P[m,j]                                           F_up = F
  *   geglu   : H~[m,j] = P[m,j] * gelu_erf(P[m,F+j])                      F_up = 2F
  *   H[m,j]  = round_to_nearest_even_dt(H~[m,j])        (the single rounding of H)
  *   Yx[m,n] = sum_j H[m,j] * W_down[j,n]  (+ b_down[n])
@@ -50,6 +51,7 @@
 #define KTO_GELU_ERF 0
 #define KTO_GELU_TANH 1
 #define KTO_GEGLU 2
+#define KTO_NONE 3 /* no activation: H~ = P (two chained linear layers) */
 
 /* ------------------------------------------------------------------------ */
 /* fp16 / bf16 codecs, written from the bit formats.                         */
@@ -201,6 +203,8 @@ static void activation_row(const double* p, double* h, int64_t F, int act) {
         for (int64_t j = 0; j < F; ++j) h[j] = p[j] * oracle_gelu_erf(p[F + j]);
     } else if (act == KTO_GELU_TANH) {
         for (int64_t j = 0; j < F; ++j) h[j] = oracle_gelu_tanh(p[j]);
+    } else if (act == KTO_NONE) {
+        for (int64_t j = 0; j < F; ++j) h[j] = p[j];
     } else {
         for (int64_t j = 0; j < F; ++j) h[j] = oracle_gelu_erf(p[j]);
     }
@@ -225,7 +229,7 @@ int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bia
                     const int64_t* rows, int64_t nrows,
                     uint16_t* H_out, double* Yx_out, uint16_t* Y_out) {
     if (M < 1 || D < 1 || F < 1 || nrows < 0) return -1;
-    if (act < 0 || act > 2 || (dtype != KTO_F16 && dtype != KTO_BF16)) return -1;
+    if (act < 0 || act > 3 || (dtype != KTO_F16 && dtype != KTO_BF16)) return -1;
     if (rows == NULL) nrows = M;
     for (int64_t i = 0; rows && i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= M) return -1;

@@ -1,0 +1,141 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and its
+host-only planner keeps the grid invariants ("The software stack", sections 2.1
+and 2.2: padding-discounted tile choice; every output element produced exactly
+once; SK > 1 only with a reduction).  No compute call is made here."""
+import os
+import re
+
+import pytest
+
+from transformer_mlp_gemms_gb300 import build as kbuild
+from transformer_mlp_gemms_gb300 import kt_mlp
+from transformer_mlp_gemms_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kt_mlp.h")
+SMS = 152  # GB300
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kt_mlp.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kt_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("kt_mlp_plan", "kt_mlp_run", "kt_mlp_destroy", "kt_mlp_status", "kt_last_error",
+                     "kt_mlp_describe", "kt_mlp_run_with_h"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding wraps each of them under the same name
+    assert set(names) <= set(kt_mlp.SIGNATURES)
+    assert lib.kt_mlp_abi_version() == 1
+
+
+def test_plan_without_a_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(kt_mlp.KtError) as e:
+        kt_mlp.kt_mlp_plan(33, 64, 176, 0, 0, False)
+    assert e.value.status in (kt_mlp.KT_ERR_CUDA, kt_mlp.KT_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 64, 64, 0, 0, 0), kt_mlp.KT_ERR_INVALID),
+    ((8, -8, 64, 0, 0, 0), kt_mlp.KT_ERR_INVALID),
+    ((8, 64, 64, 7, 0, 0), kt_mlp.KT_ERR_INVALID),
+    ((8, 64, 64, 0, 2, 0), kt_mlp.KT_ERR_INVALID),
+    ((8, 64, 64, 0, 0, 2), kt_mlp.KT_ERR_INVALID),
+    ((8, 60, 64, 0, 0, 0), kt_mlp.KT_ERR_UNSUPPORTED),
+    ((8, 64, 20, 0, 0, 0), kt_mlp.KT_ERR_UNSUPPORTED),
+])
+def test_argument_errors(lib, args, status):
+    with pytest.raises(kt_mlp.KtError) as e:
+        kt_mlp.kt_mlp_plan_info(*args, SMS)
+    assert e.value.status == status
+    assert kt_mlp.kt_last_error()
+
+
+def test_null_handles_are_rejected(lib):
+    assert lib.kt_mlp_destroy(None) == kt_mlp.KT_ERR_INVALID
+    assert lib.kt_mlp_status(None) == kt_mlp.KT_ERR_INVALID
+    assert lib.kt_mlp_run(None, None, None, None, None, None, None, None) == kt_mlp.KT_ERR_INVALID
+    assert lib.kt_mlp_debug_stall(None, 1, 10) == kt_mlp.KT_ERR_INVALID
+
+
+def _check_gemm(g, M, N, K):
+    assert (g["M"], g["N"], g["K"]) == (M, N, K)
+    BM, BN, BK, SK = g["BM"], g["BN"], g["BK"], g["split_k"]
+    assert BM == 128 and BK == 64
+    assert BN % 16 == 0 and 16 <= BN <= 256
+    # the grid covers every output element exactly once: tiles_m * BM >= M > (tiles_m - 1) * BM
+    assert (g["tiles_m"] - 1) * BM < M <= g["tiles_m"] * BM
+    assert (g["tiles_n"] - 1) * BN < N <= g["tiles_n"] * BN
+    assert g["kblocks"] == -(-K // BK)
+    kps = -(-g["kblocks"] // SK)
+    assert (SK - 1) * kps < g["kblocks"]  # no empty split: every partial is real
+    tiles = g["tiles_m"] * g["tiles_n"] * SK
+    assert g["grid"] == min(tiles, SMS)
+    assert g["waves"] == -(-tiles // SMS)
+    assert 0 < g["useful_over_padded"] <= 1.0
+    assert g["useful_over_padded"] == pytest.approx(
+        M * N * K / ((g["tiles_m"] * BM) * (g["tiles_n"] * BN) * (g["kblocks"] * BK)))
+    assert 2 <= g["stages"] <= 8
+    assert g["smem_bytes"] <= 227 * 1024
+    assert g["smem_bytes"] > 227 * 1024 // 2  # one CTA per SM: the 512-column TMEM allocation never contends
+    assert g["est_us"] > 0
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+def test_planner_invariants_on_every_workload(lib, name):
+    w = wl.WORKLOADS[name]
+    info = kt_mlp.kt_mlp_plan_info(w.M, w.D, w.F, w.act, w.dtype, w.bias, SMS)
+    _check_gemm(info["up"], w.M, w.F, w.D)
+    _check_gemm(info["down"], w.M, w.D, w.F)
+    assert info["up"]["split_k"] == 1  # the activation is not linear: no split of the up projection
+    if w.act == wl.ACT_GEGLU:
+        assert info["up"]["BN"] <= 256
+
+
+@pytest.mark.parametrize("M", [1, 33, 127, 128, 129, 729, 1000, 4097])
+@pytest.mark.parametrize("F", [8, 176, 4304])
+def test_planner_invariants_on_a_shape_grid(lib, M, F):
+    for act in (0, 1, 2, 3):
+        info = kt_mlp.kt_mlp_plan_info(M, 1152, F, act, 0, act == 2, SMS)
+        _check_gemm(info["up"], M, F, 1152)
+        _check_gemm(info["down"], M, 1152, F)
+
+
+def test_planner_avoids_a_second_wave_on_siglip(lib):
+    # M = 729 leaves 6 row tiles; BN = 176 gives 25 column tiles = 150 CTAs <= 152 SMs,
+    # where BN = 160 would need 162 (two waves) and BN = 256 wastes a third of the machine
+    info = kt_mlp.kt_mlp_plan_info(729, 1152, 4304, 1, 0, False, SMS)
+    assert info["up"]["waves"] == 1
+    assert info["up"]["grid"] >= 138
+    assert info["down"]["waves"] == 1
+
+
+def test_planner_padding_discount_prefers_less_padding(lib):
+    # a problem that fits a 128-wide tile exactly must not be planned on a tile that pads it
+    info = kt_mlp.kt_mlp_plan_info(128, 64, 128, 3, 0, False, 1)
+    assert info["up"]["useful_over_padded"] == pytest.approx(1.0)
+
+
+def test_planner_uses_split_k_for_a_deep_narrow_down_projection(lib):
+    # D = 128 output columns, F = 16384-deep reduction, M = 128: one output tile,
+    # so only split-K can occupy more than one SM
+    info = kt_mlp.kt_mlp_plan_info(128, 128, 16384, 3, 0, False, SMS)
+    assert info["down"]["split_k"] > 1

@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small shapes are compared element by element (Y and the rounded H); the full
+workload sizes, in the launch configuration the bench times, are compared on
+sampled rows (first, last, tile edges and random rows), which the oracle computes
+one by one.  Y buffers are poisoned with NaN before each run so that an
+unwritten tile cannot pass.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from transformer_mlp_gemms_gb300 import kt_mlp
+from transformer_mlp_gemms_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TDT = wl.TORCH_DTYPES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transformer_mlp_gemms_gb300 import build
+    build.build()
+    kt_mlp.load()
+
+
+def _to_dev(t):
+    return {k: v.cuda() for k, v in t.items()}
+
+
+def _run(w, d, with_h=True, plan=None):
+    own = plan is None
+    if own:
+        plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    Y = torch.full((w.M, w.D), float("nan"), dtype=TDT[w.dtype], device="cuda")
+    H = torch.full((w.M, w.F), float("nan"), dtype=TDT[w.dtype], device="cuda") if with_h else None
+    if with_h:
+        plan.run_with_h(d["X"], d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Y, H)
+    else:
+        plan.run(d["X"], d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Y)
+    torch.cuda.synchronize()
+    assert plan.status() == kt_mlp.KT_OK, kt_mlp.kt_last_error()
+    if own:
+        plan.close()
+    return Y.cpu(), (H.cpu() if with_h else None)
+
+
+def _compare(w, t, Y, H, rows=None):
+    b = {k: wl.bits(v) for k, v in t.items()}
+    Ho, Yx, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"),
+                           act=w.act, dtype=w.dtype, rows=rows)
+    yb = wl.bits(Y)
+    if rows is not None:
+        yb = yb[rows]
+    parity.check_y(yb, Yx, w.dtype)
+    if H is not None:
+        hb = wl.bits(H)
+        if rows is not None:
+            hb = hb[rows]
+        parity.check_h(hb, Ho, parity.h_bound(w, b, rows), w.dtype)
+
+
+# --------------------------------------------------------------------------
+# element by element on small shapes
+# --------------------------------------------------------------------------
+
+def test_tiny_workload():
+    w = wl.WORKLOADS["tiny"]
+    t = wl.generate(w)
+    Y, H = _run(w, _to_dev(t))
+    _compare(w, t, Y, H)
+
+
+GRID = [
+    # (M, D, F, act, dtype, bias)
+    (1, 64, 64, wl.ACT_NONE, wl.DT_F16, False),
+    (33, 64, 176, wl.ACT_NONE, wl.DT_F16, False),
+    (128, 128, 256, wl.ACT_NONE, wl.DT_BF16, True),
+    (129, 192, 320, wl.ACT_GELU_ERF, wl.DT_F16, True),
+    (127, 64, 176, wl.ACT_GELU_TANH, wl.DT_F16, False),
+    (300, 256, 1000, wl.ACT_GELU_TANH, wl.DT_BF16, False),
+    (257, 1152, 4304, wl.ACT_GELU_TANH, wl.DT_F16, False),
+    (64, 320, 640, wl.ACT_GEGLU, wl.DT_BF16, True),
+    (200, 640, 2560, wl.ACT_GEGLU, wl.DT_BF16, True),
+    (77, 128, 136, wl.ACT_GEGLU, wl.DT_F16, False),
+    (5, 8, 8, wl.ACT_GELU_ERF, wl.DT_F16, True),
+    (40, 24, 40, wl.ACT_GEGLU, wl.DT_BF16, True),
+    (130, 72, 4104, wl.ACT_NONE, wl.DT_F16, True),
+    (384, 1280, 512, wl.ACT_GELU_ERF, wl.DT_BF16, False),
+]
+
+
+@pytest.mark.parametrize("M,D,F,act,dt,bias", GRID)
+def test_shape_grid(M, D, F, act, dt, bias):
+    w = wl.custom(M, D, F, act, dt, bias, seed=1000 + M + D + F + act)
+    t = wl.generate(w)
+    Y, H = _run(w, _to_dev(t))
+    _compare(w, t, Y, H)
+
+
+# --------------------------------------------------------------------------
+# full workload sizes, sampled rows
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["siglip", "sdxl_l2", "sdxl_l1", "sweep_M256", "sweep_M1000", "sweep_M4096",
+                                  "sweep_M16384"])
+def test_full_size_workload_sampled_rows(name):
+    w = wl.WORKLOADS[name]
+    t = wl.generate(w)
+    Y, H = _run(w, _to_dev(t))
+    rows = wl.sample_rows(w.M, 40, seed=w.seed)
+    assert torch.isfinite(Y.float()).all(), "unwritten or non-finite Y"
+    _compare(w, t, Y, H, rows=rows)
+
+
+# --------------------------------------------------------------------------
+# properties
+# --------------------------------------------------------------------------
+
+def test_runs_are_bitwise_deterministic_and_h_is_not_needed():
+    w = wl.WORKLOADS["siglip"]
+    t = wl.generate(w)
+    d = _to_dev(t)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    Y1, H1 = _run(w, d, with_h=True, plan=plan)
+    Y2, _ = _run(w, d, with_h=False, plan=plan)
+    Y3, _ = _run(w, d, with_h=False, plan=plan)
+    plan.close()
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(Y2.view(torch.int16), Y3.view(torch.int16))
+
+
+def test_host_buffer_entry_point_matches_device_path():
+    w = wl.WORKLOADS["sdxl_l2"]
+    t = wl.generate(w)
+    d = _to_dev(t)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    Yd, _ = _run(w, d, with_h=False, plan=plan)
+    Xh = t["X"].pin_memory()
+    Yh = torch.empty((w.M, w.D), dtype=TDT[w.dtype]).pin_memory()
+    plan.run_host(Xh, d["W_up"], d["W_down"], d["b_up"], d["b_down"], Yh)
+    assert plan.status() == kt_mlp.KT_OK
+    plan.close()
+    assert torch.equal(Yd.view(torch.int16), Yh.view(torch.int16))
+
+
+def test_overflow_rounds_to_infinity_like_the_oracle():
+    # fp16 H past 65504 must become +-inf (IEEE round to nearest), not saturate
+    w = wl.custom(16, 64, 64, wl.ACT_NONE, wl.DT_F16, False, seed=7)
+    t = wl.generate(w)
+    t["W_up"] = (t["W_up"].float() * 40000.0).half()
+    b = {k: wl.bits(v) for k, v in t.items()}
+    Ho, _, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], act=w.act, dtype=w.dtype)
+    assert np.isinf(oracle.decode(Ho, w.dtype)).any()
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    d = _to_dev(t)
+    Y = torch.empty((w.M, w.D), dtype=torch.float16, device="cuda")
+    H = torch.empty((w.M, w.F), dtype=torch.float16, device="cuda")
+    plan.run_with_h(d["X"], d["W_up"], d["W_down"], None, None, Y, H)
+    torch.cuda.synchronize()
+    plan.close()
+    hg = oracle.decode(wl.bits(H.cpu()), w.dtype)
+    ho = oracle.decode(Ho, w.dtype)
+    assert np.array_equal(np.isinf(hg), np.isinf(ho))
+    assert np.array_equal(np.sign(hg[np.isinf(ho)]), np.sign(ho[np.isinf(ho)]))
+
+
+def test_injected_stall_times_out_and_the_plan_recovers():
+    w = wl.custom(256, 256, 512, wl.ACT_GELU_ERF, wl.DT_F16, False, seed=9)
+    t = wl.generate(w)
+    d = _to_dev(t)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    kt_mlp.kt_mlp_debug_stall(plan.handle, True, 20000)  # 20 ms
+    Y = torch.empty((w.M, w.D), dtype=torch.float16, device="cuda")
+    plan.run(d["X"], d["W_up"], d["W_down"], None, None, Y)
+    assert plan.status() == kt_mlp.KT_ERR_TIMEOUT
+    assert "injected" in kt_mlp.kt_last_error()
+    kt_mlp.kt_mlp_debug_stall(plan.handle, False, 0)
+    Y2, H2 = _run(w, d, plan=plan)
+    plan.close()
+    _compare(w, t, Y2, H2)
+
+
+def test_bad_pointers_are_rejected_before_launch():
+    w = wl.custom(16, 64, 64, wl.ACT_GELU_ERF, wl.DT_F16, True, seed=3)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    t = _to_dev(wl.generate(w))
+    Y = torch.empty((w.M, w.D), dtype=torch.float16, device="cuda")
+    with pytest.raises(kt_mlp.KtError) as e:
+        plan.run(t["X"], t["W_up"], t["W_down"], None, None, Y)  # bias plan without biases
+    assert e.value.status == kt_mlp.KT_ERR_INVALID
+    with pytest.raises(kt_mlp.KtError) as e:
+        plan.run(t["X"].data_ptr() + 2, t["W_up"], t["W_down"], t["b_up"], t["b_down"], Y)  # misaligned
+    assert e.value.status == kt_mlp.KT_ERR_INVALID
+    plan.close()
+
+
+def test_plan_reports_its_choice():
+    w = wl.WORKLOADS["siglip"]
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    info = plan.info()
+    desc = plan.describe()
+    plan.close()
+    assert info["num_sms"] >= 148
+    assert info["up"]["N"] == w.F and info["down"]["N"] == w.D
+    assert "up: 128x" in desc and "down: 128x" in desc

@@ -332,6 +332,8 @@ def _brute_mlp(X, Wu, Wd, bu, bd, act, dt):
                 v = float(mpmath.mpf(p[j]) * _gelu_erf_mp(p[F + j]))
             elif act == oracle.GELU_TANH:
                 v = float(_gelu_tanh_mp(p[j]))
+            elif act == oracle.NONE:
+                v = p[j]
             else:
                 v = float(_gelu_erf_mp(p[j]))
             H[m, j] = _round_bits(v, dt)
@@ -353,6 +355,8 @@ CASES = [
     (5, 8, 4, wl.ACT_GEGLU, wl.DT_F16, False),
     (3, 8, 16, wl.ACT_GELU_TANH, wl.DT_BF16, False),
     (2, 24, 8, wl.ACT_GELU_ERF, wl.DT_BF16, True),
+    (3, 8, 8, wl.ACT_NONE, wl.DT_F16, True),
+    (2, 16, 8, wl.ACT_NONE, wl.DT_BF16, False),
 ]
 
 

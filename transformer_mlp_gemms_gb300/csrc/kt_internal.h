@@ -1,0 +1,105 @@
+// kt_internal.h -- shared between the host ABI layer, the planner and the kernels.
+// Not part of the public interface (that is include/kt_mlp.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "kt_mlp.h"
+
+namespace kt {
+
+// Fixed tile geometry of the sm_103a kernels.
+constexpr int kBM = 128;          // tcgen05 M (one CTA, cta_group::1): TMEM lane i = tile row i
+constexpr int kBK = 64;           // 64 16-bit elements = one 128-byte swizzle row
+constexpr int kEpiWarps = 8;      // epilogue warps (two per TMEM lane quadrant)
+constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer warp + MMA warp + epilogue
+constexpr int kTmemCols = 512;    // whole tensor memory of the SM (one CTA per SM)
+constexpr int kAccSlot = 256;     // TMEM columns reserved per accumulator buffer
+constexpr int kSmemBudget = 227 * 1024;  // opt-in dynamic shared memory per CTA
+// barriers, TMEM slot and flags (1 KB), 1024-byte alignment slack (1 KB), and a 16 KB
+// guard band past the ring so that no descriptor stride can reach beyond the allocation
+constexpr int kSmemReserve = 2048 + 16384;
+constexpr int kMaxStages = 8;
+
+// Epilogue kinds (one kernel instantiation each, times two dtypes).
+enum Epi : int {
+    EPI_GELU_ERF = 0,   // H = round(gelu_erf(acc + b))
+    EPI_GELU_TANH = 1,  // H = round(gelu_tanh(acc + b))
+    EPI_GEGLU = 2,      // H = round((acc_v + b_v) * gelu_erf(acc_g + b_g))
+    EPI_NONE = 3,       // H = round(acc + b)
+    EPI_DOWN = 4        // Y = round(sum_s partial_s + b)   (split-K when SK > 1)
+};
+
+// Device error word values (first writer wins).
+enum DevError : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2,
+                      DEV_TIMEOUT_EPILOGUE = 3, DEV_INJECTED_STALL = 4 };
+
+// One GEMM's launch configuration, chosen by the planner.
+struct GemmConfig {
+    int64_t M, N, K;       // output rows, output columns, reduction length
+    int BN;                // N tile, multiple of 16, 16..256
+    int stages;
+    int split_k;
+    int tiles_m, tiles_n, kblocks, kblocks_per_split;
+    int grid;
+    int waves;
+    int smem_bytes;
+    int n_b;               // B operand tiles per stage: 1, or 2 for GEGLU (value + gate)
+    double useful_over_padded;
+    double est_us;
+};
+
+struct PlanChoice {
+    GemmConfig up, down;
+};
+
+// Bytes of one pipeline stage: A tile + n_b B tiles of ceil(BN/64) 64-column boxes.
+inline int stage_bytes(int BN, int n_b) {
+    int chunks = (BN + 63) / 64;
+    return kBM * kBK * 2 + n_b * chunks * 64 * kBK * 2;
+}
+
+// Planner (host only, no GPU): returns KT_OK and fills `out`, or an error status.
+kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
+                      const char** why);
+
+// Fill the public description from a choice.
+void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* out);
+
+// Launch parameters shared by host and device.
+struct GemmParams {
+    int M, N, K;
+    int BN, n_chunks, stages, split_k;
+    int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
+    int gate_col;            // GEGLU: first gate column in W_up (= F); else 0
+    uint32_t idesc;          // tcgen05 instruction descriptor
+    uint32_t stage_bytes, a_bytes, b_bytes;  // per stage / A tile / one B operand tile
+    uint32_t acc_bufs;       // accumulator buffers in TMEM (1 or 2)
+    uint32_t gate_acc_off;   // TMEM column offset of the gate accumulator (GEGLU)
+    void* out;               // H or Y, row-major [M][ldo]
+    int ldo;
+    const void* bias;        // b_up (GEGLU: value then gate halves) / b_down / null
+    float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32
+    int* counters;           // split-K: [tiles_m*tiles_n] arrival counters (zero between runs)
+    int* error;              // device error word
+    int inject_stall;        // failure-injection hook (producer waits on a silent barrier)
+    unsigned long long wait_limit_ns;   // bound of every device-side wait
+    unsigned long long stall_limit_ns;  // bound of the injected wait
+    int pdl_wait;            // 1: griddepcontrol.wait before reading the A operand
+};
+
+// Host launch wrappers (kt_mlp_kernels.cu).  tmA / tmB point to 128-byte CUtensorMap.
+kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const GemmParams& p,
+                      int grid, int smem_bytes, void* stream, bool pdl, const char** why);
+
+// Encode a 2-D tiled tensor map over a row-major [rows][cols] 16-bit matrix with a
+// box of box_cols x box_rows and 128-byte swizzle.  Returns false on failure.
+bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols, const char** why);
+
+// tcgen05 instruction descriptor for kind::f16 with fp32 accumulation, A K-major,
+// B MN-major, M = 128, N = n.
+uint32_t make_idesc(int dtype, int n);
+
+}  // namespace kt

@@ -1,0 +1,364 @@
+// kt_mlp_abi.cpp -- the extern "C" boundary: validation, plan ownership, launches.
+//
+// A plan binds a problem (M, D, F, act, dtype, bias) to the device current at
+// plan time, holds the planner's choice and owns the device workspace: the
+// intermediate H[M][F], the split-K fp32 partials, the split-K tile counters
+// and the device error word.  kt_mlp_run encodes (and caches, per pointer set)
+// the four TMA tensor maps and enqueues two kernels on the caller's stream:
+// the up projection with its fused epilogue, then the down projection as a
+// programmatic dependent launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "kt_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kt_status fail(kt_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+kt_status ok() {
+    g_last_error.clear();
+    return KT_OK;
+}
+
+kt_status cuda_fail(const char* what, cudaError_t e) {
+    return fail(KT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+const char* act_name(int a) {
+    switch (a) {
+        case KT_ACT_GELU_ERF: return "gelu_erf";
+        case KT_ACT_GELU_TANH: return "gelu_tanh";
+        case KT_ACT_GEGLU: return "geglu";
+        case KT_ACT_NONE: return "none";
+    }
+    return "?";
+}
+
+kt_status validate_problem(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias) {
+    if (M < 1 || D < 1 || F < 1) return fail(KT_ERR_INVALID, "M, D and F must be positive");
+    if (act < KT_ACT_GELU_ERF || act > KT_ACT_NONE) return fail(KT_ERR_INVALID, "unknown activation");
+    if (dtype != KT_F16 && dtype != KT_BF16) return fail(KT_ERR_INVALID, "unknown dtype");
+    if (bias != 0 && bias != 1) return fail(KT_ERR_INVALID, "bias must be 0 or 1");
+    return KT_OK;
+}
+
+}  // namespace
+
+struct kt_mlp_plan_s {
+    int64_t M, D, F, F_up;
+    int act, dtype, bias;
+    int device, num_sms;
+    kt::PlanChoice choice;
+    // device workspace (one allocation each)
+    void* H = nullptr;          // [M][F]
+    float* partials = nullptr;  // [SK][tiles_m*128][tiles_n*BN] when the down GEMM splits K
+    int* flags = nullptr;       // [0] error word, [1..] split-K tile counters
+    void* x_stage = nullptr;    // [M][D] for kt_mlp_run_host
+    void* y_stage = nullptr;    // [M][D]
+    int64_t workspace_bytes = 0;
+    // tensor maps, cached by pointer set
+    alignas(64) CUtensorMap tm_x, tm_wu, tm_h, tm_wd;
+    const void* c_x = nullptr;
+    const void* c_wu = nullptr;
+    const void* c_h = nullptr;
+    const void* c_wd = nullptr;
+    bool cache_valid = false;
+    void* last_stream = nullptr;
+    int inject_stall = 0;
+    int64_t stall_limit_us = 0;
+};
+
+namespace {
+
+void free_plan(kt_mlp_plan_s* p) {
+    if (!p) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != p->device) cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    cudaFree(p->H);
+    cudaFree(p->partials);
+    cudaFree(p->flags);
+    cudaFree(p->x_stage);
+    cudaFree(p->y_stage);
+    if (prev >= 0 && prev != p->device) cudaSetDevice(prev);
+    delete p;
+}
+
+kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int epi) {
+    kt::GemmParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.M = (int)g.M;
+    q.N = (int)g.N;
+    q.K = (int)g.K;
+    q.BN = g.BN;
+    q.n_chunks = (g.BN + 63) / 64;
+    q.stages = g.stages;
+    q.split_k = g.split_k;
+    q.tiles_m = g.tiles_m;
+    q.tiles_n = g.tiles_n;
+    q.kblocks = g.kblocks;
+    q.kblocks_per_split = g.kblocks_per_split;
+    q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
+    q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
+    q.idesc = kt::make_idesc(P->dtype, g.BN);
+    q.a_bytes = kt::kBM * kt::kBK * 2;
+    q.b_bytes = (uint32_t)q.n_chunks * 64u * kt::kBK * 2u;
+    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b);
+    q.acc_bufs = (epi == kt::EPI_GEGLU && g.BN > 128) ? 1u : 2u;
+    q.gate_acc_off = epi == kt::EPI_GEGLU ? (g.BN <= 128 ? 128u : 256u) : 0u;
+    q.error = P->flags;
+    q.wait_limit_ns = 4000000000ull;  // 4 s: far beyond any legitimate wait
+    q.stall_limit_ns = (unsigned long long)P->stall_limit_us * 1000ull;
+    return q;
+}
+
+kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void* W_down,
+                   const void* b_up, const void* b_down, void* Y, void* H, void* stream) {
+    if (!P) return fail(KT_ERR_INVALID, "plan is NULL");
+    if (!X || !W_up || !W_down || !Y || !H) return fail(KT_ERR_INVALID, "X, W_up, W_down, Y (and H) must be non-NULL");
+    if (P->bias && (!b_up || !b_down)) return fail(KT_ERR_INVALID, "plan has bias = 1: b_up and b_down are required");
+    if (!aligned16(X) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(Y) || !aligned16(H) ||
+        (P->bias && (!aligned16(b_up) || !aligned16(b_down))))
+        return fail(KT_ERR_INVALID, "device pointers must be 16-byte aligned");
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != P->device) return fail(KT_ERR_INVALID, "the current device is not the plan's device");
+
+    const char* why = "";
+    if (!P->cache_valid || P->c_x != X || P->c_wu != W_up || P->c_h != H || P->c_wd != W_down) {
+        // A operands: [rows][K] K-major, box 128 rows x 64 columns.
+        // B operands: [K][N] N-major, box 64 rows (K) x 64 columns (N).
+        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kBK, &why) ||
+            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, kt::kBK, 64, &why) ||
+            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kBK, &why) ||
+            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, kt::kBK, 64, &why)) {
+            P->cache_valid = false;
+            return fail(KT_ERR_CUDA, std::string("tensor map: ") + why);
+        }
+        P->c_x = X;
+        P->c_wu = W_up;
+        P->c_h = H;
+        P->c_wd = W_down;
+        P->cache_valid = true;
+    }
+
+    const int epi_up = P->act == KT_ACT_GELU_ERF ? kt::EPI_GELU_ERF
+                     : P->act == KT_ACT_GELU_TANH ? kt::EPI_GELU_TANH
+                     : P->act == KT_ACT_GEGLU ? kt::EPI_GEGLU : kt::EPI_NONE;
+    kt::GemmParams up = make_params(P, P->choice.up, epi_up);
+    up.out = H;
+    up.ldo = (int)P->F;
+    up.bias = P->bias ? b_up : nullptr;
+    up.inject_stall = P->inject_stall;
+    up.pdl_wait = 0;
+    kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, up, P->choice.up.grid,
+                                  P->choice.up.smem_bytes, stream, false, &why);
+    if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
+
+    kt::GemmParams dn = make_params(P, P->choice.down, kt::EPI_DOWN);
+    dn.out = Y;
+    dn.ldo = (int)P->D;
+    dn.bias = P->bias ? b_down : nullptr;
+    dn.partials = P->partials;
+    dn.counters = P->flags + 1;
+    dn.pdl_wait = 1;
+    s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, dn, P->choice.down.grid,
+                        P->choice.down.smem_bytes, stream, true, &why);
+    if (s != KT_OK) return fail(s, std::string("down projection launch: ") + why);
+    P->last_stream = stream;
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int kt_mlp_abi_version(void) { return KT_MLP_ABI_VERSION; }
+
+const char* kt_last_error(void) { return g_last_error.c_str(); }
+
+kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtype, int bias,
+                           int num_sms, kt_plan_info* out) {
+    if (!out) return fail(KT_ERR_INVALID, "out is NULL");
+    kt_status s = validate_problem(M, D, F, act, dtype, bias);
+    if (s != KT_OK) return s;
+    kt::PlanChoice c;
+    const char* why = "";
+    s = kt::plan_choose(M, D, F, act, num_sms, &c, &why);
+    if (s != KT_OK) return fail(s, why);
+    std::memset(out, 0, sizeof(*out));
+    out->M = M; out->D = D; out->F = F;
+    out->act = act; out->dtype = dtype; out->bias = bias;
+    out->num_sms = num_sms;
+    kt::plan_fill_info(c.up, &out->up);
+    kt::plan_fill_info(c.down, &out->down);
+    int64_t ws = M * F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n) + 2 * 2 * M * D;
+    if (c.down.split_k > 1)
+        ws += (int64_t)c.down.split_k * c.down.tiles_m * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
+    out->workspace_bytes = ws;
+    return ok();
+}
+
+kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtype, int bias,
+                      kt_mlp_plan_t* out) {
+    if (!out) return fail(KT_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    kt_status s = validate_problem(M, D, F, act, dtype, bias);
+    if (s != KT_OK) return s;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDeviceProperties", e);
+    if (prop.major != 10 || prop.minor != 3) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf), "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
+                      prop.major, prop.minor);
+        return fail(KT_ERR_UNSUPPORTED, buf);
+    }
+    kt_mlp_plan_s* P = new (std::nothrow) kt_mlp_plan_s();
+    if (!P) return fail(KT_ERR_NOMEM, "host allocation of the plan failed");
+    P->M = M; P->D = D; P->F = F;
+    P->F_up = act == KT_ACT_GEGLU ? 2 * F : F;
+    P->act = act; P->dtype = dtype; P->bias = bias;
+    P->device = dev;
+    P->num_sms = prop.multiProcessorCount;
+    const char* why = "";
+    s = kt::plan_choose(M, D, F, act, P->num_sms, &P->choice, &why);
+    if (s != KT_OK) {
+        delete P;
+        return fail(s, why);
+    }
+    const kt::GemmConfig& dn = P->choice.down;
+    size_t h_bytes = (size_t)M * (size_t)F * 2;
+    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n;
+    size_t flag_bytes = 4 * (1 + n_counters);
+    size_t part_bytes = dn.split_k > 1 ? (size_t)dn.split_k * dn.tiles_m * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4 : 0;
+    size_t io_bytes = (size_t)M * (size_t)D * 2;
+    if ((e = cudaMalloc(&P->H, h_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&P->flags), flag_bytes)) != cudaSuccess ||
+        (part_bytes && (e = cudaMalloc(reinterpret_cast<void**>(&P->partials), part_bytes)) != cudaSuccess) ||
+        (e = cudaMalloc(&P->x_stage, io_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(&P->y_stage, io_bytes)) != cudaSuccess) {
+        free_plan(P);
+        cudaGetLastError();
+        return fail(KT_ERR_NOMEM, std::string("workspace allocation: ") + cudaGetErrorString(e));
+    }
+    if ((e = cudaMemset(P->flags, 0, flag_bytes)) != cudaSuccess) {
+        free_plan(P);
+        return cuda_fail("cudaMemset", e);
+    }
+    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + part_bytes + 2 * io_bytes);
+    *out = P;
+    return ok();
+}
+
+kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                     const void* b_up, const void* b_down, void* Y, void* stream) {
+    return run_impl(plan, X, W_up, W_down, b_up, b_down, Y, plan ? plan->H : nullptr, stream);
+}
+
+kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                            const void* b_up, const void* b_down, void* Y, void* H_out, void* stream) {
+    if (!H_out) return fail(KT_ERR_INVALID, "H_out is NULL");
+    return run_impl(plan, X, W_up, W_down, b_up, b_down, Y, H_out, stream);
+}
+
+kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_up, const void* W_down,
+                          const void* b_up, const void* b_down, void* Y_host, void* stream) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    if (!X_host || !Y_host) return fail(KT_ERR_INVALID, "X_host and Y_host must be non-NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    size_t bytes = (size_t)plan->M * (size_t)plan->D * 2;
+    cudaError_t e = cudaMemcpyAsync(plan->x_stage, X_host, bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail("copy of X to the device", e);
+    kt_status s = run_impl(plan, plan->x_stage, W_up, W_down, b_up, b_down, plan->y_stage, plan->H, stream);
+    if (s != KT_OK) return s;
+    e = cudaMemcpyAsync(Y_host, plan->y_stage, bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail("copy of Y to the host", e);
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    return ok();
+}
+
+kt_status kt_mlp_status(kt_mlp_plan_t plan) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(plan->last_stream));
+    if (e != cudaSuccess) return cuda_fail("stream", e);
+    int word = 0;
+    e = cudaMemcpy(&word, plan->flags, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("reading the error word", e);
+    if (word != kt::DEV_OK) {
+        // clear the word and the split-K counters an aborted run may have left behind
+        const kt::GemmConfig& dn = plan->choice.down;
+        size_t flag_bytes = 4 * (1 + (size_t)dn.tiles_m * dn.tiles_n);
+        cudaMemset(plan->flags, 0, flag_bytes);
+        cudaDeviceSynchronize();
+        const char* where = word == kt::DEV_TIMEOUT_PRODUCER ? "producer"
+                          : word == kt::DEV_TIMEOUT_MMA ? "MMA issuer"
+                          : word == kt::DEV_TIMEOUT_EPILOGUE ? "epilogue"
+                          : word == kt::DEV_INJECTED_STALL ? "injected stall" : "unknown";
+        return fail(KT_ERR_TIMEOUT, std::string("a bounded device wait ran out (") + where + ")");
+    }
+    return ok();
+}
+
+kt_status kt_mlp_destroy(kt_mlp_plan_t plan) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    free_plan(plan);
+    return ok();
+}
+
+kt_status kt_mlp_get_info(kt_mlp_plan_t plan, kt_plan_info* out) {
+    if (!plan || !out) return fail(KT_ERR_INVALID, "plan and out must be non-NULL");
+    std::memset(out, 0, sizeof(*out));
+    out->M = plan->M; out->D = plan->D; out->F = plan->F;
+    out->act = plan->act; out->dtype = plan->dtype; out->bias = plan->bias;
+    out->num_sms = plan->num_sms;
+    kt::plan_fill_info(plan->choice.up, &out->up);
+    kt::plan_fill_info(plan->choice.down, &out->down);
+    out->workspace_bytes = plan->workspace_bytes;
+    return ok();
+}
+
+kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
+    if (!plan || !buf || len == 0) return fail(KT_ERR_INVALID, "plan and buf must be non-NULL, len > 0");
+    const kt::GemmConfig& u = plan->choice.up;
+    const kt::GemmConfig& d = plan->choice.down;
+    std::snprintf(buf, len,
+                  "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d sms=%d | up: 128x%d tiles %dx%d (grid %d, %d "
+                  "wave%s, %d stages, useful %.3f, model %.2f us) | down: 128x%d tiles %dx%d split_k %d (grid %d, "
+                  "%d wave%s, %d stages, useful %.3f, model %.2f us) | workspace %lld B",
+                  (long long)plan->M, (long long)plan->D, (long long)plan->F, act_name(plan->act),
+                  plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->num_sms, u.BN, u.tiles_m, u.tiles_n,
+                  u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, d.BN,
+                  d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
+                  d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
+    return ok();
+}
+
+kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    if (enable && (limit_us < 1 || limit_us > 10000000))
+        return fail(KT_ERR_INVALID, "limit_us must be in [1, 10 000 000]");
+    plan->inject_stall = enable ? 1 : 0;
+    plan->stall_limit_us = enable ? limit_us : 0;
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,738 @@
+// kt_mlp_kernels.cu -- the sm_103a GEMM kernels of the fused MLP.
+//
+// One persistent, warp-specialised kernel template serves both projections:
+//
+//   warp 0      producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
+//               A tile (128 x 64, K-major) and the B tile(s) (64 x BN in 64-column
+//               boxes, N-major) into an S-stage shared-memory ring, one mbarrier
+//               pair (full / empty) per stage.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f16 (M=128, N=BN,
+//               K=16, fp32 accumulation in tensor memory), four per k-block, and
+//               tcgen05.commit hands the stage back to the producer.  Two TMEM
+//               accumulator buffers let tile i+1's main loop run under tile i's
+//               epilogue.  GEGLU issues a second MMA per step into a gate
+//               accumulator that shares the A tile (one X stream, two weights).
+//   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers
+//               (TMEM lane = tile row), adds the bias, applies the activation
+//               (GELU erf / tanh, GEGLU value*gelu(gate)), rounds ONCE to the I/O
+//               dtype and stores H; the down projection adds b_down and stores Y,
+//               or, with split-K, writes an fp32 partial and the last CTA to arrive
+//               on the tile sums the partials in split order (deterministic).
+//
+// Sources: "SDXL as a requirements inventory", section 1.3 (FeedForward: value =
+// first half, gate = second half) and 9.3 (erf GELU); "MLP layout sweep and
+// remaining representation limits" (the SigLIP MLP, tanh GELU, K-partitioned
+// down projection with a reduction); "The software stack", sections 2.2 (3-D grid,
+// split-K needs a reduction, every output element produced exactly once), 2.3
+// (epilogue folding; the accumulator is never a memory word) and 2.4 (B resident,
+// A double-buffered -> here a multi-stage ring).
+//
+// Every device-side wait is bounded by %globaltimer; on expiry the kernel records
+// an error code, raises a CTA-wide abort flag, drains its own in-flight copies and
+// MMAs (again bounded), frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "kt_internal.h"
+
+namespace kt {
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+// Wait for the phase of parity `parity` of barrier `bar` to complete.  Returns
+// false if the CTA is aborting or if `limit_ns` passed (then raises the abort
+// flag and records `code` in the error word, first writer wins).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err, int code, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Drain wait used on the abort path: ignores the abort flag, bounded by limit_ns.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading-dimension and
+// stride-dimension byte offsets (all >> 4), descriptor version 1 (bits 46-48 =
+// 0b001), base offset 0 (tiles are 1024-byte aligned), 128-byte swizzle (= 2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns; thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// tcgen05.wait::ld, with the loaded registers threaded through so that no use
+// of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r)[16], uint32_t (&s)[16]) {
+    tmem_wait_ld(r);
+    asm volatile(""
+                 : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]),
+                   "+r"(s[6]), "+r"(s[7]), "+r"(s[8]), "+r"(s[9]), "+r"(s[10]), "+r"(s[11]),
+                   "+r"(s[12]), "+r"(s[13]), "+r"(s[14]), "+r"(s[15])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
+
+// Barrier over the epilogue warps that also ANDs a predicate across them, so that
+// all of them take the same branch after a bounded wait (no warp is left behind
+// at a later named barrier).
+__device__ __forceinline__ bool epi_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "n"(kEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue arithmetic (fp32)
+// ---------------------------------------------------------------------------
+
+// gelu_erf(z) = z * Phi(z) = 0.5 z erfc(-z / sqrt 2)   (no cancellation for z < 0)
+__device__ __forceinline__ float gelu_erf_f(float z) { return 0.5f * z * erfcf(-0.70710678118654752f * z); }
+
+// gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3)
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+    const float u = 0.79788456080286536f * fmaf(0.044715f * z, z * z, z);
+    return z / (1.0f + __expf(-2.0f * u));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (DT == KT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& w, float* f) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (DT == KT_BF16) {
+            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&u[i]);
+            float2 t = __bfloat1622float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        } else {
+            __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+            float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+}
+
+// 16 bias values starting at column `col` (groups of 8 past `limit` read as 0).
+template <int DT>
+__device__ __forceinline__ void load_bias16(const void* bias, int col, int limit, float* b) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(bias) + col;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        if (col + 8 * g < limit) {
+            uint4 w = __ldg(reinterpret_cast<const uint4*>(p + 8 * g));
+            unpack8<DT>(w, b + 8 * g);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) b[8 * g + i] = 0.0f;
+        }
+    }
+}
+
+// Round 16 values to the I/O dtype and store them at out[m][col..col+15]; groups
+// of 8 columns at or past N are dropped (N is a multiple of 8), rows >= M too.
+template <int DT>
+__device__ __forceinline__ void store16(void* out, int ldo, int m, int M, int col, int N,
+                                        const float* v) {
+    if (m >= M) return;
+    uint16_t* p = reinterpret_cast<uint16_t*>(out) + (size_t)m * (size_t)ldo + col;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        if (col + 8 * g < N) {
+            uint4 w;
+            w.x = pack2<DT>(v[8 * g + 0], v[8 * g + 1]);
+            w.y = pack2<DT>(v[8 * g + 2], v[8 * g + 3]);
+            w.z = pack2<DT>(v[8 * g + 4], v[8 * g + 5]);
+            w.w = pack2<DT>(v[8 * g + 6], v[8 * g + 7]);
+            *reinterpret_cast<uint4*>(p + 8 * g) = w;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+struct TileCoord {
+    int split, tm, tn, mn;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
+    TileCoord c;
+    const int per_split = p.tiles_m * p.tiles_n;
+    c.split = t / per_split;
+    c.mn = t - c.split * per_split;
+    c.tm = c.mn / p.tiles_n;
+    c.tn = c.mn - c.tm * p.tiles_n;
+    return c;
+}
+
+template <int EPI, int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles want 1024-byte alignment
+    uint8_t* base_ptr = smem_raw + (base - raw);
+
+    const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
+    const uint32_t bar_full = base + tiles_bytes;
+    const uint32_t bar_empty = bar_full + 8u * kMaxStages;
+    const uint32_t bar_accf = bar_empty + 8u * kMaxStages;
+    const uint32_t bar_acce = bar_accf + 16u;
+    const uint32_t bar_stall = bar_acce + 16u;
+    const uint32_t bar_drain = bar_stall + 8u;
+    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + 8u * (2 * kMaxStages + 6));
+    uint32_t* tmem_slot = slots;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_accf + 8u * b, 1);
+            mbar_init(bar_acce + 8u * b, kEpiWarps);
+        }
+        mbar_init(bar_stall, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if constexpr (EPI != EPI_DOWN) {
+        // let the dependent down projection get its CTAs resident as SMs free up
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    if (p.pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed = 0, armed_phase = 0;  // per-stage bits: loads issued / their phase
+            if (p.inject_stall) {
+                // failure injection: a barrier nobody arrives on, bounded wait
+                wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
+            }
+            for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+                const TileCoord c = decode_tile(t, p);
+                const int kb0 = c.split * p.kblocks_per_split;
+                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
+                const int n0 = c.tn * p.BN;
+                int chunks = 0;  // 64-column boxes of this tile inside [0, N)
+                for (int ch = 0; ch < p.n_chunks; ++ch)
+                    if (n0 + 64 * ch < p.N) chunks = ch + 1;
+                const uint32_t tx = p.a_bytes + (uint32_t)(n_b * chunks) * 8192u;
+                bool ok = true;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.error,
+                                    DEV_TIMEOUT_PRODUCER, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full + 8u * stage;
+                    const uint32_t sA = base + stage * p.stage_bytes;
+                    const uint32_t sB = sA + p.a_bytes;
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_2d(sA, &tmA, fb, kb * kBK, c.tm * kBM);
+                    for (int ch = 0; ch < chunks; ++ch)
+                        tma_load_2d(sB + 8192u * ch, &tmB, fb, n0 + 64 * ch, kb * kBK);
+                    if (EPI == EPI_GEGLU) {
+                        for (int ch = 0; ch < chunks; ++ch)
+                            tma_load_2d(sB + p.b_bytes + 8192u * ch, &tmB, fb, p.gate_col + n0 + 64 * ch,
+                                        kb * kBK);
+                    }
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == (uint32_t)p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // do not leave copies in flight into shared memory we are about to release
+                for (int s = 0; s < p.stages; ++s)
+                    if (armed & (1u << s)) wait_drain(bar_full + 8u * s, (armed_phase >> s) & 1u, 100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool issued_any = false;
+            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+                const TileCoord c = decode_tile(t, p);
+                const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
+                const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
+                if (!wait_phase(bar_acce + 8u * buf, (use & 1u) ^ 1u, abort_flag, p.error, DEV_TIMEOUT_MMA,
+                                p.wait_limit_ns))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
+                const int kb0 = c.split * p.kblocks_per_split;
+                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
+                bool ok = true;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(bar_full + 8u * stage, phase, abort_flag, p.error, DEV_TIMEOUT_MMA,
+                                    p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = base + stage * p.stage_bytes;
+                    const uint32_t sB = sA + p.a_bytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // A: K-major, +32 bytes per 16-element K step inside the 128-byte row.
+                        const uint64_t ad = smem_desc(sA + 32u * k, 16u, 1024u);
+                        // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row groups 1 KB apart
+                        // (SBO), +2 KB per 16-row K step.
+                        const uint64_t bd = smem_desc(sB + 2048u * k, 8192u, 1024u);
+                        const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                        mma_f16(d, ad, bd, p.idesc, acc);
+                        if (EPI == EPI_GEGLU) {
+                            const uint64_t gd = smem_desc(sB + p.b_bytes + 2048u * k, 8192u, 1024u);
+                            mma_f16(d + p.gate_acc_off, ad, gd, p.idesc, acc);
+                        }
+                    }
+                    issued_any = true;
+                    mma_commit(bar_empty + 8u * stage);  // stage free once these MMAs completed
+                    if (++stage == (uint32_t)p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar_accf + 8u * buf);  // accumulator ready for the epilogue
+            }
+            if (*abort_flag && issued_any) {
+                mma_commit(bar_drain);
+                wait_drain(bar_drain, 0u, 100000000ull);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int ew = warp - 2;
+        const int q = warp & 3;    // TMEM lane quadrant this warp may access
+        const int half = ew >> 2;  // interleaved half of the 16-column chunks
+        const int row = q * 32 + lane;
+        const int nchunks16 = p.BN / 16;
+        int local = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+            const TileCoord c = decode_tile(t, p);
+            const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
+            const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
+            const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
+                                        DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
+            if (!epi_all(got)) break;
+            tc_fence_after();
+            const int m = c.tm * kBM + row;
+            const int n0 = c.tn * p.BN;
+            const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)kAccSlot;
+
+            if (EPI != EPI_DOWN || p.split_k == 1) {
+                for (int j = half; j < nchunks16; j += 2) {
+                    const int col = n0 + 16 * j;
+                    uint32_t r[16];
+                    tmem_ld16(tq + 16u * j, r);
+                    if constexpr (EPI == EPI_GEGLU) {
+                        uint32_t g[16];
+                        tmem_ld16(tq + p.gate_acc_off + 16u * j, g);
+                        tmem_wait_ld2(r, g);
+                        if (col < p.N) {
+                            float bv[16], bg[16], v[16];
+                            if (p.bias) {
+                                load_bias16<DT>(p.bias, col, p.N, bv);
+                                load_bias16<DT>(p.bias, p.gate_col + col, p.gate_col + p.N, bg);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) bv[i] = bg[i] = 0.0f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(g[i]) + bg[i]);
+                            store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                        }
+                    } else {
+                        tmem_wait_ld(r);
+                        if (col < p.N) {
+                            float b[16], v[16];
+                            if (p.bias) {
+                                load_bias16<DT>(p.bias, col, p.N, b);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) b[i] = 0.0f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float z = __uint_as_float(r[i]) + b[i];
+                                if (EPI == EPI_GELU_ERF) v[i] = gelu_erf_f(z);
+                                else if (EPI == EPI_GELU_TANH) v[i] = gelu_tanh_f(z);
+                                else v[i] = z;
+                            }
+                            store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
+            } else {
+                // split-K: fp32 partial of this split, then the last CTA on the tile reduces
+                const size_t Mp = (size_t)p.tiles_m * kBM, Np = (size_t)p.tiles_n * p.BN;
+                float* part = p.partials + ((size_t)c.split * Mp + (size_t)m) * Np + (size_t)n0;
+                for (int j = half; j < nchunks16; j += 2) {
+                    uint32_t r[16];
+                    tmem_ld16(tq + 16u * j, r);
+                    tmem_wait_ld(r);
+                    float4* dst = reinterpret_cast<float4*>(part + 16 * j);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
+                __threadfence();
+                epi_bar_sync();
+                if (ew == 0 && lane == 0) {
+                    const int prev = atomicAdd(p.counters + c.mn, 1);
+                    const int last = (prev == p.split_k - 1);
+                    if (last) atomicExch(p.counters + c.mn, 0);  // ready for the next run
+                    *last_flag = last;
+                }
+                epi_bar_sync();
+                if (*last_flag) {
+                    __threadfence();
+                    const float* base_p = p.partials + (size_t)m * Np + (size_t)n0;
+                    for (int j = half; j < nchunks16; j += 2) {
+                        const int col = n0 + 16 * j;
+                        if (col >= p.N) continue;
+                        float v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                        for (int s = 0; s < p.split_k; ++s) {  // fixed split order: deterministic
+                            const float4* src = reinterpret_cast<const float4*>(base_p + (size_t)s * Mp * Np + 16 * j);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 x = __ldcg(src + i);
+                                v[4 * i] += x.x;
+                                v[4 * i + 1] += x.y;
+                                v[4 * i + 2] += x.z;
+                                v[4 * i + 3] += x.w;
+                            }
+                        }
+                        if (p.bias) {
+                            float b[16];
+                            load_bias16<DT>(p.bias, col, p.N, b);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] += b[i];
+                        }
+                        store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                    }
+                }
+                epi_bar_sync();  // last_flag is rewritten for the next tile
+            }
+        }
+    }
+
+    // ------------------------------ teardown ------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+uint32_t make_idesc(int dtype, int n) {
+    uint32_t d = 0;
+    d |= 1u << 4;                                   // D (accumulator) format: f32
+    d |= (dtype == KT_BF16 ? 1u : 0u) << 7;         // A format: f16 = 0, bf16 = 1
+    d |= (dtype == KT_BF16 ? 1u : 0u) << 10;        // B format
+    /* bit 15 = 0: A is K-major */
+    d |= 1u << 16;                                  // B is MN-major
+    d |= (uint32_t)(n >> 3) << 17;                  // N >> 3
+    d |= (uint32_t)(kBM >> 4) << 24;                // M >> 4
+    return d;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+template <int EPI, int DT>
+kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p, int grid,
+                     int smem, void* stream, bool pdl, const char** why) {
+    auto kern = kt_gemm_kernel<EPI, DT>;
+    // opt in to the shared memory this launch needs (idempotent, cheap after the first call)
+    static std::atomic<int> max_set[16];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 16 || max_set[dev].load(std::memory_order_relaxed) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+        if (e != cudaSuccess) {
+            *why = cudaGetErrorString(e);
+            return KT_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 16) max_set[dev].store(kSmemBudget);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, p);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    return KT_OK;
+}
+
+}  // namespace
+
+bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols, const char** why) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) {
+        *why = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(tmap128),
+                    dtype == KT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *why = "cuTensorMapEncodeTiled rejected the tensor (alignment, stride or box)";
+        return false;
+    }
+    return true;
+}
+
+kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const GemmParams& p, int grid,
+                      int smem_bytes, void* stream, bool pdl, const char** why) {
+    const CUtensorMap* a = reinterpret_cast<const CUtensorMap*>(tmA);
+    const CUtensorMap* b = reinterpret_cast<const CUtensorMap*>(tmB);
+#define KT_LAUNCH(E, D) return launch_one<E, D>(a, b, p, grid, smem_bytes, stream, pdl, why)
+    if (dtype == KT_F16) {
+        switch (epi) {
+            case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_F16);
+            case EPI_GELU_TANH: KT_LAUNCH(EPI_GELU_TANH, KT_F16);
+            case EPI_GEGLU: KT_LAUNCH(EPI_GEGLU, KT_F16);
+            case EPI_NONE: KT_LAUNCH(EPI_NONE, KT_F16);
+            case EPI_DOWN: KT_LAUNCH(EPI_DOWN, KT_F16);
+        }
+    } else {
+        switch (epi) {
+            case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_BF16);
+            case EPI_GELU_TANH: KT_LAUNCH(EPI_GELU_TANH, KT_BF16);
+            case EPI_GEGLU: KT_LAUNCH(EPI_GEGLU, KT_BF16);
+            case EPI_NONE: KT_LAUNCH(EPI_NONE, KT_BF16);
+            case EPI_DOWN: KT_LAUNCH(EPI_DOWN, KT_BF16);
+        }
+    }
+#undef KT_LAUNCH
+    *why = "unknown epilogue kind";
+    return KT_ERR_INVALID;
+}
+
+}  // namespace kt

@@ -1,0 +1,161 @@
+// kt_planner.cpp -- padding-aware, wave-aware tile planner (host only, no GPU).
+//
+// Principle ("The software stack", section 2.1): candidates are ranked by the
+// work they do, discounted by the padding they add, not by raw tile size; and
+// section 2.2: the grid is (ceil(M/BM), ceil(N/BN), SK), SK > 1 needs a
+// reduction, and every output element must be produced exactly once.  Section
+// 6 of the same page: the choice is analytic -- no autotuning; measurements are
+// the second opinion.  The KohakuTPU residency limits are replaced by the
+// sm_103a ones: TMEM columns per accumulator (<= 256 per buffer), shared memory
+// per CTA (227 KB), tcgen05 N a multiple of 16 up to 256, one CTA per SM.
+//
+// Model, per candidate (BN, SK):
+//   tiles   = ceil(M/128) * ceil(N/BN) * SK,  waves = ceil(tiles / SMs)
+//   t_mma   = n_b * 2 * 128 * BN * 64 * kblocks_per_split / R_sm
+//   t_feed  = bytes staged per tile / per-SM share of the L2 feed
+//   t_main  = max(t_mma, t_feed) + t_fill
+//   t_epi   = 128 * BN * c_epi          (per-element epilogue cost of the kind)
+//           + 2 * 128 * BN * 4 bytes / per-SM bandwidth   (SK > 1: write the fp32
+//             partial, and on average one more partial-sized pass for the reduction)
+//   t_cta   = t_main + (waves-1) * max(t_main, t_epi) + t_epi   (two TMEM buffers)
+//           = waves * (t_main + t_epi)                           (one buffer)
+// and the candidate with the smallest t_cta wins; ties go to the larger
+// tile (fewer, more intense tiles).  All constants are a model; est_us is never
+// reported as a measurement.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+
+#include "kt_internal.h"
+
+namespace kt {
+namespace {
+
+constexpr double kRsm = 2.25e15 / 152.0;  // dense 16-bit FLOP/s per SM (nominal)
+constexpr double kL2Feed = 20e12;         // aggregate L2 -> SM bytes/s (model)
+constexpr double kSmFeedMax = 240e9;      // one SM's fill bandwidth (model)
+constexpr double kTFill = 0.35e-6;        // pipeline fill + drain latency per tile (model)
+
+double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
+    switch (epi) {
+        case EPI_GELU_ERF: return 0.11e-9;
+        case EPI_GELU_TANH: return 0.07e-9;
+        case EPI_GEGLU: return 0.13e-9;
+        case EPI_NONE: return 0.03e-9;
+        default: return 0.03e-9;
+    }
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int max_stages(int BN, int n_b) {
+    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b);
+    return std::min(s, kMaxStages);
+}
+
+bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms,
+              GemmConfig* g) {
+    int stages = max_stages(BN, n_b);
+    if (stages < 2) return false;
+    int64_t tm = cdiv(M, kBM), tn = cdiv(N, BN), kb = cdiv(K, kBK);
+    int64_t kps = cdiv(kb, SK);
+    int64_t sk_eff = cdiv(kb, kps);  // no empty split
+    if (sk_eff != SK) return false;
+    int64_t tiles = tm * tn * SK;
+    if (tiles > (int64_t)1 << 30) return false;
+    int64_t grid = std::min<int64_t>(tiles, num_sms);
+    int64_t waves = cdiv(tiles, num_sms);
+
+    double t_mma = n_b * 2.0 * kBM * BN * kBK * (double)kps / kRsm;
+    double bytes_tile = (double)kps * stage_bytes(BN, n_b);
+    double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
+    double t_feed = bytes_tile / feed;
+    double t_main = std::max(t_mma, t_feed) + kTFill;
+    double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
+    if (SK > 1) t_epi += 2.0 * kBM * BN * 4.0 / kSmFeedMax;
+    bool two_bufs = !(n_b == 2 && BN > 128);
+    double t_cta = two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
+                            : waves * (t_main + t_epi);
+
+    g->M = M; g->N = N; g->K = K;
+    g->BN = BN; g->stages = stages; g->split_k = SK;
+    g->tiles_m = (int)tm; g->tiles_n = (int)tn; g->kblocks = (int)kb;
+    g->kblocks_per_split = (int)kps;
+    g->grid = (int)grid; g->waves = (int)waves;
+    g->smem_bytes = stages * stage_bytes(BN, n_b) + kSmemReserve;
+    g->n_b = n_b;
+    g->useful_over_padded = (double)M * N * K /
+                            ((double)(tm * kBM) * (double)(tn * BN) * (double)(kb * kBK));
+    g->est_us = t_cta * 1e6;
+    return true;
+}
+
+bool better(const GemmConfig& a, const GemmConfig& b) {
+    // a strictly better than b?
+    if (a.est_us < b.est_us * (1.0 - 1e-9)) return true;
+    if (b.est_us < a.est_us * (1.0 - 1e-9)) return false;
+    if (a.BN != b.BN) return a.BN > b.BN;
+    return a.split_k < b.split_k;
+}
+
+bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int num_sms,
+            GemmConfig* best) {
+    bool found = false;
+    for (int BN = 16; BN <= 256; BN += 16) {
+        for (int SK = 1; SK <= max_sk; ++SK) {
+            GemmConfig g;
+            if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, &g)) continue;
+            if (!found || better(g, *best)) {
+                *best = g;
+                found = true;
+            }
+        }
+    }
+    return found;
+}
+
+}  // namespace
+
+kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
+                      const char** why) {
+    if (M < 1 || D < 1 || F < 1) { *why = "M, D and F must be positive"; return KT_ERR_INVALID; }
+    if (act < 0 || act > 3) { *why = "unknown activation"; return KT_ERR_INVALID; }
+    if (num_sms < 1) { *why = "num_sms must be positive"; return KT_ERR_INVALID; }
+    if (D % 8 != 0 || F % 8 != 0) {
+        *why = "D and F must be multiples of 8 (16-byte row pitch for TMA)";
+        return KT_ERR_UNSUPPORTED;
+    }
+    const int64_t lim = (int64_t)1 << 30;
+    int64_t F_up = act == KT_ACT_GEGLU ? 2 * F : F;
+    if (M >= lim || D >= lim || F_up >= lim || M * F >= ((int64_t)1 << 40) ||
+        M * D >= ((int64_t)1 << 40)) {
+        *why = "sizes beyond the supported index range";
+        return KT_ERR_UNSUPPORTED;
+    }
+    int epi_up = act == KT_ACT_GELU_ERF ? EPI_GELU_ERF
+               : act == KT_ACT_GELU_TANH ? EPI_GELU_TANH
+               : act == KT_ACT_GEGLU ? EPI_GEGLU : EPI_NONE;
+    int n_b = act == KT_ACT_GEGLU ? 2 : 1;
+    if (!choose(M, F, D, n_b, epi_up, 1, num_sms, &out->up)) {
+        *why = "no feasible tile for the up projection";
+        return KT_ERR_UNSUPPORTED;
+    }
+    if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down)) {
+        *why = "no feasible tile for the down projection";
+        return KT_ERR_UNSUPPORTED;
+    }
+    return KT_OK;
+}
+
+void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* o) {
+    o->BM = kBM; o->BN = g.BN; o->BK = kBK;
+    o->stages = g.stages; o->split_k = g.split_k;
+    o->tiles_m = g.tiles_m; o->tiles_n = g.tiles_n; o->kblocks = g.kblocks;
+    o->grid = g.grid; o->waves = g.waves;
+    o->smem_bytes = g.smem_bytes; o->tmem_cols = kTmemCols;
+    o->M = g.M; o->N = g.N; o->K = g.K;
+    o->useful_over_padded = g.useful_over_padded;
+    o->est_us = g.est_us;
+}
+
+}  // namespace kt

@@ -1,0 +1,217 @@
+"""Thin ctypes binding of ``include/kt_mlp.h`` (argument marshalling only).
+
+Every function here has the name of the C entry point it wraps and does no
+arithmetic of its own: it converts torch tensors / ints to pointers, the
+current torch CUDA stream to a ``cudaStream_t``, and non-OK statuses to
+``KtError``.  The library is loaded from the package's in-tree ``_build``
+directory; if it is missing the import of a compute entry point fails loudly
+(there is no fallback of any kind).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libkt_mlp.so")
+
+KT_ACT_GELU_ERF, KT_ACT_GELU_TANH, KT_ACT_GEGLU, KT_ACT_NONE = 0, 1, 2, 3
+KT_F16, KT_BF16 = 0, 1
+KT_OK, KT_ERR_INVALID, KT_ERR_UNSUPPORTED, KT_ERR_CUDA, KT_ERR_TIMEOUT, KT_ERR_NOMEM = range(6)
+STATUS_NAMES = {0: "KT_OK", 1: "KT_ERR_INVALID", 2: "KT_ERR_UNSUPPORTED", 3: "KT_ERR_CUDA",
+                4: "KT_ERR_TIMEOUT", 5: "KT_ERR_NOMEM"}
+
+
+class KtError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {message}")
+
+
+class kt_gemm_plan_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("BM", "BN", "BK", "stages", "split_k", "tiles_m", "tiles_n", "kblocks", "grid", "waves",
+                 "smem_bytes", "tmem_cols")] + \
+               [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("useful_over_padded", ctypes.c_double), ("est_us", ctypes.c_double)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class kt_plan_info(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("F", ctypes.c_int64),
+                ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("bias", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32),
+                ("up", kt_gemm_plan_info), ("down", kt_gemm_plan_info),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        d = {n: getattr(self, n) for n, _ in self._fields_ if n not in ("up", "down")}
+        d["up"] = self.up.as_dict()
+        d["down"] = self.down.as_dict()
+        return d
+
+
+_lock = threading.Lock()
+_lib = None
+
+# every entry point declared in include/kt_mlp.h, with its ctypes signature
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+SIGNATURES = {
+    "kt_mlp_plan": ([_I64, _I64, _I64, _I32, _I32, _I32, ctypes.POINTER(_VP)], _I32),
+    "kt_mlp_run": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "kt_mlp_run_with_h": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "kt_mlp_run_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "kt_mlp_status": ([_VP], _I32),
+    "kt_mlp_destroy": ([_VP], _I32),
+    "kt_mlp_describe": ([_VP, ctypes.c_char_p, ctypes.c_size_t], _I32),
+    "kt_mlp_get_info": ([_VP, ctypes.POINTER(kt_plan_info)], _I32),
+    "kt_mlp_plan_info": ([_I64, _I64, _I64, _I32, _I32, _I32, _I32, ctypes.POINTER(kt_plan_info)], _I32),
+    "kt_mlp_debug_stall": ([_VP, _I32, _I64], _I32),
+    "kt_last_error": ([], ctypes.c_char_p),
+    "kt_mlp_abi_version": ([], _I32),
+}
+
+
+def load(path: str | None = None):
+    """Load the shared library once (raises OSError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise OSError(f"{p} not found: build it with `python -m transformer_mlp_gemms_gb300.build`")
+        lib = ctypes.CDLL(p)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != KT_OK:
+        raise KtError(status, where, load().kt_last_error().decode(errors="replace"))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor, an int address or None, got {type(x)}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def kt_mlp_abi_version() -> int:
+    return load().kt_mlp_abi_version()
+
+
+def kt_last_error() -> str:
+    return load().kt_last_error().decode(errors="replace")
+
+
+def kt_mlp_plan(M: int, D: int, F: int, act: int, dtype: int, bias: bool) -> int:
+    out = _VP()
+    _check(load().kt_mlp_plan(M, D, F, act, dtype, int(bias), ctypes.byref(out)), "kt_mlp_plan")
+    return out.value
+
+
+def kt_mlp_run(plan: int, X, W_up, W_down, b_up, b_down, Y, stream=None) -> None:
+    _check(load().kt_mlp_run(plan, _ptr(X), _ptr(W_up), _ptr(W_down), _ptr(b_up), _ptr(b_down), _ptr(Y),
+                             _stream(stream)), "kt_mlp_run")
+
+
+def kt_mlp_run_with_h(plan: int, X, W_up, W_down, b_up, b_down, Y, H_out, stream=None) -> None:
+    _check(load().kt_mlp_run_with_h(plan, _ptr(X), _ptr(W_up), _ptr(W_down), _ptr(b_up), _ptr(b_down),
+                                    _ptr(Y), _ptr(H_out), _stream(stream)), "kt_mlp_run_with_h")
+
+
+def kt_mlp_run_host(plan: int, X_host, W_up, W_down, b_up, b_down, Y_host, stream=None) -> None:
+    _check(load().kt_mlp_run_host(plan, _ptr(X_host), _ptr(W_up), _ptr(W_down), _ptr(b_up), _ptr(b_down),
+                                  _ptr(Y_host), _stream(stream)), "kt_mlp_run_host")
+
+
+def kt_mlp_status(plan: int) -> int:
+    """Returns the status code (does not raise on KT_ERR_TIMEOUT)."""
+    return load().kt_mlp_status(plan)
+
+
+def kt_mlp_destroy(plan: int) -> None:
+    _check(load().kt_mlp_destroy(plan), "kt_mlp_destroy")
+
+
+def kt_mlp_describe(plan: int) -> str:
+    buf = ctypes.create_string_buffer(1024)
+    _check(load().kt_mlp_describe(plan, buf, len(buf)), "kt_mlp_describe")
+    return buf.value.decode()
+
+
+def kt_mlp_get_info(plan: int) -> dict:
+    info = kt_plan_info()
+    _check(load().kt_mlp_get_info(plan, ctypes.byref(info)), "kt_mlp_get_info")
+    return info.as_dict()
+
+
+def kt_mlp_plan_info(M: int, D: int, F: int, act: int, dtype: int, bias: bool, num_sms: int) -> dict:
+    info = kt_plan_info()
+    _check(load().kt_mlp_plan_info(M, D, F, act, dtype, int(bias), num_sms, ctypes.byref(info)),
+           "kt_mlp_plan_info")
+    return info.as_dict()
+
+
+def kt_mlp_debug_stall(plan: int, enable: bool, limit_us: int = 0) -> None:
+    _check(load().kt_mlp_debug_stall(plan, int(bool(enable)), limit_us), "kt_mlp_debug_stall")
+
+
+class Plan:
+    """Owning handle: ``Plan(M, D, F, act, dtype, bias)``; destroyed with the object."""
+
+    def __init__(self, M, D, F, act, dtype, bias):
+        self.M, self.D, self.F, self.act, self.dtype, self.bias = M, D, F, act, dtype, bool(bias)
+        self.handle = kt_mlp_plan(M, D, F, act, dtype, bias)
+
+    def run(self, X, W_up, W_down, b_up, b_down, Y, stream=None):
+        kt_mlp_run(self.handle, X, W_up, W_down, b_up, b_down, Y, stream)
+
+    def run_with_h(self, X, W_up, W_down, b_up, b_down, Y, H, stream=None):
+        kt_mlp_run_with_h(self.handle, X, W_up, W_down, b_up, b_down, Y, H, stream)
+
+    def run_host(self, X_host, W_up, W_down, b_up, b_down, Y_host, stream=None):
+        kt_mlp_run_host(self.handle, X_host, W_up, W_down, b_up, b_down, Y_host, stream)
+
+    def status(self) -> int:
+        return kt_mlp_status(self.handle)
+
+    def describe(self) -> str:
+        return kt_mlp_describe(self.handle)
+
+    def info(self) -> dict:
+        return kt_mlp_get_info(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            kt_mlp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

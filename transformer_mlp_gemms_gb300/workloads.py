@@ -27,9 +27,9 @@ import math
 import numpy as np
 import torch
 
-ACT_GELU_ERF, ACT_GELU_TANH, ACT_GEGLU = 0, 1, 2
+ACT_GELU_ERF, ACT_GELU_TANH, ACT_GEGLU, ACT_NONE = 0, 1, 2, 3
 DT_F16, DT_BF16 = 0, 1
-ACT_NAMES = {ACT_GELU_ERF: "gelu_erf", ACT_GELU_TANH: "gelu_tanh", ACT_GEGLU: "geglu"}
+ACT_NAMES = {ACT_GELU_ERF: "gelu_erf", ACT_GELU_TANH: "gelu_tanh", ACT_GEGLU: "geglu", ACT_NONE: "none"}
 DT_NAMES = {DT_F16: "f16", DT_BF16: "bf16"}
 TORCH_DTYPES = {DT_F16: torch.float16, DT_BF16: torch.bfloat16}
 
