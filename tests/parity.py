@@ -2,8 +2,10 @@
 
 Tolerances, derived from the arithmetic (and stated once more in the design notes):
 
-* Y: ``max |Y_gpu - Yx_oracle| <= 1e-2 * RMS(Yx_oracle) + 1e-3`` per element, the bar
-  of the specification, with RMS over the compared rows.
+* Y: ``|Y_gpu - Yx_oracle| <= 1e-2 * RMS(Yx_oracle) + 1e-3 + ulp_dt(Y)/2`` per element:
+  the bar of the specification on the error of the computation, with RMS over the
+  compared rows, plus the unavoidable final rounding of Y to the I/O dtype (half an
+  ulp), which on its own exceeds 1e-2 * RMS for bf16 outputs beyond ~2.5 RMS.
 * H: within 1 ulp of the I/O dtype (ordered bit distance <= 1) for every element
   whose pre-activation fp32 accumulation cannot move it further.  The GPU sums K
   products in fp32; the classical bound |fl(sum) - sum| <= gamma_K * sum |x_k w_k|,
@@ -48,10 +50,14 @@ def check_y(Y_gpu_bits: np.ndarray, Yx: np.ndarray, dtype: int, what: str = "Y")
     assert np.all(np.isfinite(y)), f"{what}: non-finite outputs (unwritten or overflowed)"
     rms = float(np.sqrt(np.mean(Yx * Yx)))
     tol = 1e-2 * rms + 1e-3
+    tol_el = tol + 0.5 * ulp(np.abs(Yx) + tol, dtype)
     err = np.abs(y - Yx)
-    worst = float(err.max()) if err.size else 0.0
-    assert worst <= tol, f"{what}: max |err| {worst:.3e} > tol {tol:.3e} (rms {rms:.3e})"
-    return worst, tol
+    excess = err - tol_el
+    i = int(np.argmax(excess)) if err.size else 0
+    assert err.size == 0 or excess.flat[i] <= 0, (
+        f"{what}: |err| {err.flat[i]:.3e} > tol {tol_el.flat[i]:.3e} at {np.unravel_index(i, err.shape)} "
+        f"(Yx {Yx.flat[i]:.4e}, rms {rms:.3e})")
+    return float(err.max()) if err.size else 0.0, tol
 
 
 def h_bound(w, t_bits: dict, rows=None) -> np.ndarray:
