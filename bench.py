@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Fused transformer MLP benchmark on GB300: us/call, TFLOP/s and roofline fraction.
+
+One "step" is one call of the whole hot path -- the up projection with its fused
+bias/activation/rounding epilogue and the down projection -- on one batch of
+seeded synthetic input already resident in HBM.  The default workload is the F16
+SigLIP MLP X[1,729,1152] -> 4304 -> 1152 with tanh GELU and no biases.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl kt|reference]
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronize on both sides.  Each step's device time is taken with CUDA
+events on the launching stream; a 256 MiB buffer (> the 129 MB L2) is written
+between steps, outside the events, so every step reads its inputs from HBM.
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
+workload (no collective on the data path: "scaling": "weak"); the time is the
+maximum over ranks and the value the work of all ranks over that time.
+
+The JSON line also carries: the per-kernel roofline of the dominant kernel
+(device time per launch from CUDA events, against MEASURED_PEAKS.json), the
+end-to-end number through the C ABI with host buffers (kt_mlp_run_host), the
+SM clocks sampled with nvidia-smi during the timed region, and the float64 CPU
+oracle timed on the host cores as a reported baseline.
+
+``--impl reference`` times the oracle itself (the reference arm of this build):
+each step computes a bounded sample of the workload's rows on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MLP µs/call and TFLOP/s at 1 GB300; % of dense FP16/BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="siglip")
+    ap.add_argument("--impl", choices=["kt", "reference"], default="kt")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time of the oracle baseline sample (kt arm)")
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="target total CPU time of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--json-out", default=None, help="also write the JSON line to this file")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("kt_mlp_kernels.cu", "kt_internal.h"):
+        with open(os.path.join(ROOT, "transformer_mlp_gemms_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is still current."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    entry = d.get("workloads", {}).get(workload, {}).get(kernel)
+    return entry.get("dram_bytes_per_launch") if entry else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                             "hw_slowdown": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power_cap": parts[8]})
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+
+def summarize_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+    powers = [r["power"] for r in rows if r["power"] is not None]
+    pmax = max(powers) if powers else None
+    loaded = [r for r in rows if r["power"] is not None and pmax and r["power"] >= 0.5 * pmax] or rows
+    reasons = []
+    for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                      ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+        if any(r[key] == "Active" for r in loaded):
+            reasons.append(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+            "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+            "samples": len(rows), "samples_under_load": len(loaded), "power_w_max": pmax}
+
+
+def oracle_baseline(w, t_bits, min_seconds: float, max_seconds: float = 30.0):
+    """The float64 oracle, as it stands, on the host cores: whole workload, repeated."""
+    import numpy as np
+    import oracle
+    flops_row = 2 * (w.D * w.F_up + w.F * w.D)
+    rows = np.arange(w.M, dtype=np.int64)
+    if w.M * flops_row > 5e11:  # very large M: a fixed row sample keeps one pass near seconds
+        rows = np.linspace(0, w.M - 1, num=max(1, int(5e11 // flops_row)), dtype=np.int64)
+    done_rows, t_total, passes = 0, 0.0, 0
+    while True:
+        t0 = time.perf_counter()
+        oracle.mlp(t_bits["X"], t_bits["W_up"], t_bits["W_down"], t_bits.get("b_up"), t_bits.get("b_down"),
+                   act=w.act, dtype=w.dtype, rows=rows)
+        t_total += time.perf_counter() - t0
+        done_rows += rows.size
+        passes += 1
+        if t_total >= min_seconds or t_total + t_total / passes > max_seconds:
+            break
+    value = done_rows * flops_row / t_total / 1e12
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{passes} pass(es) over {rows.size} of {w.M} rows of {w.name} "
+                      f"({done_rows * flops_row / 1e9:.1f} GFLOP in {t_total:.1f} s, float64, OpenMP over rows)"}
+
+
+def workload_config(w, l2):
+    from transformer_mlp_gemms_gb300 import workloads as wl
+    return {"workload": f"{w.name}: X[{w.batch},{w.tokens},{w.D}] -> {w.F_up} -> {w.D}",
+            "M": w.M, "D": w.D, "F": w.F, "F_up": w.F_up, "act": wl.ACT_NAMES[w.act],
+            "io_dtype": wl.DT_NAMES[w.dtype], "bias": w.bias, "seed": w.seed,
+            "flops_per_call": w.flops, "l2": l2}
+
+
+def emit(line, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.json_out:
+        with open(args.json_out, "w") as f:
+            f.write(s + "\n")
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the float64 oracle on the host cores, bounded samples per step."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from transformer_mlp_gemms_gb300 import workloads as wl
+    b = {k: wl.bits(v) for k, v in wl.generate(w).items()}
+    flops_row = 2 * (w.D * w.F_up + w.F * w.D)
+    oracle.build()
+    cal = np.arange(min(w.M, 32), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"), act=w.act, dtype=w.dtype, rows=cal)
+    rate = cal.size * flops_row / max(time.perf_counter() - t0, 1e-6)
+    steps_total = args.steps + args.warmup
+    rows_per_step = int(max(1, min(w.M, args.reference_seconds * rate / (steps_total * flops_row))))
+    rng = np.random.default_rng(w.seed)
+    samples = [np.sort(rng.choice(w.M, size=rows_per_step, replace=False)).astype(np.int64)
+               for _ in range(steps_total)]
+
+    def step(i):
+        oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"), act=w.act, dtype=w.dtype,
+                   rows=samples[i])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, steps_total):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps * rows_per_step * flops_row / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, l2="host memory"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows_per_step} random rows of {w.M} per step, float64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    emit(line, args)
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    from transformer_mlp_gemms_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    from transformer_mlp_gemms_gb300 import build as kbuild
+    from transformer_mlp_gemms_gb300 import kt_mlp
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        kbuild.build()
+    if dist is not None:
+        dist.barrier()
+    kt_mlp.load()
+
+    t = wl.generate(w)
+    d = {k: v.cuda() for k, v in t.items()}
+    tdt = wl.TORCH_DTYPES[w.dtype]
+    Y = torch.empty((w.M, w.D), dtype=tdt, device="cuda")
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    info = plan.info()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    args_run = (d["X"], d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Y)
+
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = str(local)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        gpu_id = str(uuid) if str(uuid).startswith("GPU-") else "GPU-" + str(uuid)
+    sampler = ClockSampler(gpu_id)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan.run(*args_run)
+    torch.cuda.synchronize()
+    if plan.status() != kt_mlp.KT_OK:
+        raise RuntimeError("device status after warm-up: " + kt_mlp.kt_last_error())
+
+    # ---------------- timed region: K steps, barrier + synchronize on both sides ----------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                 # L2 scrub, outside the step's events
+        starts[i].record(stream)
+        plan.run(*args_run)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if plan.status() != kt_mlp.KT_OK:
+        raise RuntimeError("device status after the timed steps: " + kt_mlp.kt_last_error())
+
+    # ---------------- per-kernel device time (same steps, events between the kernels) ----------------
+    ms_up, ms_dn = [], []
+    for _ in range(max(1, min(args.steps, 500))):
+        flush.zero_()
+        a, b = plan.run_timed(*args_run)
+        ms_up.append(a)
+        ms_dn.append(b)
+
+    # ---------------- end to end through the C ABI with host buffers ----------------
+    Xh = t["X"].pin_memory()
+    Yh = torch.empty((w.M, w.D), dtype=tdt).pin_memory()
+    e2e_steps = max(1, min(args.steps, 500))
+    for _ in range(min(args.warmup, 5)):
+        plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+    e2e_s = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+        e2e_s += time.perf_counter() - t0
+    clocks = summarize_clocks(sampler.stop())
+
+    if dist is not None:
+        v = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        total_ms, e2e_s = float(v[0]), float(v[1])
+    if rank != 0:
+        plan.close()
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    value = world * args.steps * w.flops / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+    e2e_value = world * e2e_steps * w.flops / e2e_s / 1e12
+    up_flops = 2 * w.M * w.D * w.F_up
+    dn_flops = 2 * w.M * w.F * w.D
+    mu, md = statistics.mean(ms_up), statistics.mean(ms_dn)
+    dominant = "up" if mu >= md else "down"
+    k_ms, k_flops = (mu, up_flops) if dominant == "up" else (md, dn_flops)
+    peak_tflops = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])  # fp16 : bf16 nominal 1 : 1
+    achieved = k_flops / (k_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.DT_NAMES[w.dtype], "data": "synthetic",
+        "config": workload_config(w, l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"),
+        "us_per_call": ms_per_step * 1e3,
+        "pct_of_peak": 100.0 * value / world / peak_tflops,
+        "peak_tflops": peak_tflops, "peak_source": peak_src,
+        "roofline": {"bound": "tensor", "kernel": f"kt_gemm_kernel ({dominant} projection)",
+                     "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tflops, "traffic": ncu_traffic(w.name, dominant),
+                     "algorithmic_flops_per_launch": k_flops, "ms_per_launch": k_ms,
+                     "peak_note": (f"{peak_src} bf16 dense burst from MEASURED_PEAKS.json (fp16 has the "
+                                   f"same nominal rate)") if peak_src == "measured" else "fallback"},
+        "kernels_ms": {"up": mu, "down": md, "up_tflops": up_flops / (mu * 1e-3) / 1e12,
+                       "down_tflops": dn_flops / (md * 1e-3) / 1e12},
+        "plan": {"up": {k: info["up"][k] for k in ("BN", "stages", "split_k", "grid", "waves")},
+                 "down": {k: info["down"][k] for k in ("BN", "stages", "split_k", "grid", "waves")}},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.D * 2,
+                "d2h_bytes_per_step": w.M * w.D * 2, "us_per_call": e2e_s / e2e_steps * 1e6,
+                "entry_point": "kt_mlp_run_host (pinned X in, Y out; weights resident)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "gpu": props.name, "sms": props.multi_processor_count,
+    }
+    plan.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = oracle_baseline(w, {k: wl.bits(v) for k, v in t.items()}, args.cpu_seconds)
+    emit(line, args)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

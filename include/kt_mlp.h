@@ -139,6 +139,17 @@ kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_
                           void* Y_host, void* stream);
 
 /*
+ * kt_mlp_run_timed -- as kt_mlp_run, with CUDA events recorded on `stream` before,
+ * between and after the two kernels; waits for the last event and writes each
+ * kernel's device time in milliseconds to *ms_up / *ms_down (either may be NULL).
+ * The down kernel is launched without the programmatic dependency here, so the two
+ * kernels do not overlap and each time is that kernel's alone.  For measurement.
+ */
+kt_status kt_mlp_run_timed(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                           const void* b_up, const void* b_down, void* Y, void* stream,
+                           float* ms_up, float* ms_down);
+
+/*
  * kt_mlp_status -- synchronise the plan's last stream and read its device error
  * word.  KT_OK, or KT_ERR_TIMEOUT when a bounded wait ran out in an earlier run
  * (the word is then cleared), or KT_ERR_CUDA if the stream reported an error.
@@ -170,6 +181,24 @@ kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype
  * enable = 0 restores normal runs.  No GPU fault is involved.
  */
 kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us);
+
+/*
+ * kt_mlp_debug_trace -- timeline tracing for tests and profiling.  With non-NULL
+ * device buffers, the next runs of this plan write, per CTA of the up / down kernel,
+ * 16 uint64 slots: %globaltimer (ns) at CTA entry, set-up done, first copy issued,
+ * first stage landed, first tile's main loop done, epilogue start / done, exit;
+ * then the SM id, the number of tiles, the last tile's main-loop / epilogue end,
+ * and four epilogue sub-phase marks of the first epilogue warp.  Each buffer must
+ * hold 16 * grid uint64 (grid from kt_mlp_get_info); the caller owns them.  NULL
+ * buffers switch tracing off.
+ */
+kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_down);
+
+/*
+ * kt_debug_timestamp -- enqueue a one-thread kernel on `stream` that writes
+ * %globaltimer (ns) to the device uint64 at dst.  Brackets launches in traces.
+ */
+kt_status kt_debug_timestamp(void* dst, void* stream);
 
 /* Thread-local message for the calling thread's last non-OK status ("" if none). */
 const char* kt_last_error(void);

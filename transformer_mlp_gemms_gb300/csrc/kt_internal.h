@@ -87,7 +87,32 @@ struct GemmParams {
     unsigned long long wait_limit_ns;   // bound of every device-side wait
     unsigned long long stall_limit_ns;  // bound of the injected wait
     int pdl_wait;            // 1: griddepcontrol.wait before reading the A operand
+    unsigned long long* trace;  // optional per-CTA timeline (kTraceSlots u64 per CTA) or null
 };
+
+// Per-CTA trace slots (globaltimer ns unless noted), written when GemmParams::trace is set.
+enum TraceSlot : int {
+    TR_ENTRY = 0,        // first instruction of the CTA
+    TR_SETUP = 1,        // barriers initialised, TMEM allocated
+    TR_FIRST_TMA = 2,    // producer issued its first copy
+    TR_FIRST_FULL = 3,   // MMA issuer saw the first stage land
+    TR_MAIN_DONE = 4,    // MMA issuer committed the last k-block of its first tile
+    TR_EPI_START = 5,    // epilogue saw the first accumulator ready
+    TR_EPI_DONE = 6,     // epilogue finished its first tile
+    TR_EXIT = 7,         // after the teardown barrier
+    TR_SMID = 8,         // %smid
+    TR_TILES = 9,        // tiles this CTA processed
+    TR_LAST_MAIN = 10,   // MMA issuer committed its last tile
+    TR_LAST_EPI = 11,    // epilogue finished its last tile
+    TR_EPI_LD = 12,      // first epilogue warp: first accumulator group in registers
+    TR_EPI_MATH = 13,    //   ... its bias / activation done
+    TR_EPI_STORE = 14,   //   ... its first store issued
+    TR_EPI_DRAIN = 15,   //   ... all its stores complete
+    kTraceSlots = 16
+};
+
+// One-thread kernel writing %globaltimer to dst (kt_mlp_kernels.cu).
+kt_status launch_timestamp(void* dst, void* stream, const char** why);
 
 // Host launch wrappers (kt_mlp_kernels.cu).  tmA / tmB point to 128-byte CUtensorMap.
 kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const GemmParams& p,

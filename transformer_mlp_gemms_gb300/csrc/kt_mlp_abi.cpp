@@ -77,8 +77,11 @@ struct kt_mlp_plan_s {
     const void* c_wd = nullptr;
     bool cache_valid = false;
     void* last_stream = nullptr;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // kt_mlp_run_timed, created on first use
     int inject_stall = 0;
     int64_t stall_limit_us = 0;
+    unsigned long long* trace_up = nullptr;    // caller-owned device buffers, or null
+    unsigned long long* trace_down = nullptr;
 };
 
 namespace {
@@ -89,6 +92,8 @@ void free_plan(kt_mlp_plan_s* p) {
     cudaGetDevice(&prev);
     if (prev != p->device) cudaSetDevice(p->device);
     cudaDeviceSynchronize();
+    for (cudaEvent_t e : p->ev)
+        if (e) cudaEventDestroy(e);
     cudaFree(p->H);
     cudaFree(p->partials);
     cudaFree(p->flags);
@@ -127,7 +132,8 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
 }
 
 kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void* W_down,
-                   const void* b_up, const void* b_down, void* Y, void* H, void* stream) {
+                   const void* b_up, const void* b_down, void* Y, void* H, void* stream,
+                   bool timed = false) {
     if (!P) return fail(KT_ERR_INVALID, "plan is NULL");
     if (!X || !W_up || !W_down || !Y || !H) return fail(KT_ERR_INVALID, "X, W_up, W_down, Y (and H) must be non-NULL");
     if (P->bias && (!b_up || !b_down)) return fail(KT_ERR_INVALID, "plan has bias = 1: b_up and b_down are required");
@@ -165,6 +171,9 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
     up.bias = P->bias ? b_up : nullptr;
     up.inject_stall = P->inject_stall;
     up.pdl_wait = 0;
+    up.trace = P->trace_up;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (timed) cudaEventRecord(P->ev[0], st);
     kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, up, P->choice.up.grid,
                                   P->choice.up.smem_bytes, stream, false, &why);
     if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
@@ -176,9 +185,12 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
     dn.partials = P->partials;
     dn.counters = P->flags + 1;
     dn.pdl_wait = 1;
+    dn.trace = P->trace_down;
+    if (timed) cudaEventRecord(P->ev[1], st);
     s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, dn, P->choice.down.grid,
-                        P->choice.down.smem_bytes, stream, true, &why);
+                        P->choice.down.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("down projection launch: ") + why);
+    if (timed) cudaEventRecord(P->ev[2], st);
     P->last_stream = stream;
     return ok();
 }
@@ -279,6 +291,28 @@ kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up,
     return run_impl(plan, X, W_up, W_down, b_up, b_down, Y, H_out, stream);
 }
 
+kt_status kt_mlp_run_timed(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
+                           const void* b_up, const void* b_down, void* Y, void* stream,
+                           float* ms_up, float* ms_down) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    for (cudaEvent_t& e : plan->ev) {
+        if (!e) {
+            cudaError_t ce = cudaEventCreate(&e);
+            if (ce != cudaSuccess) return cuda_fail("cudaEventCreate", ce);
+        }
+    }
+    kt_status s = run_impl(plan, X, W_up, W_down, b_up, b_down, Y, plan->H, stream, true);
+    if (s != KT_OK) return s;
+    cudaError_t e = cudaEventSynchronize(plan->ev[2]);
+    if (e != cudaSuccess) return cuda_fail("cudaEventSynchronize", e);
+    float a = 0.f, b = 0.f;
+    cudaEventElapsedTime(&a, plan->ev[0], plan->ev[1]);
+    cudaEventElapsedTime(&b, plan->ev[1], plan->ev[2]);
+    if (ms_up) *ms_up = a;
+    if (ms_down) *ms_down = b;
+    return ok();
+}
+
 kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_up, const void* W_down,
                           const void* b_up, const void* b_down, void* Y_host, void* stream) {
     if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
@@ -349,6 +383,23 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
                   u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, d.BN,
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
+    return ok();
+}
+
+kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_down) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    if ((trace_up && !aligned16(trace_up)) || (trace_down && !aligned16(trace_down)))
+        return fail(KT_ERR_INVALID, "trace buffers must be 16-byte aligned");
+    plan->trace_up = static_cast<unsigned long long*>(trace_up);
+    plan->trace_down = static_cast<unsigned long long*>(trace_down);
+    return ok();
+}
+
+kt_status kt_debug_timestamp(void* dst, void* stream) {
+    if (!dst || (reinterpret_cast<uintptr_t>(dst) & 7u)) return fail(KT_ERR_INVALID, "dst must be an aligned device uint64");
+    const char* why = "";
+    kt_status s = kt::launch_timestamp(dst, stream, &why);
+    if (s != KT_OK) return fail(s, why);
     return ok();
 }
 

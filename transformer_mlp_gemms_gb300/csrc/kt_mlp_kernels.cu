@@ -57,6 +57,16 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void trace_mark(unsigned long long* tr, int slot) {
+    if (tr) tr[(size_t)blockIdx.x * kTraceSlots + slot] = global_ns();
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -337,6 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    unsigned long long* const tr = p.trace;
+    if (threadIdx.x == 0) trace_mark(tr, TR_ENTRY);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -363,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
 
     if constexpr (EPI != EPI_DOWN) {
         // let the dependent down projection get its CTAs resident as SMs free up
@@ -401,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
                     mbar_arrive_expect_tx(fb, tx);
+                    if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
                     tma_load_2d(sA, &tmA, fb, kb * kBK, c.tm * kBM);
                     for (int ch = 0; ch < chunks; ++ch)
                         tma_load_2d(sB + 8192u * ch, &tmB, fb, n0 + 64 * ch, kb * kBK);
@@ -449,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (tr && !issued_any) trace_mark(tr, TR_FIRST_FULL);
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
 #pragma unroll
@@ -474,6 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(bar_accf + 8u * buf);  // accumulator ready for the epilogue
+                if (tr) {
+                    if (local == 0) trace_mark(tr, TR_MAIN_DONE);
+                    trace_mark(tr, TR_LAST_MAIN);
+                    tr[(size_t)blockIdx.x * kTraceSlots + TR_TILES] = (unsigned long long)(local + 1);
+                }
             }
             if (*abort_flag && issued_any) {
                 mma_commit(bar_drain);
@@ -496,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             if (!epi_all(got)) break;
             tc_fence_after();
+            if (tr && local == 0 && warp == 2 && lane == 0) trace_mark(tr, TR_EPI_START);
             const int m = c.tm * kBM + row;
             const int n0 = c.tn * p.BN;
             const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)kAccSlot;
@@ -604,18 +625,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 epi_bar_sync();  // last_flag is rewritten for the next tile
             }
+            if (tr && warp == 2 && lane == 0) {
+                if (local == 0) trace_mark(tr, TR_EPI_DONE);
+                trace_mark(tr, TR_LAST_EPI);
+            }
         }
     }
 
     // ------------------------------ teardown ------------------------------
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && tr) {
+        trace_mark(tr, TR_EXIT);
+        tr[(size_t)blockIdx.x * kTraceSlots + TR_SMID] = sm_id();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
 }
+
+__global__ void kt_timestamp_kernel(unsigned long long* dst) { *dst = global_ns(); }
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -684,6 +715,16 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmP
 }
 
 }  // namespace
+
+kt_status launch_timestamp(void* dst, void* stream, const char** why) {
+    kt_timestamp_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<unsigned long long*>(dst));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    return KT_OK;
+}
 
 bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols, const char** why) {

@@ -66,12 +66,16 @@ SIGNATURES = {
     "kt_mlp_run": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "kt_mlp_run_with_h": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "kt_mlp_run_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "kt_mlp_run_timed": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_float),
+                          ctypes.POINTER(ctypes.c_float)], _I32),
     "kt_mlp_status": ([_VP], _I32),
     "kt_mlp_destroy": ([_VP], _I32),
     "kt_mlp_describe": ([_VP, ctypes.c_char_p, ctypes.c_size_t], _I32),
     "kt_mlp_get_info": ([_VP, ctypes.POINTER(kt_plan_info)], _I32),
     "kt_mlp_plan_info": ([_I64, _I64, _I64, _I32, _I32, _I32, _I32, ctypes.POINTER(kt_plan_info)], _I32),
     "kt_mlp_debug_stall": ([_VP, _I32, _I64], _I32),
+    "kt_mlp_debug_trace": ([_VP, _VP, _VP], _I32),
+    "kt_debug_timestamp": ([_VP, _VP], _I32),
     "kt_last_error": ([], ctypes.c_char_p),
     "kt_mlp_abi_version": ([], _I32),
 }
@@ -148,6 +152,15 @@ def kt_mlp_run_host(plan: int, X_host, W_up, W_down, b_up, b_down, Y_host, strea
                                   _ptr(Y_host), _stream(stream)), "kt_mlp_run_host")
 
 
+def kt_mlp_run_timed(plan: int, X, W_up, W_down, b_up, b_down, Y, stream=None):
+    """Returns (ms_up, ms_down): device time of each kernel, measured with CUDA events."""
+    a, b = ctypes.c_float(), ctypes.c_float()
+    _check(load().kt_mlp_run_timed(plan, _ptr(X), _ptr(W_up), _ptr(W_down), _ptr(b_up), _ptr(b_down),
+                                   _ptr(Y), _stream(stream), ctypes.byref(a), ctypes.byref(b)),
+           "kt_mlp_run_timed")
+    return a.value, b.value
+
+
 def kt_mlp_status(plan: int) -> int:
     """Returns the status code (does not raise on KT_ERR_TIMEOUT)."""
     return load().kt_mlp_status(plan)
@@ -180,6 +193,14 @@ def kt_mlp_debug_stall(plan: int, enable: bool, limit_us: int = 0) -> None:
     _check(load().kt_mlp_debug_stall(plan, int(bool(enable)), limit_us), "kt_mlp_debug_stall")
 
 
+def kt_mlp_debug_trace(plan: int, trace_up=None, trace_down=None) -> None:
+    _check(load().kt_mlp_debug_trace(plan, _ptr(trace_up), _ptr(trace_down)), "kt_mlp_debug_trace")
+
+
+def kt_debug_timestamp(dst, stream=None) -> None:
+    _check(load().kt_debug_timestamp(_ptr(dst), _stream(stream)), "kt_debug_timestamp")
+
+
 class Plan:
     """Owning handle: ``Plan(M, D, F, act, dtype, bias)``; destroyed with the object."""
 
@@ -195,6 +216,9 @@ class Plan:
 
     def run_host(self, X_host, W_up, W_down, b_up, b_down, Y_host, stream=None):
         kt_mlp_run_host(self.handle, X_host, W_up, W_down, b_up, b_down, Y_host, stream)
+
+    def run_timed(self, X, W_up, W_down, b_up, b_down, Y, stream=None):
+        return kt_mlp_run_timed(self.handle, X, W_up, W_down, b_up, b_down, Y, stream)
 
     def status(self) -> int:
         return kt_mlp_status(self.handle)
