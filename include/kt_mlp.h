@@ -195,6 +195,16 @@ kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us);
 kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_down);
 
 /*
+ * kt_debug_activation -- evaluate the epilogue's fp32 activation elementwise on
+ * device arrays: out[i] = gelu_erf(z[i]) / gelu_tanh(z[i]) / z[i] * gelu_erf(gate[i])
+ * (GEGLU) / z[i] (none), for i < n, enqueued on `stream`.  The same device
+ * functions as the fused epilogue; exposed so that their accuracy can be tested
+ * against the oracle on their own.  gate is read only for GEGLU.
+ */
+kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, float* out, int64_t n,
+                              void* stream);
+
+/*
  * kt_debug_timestamp -- enqueue a one-thread kernel on `stream` that writes
  * %globaltimer (ns) to the device uint64 at dst.  Brackets launches in traces.
  */

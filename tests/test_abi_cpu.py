@@ -80,7 +80,7 @@ def _check_gemm(g, M, N, K):
     assert (g["M"], g["N"], g["K"]) == (M, N, K)
     BM, BN, BK, SK = g["BM"], g["BN"], g["BK"], g["split_k"]
     assert BM == 128 and BK == 64
-    assert BN % 16 == 0 and 16 <= BN <= 256
+    assert BN % 32 == 0 and 32 <= BN <= 256
     # the grid covers every output element exactly once: tiles_m * BM >= M > (tiles_m - 1) * BM
     assert (g["tiles_m"] - 1) * BM < M <= g["tiles_m"] * BM
     assert (g["tiles_n"] - 1) * BN < N <= g["tiles_n"] * BN

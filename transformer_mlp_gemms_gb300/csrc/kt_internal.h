@@ -19,7 +19,10 @@ constexpr int kAccSlot = 256;     // TMEM columns reserved per accumulator buffe
 constexpr int kSmemBudget = 227 * 1024;  // opt-in dynamic shared memory per CTA
 // barriers, TMEM slot and flags (1 KB), 1024-byte alignment slack (1 KB), and a 16 KB
 // guard band past the ring so that no descriptor stride can reach beyond the allocation
-constexpr int kSmemReserve = 2048 + 16384;
+constexpr int kStoreCols = 32;    // columns per epilogue TMA store box (32 rows x 32 columns)
+constexpr int kStagingBytes = kEpiWarps * 32 * kStoreCols * 2;  // one 2 KB buffer per epilogue warp
+// output staging, barriers / TMEM slot / flags (1 KB) and 1024-byte alignment slack (1 KB)
+constexpr int kSmemReserve = kStagingBytes + 2048;
 constexpr int kMaxStages = 8;
 
 // Epilogue kinds (one kernel instantiation each, times two dtypes).
@@ -38,7 +41,7 @@ enum DevError : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2,
 // One GEMM's launch configuration, chosen by the planner.
 struct GemmConfig {
     int64_t M, N, K;       // output rows, output columns, reduction length
-    int BN;                // N tile, multiple of 16, 16..256
+    int BN;                // N tile, multiple of 32, 32..256
     int stages;
     int split_k;
     int tiles_m, tiles_n, kblocks, kblocks_per_split;
@@ -77,8 +80,6 @@ struct GemmParams {
     uint32_t stage_bytes, a_bytes, b_bytes;  // per stage / A tile / one B operand tile
     uint32_t acc_bufs;       // accumulator buffers in TMEM (1 or 2)
     uint32_t gate_acc_off;   // TMEM column offset of the gate accumulator (GEGLU)
-    void* out;               // H or Y, row-major [M][ldo]
-    int ldo;
     const void* bias;        // b_up (GEGLU: value then gate halves) / b_down / null
     float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32
     int* counters;           // split-K: [tiles_m*tiles_n] arrival counters (zero between runs)
@@ -111,17 +112,22 @@ enum TraceSlot : int {
     kTraceSlots = 16
 };
 
+// Elementwise activation test kernel (kt_mlp_kernels.cu).
+kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
+                            const char** why);
+
 // One-thread kernel writing %globaltimer to dst (kt_mlp_kernels.cu).
 kt_status launch_timestamp(void* dst, void* stream, const char** why);
 
-// Host launch wrappers (kt_mlp_kernels.cu).  tmA / tmB point to 128-byte CUtensorMap.
-kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const GemmParams& p,
+// Host launch wrappers (kt_mlp_kernels.cu).  tmA / tmB / tmC point to 128-byte
+// CUtensorMaps: the A operand, the B operand and the output (H or Y) store map.
+kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const void* tmC, const GemmParams& p,
                       int grid, int smem_bytes, void* stream, bool pdl, const char** why);
 
 // Encode a 2-D tiled tensor map over a row-major [rows][cols] 16-bit matrix with a
-// box of box_cols x box_rows and 128-byte swizzle.  Returns false on failure.
+// box of box_cols x box_rows and a 128- or 64-byte swizzle.  Returns false on failure.
 bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows, uint32_t box_cols, const char** why);
+                 uint32_t box_rows, uint32_t box_cols, int swizzle_bytes, const char** why);
 
 // tcgen05 instruction descriptor for kind::f16 with fp32 accumulation, A K-major,
 // B MN-major, M = 128, N = n.

@@ -70,11 +70,12 @@ struct kt_mlp_plan_s {
     void* y_stage = nullptr;    // [M][D]
     int64_t workspace_bytes = 0;
     // tensor maps, cached by pointer set
-    alignas(64) CUtensorMap tm_x, tm_wu, tm_h, tm_wd;
+    alignas(64) CUtensorMap tm_x, tm_wu, tm_h, tm_wd, tm_hs, tm_ys;  // loads, then H / Y stores
     const void* c_x = nullptr;
     const void* c_wu = nullptr;
     const void* c_h = nullptr;
     const void* c_wd = nullptr;
+    const void* c_y = nullptr;
     bool cache_valid = false;
     void* last_stream = nullptr;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // kt_mlp_run_timed, created on first use
@@ -145,13 +146,16 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
     if (cur != P->device) return fail(KT_ERR_INVALID, "the current device is not the plan's device");
 
     const char* why = "";
-    if (!P->cache_valid || P->c_x != X || P->c_wu != W_up || P->c_h != H || P->c_wd != W_down) {
-        // A operands: [rows][K] K-major, box 128 rows x 64 columns.
-        // B operands: [K][N] N-major, box 64 rows (K) x 64 columns (N).
-        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kBK, &why) ||
-            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, kt::kBK, 64, &why) ||
-            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kBK, &why) ||
-            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, kt::kBK, 64, &why)) {
+    if (!P->cache_valid || P->c_x != X || P->c_wu != W_up || P->c_h != H || P->c_wd != W_down || P->c_y != Y) {
+        // A operands: [rows][K] K-major, box 128 rows x 64 columns, 128-byte swizzle.
+        // B operands: [K][N] N-major, box 64 rows (K) x 64 columns (N), 128-byte swizzle.
+        // Stores of H and Y: box 32 rows x 32 columns, 64-byte swizzle.
+        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kBK, 128, &why) ||
+            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, kt::kBK, 64, 128, &why) ||
+            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kBK, 128, &why) ||
+            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, kt::kBK, 64, 128, &why) ||
+            !kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) ||
+            !kt::encode_tmap(&P->tm_ys, Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why)) {
             P->cache_valid = false;
             return fail(KT_ERR_CUDA, std::string("tensor map: ") + why);
         }
@@ -159,6 +163,7 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
         P->c_wu = W_up;
         P->c_h = H;
         P->c_wd = W_down;
+        P->c_y = Y;
         P->cache_valid = true;
     }
 
@@ -166,28 +171,24 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
                      : P->act == KT_ACT_GELU_TANH ? kt::EPI_GELU_TANH
                      : P->act == KT_ACT_GEGLU ? kt::EPI_GEGLU : kt::EPI_NONE;
     kt::GemmParams up = make_params(P, P->choice.up, epi_up);
-    up.out = H;
-    up.ldo = (int)P->F;
     up.bias = P->bias ? b_up : nullptr;
     up.inject_stall = P->inject_stall;
     up.pdl_wait = 0;
     up.trace = P->trace_up;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (timed) cudaEventRecord(P->ev[0], st);
-    kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, up, P->choice.up.grid,
+    kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
                                   P->choice.up.smem_bytes, stream, false, &why);
     if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
 
     kt::GemmParams dn = make_params(P, P->choice.down, kt::EPI_DOWN);
-    dn.out = Y;
-    dn.ldo = (int)P->D;
     dn.bias = P->bias ? b_down : nullptr;
     dn.partials = P->partials;
     dn.counters = P->flags + 1;
     dn.pdl_wait = 1;
     dn.trace = P->trace_down;
     if (timed) cudaEventRecord(P->ev[1], st);
-    s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, dn, P->choice.down.grid,
+    s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, &P->tm_ys, dn, P->choice.down.grid,
                         P->choice.down.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("down projection launch: ") + why);
     if (timed) cudaEventRecord(P->ev[2], st);
@@ -392,6 +393,17 @@ kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_dow
         return fail(KT_ERR_INVALID, "trace buffers must be 16-byte aligned");
     plan->trace_up = static_cast<unsigned long long*>(trace_up);
     plan->trace_down = static_cast<unsigned long long*>(trace_down);
+    return ok();
+}
+
+kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, float* out, int64_t n,
+                              void* stream) {
+    if (act < KT_ACT_GELU_ERF || act > KT_ACT_NONE) return fail(KT_ERR_INVALID, "unknown activation");
+    if (n < 0 || (n > 0 && (!z || !out || (act == KT_ACT_GEGLU && !gate))))
+        return fail(KT_ERR_INVALID, "z and out (and gate for GEGLU) must be non-NULL, n >= 0");
+    const char* why = "";
+    kt_status s = kt::launch_activation(act, z, gate, out, n, stream, &why);
+    if (s != KT_OK) return fail(s, why);
     return ok();
 }
 

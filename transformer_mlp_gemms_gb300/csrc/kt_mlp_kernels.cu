@@ -15,9 +15,12 @@
 //   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers
 //               (TMEM lane = tile row), adds the bias, applies the activation
 //               (GELU erf / tanh, GEGLU value*gelu(gate)), rounds ONCE to the I/O
-//               dtype and stores H; the down projection adds b_down and stores Y,
-//               or, with split-K, writes an fp32 partial and the last CTA to arrive
-//               on the tile sums the partials in split order (deterministic).
+//               dtype, stages each warp's 32 x 32 block in swizzled shared memory
+//               and writes it with a TMA tensor store (coalesced, clipped at the
+//               ragged edges); the down projection adds b_down and stores Y, or,
+//               with split-K, writes an fp32 partial (warp-contiguous layout) and
+//               the last CTA to arrive on the tile sums the partials in split
+//               order (deterministic).
 //
 // Sources: "SDXL as a requirements inventory", section 1.3 (FeedForward: value =
 // first half, gate = second half) and 9.3 (erf GELU); "MLP layout sweep and
@@ -36,6 +39,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -207,6 +211,58 @@ __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r)[16], uint32_t (&s)[1
                  : "memory");
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Pass 32 registers through an empty asm so that no use of them is scheduled
+// before the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+    asm volatile(""
+                 : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld_only() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// TMA tensor store of a box from shared memory (clipped at the tensor's bounds).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void epi_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
@@ -231,13 +287,45 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 // Epilogue arithmetic (fp32)
 // ---------------------------------------------------------------------------
 
-// gelu_erf(z) = z * Phi(z) = 0.5 z erfc(-z / sqrt 2)   (no cancellation for z < 0)
-__device__ __forceinline__ float gelu_erf_f(float z) { return 0.5f * z * erfcf(-0.70710678118654752f * z); }
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, hardware approximation (ftz)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approximation (ftz)
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-// gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3)
+// gelu_erf(z) = z * Phi(z),  Phi(z) = erfc(-z / sqrt 2) / 2.
+// erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
+// 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), fractional error
+// below 1.2e-7 for every a >= 0; erfc(-a) = 2 - erfc(a).  Evaluated in fp32 with the
+// hardware exp2 and reciprocal: no cancellation for z < 0, no branches.
+__device__ __forceinline__ float gelu_erf_f(float z) {
+    const float a = fabsf(z) * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(0.5f, a, 1.0f));
+    float p = 0.17087277f;
+    p = fmaf(p, t, -0.82215223f);
+    p = fmaf(p, t, 1.48851587f);
+    p = fmaf(p, t, -1.13520398f);
+    p = fmaf(p, t, 0.27886807f);
+    p = fmaf(p, t, -0.18628806f);
+    p = fmaf(p, t, 0.09678418f);
+    p = fmaf(p, t, 0.37409196f);
+    p = fmaf(p, t, 1.00002368f);
+    p = fmaf(p, t, -1.26551223f);
+    const float e = t * ex2_approx((p - a * a) * 1.4426950408889634f);  // erfc(|z| / sqrt 2)
+    const float phi = z >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
+    return z * phi;
+}
+
+// gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
+// exp(-2u) = 2^(z (c1 + c2 z^2)), c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1.
 __device__ __forceinline__ float gelu_tanh_f(float z) {
-    const float u = 0.79788456080286536f * fmaf(0.044715f * z, z * z, z);
-    return z / (1.0f + __expf(-2.0f * u));
+    const float x = z * fmaf(-0.1029432395800235f, z * z, -2.302208198144325f);
+    return z * rcp_approx(1.0f + ex2_approx(x));
 }
 
 template <int DT>
@@ -270,14 +358,14 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* f) {
     }
 }
 
-// 16 bias values starting at column `col` (groups of 8 past `limit` read as 0).
+// 32 bias values starting at column `col` (groups of 8 at or past `limit` read as 0).
 template <int DT>
-__device__ __forceinline__ void load_bias16(const void* bias, int col, int limit, float* b) {
-    const uint16_t* p = reinterpret_cast<const uint16_t*>(bias) + col;
+__device__ __forceinline__ void load_bias32(const void* bias, int col, int limit, float* b) {
+    const uint16_t* ptr = reinterpret_cast<const uint16_t*>(bias) + col;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < 4; ++g) {
         if (col + 8 * g < limit) {
-            uint4 w = __ldg(reinterpret_cast<const uint4*>(p + 8 * g));
+            uint4 w = __ldg(reinterpret_cast<const uint4*>(ptr + 8 * g));
             unpack8<DT>(w, b + 8 * g);
         } else {
 #pragma unroll
@@ -286,23 +374,29 @@ __device__ __forceinline__ void load_bias16(const void* bias, int col, int limit
     }
 }
 
-// Round 16 values to the I/O dtype and store them at out[m][col..col+15]; groups
-// of 8 columns at or past N are dropped (N is a multiple of 8), rows >= M too.
+// Round a warp's 32 x 32 block (this lane's row, 32 columns in v) to the I/O dtype,
+// stage it in the warp's 2 KB shared-memory buffer in the 64-byte swizzled layout
+// the output tensor map expects (16-byte chunk c of row r lands at chunk
+// c ^ ((r >> 1) & 3)), and store it with one TMA tensor store at (x, y).  Rows and
+// columns past the tensor's bounds are clipped by the TMA unit.
 template <int DT>
-__device__ __forceinline__ void store16(void* out, int ldo, int m, int M, int col, int N,
-                                        const float* v) {
-    if (m >= M) return;
-    uint16_t* p = reinterpret_cast<uint16_t*>(out) + (size_t)m * (size_t)ldo + col;
+__device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t stg, int lane, const float* v,
+                                                int x, int y) {
+    if (lane == 0) bulk_wait_read0();  // the previous store from this buffer has read it
+    __syncwarp();
+    const uint32_t row_base = stg + (uint32_t)lane * 64u;
+    const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        if (col + 8 * g < N) {
-            uint4 w;
-            w.x = pack2<DT>(v[8 * g + 0], v[8 * g + 1]);
-            w.y = pack2<DT>(v[8 * g + 2], v[8 * g + 3]);
-            w.z = pack2<DT>(v[8 * g + 4], v[8 * g + 5]);
-            w.w = pack2<DT>(v[8 * g + 6], v[8 * g + 7]);
-            *reinterpret_cast<uint4*>(p + 8 * g) = w;
-        }
+    for (int c = 0; c < 4; ++c) {
+        st_shared_v4(row_base + ((c ^ sw) << 4), pack2<DT>(v[8 * c + 0], v[8 * c + 1]),
+                     pack2<DT>(v[8 * c + 2], v[8 * c + 3]), pack2<DT>(v[8 * c + 4], v[8 * c + 5]),
+                     pack2<DT>(v[8 * c + 6], v[8 * c + 7]));
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmC, stg, x, y);
+        bulk_commit();
     }
 }
 
@@ -327,20 +421,21 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
 template <int EPI, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles want 1024-byte alignment
     uint8_t* base_ptr = smem_raw + (base - raw);
 
     const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
-    const uint32_t bar_full = base + tiles_bytes;
+    const uint32_t staging = base + tiles_bytes;  // kEpiWarps x 2 KB output staging buffers
+    const uint32_t bar_full = staging + (uint32_t)kStagingBytes;
     const uint32_t bar_empty = bar_full + 8u * kMaxStages;
     const uint32_t bar_accf = bar_empty + 8u * kMaxStages;
     const uint32_t bar_acce = bar_accf + 16u;
     const uint32_t bar_stall = bar_acce + 16u;
     const uint32_t bar_drain = bar_stall + 8u;
-    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + 8u * (2 * kMaxStages + 6));
+    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 6));
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
@@ -369,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
@@ -504,9 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - 2;
         const int q = warp & 3;    // TMEM lane quadrant this warp may access
-        const int half = ew >> 2;  // interleaved half of the 16-column chunks
+        const int half = ew >> 2;  // which of the interleaved 32-column groups
         const int row = q * 32 + lane;
-        const int nchunks16 = p.BN / 16;
+        const int ngroups = p.BN / 32;
+        const uint32_t stg = staging + (uint32_t)ew * 2048u;
+        const int tiles_mn = p.tiles_m * p.tiles_n;
+        const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
         int local = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
             const TileCoord c = decode_tile(t, p);
@@ -516,52 +615,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             if (!epi_all(got)) break;
             tc_fence_after();
-            if (tr && local == 0 && warp == 2 && lane == 0) trace_mark(tr, TR_EPI_START);
-            const int m = c.tm * kBM + row;
+            const bool tr0 = tr && local == 0 && warp == 2 && lane == 0;
+            if (tr0) trace_mark(tr, TR_EPI_START);
+            const int m0 = c.tm * kBM;
+            const int y0 = m0 + q * 32;              // first row of this warp's block
+            const bool rows_live = y0 < p.M;         // warp-uniform
             const int n0 = c.tn * p.BN;
             const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)kAccSlot;
 
             if (EPI != EPI_DOWN || p.split_k == 1) {
-                for (int j = half; j < nchunks16; j += 2) {
-                    const int col = n0 + 16 * j;
-                    uint32_t r[16];
-                    tmem_ld16(tq + 16u * j, r);
+                for (int g = half; g < ngroups; g += 2) {
+                    const int col = n0 + 32 * g;
+                    const bool mark = tr0 && g == half;
+                    uint32_t r[32];
+                    tmem_ld32(tq + 32u * g, r);
+                    float v[32];
                     if constexpr (EPI == EPI_GEGLU) {
-                        uint32_t g[16];
-                        tmem_ld16(tq + p.gate_acc_off + 16u * j, g);
-                        tmem_wait_ld2(r, g);
-                        if (col < p.N) {
-                            float bv[16], bg[16], v[16];
+                        uint32_t gr[32];
+                        tmem_ld32(tq + p.gate_acc_off + 32u * g, gr);
+                        tmem_wait_ld_only();
+                        reg_fence32(r);
+                        reg_fence32(gr);
+                        if (mark) trace_mark(tr, TR_EPI_LD);
+                        if (col < p.N && rows_live) {
+                            float bv[32], bg[32];
                             if (p.bias) {
-                                load_bias16<DT>(p.bias, col, p.N, bv);
-                                load_bias16<DT>(p.bias, p.gate_col + col, p.gate_col + p.N, bg);
+                                load_bias32<DT>(p.bias, col, p.N, bv);
+                                load_bias32<DT>(p.bias, p.gate_col + col, p.gate_col + p.N, bg);
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) bv[i] = bg[i] = 0.0f;
+                                for (int i = 0; i < 32; ++i) bv[i] = bg[i] = 0.0f;
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(g[i]) + bg[i]);
-                            store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(gr[i]) + bg[i]);
+                            if (mark) trace_mark(tr, TR_EPI_MATH);
+                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                            if (mark) trace_mark(tr, TR_EPI_STORE);
                         }
                     } else {
-                        tmem_wait_ld(r);
-                        if (col < p.N) {
-                            float b[16], v[16];
+                        tmem_wait_ld_only();
+                        reg_fence32(r);
+                        if (mark) trace_mark(tr, TR_EPI_LD);
+                        if (col < p.N && rows_live) {
+                            float b[32];
                             if (p.bias) {
-                                load_bias16<DT>(p.bias, col, p.N, b);
+                                load_bias32<DT>(p.bias, col, p.N, b);
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) b[i] = 0.0f;
+                                for (int i = 0; i < 32; ++i) b[i] = 0.0f;
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
+                            for (int i = 0; i < 32; ++i) {
                                 const float z = __uint_as_float(r[i]) + b[i];
                                 if (EPI == EPI_GELU_ERF) v[i] = gelu_erf_f(z);
                                 else if (EPI == EPI_GELU_TANH) v[i] = gelu_tanh_f(z);
                                 else v[i] = z;
                             }
-                            store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                            if (mark) trace_mark(tr, TR_EPI_MATH);
+                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                            if (mark) trace_mark(tr, TR_EPI_STORE);
                         }
                     }
                 }
@@ -569,18 +682,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
             } else {
-                // split-K: fp32 partial of this split, then the last CTA on the tile reduces
-                const size_t Mp = (size_t)p.tiles_m * kBM, Np = (size_t)p.tiles_n * p.BN;
-                float* part = p.partials + ((size_t)c.split * Mp + (size_t)m) * Np + (size_t)n0;
-                for (int j = half; j < nchunks16; j += 2) {
-                    uint32_t r[16];
-                    tmem_ld16(tq + 16u * j, r);
-                    tmem_wait_ld(r);
-                    float4* dst = reinterpret_cast<float4*>(part + 16 * j);
+                // split-K: this split's fp32 partial in a private layout in which a warp
+                // writes (and later reads) 2 KB contiguous: [16-column chunk][row][16]
+                float* part = p.partials + ((size_t)c.split * tiles_mn + (size_t)c.mn) * tile_elems;
+                for (int g = half; g < ngroups; g += 2) {
+                    uint32_t r[32];
+                    tmem_ld32(tq + 32u * g, r);
+                    tmem_wait_ld_only();
+                    reg_fence32(r);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    for (int h = 0; h < 2; ++h) {
+                        float4* dst = reinterpret_cast<float4*>(part + ((size_t)(2 * g + h) * kBM + row) * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(__uint_as_float(r[16 * h + 4 * i]), __uint_as_float(r[16 * h + 4 * i + 1]),
+                                                 __uint_as_float(r[16 * h + 4 * i + 2]),
+                                                 __uint_as_float(r[16 * h + 4 * i + 3]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -596,31 +714,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epi_bar_sync();
                 if (*last_flag) {
                     __threadfence();
-                    const float* base_p = p.partials + (size_t)m * Np + (size_t)n0;
-                    for (int j = half; j < nchunks16; j += 2) {
-                        const int col = n0 + 16 * j;
-                        if (col >= p.N) continue;
-                        float v[16];
+                    for (int g = half; g < ngroups; g += 2) {
+                        const int col = n0 + 32 * g;
+                        if (col >= p.N || !rows_live) continue;  // warp-uniform
+                        float v[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-                        for (int s = 0; s < p.split_k; ++s) {  // fixed split order: deterministic
-                            const float4* src = reinterpret_cast<const float4*>(base_p + (size_t)s * Mp * Np + 16 * j);
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        for (int sp = 0; sp < p.split_k; ++sp) {  // fixed split order: deterministic
+                            const float* src_tile = p.partials + ((size_t)sp * tiles_mn + (size_t)c.mn) * tile_elems;
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float4 x = __ldcg(src + i);
-                                v[4 * i] += x.x;
-                                v[4 * i + 1] += x.y;
-                                v[4 * i + 2] += x.z;
-                                v[4 * i + 3] += x.w;
+                            for (int h = 0; h < 2; ++h) {
+                                const float4* src =
+                                    reinterpret_cast<const float4*>(src_tile + ((size_t)(2 * g + h) * kBM + row) * 16);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 x = __ldcg(src + i);
+                                    v[16 * h + 4 * i] += x.x;
+                                    v[16 * h + 4 * i + 1] += x.y;
+                                    v[16 * h + 4 * i + 2] += x.z;
+                                    v[16 * h + 4 * i + 3] += x.w;
+                                }
                             }
                         }
                         if (p.bias) {
-                            float b[16];
-                            load_bias16<DT>(p.bias, col, p.N, b);
+                            float b[32];
+                            load_bias32<DT>(p.bias, col, p.N, b);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] += b[i];
+                            for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
-                        store16<DT>(p.out, p.ldo, m, p.M, col, p.N, v);
+                        stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
                     }
                 }
                 epi_bar_sync();  // last_flag is rewritten for the next tile
@@ -630,6 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 trace_mark(tr, TR_LAST_EPI);
             }
         }
+        // every TMA store of this warp has completed before the CTA may exit
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
+        if (tr && warp == 2 && lane == 0) trace_mark(tr, TR_EPI_DRAIN);
     }
 
     // ------------------------------ teardown ------------------------------
@@ -647,6 +773,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 __global__ void kt_timestamp_kernel(unsigned long long* dst) { *dst = global_ns(); }
+
+// Elementwise evaluation of the epilogue's fp32 activations (test hook).
+__global__ void kt_activation_kernel(int act, const float* __restrict__ z, const float* __restrict__ g,
+                                     float* __restrict__ out, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float x = z[i];
+        float y;
+        if (act == KT_ACT_GELU_ERF) y = gelu_erf_f(x);
+        else if (act == KT_ACT_GELU_TANH) y = gelu_tanh_f(x);
+        else if (act == KT_ACT_GEGLU) y = x * gelu_erf_f(g[i]);
+        else y = x;
+        out[i] = y;
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -681,8 +821,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int EPI, int DT>
-kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p, int grid,
-                     int smem, void* stream, bool pdl, const char** why) {
+kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmParams& p,
+                     int grid, int smem, void* stream, bool pdl, const char** why) {
     auto kern = kt_gemm_kernel<EPI, DT>;
     // opt in to the shared memory this launch needs (idempotent, cheap after the first call)
     static std::atomic<int> max_set[16];
@@ -706,7 +846,7 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pdl ? attr : nullptr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return KT_ERR_CUDA;
@@ -726,8 +866,21 @@ kt_status launch_timestamp(void* dst, void* stream, const char** why) {
     return KT_OK;
 }
 
+kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
+                            const char** why) {
+    const int64_t blocks = n == 0 ? 0 : std::min<int64_t>((n + 255) / 256, 4096);
+    if (blocks > 0)
+        kt_activation_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(act, z, g, out, n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    return KT_OK;
+}
+
 bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows, uint32_t box_cols, const char** why) {
+                 uint32_t box_rows, uint32_t box_cols, int swizzle_bytes, const char** why) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) {
         *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -740,7 +893,8 @@ bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint
     CUresult r = fn(reinterpret_cast<CUtensorMap*>(tmap128),
                     dtype == KT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *why = "cuTensorMapEncodeTiled rejected the tensor (alignment, stride or box)";
@@ -749,11 +903,12 @@ bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint
     return true;
 }
 
-kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const GemmParams& p, int grid,
-                      int smem_bytes, void* stream, bool pdl, const char** why) {
+kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const void* tmC, const GemmParams& p,
+                      int grid, int smem_bytes, void* stream, bool pdl, const char** why) {
     const CUtensorMap* a = reinterpret_cast<const CUtensorMap*>(tmA);
     const CUtensorMap* b = reinterpret_cast<const CUtensorMap*>(tmB);
-#define KT_LAUNCH(E, D) return launch_one<E, D>(a, b, p, grid, smem_bytes, stream, pdl, why)
+    const CUtensorMap* c = reinterpret_cast<const CUtensorMap*>(tmC);
+#define KT_LAUNCH(E, D) return launch_one<E, D>(a, b, c, p, grid, smem_bytes, stream, pdl, why)
     if (dtype == KT_F16) {
         switch (epi) {
             case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_F16);

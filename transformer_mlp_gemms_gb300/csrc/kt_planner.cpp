@@ -7,7 +7,8 @@
 // 6 of the same page: the choice is analytic -- no autotuning; measurements are
 // the second opinion.  The KohakuTPU residency limits are replaced by the
 // sm_103a ones: TMEM columns per accumulator (<= 256 per buffer), shared memory
-// per CTA (227 KB), tcgen05 N a multiple of 16 up to 256, one CTA per SM.
+// per CTA (227 KB), tcgen05 N a multiple of 16 up to 256 (here of 32: the epilogue
+// stores whole 32 x 32 boxes), one CTA per SM.
 //
 // Model, per candidate (BN, SK):
 //   tiles   = ceil(M/128) * ceil(N/BN) * SK,  waves = ceil(tiles / SMs)
@@ -101,7 +102,7 @@ bool better(const GemmConfig& a, const GemmConfig& b) {
 bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int num_sms,
             GemmConfig* best) {
     bool found = false;
-    for (int BN = 16; BN <= 256; BN += 16) {
+    for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
         for (int SK = 1; SK <= max_sk; ++SK) {
             GemmConfig g;
             if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, &g)) continue;

@@ -76,6 +76,7 @@ SIGNATURES = {
     "kt_mlp_debug_stall": ([_VP, _I32, _I64], _I32),
     "kt_mlp_debug_trace": ([_VP, _VP, _VP], _I32),
     "kt_debug_timestamp": ([_VP, _VP], _I32),
+    "kt_debug_activation": ([_I32, _VP, _VP, _VP, _I64, _VP], _I32),
     "kt_last_error": ([], ctypes.c_char_p),
     "kt_mlp_abi_version": ([], _I32),
 }
@@ -195,6 +196,11 @@ def kt_mlp_debug_stall(plan: int, enable: bool, limit_us: int = 0) -> None:
 
 def kt_mlp_debug_trace(plan: int, trace_up=None, trace_down=None) -> None:
     _check(load().kt_mlp_debug_trace(plan, _ptr(trace_up), _ptr(trace_down)), "kt_mlp_debug_trace")
+
+
+def kt_debug_activation(act: int, z, gate, out, n: int, stream=None) -> None:
+    _check(load().kt_debug_activation(act, _ptr(z), _ptr(gate), _ptr(out), n, _stream(stream)),
+           "kt_debug_activation")
 
 
 def kt_debug_timestamp(dst, stream=None) -> None:
