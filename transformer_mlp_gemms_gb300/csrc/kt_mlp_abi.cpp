@@ -173,12 +173,12 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
     kt::GemmParams up = make_params(P, P->choice.up, epi_up);
     up.bias = P->bias ? b_up : nullptr;
     up.inject_stall = P->inject_stall;
-    up.pdl_wait = 0;
+    up.pdl_wait = 1;
     up.trace = P->trace_up;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (timed) cudaEventRecord(P->ev[0], st);
     kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
-                                  P->choice.up.smem_bytes, stream, false, &why);
+                                  P->choice.up.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
 
     kt::GemmParams dn = make_params(P, P->choice.down, kt::EPI_DOWN);

@@ -473,10 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
 
-    if constexpr (EPI != EPI_DOWN) {
-        // let the dependent down projection get its CTAs resident as SMs free up
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    }
+    // Programmatic dependent launch: let the next kernel in the stream get its CTAs
+    // resident (and through their set-up) as SMs free up; every kernel here waits for
+    // its predecessor's completion before its first global-memory access.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (p.pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
@@ -682,9 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
             } else {
-                // split-K: this split's fp32 partial in a private layout in which a warp
-                // writes (and later reads) 2 KB contiguous: [16-column chunk][row][16]
-                float* part = p.partials + ((size_t)c.split * tiles_mn + (size_t)c.mn) * tile_elems;
+                // split-K: this split's fp32 partial in a private layout in which every
+                // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]
+                float4* part = reinterpret_cast<float4*>(p.partials + ((size_t)c.split * tiles_mn + (size_t)c.mn) * tile_elems);
                 for (int g = half; g < ngroups; g += 2) {
                     uint32_t r[32];
                     tmem_ld32(tq + 32u * g, r);
@@ -692,10 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reg_fence32(r);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        float4* dst = reinterpret_cast<float4*>(part + ((size_t)(2 * g + h) * kBM + row) * 16);
+                        float4* dst = part + (size_t)(2 * g + h) * 4 * kBM + row;
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[16 * h + 4 * i]), __uint_as_float(r[16 * h + 4 * i + 1]),
+                            dst[i * kBM] = make_float4(__uint_as_float(r[16 * h + 4 * i]), __uint_as_float(r[16 * h + 4 * i + 1]),
                                                  __uint_as_float(r[16 * h + 4 * i + 2]),
                                                  __uint_as_float(r[16 * h + 4 * i + 3]));
                     }
@@ -703,36 +703,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
-                __threadfence();
+                // the barrier orders every epilogue thread's partial stores before the
+                // arrival thread's gpu-scope release (fences are cumulative)
                 epi_bar_sync();
                 if (ew == 0 && lane == 0) {
+                    __threadfence();
                     const int prev = atomicAdd(p.counters + c.mn, 1);
                     const int last = (prev == p.split_k - 1);
-                    if (last) atomicExch(p.counters + c.mn, 0);  // ready for the next run
+                    if (last) {
+                        atomicExch(p.counters + c.mn, 0);  // ready for the next run
+                        __threadfence();                   // acquire the other splits' partials
+                    }
                     *last_flag = last;
                 }
                 epi_bar_sync();
                 if (*last_flag) {
-                    __threadfence();
                     for (int g = half; g < ngroups; g += 2) {
                         const int col = n0 + 32 * g;
                         if (col >= p.N || !rows_live) continue;  // warp-uniform
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                        for (int sp = 0; sp < p.split_k; ++sp) {  // fixed split order: deterministic
-                            const float* src_tile = p.partials + ((size_t)sp * tiles_mn + (size_t)c.mn) * tile_elems;
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const float4* src =
-                                    reinterpret_cast<const float4*>(src_tile + ((size_t)(2 * g + h) * kBM + row) * 16);
+                        for (int h = 0; h < 2; ++h) {
+                            // 16 columns of this row from every split: up to 4 splits' loads in
+                            // flight at once, summed in split order (deterministic)
+                            const size_t off = (size_t)(2 * g + h) * 4 * kBM + row;  // in float4
+                            for (int s0 = 0; s0 < p.split_k; s0 += 4) {
+                                float4 x[4][4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float4 x = __ldcg(src + i);
-                                    v[16 * h + 4 * i] += x.x;
-                                    v[16 * h + 4 * i + 1] += x.y;
-                                    v[16 * h + 4 * i + 2] += x.z;
-                                    v[16 * h + 4 * i + 3] += x.w;
+                                for (int j = 0; j < 4; ++j) {
+                                    if (s0 + j < p.split_k) {
+                                        const float4* src = reinterpret_cast<const float4*>(
+                                            p.partials + ((size_t)(s0 + j) * tiles_mn + (size_t)c.mn) * tile_elems) + off;
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) x[j][i] = __ldcg(src + i * kBM);
+                                    }
+                                }
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    if (s0 + j < p.split_k) {
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            v[16 * h + 4 * i] += x[j][i].x;
+                                            v[16 * h + 4 * i + 1] += x[j][i].y;
+                                            v[16 * h + 4 * i + 2] += x[j][i].z;
+                                            v[16 * h + 4 * i + 3] += x[j][i].w;
+                                        }
+                                    }
                                 }
                             }
                         }

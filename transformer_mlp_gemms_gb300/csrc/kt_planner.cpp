@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 
 #include "kt_internal.h"
 
@@ -144,6 +145,28 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down)) {
         *why = "no feasible tile for the down projection";
         return KT_ERR_UNSUPPORTED;
+    }
+    // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN" and
+    // KT_FORCE_DOWN="BN,SK".  An infeasible override is an error, never ignored.
+    if (const char* e = std::getenv("KT_FORCE_UP")) {
+        int bn = 0;
+        GemmConfig g;
+        if (std::sscanf(e, "%d", &bn) != 1 || bn % 32 != 0 || bn < 32 || bn > 256 ||
+            !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, &g)) {
+            *why = "KT_FORCE_UP must be a feasible N tile (a multiple of 32 in 32..256)";
+            return KT_ERR_INVALID;
+        }
+        out->up = g;
+    }
+    if (const char* e = std::getenv("KT_FORCE_DOWN")) {
+        int bn = 0, sk = 0;
+        GemmConfig g;
+        if (std::sscanf(e, "%d,%d", &bn, &sk) != 2 || bn % 32 != 0 || bn < 32 || bn > 256 || sk < 1 ||
+            sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, &g)) {
+            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK\" (BN a multiple of 32 in 32..256, no empty split)";
+            return KT_ERR_INVALID;
+        }
+        out->down = g;
     }
     return KT_OK;
 }
