@@ -210,6 +210,36 @@ kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, flo
  */
 kt_status kt_debug_timestamp(void* dst, void* stream);
 
+/*
+ * kt_down_proj_noalloc -- the down projection on its own, Y[M][D] = round(H[M][F] .
+ * W_down[F][D] (+ b_down[D])), fp32 accumulation, that allocates no device memory.
+ * The pages have no counterpart to this entry point; it exists for callers of the
+ * library that cannot allocate: for example a host framework's plugin hook that is
+ * handed only input / output pointers and a stream and must not allocate there, or
+ * a latency-critical serving loop that must never call cudaMalloc / cudaFree
+ * (cudaFree synchronises the whole device, cudaMalloc can block).
+ *   H, W_down, Y : device pointers (16-byte aligned, row-major, dtype); the caller
+ *                  owns them.  b_down: device pointer or NULL (no bias).
+ * It runs the same kernel, with the same tile plan, as the down projection of
+ * kt_mlp_run.  Instead of a plan's workspace, its split-K partials, tile counters and
+ * error word live in one static device array of 16 MiB that the library holds on
+ * every GPU that loads it, until the process exits.  A problem whose plan needs
+ * more scratch than that is rejected with KT_ERR_UNSUPPORTED and a message giving
+ * both sizes; nothing is launched.  Each call clears the counters and error word
+ * (cudaMemsetAsync on `stream`) before its kernel; otherwise the array keeps the
+ * last call's contents.  All calls on a device share the array, so calls that
+ * overlap on the GPU (on two streams, or from two host threads) race and give wrong
+ * results.  The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and the SM count; make that first
+ * call before any stream capture.  There is no status word to read afterwards: a
+ * device-side wait that runs out (never in normal operation) leaves Y incomplete.
+ * Errors: INVALID (NULL / misaligned pointer, bad size or dtype), UNSUPPORTED (not
+ * sm_103, D or F not a multiple of 8, scratch too small), CUDA (a runtime call or
+ * the launch failed).
+ */
+kt_status kt_down_proj_noalloc(int64_t M, int64_t F, int64_t D, kt_dtype dtype, const void* H,
+                               const void* W_down, const void* b_down, void* Y, void* stream);
+
 /* Thread-local message for the calling thread's last non-OK status ("" if none). */
 const char* kt_last_error(void);
 

@@ -112,6 +112,12 @@ enum TraceSlot : int {
     kTraceSlots = 16
 };
 
+// Allocation-free down projection (kt_mlp_kernels.cu): its split-K partials, tile
+// counters and error word live in a static device array of this many bytes.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const void* H, const void* W_down,
+                            const void* b_down, void* Y, void* stream, const char** why);
+
 // Elementwise activation test kernel (kt_mlp_kernels.cu).
 kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
                             const char** why);

@@ -407,6 +407,14 @@ kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, flo
     return ok();
 }
 
+kt_status kt_down_proj_noalloc(int64_t M, int64_t F, int64_t D, kt_dtype dtype, const void* H,
+                               const void* W_down, const void* b_down, void* Y, void* stream) {
+    const char* why = "";
+    kt_status s = kt::noalloc_down_proj(M, F, D, dtype, H, W_down, b_down, Y, stream, &why);
+    if (s != KT_OK) return fail(s, why);
+    return ok();
+}
+
 kt_status kt_debug_timestamp(void* dst, void* stream) {
     if (!dst || (reinterpret_cast<uintptr_t>(dst) & 7u)) return fail(KT_ERR_INVALID, "dst must be an aligned device uint64");
     const char* why = "";

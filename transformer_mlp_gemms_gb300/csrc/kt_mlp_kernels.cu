@@ -41,6 +41,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "kt_internal.h"
@@ -873,6 +875,132 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Allocation-free down projection (kt_down_proj_noalloc)
+// ---------------------------------------------------------------------------
+// Scratch of the allocation-free entry point, laid out as [error word, padded to
+// 256 B][split-K tile counters, padded to 256 B][fp32 split-K partials].  It is
+// file-scope device memory: every GPU that loads this library holds these bytes
+// until the process exits.  Host code must not use the symbol itself (on the host it
+// is only a stand-in); it uses the device address cudaGetSymbolAddress returns.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned char* g_noalloc_ptr[kNoAllocMaxDevices] = {};  // device address of the scratch, per device
+int g_noalloc_sms[kNoAllocMaxDevices] = {};
+thread_local char g_noalloc_msg[192];
+}  // namespace
+
+kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const void* H, const void* W_down,
+                            const void* b_down, void* Y, void* stream, const char** why) {
+    if (M < 1 || F < 1 || D < 1) {
+        *why = "M, F and D must be positive";
+        return KT_ERR_INVALID;
+    }
+    if (dtype != KT_F16 && dtype != KT_BF16) {
+        *why = "unknown dtype";
+        return KT_ERR_INVALID;
+    }
+    auto misaligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+    if (!H || !W_down || !Y || misaligned(H) || misaligned(W_down) || misaligned(Y) || misaligned(b_down)) {
+        *why = "H, W_down and Y must be non-NULL, and all pointers 16-byte aligned";
+        return KT_ERR_INVALID;
+    }
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kNoAllocMaxDevices) {
+        *why = "device ordinal beyond the allocation-free entry point's table";
+        return KT_ERR_UNSUPPORTED;
+    }
+    unsigned char* scratch = nullptr;
+    int sms = 0;
+    {
+        // once per device, with that device current: its SM count and the device
+        // address of the static scratch
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_ptr[dev]) {
+            int major = 0, minor = 0, count = 0;
+            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+                *why = cudaGetErrorString(e);
+                return KT_ERR_CUDA;
+            }
+            if (major != 10 || minor != 3) {
+                *why = "this library is built for sm_103a (GB300)";
+                return KT_ERR_UNSUPPORTED;
+            }
+            void* addr = nullptr;
+            if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) != cudaSuccess || !addr) {
+                *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned NULL";
+                return KT_ERR_CUDA;
+            }
+            g_noalloc_sms[dev] = count;
+            g_noalloc_ptr[dev] = static_cast<unsigned char*>(addr);
+        }
+        scratch = g_noalloc_ptr[dev];
+        sms = g_noalloc_sms[dev];
+    }
+    // the same tile plan as the MLP's down projection
+    PlanChoice pc;
+    kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why);
+    if (st != KT_OK) return st;
+    const GemmConfig& g = pc.down;
+    const size_t n_counters = (size_t)g.tiles_m * (size_t)g.tiles_n;
+    const size_t counter_bytes = (n_counters * 4 + 255) / 256 * 256;
+    const size_t part_bytes =
+        g.split_k > 1 ? (size_t)g.split_k * g.tiles_m * kBM * (size_t)g.tiles_n * g.BN * sizeof(float) : 0;
+    const size_t need = 256 + counter_bytes + part_bytes;
+    if (need > kNoAllocScratchBytes) {
+        std::snprintf(g_noalloc_msg, sizeof(g_noalloc_msg),
+                      "this problem needs %zu bytes of scratch; the allocation-free entry point has %zu",
+                      need, (size_t)kNoAllocScratchBytes);
+        *why = g_noalloc_msg;
+        return KT_ERR_UNSUPPORTED;
+    }
+    // the error word and the tile counters must start at zero
+    if ((e = cudaMemsetAsync(scratch, 0, 256 + counter_bytes, static_cast<cudaStream_t>(stream))) != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    alignas(64) CUtensorMap tmA, tmB, tmC;
+    if (!encode_tmap(&tmA, H, dtype, M, F, kBM, kBK, 128, why) ||
+        !encode_tmap(&tmB, W_down, dtype, F, D, kBK, 64, 128, why) ||
+        !encode_tmap(&tmC, Y, dtype, M, D, 32, kStoreCols, 64, why))
+        return KT_ERR_CUDA;
+    GemmParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.M = (int)M;
+    q.N = (int)D;
+    q.K = (int)F;
+    q.BN = g.BN;
+    q.n_chunks = (g.BN + 63) / 64;
+    q.stages = g.stages;
+    q.split_k = g.split_k;
+    q.tiles_m = g.tiles_m;
+    q.tiles_n = g.tiles_n;
+    q.kblocks = g.kblocks;
+    q.kblocks_per_split = g.kblocks_per_split;
+    q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
+    q.idesc = make_idesc(dtype, g.BN);
+    q.a_bytes = kBM * kBK * 2;
+    q.b_bytes = (uint32_t)q.n_chunks * 64u * kBK * 2u;
+    q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1);
+    q.acc_bufs = 2u;
+    q.bias = b_down;
+    q.error = reinterpret_cast<int*>(scratch);
+    q.counters = reinterpret_cast<int*>(scratch + 256);
+    q.partials = reinterpret_cast<float*>(scratch + 256 + counter_bytes);
+    q.wait_limit_ns = 4000000000ull;
+    return launch_gemm(EPI_DOWN, dtype, &tmA, &tmB, &tmC, q, g.grid, g.smem_bytes, stream, false, why);
+}
 
 kt_status launch_timestamp(void* dst, void* stream, const char** why) {
     kt_timestamp_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<unsigned long long*>(dst));

@@ -77,6 +77,7 @@ SIGNATURES = {
     "kt_mlp_debug_trace": ([_VP, _VP, _VP], _I32),
     "kt_debug_timestamp": ([_VP, _VP], _I32),
     "kt_debug_activation": ([_I32, _VP, _VP, _VP, _I64, _VP], _I32),
+    "kt_down_proj_noalloc": ([_I64, _I64, _I64, _I32, _VP, _VP, _VP, _VP, _VP], _I32),
     "kt_last_error": ([], ctypes.c_char_p),
     "kt_mlp_abi_version": ([], _I32),
 }
@@ -201,6 +202,12 @@ def kt_mlp_debug_trace(plan: int, trace_up=None, trace_down=None) -> None:
 def kt_debug_activation(act: int, z, gate, out, n: int, stream=None) -> None:
     _check(load().kt_debug_activation(act, _ptr(z), _ptr(gate), _ptr(out), n, _stream(stream)),
            "kt_debug_activation")
+
+
+def kt_down_proj_noalloc(M: int, F: int, D: int, dtype: int, H, W_down, b_down, Y, stream=None) -> None:
+    """The down projection without any device allocation (static 16 MiB scratch per device)."""
+    _check(load().kt_down_proj_noalloc(M, F, D, dtype, _ptr(H), _ptr(W_down), _ptr(b_down), _ptr(Y),
+                                       _stream(stream)), "kt_down_proj_noalloc")
 
 
 def kt_debug_timestamp(dst, stream=None) -> None:
