@@ -79,17 +79,20 @@ def test_null_handles_are_rejected(lib):
 def _check_gemm(g, M, N, K):
     assert (g["M"], g["N"], g["K"]) == (M, N, K)
     BM, BN, BK, SK = g["BM"], g["BN"], g["BK"], g["split_k"]
-    assert BM == 128 and BK == 64
+    assert BM in (128, 256) and BK == 64  # 256: a CTA pair (cta_group::2) per tile
+    pair = BM // 128
     assert BN % 32 == 0 and 32 <= BN <= 256
+    assert BN % (32 * (BM // 128)) == 0
     # the grid covers every output element exactly once: tiles_m * BM >= M > (tiles_m - 1) * BM
     assert (g["tiles_m"] - 1) * BM < M <= g["tiles_m"] * BM
     assert (g["tiles_n"] - 1) * BN < N <= g["tiles_n"] * BN
     assert g["kblocks"] == -(-K // BK)
     kps = -(-g["kblocks"] // SK)
     assert (SK - 1) * kps < g["kblocks"]  # no empty split: every partial is real
-    tiles = g["tiles_m"] * g["tiles_n"] * SK
-    assert g["grid"] == min(tiles, SMS)
-    assert g["waves"] == -(-tiles // SMS)
+    ctas = g["tiles_m"] * g["tiles_n"] * SK * pair
+    slots = (SMS // pair) * pair
+    assert g["grid"] == min(ctas, slots) and g["grid"] % pair == 0
+    assert g["waves"] == -(-ctas // slots)
     assert 0 < g["useful_over_padded"] <= 1.0
     assert g["useful_over_padded"] == pytest.approx(
         M * N * K / ((g["tiles_m"] * BM) * (g["tiles_n"] * BN) * (g["kblocks"] * BK)))

@@ -49,6 +49,7 @@ struct GemmConfig {
     int waves;
     int smem_bytes;
     int n_b;               // B operand tiles per stage: 1, or 2 for GEGLU (value + gate)
+    int pair;              // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile (cta_group::2)
     double useful_over_padded;
     double est_us;
 };
@@ -57,9 +58,10 @@ struct PlanChoice {
     GemmConfig up, down;
 };
 
-// Bytes of one pipeline stage: A tile + n_b B tiles of ceil(BN/64) 64-column boxes.
-inline int stage_bytes(int BN, int n_b) {
-    int chunks = (BN + 63) / 64;
+// Bytes of one pipeline stage in one CTA: its 128-row A tile + n_b B tiles holding
+// its share of the columns (BN, or BN/2 in a CTA pair) in 64-column boxes.
+inline int stage_bytes(int BN, int n_b, int pair) {
+    int chunks = (BN / pair + 63) / 64;
     return kBM * kBK * 2 + n_b * chunks * 64 * kBK * 2;
 }
 
@@ -73,7 +75,8 @@ void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* out);
 // Launch parameters shared by host and device.
 struct GemmParams {
     int M, N, K;
-    int BN, n_chunks, stages, split_k;
+    int BN, n_chunks, stages, split_k;  // n_chunks: 64-column B boxes per CTA
+    int pair;                // 1 or 2 (CTA pair, tiles of 256 rows); tiles_m counts pair-tiles
     int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
     int gate_col;            // GEGLU: first gate column in W_up (= F); else 0
     uint32_t idesc;          // tcgen05 instruction descriptor
@@ -136,7 +139,7 @@ bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint
                  uint32_t box_rows, uint32_t box_cols, int swizzle_bytes, const char** why);
 
 // tcgen05 instruction descriptor for kind::f16 with fp32 accumulation, A K-major,
-// B MN-major, M = 128, N = n.
-uint32_t make_idesc(int dtype, int n);
+// B MN-major, M = m (128, or 256 for a CTA pair), N = n.
+uint32_t make_idesc(int dtype, int n, int m);
 
 }  // namespace kt

@@ -111,7 +111,8 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.N = (int)g.N;
     q.K = (int)g.K;
     q.BN = g.BN;
-    q.n_chunks = (g.BN + 63) / 64;
+    q.pair = g.pair;
+    q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.stages = g.stages;
     q.split_k = g.split_k;
     q.tiles_m = g.tiles_m;
@@ -120,10 +121,10 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.kblocks_per_split = g.kblocks_per_split;
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
-    q.idesc = kt::make_idesc(P->dtype, g.BN);
+    q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair);
     q.a_bytes = kt::kBM * kt::kBK * 2;
     q.b_bytes = (uint32_t)q.n_chunks * 64u * kt::kBK * 2u;
-    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b);
+    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair);
     q.acc_bufs = (epi == kt::EPI_GEGLU && g.BN > 128) ? 1u : 2u;
     q.gate_acc_off = epi == kt::EPI_GEGLU ? (g.BN <= 128 ? 128u : 256u) : 0u;
     q.error = P->flags;
@@ -219,9 +220,9 @@ kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype
     out->num_sms = num_sms;
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
-    int64_t ws = M * F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n) + 2 * 2 * M * D;
+    int64_t ws = M * F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * M * D;
     if (c.down.split_k > 1)
-        ws += (int64_t)c.down.split_k * c.down.tiles_m * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
+        ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
     out->workspace_bytes = ws;
     return ok();
 }
@@ -259,9 +260,10 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
     }
     const kt::GemmConfig& dn = P->choice.down;
     size_t h_bytes = (size_t)M * (size_t)F * 2;
-    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n;
+    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
     size_t flag_bytes = 4 * (1 + n_counters);
-    size_t part_bytes = dn.split_k > 1 ? (size_t)dn.split_k * dn.tiles_m * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4 : 0;
+    size_t part_bytes =
+        dn.split_k > 1 ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4 : 0;
     size_t io_bytes = (size_t)M * (size_t)D * 2;
     if ((e = cudaMalloc(&P->H, h_bytes)) != cudaSuccess ||
         (e = cudaMalloc(reinterpret_cast<void**>(&P->flags), flag_bytes)) != cudaSuccess ||
@@ -341,7 +343,7 @@ kt_status kt_mlp_status(kt_mlp_plan_t plan) {
     if (word != kt::DEV_OK) {
         // clear the word and the split-K counters an aborted run may have left behind
         const kt::GemmConfig& dn = plan->choice.down;
-        size_t flag_bytes = 4 * (1 + (size_t)dn.tiles_m * dn.tiles_n);
+        size_t flag_bytes = 4 * (1 + (size_t)dn.tiles_m * dn.tiles_n * dn.pair);
         cudaMemset(plan->flags, 0, flag_bytes);
         cudaDeviceSynchronize();
         const char* where = word == kt::DEV_TIMEOUT_PRODUCER ? "producer"
@@ -376,12 +378,12 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
     const kt::GemmConfig& u = plan->choice.up;
     const kt::GemmConfig& d = plan->choice.down;
     std::snprintf(buf, len,
-                  "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d sms=%d | up: 128x%d tiles %dx%d (grid %d, %d "
-                  "wave%s, %d stages, useful %.3f, model %.2f us) | down: 128x%d tiles %dx%d split_k %d (grid %d, "
+                  "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d sms=%d | up: %dx%d tiles %dx%d (grid %d, %d "
+                  "wave%s, %d stages, useful %.3f, model %.2f us) | down: %dx%d tiles %dx%d split_k %d (grid %d, "
                   "%d wave%s, %d stages, useful %.3f, model %.2f us) | workspace %lld B",
                   (long long)plan->M, (long long)plan->D, (long long)plan->F, act_name(plan->act),
-                  plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->num_sms, u.BN, u.tiles_m, u.tiles_n,
-                  u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, d.BN,
+                  plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->num_sms, kt::kBM * u.pair, u.BN, u.tiles_m, u.tiles_n,
+                  u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, kt::kBM * d.pair, d.BN,
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
     return ok();

@@ -146,16 +146,62 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Tensor-memory allocation.  With PAIR = 2 (cta_group::2) one warp of each CTA of the
+// pair performs the allocation collectively; the same columns are allocated in both.
+template <int PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR == 2) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
 }
 
+template <int PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (PAIR == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster shared window, of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its cluster-window address (possibly in the peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int x,
+                                                 int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading-dimension and
@@ -179,6 +225,27 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// M = 256 across the CTA pair: this CTA's smem holds A rows [0,128) and B columns
+// [0, N/2) of its half; the peer's the other halves (same offsets).
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at this offset in both CTAs of the pair once all prior MMAs finish.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"((unsigned short)3)
+        : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns; thread i gets lane (base + i).
@@ -420,7 +487,12 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     return c;
 }
 
-template <int EPI, int DT>
+// PAIR = 1: one CTA per 128 x BN tile (cta_group::1).  PAIR = 2: a cluster pair per
+// 256 x BN tile (cta_group::2): each CTA loads its 128 rows of A and half of the B
+// columns; the even CTA (the leader) issues the MMAs, which write each CTA's 128
+// rows of the accumulator into that CTA's tensor memory; each CTA's epilogue stores
+// its own rows.
+template <int EPI, int DT, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
@@ -446,6 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     unsigned long long* const tr = p.trace;
     if (threadIdx.x == 0) trace_mark(tr, TR_ENTRY);
+    const uint32_t rank = PAIR == 2 ? (cluster_ctarank() & 1u) : 0u;  // position in the CTA pair
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / PAIR;        // first tile of this CTA (or pair)
+    const int unit_step = (int)gridDim.x / PAIR;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -454,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accf + 8u * b, 1);
-            mbar_init(bar_acce + 8u * b, kEpiWarps);
+            mbar_init(bar_acce + 8u * b, kEpiWarps * PAIR);  // both CTAs' epilogues (leader's copy)
         }
         mbar_init(bar_stall, 1);
         mbar_init(bar_drain, 1);
@@ -468,9 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR == 2) cluster_sync_all();  // peers' barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
@@ -492,15 +569,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // failure injection: a barrier nobody arrives on, bounded wait
                 wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
             }
-            for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+            for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step) {
                 const TileCoord c = decode_tile(t, p);
                 const int kb0 = c.split * p.kblocks_per_split;
                 const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
-                const int n0 = c.tn * p.BN;
-                int chunks = 0;  // 64-column boxes of this tile inside [0, N)
-                for (int ch = 0; ch < p.n_chunks; ++ch)
-                    if (n0 + 64 * ch < p.N) chunks = ch + 1;
-                const uint32_t tx = p.a_bytes + (uint32_t)(n_b * chunks) * 8192u;
+                // this CTA's rows of A and its share of the B columns
+                const int bcols = p.BN / PAIR;
+                auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
+                    m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
+                    nb_r = c.tn * p.BN + (int)r * bcols;
+                    chunks_r = 0;  // 64-column boxes of the share that start inside [0, N)
+                    for (int ch = 0; ch * 64 < bcols; ++ch)
+                        if (nb_r + 64 * ch < p.N) chunks_r = ch + 1;
+                    // boxes entirely past the tensor are not loaded: they would only feed
+                    // accumulator rows / columns that are never stored
+                    return (m_r < p.M ? p.a_bytes : 0u) + (uint32_t)(n_b * chunks_r) * 8192u;
+                };
+                int m_me, nb_me, chunks;
+                uint32_t tx = cta_share(rank, m_me, nb_me, chunks);
+                if (PAIR == 2) {  // the leader's full barrier counts the bytes of both CTAs
+                    int m_o, nb_o, ch_o;
+                    tx += cta_share(rank ^ 1u, m_o, nb_o, ch_o);
+                }
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.error,
@@ -511,15 +601,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = bar_full + 8u * stage;
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
-                    mbar_arrive_expect_tx(fb, tx);
                     if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
-                    tma_load_2d(sA, &tmA, fb, kb * kBK, c.tm * kBM);
-                    for (int ch = 0; ch < chunks; ++ch)
-                        tma_load_2d(sB + 8192u * ch, &tmB, fb, n0 + 64 * ch, kb * kBK);
-                    if (EPI == EPI_GEGLU) {
+                    if constexpr (PAIR == 2) {
+                        const uint32_t fb_leader = mapa_rank(fb, 0);
+                        if (leader) mbar_arrive_expect_tx(fb, tx);
+                        if (m_me < p.M) tma_load_2d_pair(sA, &tmA, fb_leader, kb * kBK, m_me);
                         for (int ch = 0; ch < chunks; ++ch)
-                            tma_load_2d(sB + p.b_bytes + 8192u * ch, &tmB, fb, p.gate_col + n0 + 64 * ch,
-                                        kb * kBK);
+                            tma_load_2d_pair(sB + 8192u * ch, &tmB, fb_leader, nb_me + 64 * ch, kb * kBK);
+                        if (EPI == EPI_GEGLU) {
+                            for (int ch = 0; ch < chunks; ++ch)
+                                tma_load_2d_pair(sB + p.b_bytes + 8192u * ch, &tmB, fb_leader,
+                                                 p.gate_col + nb_me + 64 * ch, kb * kBK);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(fb, tx);
+                        if (m_me < p.M) tma_load_2d(sA, &tmA, fb, kb * kBK, m_me);
+                        for (int ch = 0; ch < chunks; ++ch)
+                            tma_load_2d(sB + 8192u * ch, &tmB, fb, nb_me + 64 * ch, kb * kBK);
+                        if (EPI == EPI_GEGLU) {
+                            for (int ch = 0; ch < chunks; ++ch)
+                                tma_load_2d(sB + p.b_bytes + 8192u * ch, &tmB, fb, p.gate_col + nb_me + 64 * ch,
+                                            kb * kBK);
+                        }
                     }
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -530,19 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
             }
-            if (*abort_flag) {
+            if (*abort_flag && leader) {
                 // do not leave copies in flight into shared memory we are about to release
+                // (the leader's full barriers count the peer's copies too)
                 for (int s = 0; s < p.stages; ++s)
                     if (armed & (1u << s)) wait_drain(bar_full + 8u * s, (armed_phase >> s) & 1u, 100000000ull);
             }
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ----------------------------
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool issued_any = false;
-            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+            for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
                 const TileCoord c = decode_tile(t, p);
                 const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
                 const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
@@ -572,21 +676,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // (SBO), +2 KB per 16-row K step.
                         const uint64_t bd = smem_desc(sB + 2048u * k, 8192u, 1024u);
                         const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                        mma_f16(d, ad, bd, p.idesc, acc);
+                        if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, p.idesc, acc);
+                        else mma_f16(d, ad, bd, p.idesc, acc);
                         if (EPI == EPI_GEGLU) {
                             const uint64_t gd = smem_desc(sB + p.b_bytes + 2048u * k, 8192u, 1024u);
-                            mma_f16(d + p.gate_acc_off, ad, gd, p.idesc, acc);
+                            if constexpr (PAIR == 2) mma_f16_pair(d + p.gate_acc_off, ad, gd, p.idesc, acc);
+                            else mma_f16(d + p.gate_acc_off, ad, gd, p.idesc, acc);
                         }
                     }
                     issued_any = true;
-                    mma_commit(bar_empty + 8u * stage);  // stage free once these MMAs completed
+                    // stage free (in both CTAs of a pair) once these MMAs completed
+                    if constexpr (PAIR == 2) mma_commit_pair(bar_empty + 8u * stage);
+                    else mma_commit(bar_empty + 8u * stage);
                     if (++stage == (uint32_t)p.stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar_accf + 8u * buf);  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue (of both CTAs of a pair)
+                if constexpr (PAIR == 2) mma_commit_pair(bar_accf + 8u * buf);
+                else mma_commit(bar_accf + 8u * buf);
                 if (tr) {
                     if (local == 0) trace_mark(tr, TR_MAIN_DONE);
                     trace_mark(tr, TR_LAST_MAIN);
@@ -594,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (*abort_flag && issued_any) {
-                mma_commit(bar_drain);
+                if constexpr (PAIR == 2) mma_commit_pair(bar_drain);
+                else mma_commit(bar_drain);
                 wait_drain(bar_drain, 0u, 100000000ull);
             }
         }
@@ -609,17 +720,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tiles_mn = p.tiles_m * p.tiles_n;
         const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
         int local = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+        for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
             const TileCoord c = decode_tile(t, p);
             const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
             const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
+            // the accumulator-empty barrier lives in the leader CTA
+            const uint32_t acce = PAIR == 2 ? mapa_rank(bar_acce + 8u * buf, 0) : bar_acce + 8u * buf;
             const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             if (!epi_all(got)) break;
             tc_fence_after();
             const bool tr0 = tr && local == 0 && warp == 2 && lane == 0;
             if (tr0) trace_mark(tr, TR_EPI_START);
-            const int m0 = c.tm * kBM;
+            const int m0 = c.tm * (kBM * PAIR) + (int)rank * kBM;  // this CTA's first row
             const int y0 = m0 + q * 32;              // first row of this warp's block
             const bool rows_live = y0 < p.M;         // warp-uniform
             const int n0 = c.tn * p.BN;
@@ -682,11 +795,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
+                if (lane == 0) {
+                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
+                    else mbar_arrive(acce);
+                }
             } else {
                 // split-K: this split's fp32 partial in a private layout in which every
                 // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]
-                float4* part = reinterpret_cast<float4*>(p.partials + ((size_t)c.split * tiles_mn + (size_t)c.mn) * tile_elems);
+                const size_t half_tile = (size_t)c.mn * PAIR + rank;  // this CTA's 128-row half of the tile
+                float4* part = reinterpret_cast<float4*>(
+                    p.partials + (((size_t)c.split * tiles_mn) * PAIR + half_tile) * tile_elems);
                 for (int g = half; g < ngroups; g += 2) {
                     uint32_t r[32];
                     tmem_ld32(tq + 32u * g, r);
@@ -704,16 +822,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acce + 8u * buf);
+                if (lane == 0) {
+                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
+                    else mbar_arrive(acce);
+                }
                 // the barrier orders every epilogue thread's partial stores before the
                 // arrival thread's gpu-scope release (fences are cumulative)
                 epi_bar_sync();
                 if (ew == 0 && lane == 0) {
                     __threadfence();
-                    const int prev = atomicAdd(p.counters + c.mn, 1);
+                    const int prev = atomicAdd(p.counters + half_tile, 1);
                     const int last = (prev == p.split_k - 1);
                     if (last) {
-                        atomicExch(p.counters + c.mn, 0);  // ready for the next run
+                        atomicExch(p.counters + half_tile, 0);  // ready for the next run
                         __threadfence();                   // acquire the other splits' partials
                     }
                     *last_flag = last;
@@ -737,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 4; ++j) {
                                     if (s0 + j < p.split_k) {
                                         const float4* src = reinterpret_cast<const float4*>(
-                                            p.partials + ((size_t)(s0 + j) * tiles_mn + (size_t)c.mn) * tile_elems) + off;
+                                            p.partials + (((size_t)(s0 + j) * tiles_mn) * PAIR + half_tile) * tile_elems) + off;
 #pragma unroll
                                         for (int i = 0; i < 4; ++i) x[j][i] = __ldcg(src + i * kBM);
                                     }
@@ -781,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ teardown ------------------------------
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR == 2) cluster_sync_all();  // no CTA leaves while its peer may still signal it
     if (threadIdx.x == 0 && tr) {
         trace_mark(tr, TR_EXIT);
         tr[(size_t)blockIdx.x * kTraceSlots + TR_SMID] = sm_id();
@@ -788,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc<PAIR>(tmem_base, kTmemCols);
     }
 }
 
@@ -812,7 +934,7 @@ __global__ void kt_activation_kernel(int act, const float* __restrict__ z, const
 // Host side
 // ---------------------------------------------------------------------------
 
-uint32_t make_idesc(int dtype, int n) {
+uint32_t make_idesc(int dtype, int n, int m) {
     uint32_t d = 0;
     d |= 1u << 4;                                   // D (accumulator) format: f32
     d |= (dtype == KT_BF16 ? 1u : 0u) << 7;         // A format: f16 = 0, bf16 = 1
@@ -820,7 +942,7 @@ uint32_t make_idesc(int dtype, int n) {
     /* bit 15 = 0: A is K-major */
     d |= 1u << 16;                                  // B is MN-major
     d |= (uint32_t)(n >> 3) << 17;                  // N >> 3
-    d |= (uint32_t)(kBM >> 4) << 24;                // M >> 4
+    d |= (uint32_t)(m >> 4) << 24;                  // M >> 4 (256 for a CTA pair)
     return d;
 }
 
@@ -840,10 +962,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int EPI, int DT>
+template <int EPI, int DT, int PAIR>
 kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmParams& p,
                      int grid, int smem, void* stream, bool pdl, const char** why) {
-    auto kern = kt_gemm_kernel<EPI, DT>;
+    auto kern = kt_gemm_kernel<EPI, DT, PAIR>;
     // opt in to the shared memory this launch needs (idempotent, cheap after the first call)
     static std::atomic<int> max_set[16];
     int dev = 0;
@@ -861,11 +983,22 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? attr : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (PAIR == 2) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
@@ -953,10 +1086,10 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why);
     if (st != KT_OK) return st;
     const GemmConfig& g = pc.down;
-    const size_t n_counters = (size_t)g.tiles_m * (size_t)g.tiles_n;
+    const size_t n_counters = (size_t)g.tiles_m * (size_t)g.tiles_n * (size_t)g.pair;
     const size_t counter_bytes = (n_counters * 4 + 255) / 256 * 256;
     const size_t part_bytes =
-        g.split_k > 1 ? (size_t)g.split_k * g.tiles_m * kBM * (size_t)g.tiles_n * g.BN * sizeof(float) : 0;
+        g.split_k > 1 ? (size_t)g.split_k * g.tiles_m * g.pair * kBM * (size_t)g.tiles_n * g.BN * sizeof(float) : 0;
     const size_t need = 256 + counter_bytes + part_bytes;
     if (need > kNoAllocScratchBytes) {
         std::snprintf(g_noalloc_msg, sizeof(g_noalloc_msg),
@@ -989,10 +1122,12 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.kblocks = g.kblocks;
     q.kblocks_per_split = g.kblocks_per_split;
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
-    q.idesc = make_idesc(dtype, g.BN);
+    q.pair = g.pair;
+    q.n_chunks = (g.BN / g.pair + 63) / 64;
+    q.idesc = make_idesc(dtype, g.BN, kBM * g.pair);
     q.a_bytes = kBM * kBK * 2;
     q.b_bytes = (uint32_t)q.n_chunks * 64u * kBK * 2u;
-    q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1);
+    q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1, g.pair);
     q.acc_bufs = 2u;
     q.bias = b_down;
     q.error = reinterpret_cast<int*>(scratch);
@@ -1054,7 +1189,13 @@ kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, cons
     const CUtensorMap* a = reinterpret_cast<const CUtensorMap*>(tmA);
     const CUtensorMap* b = reinterpret_cast<const CUtensorMap*>(tmB);
     const CUtensorMap* c = reinterpret_cast<const CUtensorMap*>(tmC);
-#define KT_LAUNCH(E, D) return launch_one<E, D>(a, b, c, p, grid, smem_bytes, stream, pdl, why)
+    if (p.pair == 2 && (grid % 2) != 0) {
+        *why = "a CTA-pair launch needs an even grid";
+        return KT_ERR_INVALID;
+    }
+#define KT_LAUNCH(E, D)                                                                   \
+    return p.pair == 2 ? launch_one<E, D, 2>(a, b, c, p, grid, smem_bytes, stream, pdl, why) \
+                       : launch_one<E, D, 1>(a, b, c, p, grid, smem_bytes, stream, pdl, why)
     if (dtype == KT_F16) {
         switch (epi) {
             case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_F16);

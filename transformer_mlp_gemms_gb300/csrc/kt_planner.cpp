@@ -10,14 +10,13 @@
 // per CTA (227 KB), tcgen05 N a multiple of 16 up to 256 (here of 32: the epilogue
 // stores whole 32 x 32 boxes), one CTA per SM.
 //
-// Model, per candidate (BN, SK):
-//   tiles   = ceil(M/128) * ceil(N/BN) * SK,  waves = ceil(tiles / SMs)
-//   t_mma   = n_b * 2 * 128 * BN * 64 * kblocks_per_split / R_sm
-//   t_feed  = bytes staged per tile / per-SM share of the L2 feed
-//   t_main  = max(t_mma, t_feed) + t_fill
+// Model, per candidate (PAIR, BN, SK), PAIR = 2 being a CTA pair on a 256-row tile:
+//   tiles   = ceil(M/(128 PAIR)) * ceil(N/BN) * SK,  waves = ceil(PAIR tiles / SMs)
+//   per k-block and CTA: t_kb = max(MMA time of 128 x BN x 64, its stage bytes / its
+//                          share of the L2 feed, load latency / stages)
+//   t_main  = kblocks_per_split * t_kb + t_fill
 //   t_epi   = 128 * BN * c_epi          (per-element epilogue cost of the kind)
-//           + 2 * 128 * BN * 4 bytes / per-SM bandwidth   (SK > 1: write the fp32
-//             partial, and on average one more partial-sized pass for the reduction)
+//           + (SK > 1) the fp32 partial write and the last CTA's read of SK partials
 //   t_cta   = t_main + (waves-1) * max(t_main, t_epi) + t_epi   (two TMEM buffers)
 //           = waves * (t_main + t_epi)                           (one buffer)
 // and the candidate with the smallest t_cta wins; ties go to the larger
@@ -37,6 +36,9 @@ constexpr double kRsm = 2.25e15 / 152.0;  // dense 16-bit FLOP/s per SM (nominal
 constexpr double kL2Feed = 20e12;         // aggregate L2 -> SM bytes/s (model)
 constexpr double kSmFeedMax = 240e9;      // one SM's fill bandwidth (model)
 constexpr double kTFill = 0.35e-6;        // pipeline fill + drain latency per tile (model)
+// Load latency a stage ring must cover (model, calibrated on GB300: a 5-stage ring of
+// 40 KB stages ran 0.33 us per k-block against 0.19 us of MMA time).
+constexpr double kLoadLatency = 1.6e-6;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -50,31 +52,39 @@ double epi_cost_per_elem(int epi) {      // seconds per output element per SM (m
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int max_stages(int BN, int n_b) {
-    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b);
+int max_stages(int BN, int n_b, int pair) {
+    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair);
     return std::min(s, kMaxStages);
 }
 
-bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms,
+bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
               GemmConfig* g) {
-    int stages = max_stages(BN, n_b);
+    int stages = max_stages(BN, n_b, pair);
     if (stages < 2) return false;
-    int64_t tm = cdiv(M, kBM), tn = cdiv(N, BN), kb = cdiv(K, kBK);
+    if (pair == 2 && num_sms < 2) return false;
+    const int64_t bm = (int64_t)kBM * pair;  // rows per tile (a pair's tile spans two CTAs)
+    int64_t tm = cdiv(M, bm), tn = cdiv(N, BN), kb = cdiv(K, kBK);
     int64_t kps = cdiv(kb, SK);
     int64_t sk_eff = cdiv(kb, kps);  // no empty split
     if (sk_eff != SK) return false;
     int64_t tiles = tm * tn * SK;
-    if (tiles > (int64_t)1 << 30) return false;
-    int64_t grid = std::min<int64_t>(tiles, num_sms);
-    int64_t waves = cdiv(tiles, num_sms);
+    if (tiles > (int64_t)1 << 29) return false;
+    const int64_t slots = (num_sms / pair) * pair;  // CTAs resident at once (pairs need two SMs)
+    int64_t ctas = tiles * pair;
+    int64_t grid = std::min<int64_t>(ctas, slots);
+    int64_t waves = cdiv(ctas, slots);
 
-    double t_mma = n_b * 2.0 * kBM * BN * kBK * (double)kps / kRsm;
-    double bytes_tile = (double)kps * stage_bytes(BN, n_b);
+    // per CTA and k-block: the MMA time of its 128 rows, the time to stream its share of
+    // the operands, and the load latency the ring of `stages` k-blocks has to cover
+    double t_mma = n_b * 2.0 * kBM * BN * kBK / kRsm;
+    double bytes_kb = (double)stage_bytes(BN, n_b, pair);
     double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
-    double t_feed = bytes_tile / feed;
-    double t_main = std::max(t_mma, t_feed) + kTFill;
+    double t_kb = std::max(std::max(t_mma, bytes_kb / feed), kLoadLatency / stages);
+    double t_main = (double)kps * t_kb + kTFill;
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
-    if (SK > 1) t_epi += 2.0 * kBM * BN * 4.0 / kSmFeedMax;
+    // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
+    // all SK partials, both latency-bound at a few tens of GB/s per SM
+    if (SK > 1) t_epi += kBM * BN * 4.0 / 25e9 + SK * (kBM * BN * 4.0) / 60e9;
     bool two_bufs = !(n_b == 2 && BN > 128);
     double t_cta = two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
                             : waves * (t_main + t_epi);
@@ -84,10 +94,11 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->tiles_m = (int)tm; g->tiles_n = (int)tn; g->kblocks = (int)kb;
     g->kblocks_per_split = (int)kps;
     g->grid = (int)grid; g->waves = (int)waves;
-    g->smem_bytes = stages * stage_bytes(BN, n_b) + kSmemReserve;
+    g->smem_bytes = stages * stage_bytes(BN, n_b, pair) + kSmemReserve;
     g->n_b = n_b;
+    g->pair = pair;
     g->useful_over_padded = (double)M * N * K /
-                            ((double)(tm * kBM) * (double)(tn * BN) * (double)(kb * kBK));
+                            ((double)(tm * bm) * (double)(tn * BN) * (double)(kb * kBK));
     g->est_us = t_cta * 1e6;
     return true;
 }
@@ -97,19 +108,23 @@ bool better(const GemmConfig& a, const GemmConfig& b) {
     if (a.est_us < b.est_us * (1.0 - 1e-9)) return true;
     if (b.est_us < a.est_us * (1.0 - 1e-9)) return false;
     if (a.BN != b.BN) return a.BN > b.BN;
+    if (a.pair != b.pair) return a.pair > b.pair;
     return a.split_k < b.split_k;
 }
 
 bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int num_sms,
             GemmConfig* best) {
     bool found = false;
-    for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
-        for (int SK = 1; SK <= max_sk; ++SK) {
-            GemmConfig g;
-            if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, &g)) continue;
-            if (!found || better(g, *best)) {
-                *best = g;
-                found = true;
+    for (int pair = 1; pair <= 2; ++pair) {
+        for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
+            if (BN % (32 * pair) != 0) continue;   // a pair splits the columns in halves of 32s
+            for (int SK = 1; SK <= max_sk; ++SK) {
+                GemmConfig g;
+                if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, &g)) continue;
+                if (!found || better(g, *best)) {
+                    *best = g;
+                    found = true;
+                }
             }
         }
     }
@@ -146,24 +161,26 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         *why = "no feasible tile for the down projection";
         return KT_ERR_UNSUPPORTED;
     }
-    // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN" and
-    // KT_FORCE_DOWN="BN,SK".  An infeasible override is an error, never ignored.
+    // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN[,PAIR]" and
+    // KT_FORCE_DOWN="BN,SK[,PAIR]".  An infeasible override is an error, never ignored.
     if (const char* e = std::getenv("KT_FORCE_UP")) {
-        int bn = 0;
+        int bn = 0, pr = 1;
         GemmConfig g;
-        if (std::sscanf(e, "%d", &bn) != 1 || bn % 32 != 0 || bn < 32 || bn > 256 ||
-            !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, &g)) {
-            *why = "KT_FORCE_UP must be a feasible N tile (a multiple of 32 in 32..256)";
+        int nf = std::sscanf(e, "%d,%d", &bn, &pr);
+        if (nf < 1 || (pr != 1 && pr != 2) || bn % (32 * pr) != 0 || bn < 32 || bn > 256 ||
+            !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, &g)) {
+            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR]\" (BN a multiple of 32 (64 for a pair) up to 256)";
             return KT_ERR_INVALID;
         }
         out->up = g;
     }
     if (const char* e = std::getenv("KT_FORCE_DOWN")) {
-        int bn = 0, sk = 0;
+        int bn = 0, sk = 0, pr = 1;
         GemmConfig g;
-        if (std::sscanf(e, "%d,%d", &bn, &sk) != 2 || bn % 32 != 0 || bn < 32 || bn > 256 || sk < 1 ||
-            sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, &g)) {
-            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK\" (BN a multiple of 32 in 32..256, no empty split)";
+        int nf = std::sscanf(e, "%d,%d,%d", &bn, &sk, &pr);
+        if (nf < 2 || (pr != 1 && pr != 2) || bn % (32 * pr) != 0 || bn < 32 || bn > 256 || sk < 1 ||
+            sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, &g)) {
+            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR]\" (no empty split)";
             return KT_ERR_INVALID;
         }
         out->down = g;
@@ -172,7 +189,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
 }
 
 void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* o) {
-    o->BM = kBM; o->BN = g.BN; o->BK = kBK;
+    o->BM = kBM * g.pair; o->BN = g.BN; o->BK = kBK;
     o->stages = g.stages; o->split_k = g.split_k;
     o->tiles_m = g.tiles_m; o->tiles_n = g.tiles_n; o->kblocks = g.kblocks;
     o->grid = g.grid; o->waves = g.waves;
