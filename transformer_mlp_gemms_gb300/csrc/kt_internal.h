@@ -11,7 +11,7 @@ namespace kt {
 
 // Fixed tile geometry of the sm_103a kernels.
 constexpr int kBM = 128;          // tcgen05 M (one CTA, cta_group::1): TMEM lane i = tile row i
-constexpr int kBK = 64;           // 64 16-bit elements = one 128-byte swizzle row
+constexpr int kAtomK = 64;        // 64 16-bit elements = one 128-byte swizzle row (the A box width)
 constexpr int kEpiWarps = 8;      // epilogue warps (two per TMEM lane quadrant)
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer warp + MMA warp + epilogue
 constexpr int kTmemCols = 512;    // whole tensor memory of the SM (one CTA per SM)
@@ -50,6 +50,7 @@ struct GemmConfig {
     int smem_bytes;
     int n_b;               // B operand tiles per stage: 1, or 2 for GEGLU (value + gate)
     int pair;              // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile (cta_group::2)
+    int bk;                // k-block depth per pipeline stage: 64 or 128
     double useful_over_padded;
     double est_us;
 };
@@ -58,11 +59,12 @@ struct PlanChoice {
     GemmConfig up, down;
 };
 
-// Bytes of one pipeline stage in one CTA: its 128-row A tile + n_b B tiles holding
-// its share of the columns (BN, or BN/2 in a CTA pair) in 64-column boxes.
-inline int stage_bytes(int BN, int n_b, int pair) {
+// Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
+// 128 x 64) + n_b B tiles holding its share of the columns (BN, or BN/2 in a CTA
+// pair) in 64-column boxes of bk rows.
+inline int stage_bytes(int BN, int n_b, int pair, int bk) {
     int chunks = (BN / pair + 63) / 64;
-    return kBM * kBK * 2 + n_b * chunks * 64 * kBK * 2;
+    return kBM * bk * 2 + n_b * chunks * 64 * bk * 2;
 }
 
 // Planner (host only, no GPU): returns KT_OK and fills `out`, or an error status.
@@ -77,6 +79,7 @@ struct GemmParams {
     int M, N, K;
     int BN, n_chunks, stages, split_k;  // n_chunks: 64-column B boxes per CTA
     int pair;                // 1 or 2 (CTA pair, tiles of 256 rows); tiles_m counts pair-tiles
+    int bk;                  // k-block depth per stage (64 or 128)
     int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
     int gate_col;            // GEGLU: first gate column in W_up (= F); else 0
     uint32_t idesc;          // tcgen05 instruction descriptor

@@ -122,9 +122,10 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
     q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair);
-    q.a_bytes = kt::kBM * kt::kBK * 2;
-    q.b_bytes = (uint32_t)q.n_chunks * 64u * kt::kBK * 2u;
-    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair);
+    q.bk = g.bk;
+    q.a_bytes = kt::kBM * g.bk * 2;
+    q.b_bytes = (uint32_t)q.n_chunks * 64u * (uint32_t)g.bk * 2u;
+    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair, g.bk);
     q.acc_bufs = (epi == kt::EPI_GEGLU && g.BN > 128) ? 1u : 2u;
     q.gate_acc_off = epi == kt::EPI_GEGLU ? (g.BN <= 128 ? 128u : 256u) : 0u;
     q.error = P->flags;
@@ -149,12 +150,12 @@ kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void*
     const char* why = "";
     if (!P->cache_valid || P->c_x != X || P->c_wu != W_up || P->c_h != H || P->c_wd != W_down || P->c_y != Y) {
         // A operands: [rows][K] K-major, box 128 rows x 64 columns, 128-byte swizzle.
-        // B operands: [K][N] N-major, box 64 rows (K) x 64 columns (N), 128-byte swizzle.
+        // B operands: [K][N] N-major, box bk rows (K) x 64 columns (N), 128-byte swizzle.
         // Stores of H and Y: box 32 rows x 32 columns, 64-byte swizzle.
-        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kBK, 128, &why) ||
-            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, kt::kBK, 64, 128, &why) ||
-            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kBK, 128, &why) ||
-            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, kt::kBK, 64, 128, &why) ||
+        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kAtomK, 128, &why) ||
+            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, P->choice.up.bk, 64, 128, &why) ||
+            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kAtomK, 128, &why) ||
+            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, P->choice.down.bk, 64, 128, &why) ||
             !kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) ||
             !kt::encode_tmap(&P->tm_ys, Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why)) {
             P->cache_valid = false;

@@ -469,6 +469,25 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t
     }
 }
 
+// The MMAs of one k-block: NK steps of K = 16 (4 for a 64-deep stage, 8 for 128).
+template <int EPI, int PAIR, int NK>
+__device__ __forceinline__ void issue_kblock(uint32_t d, uint32_t d_gate, uint64_t ad0, uint64_t bd0, uint64_t gd0,
+                                             uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+        const uint64_t ad = ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
+        const uint64_t bd = bd0 + (uint64_t)(k * 128);
+        const uint32_t acc = k == 0 ? acc0 : 1u;
+        if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, idesc, acc);
+        else mma_f16(d, ad, bd, idesc, acc);
+        if constexpr (EPI == EPI_GEGLU) {
+            const uint64_t gd = gd0 + (uint64_t)(k * 128);
+            if constexpr (PAIR == 2) mma_f16_pair(d_gate, ad, gd, idesc, acc);
+            else mma_f16(d_gate, ad, gd, idesc, acc);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -583,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (nb_r + 64 * ch < p.N) chunks_r = ch + 1;
                     // boxes entirely past the tensor are not loaded: they would only feed
                     // accumulator rows / columns that are never stored
-                    return (m_r < p.M ? p.a_bytes : 0u) + (uint32_t)(n_b * chunks_r) * 8192u;
+                    return (m_r < p.M ? p.a_bytes : 0u) + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * 128u);
                 };
                 int m_me, nb_me, chunks;
                 uint32_t tx = cta_share(rank, m_me, nb_me, chunks);
@@ -602,26 +621,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
                     if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
+                    const int k0 = kb * p.bk;
+                    const uint32_t chunk_bytes = (uint32_t)p.bk * 128u;  // 64 columns x bk rows
                     if constexpr (PAIR == 2) {
                         const uint32_t fb_leader = mapa_rank(fb, 0);
                         if (leader) mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M) tma_load_2d_pair(sA, &tmA, fb_leader, kb * kBK, m_me);
+                        if (m_me < p.M)
+                            for (int a = 0; a < p.bk / kAtomK; ++a)
+                                tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
                         for (int ch = 0; ch < chunks; ++ch)
-                            tma_load_2d_pair(sB + 8192u * ch, &tmB, fb_leader, nb_me + 64 * ch, kb * kBK);
+                            tma_load_2d_pair(sB + chunk_bytes * ch, &tmB, fb_leader, nb_me + 64 * ch, k0);
                         if (EPI == EPI_GEGLU) {
                             for (int ch = 0; ch < chunks; ++ch)
-                                tma_load_2d_pair(sB + p.b_bytes + 8192u * ch, &tmB, fb_leader,
-                                                 p.gate_col + nb_me + 64 * ch, kb * kBK);
+                                tma_load_2d_pair(sB + p.b_bytes + chunk_bytes * ch, &tmB, fb_leader,
+                                                 p.gate_col + nb_me + 64 * ch, k0);
                         }
                     } else {
                         mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M) tma_load_2d(sA, &tmA, fb, kb * kBK, m_me);
+                        if (m_me < p.M)
+                            for (int a = 0; a < p.bk / kAtomK; ++a)
+                                tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
                         for (int ch = 0; ch < chunks; ++ch)
-                            tma_load_2d(sB + 8192u * ch, &tmB, fb, nb_me + 64 * ch, kb * kBK);
+                            tma_load_2d(sB + chunk_bytes * ch, &tmB, fb, nb_me + 64 * ch, k0);
                         if (EPI == EPI_GEGLU) {
                             for (int ch = 0; ch < chunks; ++ch)
-                                tma_load_2d(sB + p.b_bytes + 8192u * ch, &tmB, fb, p.gate_col + nb_me + 64 * ch,
-                                            kb * kBK);
+                                tma_load_2d(sB + p.b_bytes + chunk_bytes * ch, &tmB, fb, p.gate_col + nb_me + 64 * ch,
+                                            k0);
                         }
                     }
                     armed |= 1u << stage;
@@ -668,21 +693,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (tr && !issued_any) trace_mark(tr, TR_FIRST_FULL);
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
-#pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // A: K-major, +32 bytes per 16-element K step inside the 128-byte row.
-                        const uint64_t ad = smem_desc(sA + 32u * k, 16u, 1024u);
-                        // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row groups 1 KB apart
-                        // (SBO), +2 KB per 16-row K step.
-                        const uint64_t bd = smem_desc(sB + 2048u * k, 8192u, 1024u);
-                        const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, p.idesc, acc);
-                        else mma_f16(d, ad, bd, p.idesc, acc);
-                        if (EPI == EPI_GEGLU) {
-                            const uint64_t gd = smem_desc(sB + p.b_bytes + 2048u * k, 8192u, 1024u);
-                            if constexpr (PAIR == 2) mma_f16_pair(d + p.gate_acc_off, ad, gd, p.idesc, acc);
-                            else mma_f16(d + p.gate_acc_off, ad, gd, p.idesc, acc);
-                        }
+                    // Descriptors of this stage; the K steps only move the start address, by
+                    // constant offsets (in 16-byte units): A +32 bytes per 16-element step inside
+                    // a 128 x 64 swizzle atom and +16 KB per atom; B +2 KB per 16-row step.
+                    const uint64_t ad0 = smem_desc(sA, 16u, 1024u);
+                    const uint64_t bd0 = smem_desc(sB, (uint32_t)p.bk * 128u, 1024u);
+                    const uint64_t gd0 = smem_desc(sB + p.b_bytes, (uint32_t)p.bk * 128u, 1024u);
+                    const uint32_t acc0 = kb > kb0 ? 1u : 0u;
+                    if (p.bk == 64) {
+                        issue_kblock<EPI, PAIR, 4>(d, d + p.gate_acc_off, ad0, bd0, gd0, p.idesc, acc0);
+                    } else {
+                        issue_kblock<EPI, PAIR, 8>(d, d + p.gate_acc_off, ad0, bd0, gd0, p.idesc, acc0);
                     }
                     issued_any = true;
                     // stage free (in both CTAs of a pair) once these MMAs completed
@@ -1104,8 +1125,8 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
         return KT_ERR_CUDA;
     }
     alignas(64) CUtensorMap tmA, tmB, tmC;
-    if (!encode_tmap(&tmA, H, dtype, M, F, kBM, kBK, 128, why) ||
-        !encode_tmap(&tmB, W_down, dtype, F, D, kBK, 64, 128, why) ||
+    if (!encode_tmap(&tmA, H, dtype, M, F, kBM, kAtomK, 128, why) ||
+        !encode_tmap(&tmB, W_down, dtype, F, D, g.bk, 64, 128, why) ||
         !encode_tmap(&tmC, Y, dtype, M, D, 32, kStoreCols, 64, why))
         return KT_ERR_CUDA;
     GemmParams q;
@@ -1125,9 +1146,10 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.pair = g.pair;
     q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.idesc = make_idesc(dtype, g.BN, kBM * g.pair);
-    q.a_bytes = kBM * kBK * 2;
-    q.b_bytes = (uint32_t)q.n_chunks * 64u * kBK * 2u;
-    q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1, g.pair);
+    q.bk = g.bk;
+    q.a_bytes = kBM * g.bk * 2;
+    q.b_bytes = (uint32_t)q.n_chunks * 64u * (uint32_t)g.bk * 2u;
+    q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1, g.pair, g.bk);
     q.acc_bufs = 2u;
     q.bias = b_down;
     q.error = reinterpret_cast<int*>(scratch);

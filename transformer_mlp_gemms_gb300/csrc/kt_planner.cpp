@@ -12,8 +12,9 @@
 //
 // Model, per candidate (PAIR, BN, SK), PAIR = 2 being a CTA pair on a 256-row tile:
 //   tiles   = ceil(M/(128 PAIR)) * ceil(N/BN) * SK,  waves = ceil(PAIR tiles / SMs)
-//   per k-block and CTA: t_kb = max(MMA time of 128 x BN x 64, its stage bytes / its
-//                          share of the L2 feed, load latency / stages)
+//   per k-block (depth BK = 64 or 128) and CTA: t_kb = max(MMA time of 128 x BN x BK,
+//                          the MMA thread's issue chain, its stage bytes / its share of
+//                          the L2 feed, load latency / stages)
 //   t_main  = kblocks_per_split * t_kb + t_fill
 //   t_epi   = 128 * BN * c_epi          (per-element epilogue cost of the kind)
 //           + (SK > 1) the fp32 partial write and the last CTA's read of SK partials
@@ -32,13 +33,27 @@
 namespace kt {
 namespace {
 
-constexpr double kRsm = 2.25e15 / 152.0;  // dense 16-bit FLOP/s per SM (nominal)
+constexpr double kClk = 2.0e9;             // SM clock of short kernels on GB300 (measured 1.9-2.07 GHz)
+constexpr double kRsm = 8192.0 * kClk;    // dense 16-bit FLOP/s per SM: 4096 MAC per clock
+// The single MMA-issuing thread (measured with clock64 on GB300): about 80 cycles per
+// tcgen05.mma instruction, and about 200 cycles per stage for the full-barrier wait,
+// the commit and the loop.
+constexpr double kIssuePerMma = 80.0 / kClk;
+constexpr double kIssuePerStage = 200.0 / kClk;
 constexpr double kL2Feed = 20e12;         // aggregate L2 -> SM bytes/s (model)
 constexpr double kSmFeedMax = 240e9;      // one SM's fill bandwidth (model)
 constexpr double kTFill = 0.35e-6;        // pipeline fill + drain latency per tile (model)
-// Load latency a stage ring must cover (model, calibrated on GB300: a 5-stage ring of
-// 40 KB stages ran 0.33 us per k-block against 0.19 us of MMA time).
-constexpr double kLoadLatency = 1.6e-6;
+// Load latency a stage ring must cover (calibrated on GB300 with a measured sweep of
+// tile shapes: the main loop runs at about max(MMA, issue, 2.0 us / (K depth in flight))).
+constexpr double kLoadLatency = 2.0e-6;
+// Launch, set-up, first loads and drain of one kernel (calibrated; shifts every
+// candidate equally, so it does not change the ranking).
+constexpr double kKernelOverhead = 4.0e-6;
+// Extra cost of a CTA pair (calibrated): once per kernel for cluster launch, paired
+// tensor-memory allocation and cluster barriers, and per tile for the cross-CTA
+// barrier traffic of the main loop and epilogue.
+constexpr double kPairKernelCost = 3.0e-6;
+constexpr double kPairTileCost = 0.3e-6;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -52,18 +67,18 @@ double epi_cost_per_elem(int epi) {      // seconds per output element per SM (m
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int max_stages(int BN, int n_b, int pair) {
-    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair);
+int max_stages(int BN, int n_b, int pair, int bk) {
+    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair, bk);
     return std::min(s, kMaxStages);
 }
 
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
-              GemmConfig* g) {
-    int stages = max_stages(BN, n_b, pair);
+              int bk, GemmConfig* g) {
+    int stages = max_stages(BN, n_b, pair, bk);
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
     const int64_t bm = (int64_t)kBM * pair;  // rows per tile (a pair's tile spans two CTAs)
-    int64_t tm = cdiv(M, bm), tn = cdiv(N, BN), kb = cdiv(K, kBK);
+    int64_t tm = cdiv(M, bm), tn = cdiv(N, BN), kb = cdiv(K, bk);
     int64_t kps = cdiv(kb, SK);
     int64_t sk_eff = cdiv(kb, kps);  // no empty split
     if (sk_eff != SK) return false;
@@ -74,13 +89,15 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     int64_t grid = std::min<int64_t>(ctas, slots);
     int64_t waves = cdiv(ctas, slots);
 
-    // per CTA and k-block: the MMA time of its 128 rows, the time to stream its share of
-    // the operands, and the load latency the ring of `stages` k-blocks has to cover
-    double t_mma = n_b * 2.0 * kBM * BN * kBK / kRsm;
-    double bytes_kb = (double)stage_bytes(BN, n_b, pair);
+    // per CTA and k-block: the MMA time of its 128 rows, the issue chain of the one MMA
+    // thread (in a pair it issues for both CTAs), the time to stream its share of the
+    // operands, and the load latency the ring of `stages` k-blocks has to cover
+    double t_mma = n_b * 2.0 * kBM * BN * bk / kRsm;
+    double t_issue = kIssuePerStage + n_b * (bk / 16) * kIssuePerMma;
+    double bytes_kb = (double)stage_bytes(BN, n_b, pair, bk);
     double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
-    double t_kb = std::max(std::max(t_mma, bytes_kb / feed), kLoadLatency / stages);
-    double t_main = (double)kps * t_kb + kTFill;
+    double t_kb = std::max(std::max(t_mma, t_issue), std::max(bytes_kb / feed, kLoadLatency / stages));
+    double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0);
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
     // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
     // all SK partials, both latency-bound at a few tens of GB/s per SM
@@ -94,12 +111,13 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->tiles_m = (int)tm; g->tiles_n = (int)tn; g->kblocks = (int)kb;
     g->kblocks_per_split = (int)kps;
     g->grid = (int)grid; g->waves = (int)waves;
-    g->smem_bytes = stages * stage_bytes(BN, n_b, pair) + kSmemReserve;
+    g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk) + kSmemReserve;
     g->n_b = n_b;
     g->pair = pair;
+    g->bk = bk;
     g->useful_over_padded = (double)M * N * K /
-                            ((double)(tm * bm) * (double)(tn * BN) * (double)(kb * kBK));
-    g->est_us = t_cta * 1e6;
+                            ((double)(tm * bm) * (double)(tn * BN) * (double)(kb * bk));
+    g->est_us = (t_cta + kKernelOverhead + (pair == 2 ? kPairKernelCost : 0.0)) * 1e6;
     return true;
 }
 
@@ -109,6 +127,7 @@ bool better(const GemmConfig& a, const GemmConfig& b) {
     if (b.est_us < a.est_us * (1.0 - 1e-9)) return false;
     if (a.BN != b.BN) return a.BN > b.BN;
     if (a.pair != b.pair) return a.pair > b.pair;
+    if (a.bk != b.bk) return a.bk > b.bk;
     return a.split_k < b.split_k;
 }
 
@@ -118,12 +137,14 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
     for (int pair = 1; pair <= 2; ++pair) {
         for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
             if (BN % (32 * pair) != 0) continue;   // a pair splits the columns in halves of 32s
-            for (int SK = 1; SK <= max_sk; ++SK) {
-                GemmConfig g;
-                if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, &g)) continue;
-                if (!found || better(g, *best)) {
-                    *best = g;
-                    found = true;
+            for (int bk = 64; bk <= 128; bk += 64) {
+                for (int SK = 1; SK <= max_sk; ++SK) {
+                    GemmConfig g;
+                    if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, bk, &g)) continue;
+                    if (!found || better(g, *best)) {
+                        *best = g;
+                        found = true;
+                    }
                 }
             }
         }
@@ -161,26 +182,26 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         *why = "no feasible tile for the down projection";
         return KT_ERR_UNSUPPORTED;
     }
-    // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN[,PAIR]" and
-    // KT_FORCE_DOWN="BN,SK[,PAIR]".  An infeasible override is an error, never ignored.
+    // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN[,PAIR[,BK]]" and
+    // KT_FORCE_DOWN="BN,SK[,PAIR[,BK]]".  An infeasible override is an error, never ignored.
     if (const char* e = std::getenv("KT_FORCE_UP")) {
-        int bn = 0, pr = 1;
+        int bn = 0, pr = 1, bk = 64;
         GemmConfig g;
-        int nf = std::sscanf(e, "%d,%d", &bn, &pr);
-        if (nf < 1 || (pr != 1 && pr != 2) || bn % (32 * pr) != 0 || bn < 32 || bn > 256 ||
-            !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, &g)) {
-            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR]\" (BN a multiple of 32 (64 for a pair) up to 256)";
+        int nf = std::sscanf(e, "%d,%d,%d", &bn, &pr, &bk);
+        if (nf < 1 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
+            bn > 256 || !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, bk, &g)) {
+            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32, 64 for a pair; BK 64 or 128)";
             return KT_ERR_INVALID;
         }
         out->up = g;
     }
     if (const char* e = std::getenv("KT_FORCE_DOWN")) {
-        int bn = 0, sk = 0, pr = 1;
+        int bn = 0, sk = 0, pr = 1, bk = 64;
         GemmConfig g;
-        int nf = std::sscanf(e, "%d,%d,%d", &bn, &sk, &pr);
-        if (nf < 2 || (pr != 1 && pr != 2) || bn % (32 * pr) != 0 || bn < 32 || bn > 256 || sk < 1 ||
-            sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, &g)) {
-            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR]\" (no empty split)";
+        int nf = std::sscanf(e, "%d,%d,%d,%d", &bn, &sk, &pr, &bk);
+        if (nf < 2 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
+            bn > 256 || sk < 1 || sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g)) {
+            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR[,BK]]\" (no empty split)";
             return KT_ERR_INVALID;
         }
         out->down = g;
@@ -189,7 +210,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
 }
 
 void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* o) {
-    o->BM = kBM * g.pair; o->BN = g.BN; o->BK = kBK;
+    o->BM = kBM * g.pair; o->BN = g.BN; o->BK = g.bk;
     o->stages = g.stages; o->split_k = g.split_k;
     o->tiles_m = g.tiles_m; o->tiles_n = g.tiles_n; o->kblocks = g.kblocks;
     o->grid = g.grid; o->waves = g.waves;
