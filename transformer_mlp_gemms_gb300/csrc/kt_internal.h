@@ -51,6 +51,7 @@ struct GemmConfig {
     int n_b;               // B operand tiles per stage: 1, or 2 for GEGLU (value + gate)
     int pair;              // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile (cta_group::2)
     int bk;                // k-block depth per pipeline stage: 64 or 128
+    int cluster_sk;        // 1: split-K partials reduced inside a cluster (distributed smem)
     double useful_over_padded;
     double est_us;
 };
@@ -69,7 +70,7 @@ inline int stage_bytes(int BN, int n_b, int pair, int bk) {
 
 // Planner (host only, no GPU): returns KT_OK and fills `out`, or an error status.
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why);
+                      const char** why, bool allow_cluster_sk = true);
 
 // Fill the public description from a choice.
 void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* out);
@@ -80,6 +81,7 @@ struct GemmParams {
     int BN, n_chunks, stages, split_k;  // n_chunks: 64-column B boxes per CTA
     int pair;                // 1 or 2 (CTA pair, tiles of 256 rows); tiles_m counts pair-tiles
     int bk;                  // k-block depth per stage (64 or 128)
+    int cluster_sk;          // 1: the split_k CTAs of a tile form a cluster and reduce on chip
     int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
     int gate_col;            // GEGLU: first gate column in W_up (= F); else 0
     uint32_t idesc;          // tcgen05 instruction descriptor

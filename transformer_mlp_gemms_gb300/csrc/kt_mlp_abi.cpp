@@ -112,6 +112,7 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.K = (int)g.K;
     q.BN = g.BN;
     q.pair = g.pair;
+    q.cluster_sk = g.cluster_sk;
     q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.stages = g.stages;
     q.split_k = g.split_k;
@@ -222,7 +223,7 @@ kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     int64_t ws = M * F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * M * D;
-    if (c.down.split_k > 1)
+    if (c.down.split_k > 1 && !c.down.cluster_sk)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
     out->workspace_bytes = ws;
     return ok();
@@ -263,8 +264,9 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
     size_t flag_bytes = 4 * (1 + n_counters);
-    size_t part_bytes =
-        dn.split_k > 1 ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4 : 0;
+    size_t part_bytes = dn.split_k > 1 && !dn.cluster_sk
+                            ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
+                            : 0;
     size_t io_bytes = (size_t)M * (size_t)D * 2;
     if ((e = cudaMalloc(&P->H, h_bytes)) != cudaSuccess ||
         (e = cudaMalloc(reinterpret_cast<void**>(&P->flags), flag_bytes)) != cudaSuccess ||

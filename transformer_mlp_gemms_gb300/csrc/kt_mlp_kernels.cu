@@ -194,6 +194,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// 16 bytes from a shared-memory address of any CTA of the cluster.
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int x,
                                                  int y) {
@@ -499,8 +509,13 @@ struct TileCoord {
 __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     TileCoord c;
     const int per_split = p.tiles_m * p.tiles_n;
-    c.split = t / per_split;
-    c.mn = t - c.split * per_split;
+    if (p.cluster_sk) {  // the SK splits of one tile are one cluster of consecutive CTAs
+        c.split = t % p.split_k;
+        c.mn = t / p.split_k;
+    } else {
+        c.split = t / per_split;
+        c.mn = t - c.split * per_split;
+    }
     c.tm = c.mn / p.tiles_n;
     c.tn = c.mn - c.tm * p.tiles_n;
     return c;
@@ -528,7 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_acce = bar_accf + 16u;
     const uint32_t bar_stall = bar_acce + 16u;
     const uint32_t bar_drain = bar_stall + 8u;
-    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 6));
+    const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partial is in smem
+    const uint32_t bar_rdone = bar_pready + 8u;  // cluster split-K: every CTA finished reading mine
+    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 8));
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
@@ -553,6 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar_stall, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_pready, (uint32_t)(p.split_k * kEpiWarps));
+        mbar_init(bar_rdone, (uint32_t)(p.split_k * kEpiWarps));
         *abort_flag = 0;
         *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR == 2) cluster_sync_all();  // peers' barriers initialised before any remote signal
+    if (PAIR == 2 || p.cluster_sk) cluster_sync_all();  // peers' barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
@@ -820,6 +839,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
                     else mbar_arrive(acce);
                 }
+            } else if (p.cluster_sk) {
+                // split-K inside a cluster: the SK CTAs of this tile hold their fp32 partials
+                // in their own (now idle) stage rings; each CTA reduces a share of the tile's
+                // 32 x 32 blocks by reading all SK partials through distributed shared memory,
+                // in split order, and stores them.  No global scratch, no atomics.
+                // partial layout [32-column group][16-byte chunk][row][4 floats]: a warp's access
+                // to one chunk of its 32 rows is 512 contiguous bytes, locally and remotely
+                for (int g = half; g < ngroups; g += 2) {
+                    uint32_t r[32];
+                    tmem_ld32(tq + 32u * g, r);
+                    tmem_wait_ld_only();
+                    reg_fence32(r);
+                    const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)row) * 16u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        st_shared_v4(a + 2048u * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(acce);
+                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                    for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_pready, (uint32_t)s));
+                }
+                const bool ready = wait_phase(bar_pready, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
+                                              p.wait_limit_ns);
+                if (ready) {
+                    const int units = 4 * ngroups;  // 32-row blocks x 32-column groups of the tile
+                    int mine = 0;                   // index among this CTA's units
+                    for (int u = c.split; u < units; u += p.split_k, ++mine) {
+                        if ((mine & (kEpiWarps - 1)) != ew) continue;
+                        const int rb = u / ngroups, g = u - rb * ngroups;
+                        const int col = n0 + 32 * g;
+                        const int yb = m0 + 32 * rb;
+                        if (col >= p.N || yb >= p.M) continue;  // warp-uniform
+                        const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)(32 * rb + lane)) * 16u;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        for (int sp = 0; sp < p.split_k; ++sp) {  // split order: deterministic
+                            const uint32_t ra = mapa_rank(a, (uint32_t)sp);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                float4 x[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) x[i] = ld_cluster_v4(ra + 2048u * (4u * h + i));
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    v[16 * h + 4 * i] += x[i].x;
+                                    v[16 * h + 4 * i + 1] += x[i].y;
+                                    v[16 * h + 4 * i + 2] += x[i].z;
+                                    v[16 * h + 4 * i + 3] += x[i].w;
+                                }
+                            }
+                        }
+                        if (p.bias) {
+                            float b[32];
+                            load_bias32<DT>(p.bias, col, p.N, b);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += b[i];
+                        }
+                        stage_and_store<DT>(&tmC, stg, lane, v, col, yb);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                    for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_rdone, (uint32_t)s));
+                }
+                // no CTA leaves (and frees its shared memory) while a peer still reads it
+                wait_phase(bar_rdone, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             } else {
                 // split-K: this split's fp32 partial in a private layout in which every
                 // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]
@@ -923,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ teardown ------------------------------
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR == 2) cluster_sync_all();  // no CTA leaves while its peer may still signal it
+    if (PAIR == 2 || p.cluster_sk) cluster_sync_all();  // no CTA leaves while a peer may still signal it
     if (threadIdx.x == 0 && tr) {
         trace_mark(tr, TR_EXIT);
         tr[(size_t)blockIdx.x * kTraceSlots + TR_SMID] = sm_id();
@@ -1011,9 +1101,9 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
-    if (PAIR == 2) {
+    if (PAIR == 2 || p.cluster_sk) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.x = PAIR == 2 ? 2 : (unsigned)p.split_k;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -1102,9 +1192,10 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
         scratch = g_noalloc_ptr[dev];
         sms = g_noalloc_sms[dev];
     }
-    // the same tile plan as the MLP's down projection
+    // the tile plan of the MLP's down projection, with the split-K reduction through this
+    // entry point's scratch (not through a cluster's shared memory)
     PlanChoice pc;
-    kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why);
+    kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why, /*allow_cluster_sk=*/false);
     if (st != KT_OK) return st;
     const GemmConfig& g = pc.down;
     const size_t n_counters = (size_t)g.tiles_m * (size_t)g.tiles_n * (size_t)g.pair;
@@ -1144,6 +1235,7 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.kblocks_per_split = g.kblocks_per_split;
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.pair = g.pair;
+    q.cluster_sk = 0;
     q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.idesc = make_idesc(dtype, g.BN, kBM * g.pair);
     q.bk = g.bk;
@@ -1213,6 +1305,11 @@ kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, cons
     const CUtensorMap* c = reinterpret_cast<const CUtensorMap*>(tmC);
     if (p.pair == 2 && (grid % 2) != 0) {
         *why = "a CTA-pair launch needs an even grid";
+        return KT_ERR_INVALID;
+    }
+    if (p.cluster_sk && (p.pair != 1 || epi != EPI_DOWN || p.split_k < 2 || p.split_k > 8 ||
+                         grid != p.num_tiles || grid % p.split_k != 0)) {
+        *why = "inconsistent cluster split-K launch";
         return KT_ERR_INVALID;
     }
 #define KT_LAUNCH(E, D)                                                                   \

@@ -72,8 +72,10 @@ int max_stages(int BN, int n_b, int pair, int bk) {
     return std::min(s, kMaxStages);
 }
 
+constexpr int kGpcs = 8;  // GB300: 152 SMs in 8 GPCs; a cluster must fit in one GPC
+
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
-              int bk, GemmConfig* g) {
+              int bk, GemmConfig* g, bool cluster_sk = false) {
     int stages = max_stages(BN, n_b, pair, bk);
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
@@ -88,6 +90,16 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     int64_t ctas = tiles * pair;
     int64_t grid = std::min<int64_t>(ctas, slots);
     int64_t waves = cdiv(ctas, slots);
+    if (cluster_sk) {
+        // the SK CTAs of a tile form a cluster: one tile per CTA, all clusters resident at
+        // once, and the stage ring must hold the padded fp32 partial of the tile
+        const int64_t per_gpc = (num_sms / kGpcs) / SK;
+        if (epi != EPI_DOWN || pair != 1 || SK < 2 || SK > 8 || per_gpc < 1) return false;
+        if (tm * tn > per_gpc * kGpcs) return false;
+        if ((int64_t)stages * stage_bytes(BN, n_b, pair, bk) < (int64_t)kBM * BN * 4) return false;
+        grid = ctas;
+        waves = 1;
+    }
 
     // per CTA and k-block: the MMA time of its 128 rows, the issue chain of the one MMA
     // thread (in a pair it issues for both CTAs), the time to stream its share of the
@@ -100,8 +112,10 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0);
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
     // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
-    // all SK partials, both latency-bound at a few tens of GB/s per SM
-    if (SK > 1) t_epi += kBM * BN * 4.0 / 25e9 + SK * (kBM * BN * 4.0) / 60e9;
+    // all SK partials, both latency-bound at a few tens of GB/s per SM; in a cluster: the
+    // partial to shared memory, two cluster-wide handshakes, the distributed-smem reads
+    if (SK > 1 && !cluster_sk) t_epi += kBM * BN * 4.0 / 25e9 + SK * (kBM * BN * 4.0) / 60e9;
+    if (SK > 1 && cluster_sk) t_epi += 1.0e-6 + kBM * BN * 4.0 / 150e9;
     bool two_bufs = !(n_b == 2 && BN > 128);
     double t_cta = two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
                             : waves * (t_main + t_epi);
@@ -115,6 +129,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->n_b = n_b;
     g->pair = pair;
     g->bk = bk;
+    g->cluster_sk = cluster_sk ? 1 : 0;
     g->useful_over_padded = (double)M * N * K /
                             ((double)(tm * bm) * (double)(tn * BN) * (double)(kb * bk));
     g->est_us = (t_cta + kKernelOverhead + (pair == 2 ? kPairKernelCost : 0.0)) * 1e6;
@@ -132,18 +147,20 @@ bool better(const GemmConfig& a, const GemmConfig& b) {
 }
 
 bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int num_sms,
-            GemmConfig* best) {
+            GemmConfig* best, bool allow_cluster_sk) {
     bool found = false;
     for (int pair = 1; pair <= 2; ++pair) {
         for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
             if (BN % (32 * pair) != 0) continue;   // a pair splits the columns in halves of 32s
             for (int bk = 64; bk <= 128; bk += 64) {
                 for (int SK = 1; SK <= max_sk; ++SK) {
-                    GemmConfig g;
-                    if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, bk, &g)) continue;
-                    if (!found || better(g, *best)) {
-                        *best = g;
-                        found = true;
+                    for (int cl = 0; cl <= (allow_cluster_sk ? 1 : 0); ++cl) {
+                        GemmConfig g;
+                        if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, bk, &g, cl == 1)) continue;
+                        if (!found || better(g, *best)) {
+                            *best = g;
+                            found = true;
+                        }
                     }
                 }
             }
@@ -155,7 +172,7 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
 }  // namespace
 
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why) {
+                      const char** why, bool allow_cluster_sk) {
     if (M < 1 || D < 1 || F < 1) { *why = "M, D and F must be positive"; return KT_ERR_INVALID; }
     if (act < 0 || act > 3) { *why = "unknown activation"; return KT_ERR_INVALID; }
     if (num_sms < 1) { *why = "num_sms must be positive"; return KT_ERR_INVALID; }
@@ -174,11 +191,11 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
                : act == KT_ACT_GELU_TANH ? EPI_GELU_TANH
                : act == KT_ACT_GEGLU ? EPI_GEGLU : EPI_NONE;
     int n_b = act == KT_ACT_GEGLU ? 2 : 1;
-    if (!choose(M, F, D, n_b, epi_up, 1, num_sms, &out->up)) {
+    if (!choose(M, F, D, n_b, epi_up, 1, num_sms, &out->up, false)) {
         *why = "no feasible tile for the up projection";
         return KT_ERR_UNSUPPORTED;
     }
-    if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down)) {
+    if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down, allow_cluster_sk)) {
         *why = "no feasible tile for the down projection";
         return KT_ERR_UNSUPPORTED;
     }
@@ -196,12 +213,13 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         out->up = g;
     }
     if (const char* e = std::getenv("KT_FORCE_DOWN")) {
-        int bn = 0, sk = 0, pr = 1, bk = 64;
+        int bn = 0, sk = 0, pr = 1, bk = 64, cl = 0;
         GemmConfig g;
-        int nf = std::sscanf(e, "%d,%d,%d,%d", &bn, &sk, &pr, &bk);
+        int nf = std::sscanf(e, "%d,%d,%d,%d,%d", &bn, &sk, &pr, &bk, &cl);
         if (nf < 2 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
-            bn > 256 || sk < 1 || sk > 64 || !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g)) {
-            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR[,BK]]\" (no empty split)";
+            bn > 256 || sk < 1 || sk > 64 || (cl && !allow_cluster_sk) ||
+            !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g, cl != 0)) {
+            *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR[,BK[,CLUSTER]]]\" (no empty split)";
             return KT_ERR_INVALID;
         }
         out->down = g;
