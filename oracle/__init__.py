@@ -32,7 +32,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkt_mlp_oracle.so")
 
 F16, BF16 = 0, 1
-GELU_ERF, GELU_TANH, GEGLU, NONE = 0, 1, 2, 3
+GELU_ERF, GELU_TANH, GEGLU, NONE, GELU_SIGMOID, SILU = 0, 1, 2, 3, 4, 5
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +82,11 @@ def _load():
                                         u16p, u16p, u16p, u16p, u16p,
                                         ctypes.POINTER(ctypes.c_int64), i64, u16p, f64p, u16p]
         lib.oracle_mlp_rows.restype = ctypes.c_int
+        lib.oracle_mlp_rows_ex.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           u16p, u16p, u16p, u16p, u16p, u16p, u16p, u16p, ctypes.c_double,
+                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int64), i64, u16p, f64p, u16p]
+        lib.oracle_mlp_rows_ex.restype = ctypes.c_int
+        lib.oracle_layernorm_row.argtypes = [f64p, f64p, f64p, ctypes.c_double, f64p, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -123,7 +128,7 @@ def encode(x, dtype: int) -> np.ndarray:
 
 
 def gelu(z, form: int) -> np.ndarray:
-    """gelu_erf (form=0) or gelu_tanh (form=1) in float64, elementwise."""
+    """gelu_erf (0), gelu_tanh (1), gelu_sigmoid (4) or silu (5) in float64, elementwise."""
     z = np.ascontiguousarray(z, dtype=np.float64)
     out = np.empty_like(z)
     _load().oracle_gelu_vec(_ptr(z, ctypes.c_double), _ptr(out, ctypes.c_double), z.size, form)
@@ -159,20 +164,47 @@ def activation(P, F: int, act: int) -> np.ndarray:
     return Hx
 
 
-def mlp(X, W_up, W_down, b_up=None, b_down=None, *, act: int, dtype: int, rows=None):
+def layernorm(x, gamma, beta, eps: float) -> np.ndarray:
+    """float64 LayerNorm of each row of x (biased variance over the last axis)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = np.ascontiguousarray(gamma, dtype=np.float64)
+    b = np.ascontiguousarray(beta, dtype=np.float64)
+    out = np.empty_like(x)
+    D = x.shape[-1]
+    for i in range(x.shape[0]):
+        _load().oracle_layernorm_row(_ptr(x[i], ctypes.c_double), _ptr(g, ctypes.c_double), _ptr(b, ctypes.c_double),
+                                     eps, _ptr(out[i], ctypes.c_double), D)
+    return out
+
+
+def mlp(X, W_up, W_down, b_up=None, b_down=None, *, act: int, dtype: int, rows=None,
+        R=None, ln=None, w_layout: int = 0):
     """The whole MLP on 16-bit inputs.
 
     ``X[M,D]``, ``W_up[D,F_up]``, ``W_down[F,D]``, ``b_up[F_up]``, ``b_down[D]``
     are uint16 bit patterns (or float16 arrays for dtype=F16).  ``rows`` (optional)
-    selects a subset of rows of X.  Returns ``(H_bits[R,F], Yx[R,D] float64,
-    Y_bits[R,D])`` for the R selected rows.
+    selects a subset of rows of X.  Options: ``R[M,D]`` residual added before the
+    final rounding; ``ln=(gamma[D], beta[D], eps)`` LayerNorm of X first (rounded to
+    the dtype); ``w_layout=1`` weights in [out][in] order (W_up[F_up,D],
+    W_down[D,F]).  Returns ``(H_bits[R,F], Yx[R,D] float64, Y_bits[R,D])`` for the R
+    selected rows.
     """
     X, W_up, W_down = _u16(X), _u16(W_up), _u16(W_down)
     M, D = X.shape
-    F = W_down.shape[0]
+    F = W_down.shape[1] if w_layout == 1 else W_down.shape[0]
     F_up = 2 * F if act == GEGLU else F
-    if W_up.shape != (D, F_up) or W_down.shape != (F, D):
-        raise ValueError("weight shapes do not match X and act")
+    want_up, want_dn = ((F_up, D), (D, F)) if w_layout == 1 else ((D, F_up), (F, D))
+    if W_up.shape != want_up or W_down.shape != want_dn:
+        raise ValueError("weight shapes do not match X, act and w_layout")
+    Rb = None if R is None else _u16(R)
+    if Rb is not None and Rb.shape != (M, D):
+        raise ValueError("R must be [M,D]")
+    lg = lb = None
+    eps = 0.0
+    if ln is not None:
+        lg, lb, eps = _u16(ln[0]), _u16(ln[1]), float(ln[2])
+        if lg.shape != (D,) or lb.shape != (D,):
+            raise ValueError("LayerNorm gamma / beta must be [D]")
     bias = b_up is not None or b_down is not None
     if bias:
         if b_up is None or b_down is None:
@@ -182,18 +214,19 @@ def mlp(X, W_up, W_down, b_up=None, b_down=None, *, act: int, dtype: int, rows=N
             raise ValueError("bias shapes do not match")
     if rows is None:
         r = None
-        R = M
+        NR = M
     else:
         r = np.ascontiguousarray(rows, dtype=np.int64)
-        R = r.size
-    H = np.empty((R, F), dtype=np.uint16)
-    Yx = np.empty((R, D), dtype=np.float64)
-    Y = np.empty((R, D), dtype=np.uint16)
-    rc = _load().oracle_mlp_rows(
+        NR = r.size
+    H = np.empty((NR, F), dtype=np.uint16)
+    Yx = np.empty((NR, D), dtype=np.float64)
+    Y = np.empty((NR, D), dtype=np.uint16)
+    rc = _load().oracle_mlp_rows_ex(
         M, D, F, act, dtype, 1 if bias else 0,
         _ptr(X, ctypes.c_uint16), _ptr(W_up, ctypes.c_uint16), _ptr(W_down, ctypes.c_uint16),
         _ptr(b_up if bias else None, ctypes.c_uint16), _ptr(b_down if bias else None, ctypes.c_uint16),
-        _ptr(r, ctypes.c_int64), R,
+        _ptr(Rb, ctypes.c_uint16), _ptr(lg, ctypes.c_uint16), _ptr(lb, ctypes.c_uint16), eps, w_layout,
+        _ptr(r, ctypes.c_int64), NR,
         _ptr(H, ctypes.c_uint16), _ptr(Yx, ctypes.c_double), _ptr(Y, ctypes.c_uint16))
     if rc != 0:
         raise ValueError("oracle_mlp_rows rejected its arguments")

@@ -12,10 +12,17 @@
  *   P[m,j]  = sum_k X[m,k] * W_up[k,j]  (+ b_up[j])                      j < F_up
  *   gelu    : H~[m,j] = gelu(P[m,j])                                     F_up = F
  *   none    : H~[m,j] = P[m,j]                                           F_up = F
+ *   gelu_sigmoid / silu : H~ = P * sigmoid(1.702 P) / P * sigmoid(P)     F_up = F
  *   geglu   : H~[m,j] = P[m,j] * gelu_erf(P[m,F+j])                      F_up = 2F
  *   H[m,j]  = round_to_nearest_even_dt(H~[m,j])        (the single rounding of H)
- *   Yx[m,n] = sum_j H[m,j] * W_down[j,n]  (+ b_down[n])
+ *   Yx[m,n] = sum_j H[m,j] * W_down[j,n]  (+ b_down[n])  (+ R[m,n])
  *   Y[m,n]  = round_to_nearest_even_dt(Yx[m,n])
+ *
+ * Options (oracle_mlp_rows_ex): a LayerNorm of each row of X before the up
+ * projection, X' = round_dt((x - mean) / sqrt(var + eps) * gamma + beta) with the
+ * mean and the biased variance over D in float64 (the GEMM reads 16-bit operands);
+ * a residual R added before the final rounding; weights given in PyTorch
+ * nn.Linear order ([out][in]) instead of [in][out].
  *
  * Sources on the pages:
  *   - "SDXL as a requirements inventory", section 1.3 (FeedForward): one
@@ -28,6 +35,11 @@
  *     up GEMM, GELU, down GEMM; its "ISA review" section computes GELU with tanh.
  *   - "The software stack", section 2.3: the accumulator is a resident format and
  *     never a memory word; outputs are written in the 16-bit I/O format.
+ *   - "SDXL as a requirements inventory", section 1.3 (BasicTransformerBlock): the
+ *     feed-forward is applied as x = ff(norm(x)) + x, a LayerNorm before it and the
+ *     residual after it; section 9.3: KohakuTPU's geglu lowers the sigmoid GELU
+ *     x * sigmoid(1.702 x); section 1.3 (timestep embedding): Linear -> SiLU -> Linear;
+ *     section 1.4: Linear weights are stored [out][in].
  *
  * Readings where the pages are silent (stated once more in the design notes):
  *   - tanh GELU uses the published constants sqrt(2/pi) and 0.044715
@@ -52,6 +64,8 @@
 #define KTO_GELU_TANH 1
 #define KTO_GEGLU 2
 #define KTO_NONE 3 /* no activation: H~ = P (two chained linear layers) */
+#define KTO_GELU_SIGMOID 4 /* x * sigmoid(1.702 x) */
+#define KTO_SILU 5         /* x * sigmoid(x) */
 
 /* ------------------------------------------------------------------------ */
 /* fp16 / bf16 codecs, written from the bit formats.                         */
@@ -164,9 +178,31 @@ double oracle_gelu_tanh(double z) {
     return z / (1.0 + exp(-2.0 * u));
 }
 
+/* sigmoid-weighted forms: z * sigmoid(a z) = z / (1 + exp(-a z)) */
+double oracle_gelu_sigmoid(double z) { return z / (1.0 + exp(-1.702 * z)); }
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
 void oracle_gelu_vec(const double* z, double* out, int64_t n, int form) {
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = (form == KTO_GELU_TANH) ? oracle_gelu_tanh(z[i]) : oracle_gelu_erf(z[i]);
+    for (int64_t i = 0; i < n; ++i) {
+        if (form == KTO_GELU_TANH) out[i] = oracle_gelu_tanh(z[i]);
+        else if (form == KTO_GELU_SIGMOID) out[i] = oracle_gelu_sigmoid(z[i]);
+        else if (form == KTO_SILU) out[i] = oracle_silu(z[i]);
+        else out[i] = oracle_gelu_erf(z[i]);
+    }
+}
+
+/* LayerNorm of one row, float64: mean, biased variance (divide by D), then
+ * (x - mean) / sqrt(var + eps) * gamma + beta. */
+void oracle_layernorm_row(const double* x, const double* gamma, const double* beta, double eps,
+                          double* out, int64_t D) {
+    double mean = 0.0;
+    for (int64_t k = 0; k < D; ++k) mean += x[k];
+    mean /= (double)D;
+    double var = 0.0;
+    for (int64_t k = 0; k < D; ++k) var += (x[k] - mean) * (x[k] - mean);
+    var /= (double)D;
+    double inv = 1.0 / sqrt(var + eps);
+    for (int64_t k = 0; k < D; ++k) out[k] = (x[k] - mean) * inv * gamma[k] + beta[k];
 }
 
 /* ------------------------------------------------------------------------ */
@@ -205,6 +241,10 @@ static void activation_row(const double* p, double* h, int64_t F, int act) {
         for (int64_t j = 0; j < F; ++j) h[j] = oracle_gelu_tanh(p[j]);
     } else if (act == KTO_NONE) {
         for (int64_t j = 0; j < F; ++j) h[j] = p[j];
+    } else if (act == KTO_GELU_SIGMOID) {
+        for (int64_t j = 0; j < F; ++j) h[j] = oracle_gelu_sigmoid(p[j]);
+    } else if (act == KTO_SILU) {
+        for (int64_t j = 0; j < F; ++j) h[j] = oracle_silu(p[j]);
     } else {
         for (int64_t j = 0; j < F; ++j) h[j] = oracle_gelu_erf(p[j]);
     }
@@ -223,13 +263,16 @@ void oracle_activation(const double* P, double* Hx, int64_t M, int64_t F, int ac
 /* may be NULL).  Returns 0, or -1 on a bad argument / allocation failure.    */
 /* ------------------------------------------------------------------------ */
 
-int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias,
-                    const uint16_t* X, const uint16_t* W_up, const uint16_t* W_down,
-                    const uint16_t* b_up, const uint16_t* b_down,
-                    const int64_t* rows, int64_t nrows,
-                    uint16_t* H_out, double* Yx_out, uint16_t* Y_out) {
+int oracle_mlp_rows_ex(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias,
+                       const uint16_t* X, const uint16_t* W_up, const uint16_t* W_down,
+                       const uint16_t* b_up, const uint16_t* b_down,
+                       const uint16_t* R, const uint16_t* ln_gamma, const uint16_t* ln_beta,
+                       double ln_eps, int w_layout,
+                       const int64_t* rows, int64_t nrows,
+                       uint16_t* H_out, double* Yx_out, uint16_t* Y_out) {
     if (M < 1 || D < 1 || F < 1 || nrows < 0) return -1;
-    if (act < 0 || act > 3 || (dtype != KTO_F16 && dtype != KTO_BF16)) return -1;
+    if (act < 0 || act > 5 || (dtype != KTO_F16 && dtype != KTO_BF16)) return -1;
+    if ((ln_gamma == NULL) != (ln_beta == NULL) || (w_layout != 0 && w_layout != 1)) return -1;
     if (rows == NULL) nrows = M;
     for (int64_t i = 0; rows && i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= M) return -1;
@@ -243,8 +286,28 @@ int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bia
         free(wu); free(wd); free(bu); free(bd);
         return -1;
     }
-    oracle_decode(W_up, wu, D * Fup, dtype);
-    oracle_decode(W_down, wd, F * D, dtype);
+    if (w_layout == 0) {
+        oracle_decode(W_up, wu, D * Fup, dtype);
+        oracle_decode(W_down, wd, F * D, dtype);
+    } else {
+        /* [out][in] storage: W_up is [F_up][D], W_down is [D][F]; transpose exactly */
+        for (int64_t j = 0; j < Fup; ++j)
+            for (int64_t k = 0; k < D; ++k) wu[k * Fup + j] = decode(W_up[j * D + k], dtype);
+        for (int64_t n = 0; n < D; ++n)
+            for (int64_t j = 0; j < F; ++j) wd[j * D + n] = decode(W_down[n * F + j], dtype);
+    }
+    double* lg = NULL;
+    double* lb = NULL;
+    if (ln_gamma) {
+        lg = (double*)malloc(sizeof(double) * (size_t)D);
+        lb = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!lg || !lb) {
+            free(wu); free(wd); free(bu); free(bd); free(lg); free(lb);
+            return -1;
+        }
+        oracle_decode(ln_gamma, lg, D, dtype);
+        oracle_decode(ln_beta, lb, D, dtype);
+    }
     if (bias) {
         oracle_decode(b_up, bu, Fup, dtype);
         oracle_decode(b_down, bd, D, dtype);
@@ -258,7 +321,8 @@ int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bia
         double* hx = (double*)malloc(sizeof(double) * (size_t)F);
         double* h = (double*)malloc(sizeof(double) * (size_t)F);
         double* y = (double*)malloc(sizeof(double) * (size_t)D);
-        if (!x || !p || !hx || !h || !y) {
+        double* xn = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!x || !p || !hx || !h || !y || !xn) {
 #pragma omp atomic write
             failed = 1;
         } else {
@@ -267,6 +331,11 @@ int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bia
                 int64_t m = rows ? rows[i] : i;
                 /* step 1: the row of X, exactly, in float64 */
                 oracle_decode(X + m * D, x, D, dtype);
+                if (lg) {
+                    /* optional prologue: LayerNorm, rounded once to the I/O dtype */
+                    oracle_layernorm_row(x, lg, lb, ln_eps, xn, D);
+                    for (int64_t k = 0; k < D; ++k) x[k] = decode(encode(xn[k], dtype), dtype);
+                }
                 /* step 2: up projection (+ b_up) */
                 linear_row(x, wu, bias ? bu : NULL, p, D, Fup);
                 /* step 3: activation (GEGLU: value * gelu_erf(gate)) */
@@ -279,16 +348,28 @@ int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bia
                 }
                 /* step 5: down projection (+ b_down) from the rounded H */
                 linear_row(h, wd, bias ? bd : NULL, y, F, D);
+                /* optional residual, added before the one rounding of Y */
+                if (R)
+                    for (int64_t n = 0; n < D; ++n) y[n] += decode(R[m * D + n], dtype);
                 for (int64_t n = 0; n < D; ++n) {
                     if (Yx_out) Yx_out[i * D + n] = y[n];
                     if (Y_out) Y_out[i * D + n] = encode(y[n], dtype);
                 }
             }
         }
-        free(x); free(p); free(hx); free(h); free(y);
+        free(x); free(p); free(hx); free(h); free(y); free(xn);
     }
-    free(wu); free(wd); free(bu); free(bd);
+    free(wu); free(wd); free(bu); free(bd); free(lg); free(lb);
     return failed ? -1 : 0;
+}
+
+int oracle_mlp_rows(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias,
+                    const uint16_t* X, const uint16_t* W_up, const uint16_t* W_down,
+                    const uint16_t* b_up, const uint16_t* b_down,
+                    const int64_t* rows, int64_t nrows,
+                    uint16_t* H_out, double* Yx_out, uint16_t* Y_out) {
+    return oracle_mlp_rows_ex(M, D, F, act, dtype, bias, X, W_up, W_down, b_up, b_down, NULL, NULL, NULL,
+                              0.0, 0, rows, nrows, H_out, Yx_out, Y_out);
 }
 
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */

@@ -14,7 +14,12 @@ half, a double rounding -- fails at least one test here:
   inventory", sections 1.3 and 9.3);
 * the whole MLP: a pure-Python brute force with mpmath activations and
   library / brute-force rounding on tiny shapes, W_down = I, one-hot W_up and
-  row subsets.
+  row subsets;
+* the options of a transformer block's feed-forward ("SDXL as a requirements
+  inventory", sections 1.3, 1.4, 3 and 9.3): the sigmoid GELU x*sigmoid(1.702 x)
+  and SiLU against mpmath, torch's float64 silu and their odd-part identity;
+  LayerNorm against a hand-worked row and torch's float64 layer_norm; the residual
+  and the [out][in] weight order against the brute force fed [in][out] copies.
 """
 import math
 import struct
@@ -186,6 +191,51 @@ def test_gelu_odd_part_identity(form):
     assert oracle.gelu(np.array([0.0]), form)[0] == 0.0
 
 
+def _gelu_sigmoid_mp(z):
+    z = mpmath.mpf(z)
+    return z / (1 + mpmath.exp(-mpmath.mpf("1.702") * z))
+
+
+def _silu_mp(z):
+    z = mpmath.mpf(z)
+    return z / (1 + mpmath.exp(-z))
+
+
+@pytest.mark.parametrize("form,ref", [(oracle.GELU_SIGMOID, _gelu_sigmoid_mp), (oracle.SILU, _silu_mp)])
+def test_sigmoid_forms_match_definition_at_high_precision(form, ref):
+    got = oracle.gelu(np.array(POINTS), form)
+    for z, g in zip(POINTS, got):
+        r = float(ref(z))
+        if r == 0.0:
+            assert g == 0.0
+        else:
+            assert abs(g - r) <= 1e-13 * abs(r) + 1e-300, (z, g, r)
+
+
+def test_silu_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    z = np.linspace(-30, 30, 6001)
+    ref = torch.nn.functional.silu(torch.from_numpy(z)).numpy()
+    assert np.allclose(oracle.gelu(z, oracle.SILU), ref, rtol=1e-14, atol=1e-300)
+
+
+@pytest.mark.parametrize("form", [oracle.GELU_SIGMOID, oracle.SILU])
+def test_sigmoid_forms_odd_part_identity(form):
+    z = np.linspace(-8, 8, 4001)
+    d = oracle.gelu(z, form) - oracle.gelu(-z, form)
+    assert np.max(np.abs(d - z)) < 1e-14 * 8
+    assert oracle.gelu(np.array([0.0]), form)[0] == 0.0
+
+
+def test_sigmoid_gelu_is_scaled_silu_and_near_the_erf_form():
+    z = np.linspace(-6, 6, 12001)
+    sg = oracle.gelu(z, oracle.GELU_SIGMOID)
+    assert np.allclose(sg, oracle.gelu(1.702 * z, oracle.SILU) / 1.702, rtol=1e-14, atol=1e-15)
+    # the approximation is good to about 2e-2 and no better: it is a different function
+    d = np.max(np.abs(sg - oracle.gelu(z, oracle.GELU_ERF)))
+    assert 1.5e-2 < d < 2.5e-2
+
+
 def test_gelu_forms_are_distinguishable():
     z = np.linspace(-6, 6, 120001)
     d = oracle.gelu(z, oracle.GELU_ERF) - oracle.gelu(z, oracle.GELU_TANH)
@@ -307,9 +357,27 @@ def _dec(b, dt):
     return _bf16_values_by_bits(b)
 
 
-def _brute_mlp(X, Wu, Wd, bu, bd, act, dt):
+def _brute_layernorm_row(row, g, b, eps):
+    D = len(row)
+    mean = 0.0
+    for v in row:
+        mean = mean + v
+    mean = mean / D
+    var = 0.0
+    for v in row:
+        var = var + (v - mean) * (v - mean)
+    var = var / D
+    inv = 1.0 / math.sqrt(var + eps)
+    return [(row[k] - mean) * inv * g[k] + b[k] for k in range(D)]
+
+
+def _brute_mlp(X, Wu, Wd, bu, bd, act, dt, R=None, ln=None):
     """Pure-Python MLP: scalar loops, mpmath activations, independent rounding."""
     x, wu, wd = _dec(X, dt), _dec(Wu, dt), _dec(Wd, dt)
+    if ln is not None:
+        g, b = _dec(ln[0], dt), _dec(ln[1], dt)
+        x = np.array([[float(_dec(_round_bits(v, dt), dt)) for v in _brute_layernorm_row(list(r), g, b, ln[2])]
+                      for r in x])
     M, D = x.shape
     F = wd.shape[0]
     Fup = wu.shape[1]
@@ -334,6 +402,10 @@ def _brute_mlp(X, Wu, Wd, bu, bd, act, dt):
                 v = float(_gelu_tanh_mp(p[j]))
             elif act == oracle.NONE:
                 v = p[j]
+            elif act == oracle.GELU_SIGMOID:
+                v = float(_gelu_sigmoid_mp(p[j]))
+            elif act == oracle.SILU:
+                v = float(_silu_mp(p[j]))
             else:
                 v = float(_gelu_erf_mp(p[j]))
             H[m, j] = _round_bits(v, dt)
@@ -344,6 +416,8 @@ def _brute_mlp(X, Wu, Wd, bu, bd, act, dt):
                 s = s + h[j] * wd[j, n]
             if bd_ is not None:
                 s = s + bd_[n]
+            if R is not None:
+                s = s + float(_dec(R[m, n], dt))
             Yx[m, n] = s
     return H, Yx
 
@@ -429,6 +503,99 @@ def test_mlp_row_subset_equals_full():
     assert np.array_equal(Hs, H[rows]) and np.array_equal(Yxs, Yx[rows]) and np.array_equal(Ys, Y[rows])
 
 
+# --------------------------------------------------------------------------
+# LayerNorm, residual and [out][in] weights
+# --------------------------------------------------------------------------
+
+def test_layernorm_hand_worked_row():
+    # x = 1..4: mean 2.5, biased variance 1.25, so (x - 2.5) / sqrt(1.25) = +-3/sqrt(5), +-1/sqrt(5).
+    # An unbiased (D - 1) divisor would give variance 5/3 and fail this.
+    out = oracle.layernorm(np.array([[1.0, 2.0, 3.0, 4.0]]), np.ones(4), np.zeros(4), 0.0)[0]
+    s = math.sqrt(5.0)
+    assert np.allclose(out, [-3 / s, -1 / s, 1 / s, 3 / s], rtol=0, atol=1e-15)
+    # gamma scales and beta shifts after the normalisation
+    g = np.array([2.0, -1.0, 0.5, 3.0])
+    b = np.array([0.25, 0.0, -1.0, 7.0])
+    out2 = oracle.layernorm(np.array([[1.0, 2.0, 3.0, 4.0]]), g, b, 0.0)[0]
+    assert np.allclose(out2, out * g + b, rtol=0, atol=1e-14)
+    # eps enters under the square root: a constant row normalises to beta
+    out3 = oracle.layernorm(np.array([[5.0, 5.0, 5.0, 5.0]]), g, b, 1e-5)[0]
+    assert np.array_equal(out3, b)
+
+
+def test_layernorm_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((7, 640)) * 3 + 1.5
+    g = rng.standard_normal(640)
+    b = rng.standard_normal(640)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (640,), torch.from_numpy(g),
+                                         torch.from_numpy(b), eps=1e-5).numpy()
+    assert np.allclose(oracle.layernorm(x, g, b, 1e-5), ref, rtol=1e-12, atol=1e-12)
+
+
+OPT_CASES = [
+    # M, D, F, act, dt, bias, residual, layernorm, w_layout
+    (4, 16, 8, wl.ACT_GELU_SIGMOID, wl.DT_F16, True, True, True, 1),
+    (3, 8, 8, wl.ACT_SILU, wl.DT_BF16, False, True, False, 0),
+    (2, 16, 8, wl.ACT_GEGLU, wl.DT_BF16, True, True, True, 1),
+    (3, 24, 8, wl.ACT_GELU_ERF, wl.DT_F16, False, False, True, 0),
+    (2, 8, 16, wl.ACT_GELU_TANH, wl.DT_F16, True, False, False, 1),
+]
+
+
+@pytest.mark.parametrize("M,D,F,act,dt,bias,res,ln,layout", OPT_CASES)
+def test_mlp_options_match_pure_python_bruteforce(M, D, F, act, dt, bias, res, ln, layout):
+    w = wl.custom(M, D, F, act, dt, bias, seed=200 + M + D + F)
+    t = wl.generate(w, residual=res, layernorm=ln)
+    b = {k: wl.bits(v) for k, v in t.items()}
+    lnarg = (b["ln_gamma"], b["ln_beta"], 1e-5) if ln else None
+    Wu, Wd = b["W_up"], b["W_down"]
+    if layout == 1:
+        Wu_o, Wd_o = np.ascontiguousarray(Wu.T), np.ascontiguousarray(Wd.T)
+    else:
+        Wu_o, Wd_o = Wu, Wd
+    H, Yx, Y = oracle.mlp(b["X"], Wu_o, Wd_o, b.get("b_up"), b.get("b_down"), act=act, dtype=dt,
+                          R=b.get("R"), ln=lnarg, w_layout=layout)
+    Hb, Yxb = _brute_mlp(b["X"], Wu, Wd, b.get("b_up"), b.get("b_down"), act, dt, R=b.get("R"), ln=lnarg)
+    assert np.array_equal(H, Hb)
+    assert np.allclose(Yx, Yxb, rtol=1e-13, atol=1e-15)
+    assert np.array_equal(Y, oracle.encode(Yx, dt))
+
+
+def test_weight_order_is_a_pure_transpose():
+    w = wl.custom(9, 32, 48, wl.ACT_GEGLU, wl.DT_BF16, True, seed=22)
+    t = wl.generate(w)
+    b = {k: wl.bits(v) for k, v in t.items()}
+    args = (b.get("b_up"), b.get("b_down"))
+    ref = oracle.mlp(b["X"], b["W_up"], b["W_down"], *args, act=w.act, dtype=w.dtype)
+    got = oracle.mlp(b["X"], np.ascontiguousarray(b["W_up"].T), np.ascontiguousarray(b["W_down"].T), *args,
+                     act=w.act, dtype=w.dtype, w_layout=1)
+    for r, g in zip(ref, got):
+        assert np.array_equal(r, g)
+    # the same arrays read in the other order are a different (wrong) problem
+    sq = wl.custom(9, 32, 32, wl.ACT_GELU_ERF, wl.DT_F16, False, seed=23)
+    ts = {k: wl.bits(v) for k, v in wl.generate(sq).items()}
+    a = oracle.mlp(ts["X"], ts["W_up"], ts["W_down"], act=sq.act, dtype=sq.dtype)
+    c = oracle.mlp(ts["X"], ts["W_up"], ts["W_down"], act=sq.act, dtype=sq.dtype, w_layout=1)
+    assert not np.array_equal(a[0], c[0])
+
+
+def test_residual_is_added_once_before_the_rounding():
+    w = wl.custom(6, 16, 32, wl.ACT_GELU_TANH, wl.DT_F16, False, seed=24)
+    t = wl.generate(w, residual=True)
+    b = {k: wl.bits(v) for k, v in t.items()}
+    H0, Yx0, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], act=w.act, dtype=w.dtype)
+    H1, Yx1, Y1 = oracle.mlp(b["X"], b["W_up"], b["W_down"], act=w.act, dtype=w.dtype, R=b["R"])
+    assert np.array_equal(H0, H1)
+    r = _dec(b["R"], w.dtype)
+    assert np.allclose(Yx1, Yx0 + r, rtol=1e-15, atol=0)
+    # a residual that cancels the block's output leaves only the rounding residue
+    Rneg = oracle.encode(-Yx0, w.dtype)
+    _, Yx2, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], act=w.act, dtype=w.dtype, R=Rneg)
+    assert np.max(np.abs(Yx2)) <= np.max(np.abs(Yx0)) * 2.0 ** -11
+
+
 def test_mlp_rejects_bad_arguments():
     X = np.zeros((2, 8), dtype=np.uint16)
     with pytest.raises(ValueError):
@@ -436,3 +603,12 @@ def test_mlp_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.mlp(X, np.zeros((8, 8), np.uint16), np.zeros((8, 8), np.uint16),
                    np.zeros(8, np.uint16), None, act=0, dtype=0)
+    W = np.zeros((8, 8), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.mlp(X, W, W, act=6, dtype=0)
+    with pytest.raises(ValueError):
+        oracle.mlp(X, W, W, act=0, dtype=0, R=np.zeros((3, 8), np.uint16))
+    with pytest.raises(ValueError):
+        oracle.mlp(X, W, W, act=0, dtype=0, ln=(np.zeros(7, np.uint16), np.zeros(8, np.uint16), 1e-5))
+    with pytest.raises(ValueError):
+        oracle.mlp(X, np.zeros((8, 16), np.uint16), np.zeros((8, 8), np.uint16), act=2, dtype=0, w_layout=1)

@@ -18,6 +18,11 @@ Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draw float32 ``randn`` in
 the order X, W_up, [b_up], W_down, [b_down]; scale by sqrt(variance) with weight
 variance 1/fan_in and bias variance 0.02; cast to the I/O dtype (round to
 nearest even).  The same rounded tensors go to the GPU and to the oracle.
+Options of the transformer block draw after those, in the order R (the
+residual, variance 1, like the residual stream X), LayerNorm gamma
+(1 + 0.2 * randn) and beta (0.1 * randn); they never change the tensors above.
+Weights are drawn [in][out]; ``torch_order`` returns the [out][in] copies that
+PyTorch's nn.Linear stores.
 """
 from __future__ import annotations
 
@@ -27,9 +32,10 @@ import math
 import numpy as np
 import torch
 
-ACT_GELU_ERF, ACT_GELU_TANH, ACT_GEGLU, ACT_NONE = 0, 1, 2, 3
+ACT_GELU_ERF, ACT_GELU_TANH, ACT_GEGLU, ACT_NONE, ACT_GELU_SIGMOID, ACT_SILU = 0, 1, 2, 3, 4, 5
 DT_F16, DT_BF16 = 0, 1
-ACT_NAMES = {ACT_GELU_ERF: "gelu_erf", ACT_GELU_TANH: "gelu_tanh", ACT_GEGLU: "geglu", ACT_NONE: "none"}
+ACT_NAMES = {ACT_GELU_ERF: "gelu_erf", ACT_GELU_TANH: "gelu_tanh", ACT_GEGLU: "geglu", ACT_NONE: "none",
+             ACT_GELU_SIGMOID: "gelu_sigmoid", ACT_SILU: "silu"}
 DT_NAMES = {DT_F16: "f16", DT_BF16: "bf16"}
 TORCH_DTYPES = {DT_F16: torch.float16, DT_BF16: torch.bfloat16}
 
@@ -98,11 +104,12 @@ def custom(M: int, D: int, F: int, act: int, dtype: int, bias: bool, seed: int,
     return Workload(name, 1, M, D, F, act, dtype, bias, seed)
 
 
-def generate(w: Workload) -> dict:
+def generate(w: Workload, residual: bool = False, layernorm: bool = False) -> dict:
     """Seeded CPU tensors for one workload, already rounded to the I/O dtype.
 
     Returns a dict with X[M,D], W_up[D,F_up], W_down[F,D] and, when ``w.bias``,
-    b_up[F_up], b_down[D] (torch tensors on the CPU).
+    b_up[F_up], b_down[D] (torch tensors on the CPU); with ``residual`` also R[M,D],
+    with ``layernorm`` also ln_gamma[D] and ln_beta[D].
     """
     g = torch.Generator("cpu").manual_seed(w.seed)
     dt = TORCH_DTYPES[w.dtype]
@@ -116,6 +123,19 @@ def generate(w: Workload) -> dict:
     out["W_down"] = draw((w.F, w.D), 1.0 / w.F)
     if w.bias:
         out["b_down"] = draw((w.D,), 0.02)
+    if residual:
+        out["R"] = draw((w.M, w.D), 1.0)
+    if layernorm:
+        out["ln_gamma"] = (1.0 + 0.2 * torch.randn(w.D, generator=g, dtype=torch.float32)).to(dt)
+        out["ln_beta"] = draw((w.D,), 0.01)
+    return out
+
+
+def torch_order(t: dict) -> dict:
+    """The same tensors with both weights in [out][in] order (contiguous copies)."""
+    out = dict(t)
+    out["W_up"] = t["W_up"].t().contiguous()
+    out["W_down"] = t["W_down"].t().contiguous()
     return out
 
 
