@@ -14,6 +14,14 @@
  *     then the projection back ("SDXL as a requirements inventory",
  *     section 1.3 FeedForward; section 9.3 for the erf form and the half order).
  *
+ * Options of the transformer block around the feed-forward (kt_mlp_plan_ex /
+ * kt_mlp_run_ex), from "SDXL as a requirements inventory": a LayerNorm of X before
+ * the up projection and the residual add after the down projection (section 1.3,
+ * BasicTransformerBlock: x = ff(LayerNorm(x)) + x; section 3, rows 3 and 9-10); the
+ * sigmoid GELU x * sigmoid(1.702 x) (section 9.3) and SiLU (section 1.3, timestep
+ * embedding; section 3 row 4) as further activations; weights in PyTorch's
+ * nn.Linear order [out][in] (section 1.4; section 3 row 1).
+ *
  * Numerics: operands in the 16-bit I/O dtype, products accumulated in fp32 in
  * tensor memory, bias added to the fp32 accumulator, the activation evaluated
  * in fp32, and exactly ONE rounding (to nearest even) of H to the I/O dtype
@@ -45,14 +53,23 @@
 extern "C" {
 #endif
 
-#define KT_MLP_ABI_VERSION 1
+#define KT_MLP_ABI_VERSION 2
 
 typedef enum {
     KT_ACT_GELU_ERF = 0,  /* gelu(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2))                 */
     KT_ACT_GELU_TANH = 1, /* 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))                   */
     KT_ACT_GEGLU = 2,     /* P[:, :F] * gelu_erf(P[:, F:]), F_up = 2F                          */
-    KT_ACT_NONE = 3       /* no activation (two chained linear layers); checks the GEMMs alone */
+    KT_ACT_NONE = 3,      /* no activation (two chained linear layers); checks the GEMMs alone */
+    KT_ACT_GELU_SIGMOID = 4, /* z * sigmoid(1.702 z): the sigmoid approximation of GELU        */
+    KT_ACT_SILU = 5       /* z * sigmoid(z) (SiLU / swish)                                      */
 } kt_act;
+
+/* Memory order of W_up and W_down. */
+typedef enum {
+    KT_W_IN_OUT = 0, /* W_up[D][F_up], W_down[F][D]: the layer computes X . W               */
+    KT_W_OUT_IN = 1  /* W_up[F_up][D], W_down[D][F]: PyTorch nn.Linear order, X . W^T; GEGLU's
+                        value rows are W_up[0:F], its gate rows W_up[F:2F]                   */
+} kt_weight_layout;
 
 typedef enum { KT_F16 = 0, KT_BF16 = 1 } kt_dtype;
 
@@ -90,7 +107,47 @@ typedef struct {
     kt_gemm_plan_info up;      /* X[M,D] . W_up[D,F_up] with the fused epilogue -> H[M,F] */
     kt_gemm_plan_info down;    /* H[M,F] . W_down[F,D] (+ b_down) -> Y[M,D]               */
     int64_t workspace_bytes;   /* device bytes the plan owns (H, split-K partials, flags) */
+    int32_t residual, layernorm, weight_layout;  /* the kt_mlp_options of the plan (0 for kt_mlp_plan) */
+    float ln_eps;
 } kt_plan_info;
+
+/*
+ * Problem description for kt_mlp_plan_ex.  Zero-initialise it and set the fields;
+ * with residual = layernorm = 0 and weight_layout = KT_W_IN_OUT it describes the same
+ * problem as kt_mlp_plan(M, D, F, act, dtype, bias).
+ */
+typedef struct {
+    int64_t M, D, F;        /* rows (tokens), model dim, hidden dim                          */
+    int32_t act;            /* kt_act                                                        */
+    int32_t dtype;          /* kt_dtype: the I/O dtype of every tensor                       */
+    int32_t bias;           /* 1: b_up[F_up] and b_down[D]                                   */
+    int32_t residual;       /* 1: Y = R + FF(.), R[M][D] added to the fp32 result before the
+                               one rounding of Y                                             */
+    int32_t layernorm;      /* 1: the up projection reads LayerNorm(X) instead of X:
+                               (x - mean) / sqrt(var + ln_eps) * gamma + beta per row, mean
+                               and biased variance over D in fp32, rounded once to dtype     */
+    int32_t weight_layout;  /* kt_weight_layout                                              */
+    float ln_eps;           /* LayerNorm epsilon (> 0; PyTorch's default is 1e-5)            */
+} kt_mlp_options;
+
+/*
+ * Device tensors of one kt_mlp_run_ex call (row-major, contiguous, 16-byte aligned,
+ * the plan's dtype).  Pointers the plan does not use must be NULL.
+ */
+typedef struct {
+    const void* X;          /* [M][D]                                                        */
+    const void* W_up;       /* [D][F_up] (KT_W_IN_OUT) or [F_up][D] (KT_W_OUT_IN)            */
+    const void* W_down;     /* [F][D]    (KT_W_IN_OUT) or [D][F]    (KT_W_OUT_IN)            */
+    const void* b_up;       /* [F_up], iff bias                                              */
+    const void* b_down;     /* [D], iff bias                                                 */
+    const void* R;          /* [M][D], iff residual; may be X itself, and may equal Y
+                               (in-place update of a residual stream)                        */
+    const void* ln_gamma;   /* [D], iff layernorm                                            */
+    const void* ln_beta;    /* [D], iff layernorm                                            */
+    void* Y;                /* [M][D]; may equal X and / or R, must not partially overlap them */
+    void* H_out;            /* [M][F] to receive the rounded intermediate, or NULL (the plan's
+                               workspace is used)                                            */
+} kt_mlp_tensors;
 
 /*
  * kt_mlp_plan -- validate the problem, choose tiles / pipeline depth / split-K
@@ -118,6 +175,35 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
  */
 kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                      const void* b_up, const void* b_down, void* Y, void* stream);
+
+/*
+ * kt_mlp_plan_ex -- kt_mlp_plan for a problem with the options of kt_mlp_options: a
+ * LayerNorm prologue, a residual add, the sigmoid GELU / SiLU activations and the
+ * [out][in] weight order.  A layernorm plan also owns a workspace Xn[M][D] for the
+ * normalised X.  Errors as kt_mlp_plan, plus INVALID for a flag outside {0, 1}, an
+ * unknown weight layout or ln_eps <= 0 (or not finite) with layernorm = 1.
+ */
+kt_status kt_mlp_plan_ex(const kt_mlp_options* options, kt_mlp_plan_t* out);
+
+/* kt_mlp_plan_info_ex -- kt_mlp_plan_info for a kt_mlp_options problem (host only). */
+kt_status kt_mlp_plan_info_ex(const kt_mlp_options* options, int num_sms, kt_plan_info* out);
+
+/*
+ * kt_mlp_run_ex -- enqueue the block on `stream`: with layernorm, a LayerNorm kernel
+ * writes Xn (one warp per row); the up GEMM (fused epilogue, programmatic dependent
+ * launch) writes H; the down GEMM adds b_down and R to the fp32 result, rounds once
+ * and writes Y.  Any plan may be run with it (a kt_mlp_plan plan takes the tensors
+ * of kt_mlp_run).  Asynchronous.  Errors: INVALID (null tensors, a pointer present or
+ * absent against the plan's options, misaligned pointer), CUDA (launch failed).
+ */
+kt_status kt_mlp_run_ex(kt_mlp_plan_t plan, const kt_mlp_tensors* tensors, void* stream);
+
+/*
+ * kt_mlp_run_ex_timed -- kt_mlp_run_ex with CUDA events around each kernel, no
+ * programmatic overlap between them; waits and writes the device times in ms to
+ * ms[0] (LayerNorm, 0 without it), ms[1] (up GEMM) and ms[2] (down GEMM).
+ */
+kt_status kt_mlp_run_ex_timed(kt_mlp_plan_t plan, const kt_mlp_tensors* tensors, void* stream, float* ms);
 
 /*
  * kt_mlp_run_with_h -- as kt_mlp_run, but the rounded intermediate H[M][F] is
@@ -197,7 +283,8 @@ kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_dow
 /*
  * kt_debug_activation -- evaluate the epilogue's fp32 activation elementwise on
  * device arrays: out[i] = gelu_erf(z[i]) / gelu_tanh(z[i]) / z[i] * gelu_erf(gate[i])
- * (GEGLU) / z[i] (none), for i < n, enqueued on `stream`.  The same device
+ * (GEGLU) / z[i] (none) / gelu_sigmoid(z[i]) / silu(z[i]), for i < n, enqueued on
+ * `stream`.  The same device
  * functions as the fused epilogue; exposed so that their accuracy can be tested
  * against the oracle on their own.  gate is read only for GEGLU.
  */

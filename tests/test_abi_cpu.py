@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
     # and the binding wraps each of them under the same name
     assert set(names) <= set(kt_mlp.SIGNATURES)
-    assert lib.kt_mlp_abi_version() == 1
+    assert lib.kt_mlp_abi_version() == 2
 
 
 def test_plan_without_a_gpu_fails_cleanly(lib):
@@ -74,6 +74,43 @@ def test_null_handles_are_rejected(lib):
     assert lib.kt_mlp_status(None) == kt_mlp.KT_ERR_INVALID
     assert lib.kt_mlp_run(None, None, None, None, None, None, None, None) == kt_mlp.KT_ERR_INVALID
     assert lib.kt_mlp_debug_stall(None, 1, 10) == kt_mlp.KT_ERR_INVALID
+    t = kt_mlp.tensors(None, None, None, None)
+    assert lib.kt_mlp_run_ex(None, t, None) == kt_mlp.KT_ERR_INVALID
+    assert lib.kt_mlp_run_ex_timed(None, t, None, None) == kt_mlp.KT_ERR_INVALID
+    assert lib.kt_mlp_plan_ex(None, None) == kt_mlp.KT_ERR_INVALID
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(residual=2), kt_mlp.KT_ERR_INVALID),
+    (dict(layernorm=2), kt_mlp.KT_ERR_INVALID),
+    (dict(layernorm=1, ln_eps=0.0), kt_mlp.KT_ERR_INVALID),
+    (dict(layernorm=1, ln_eps=-1e-5), kt_mlp.KT_ERR_INVALID),
+    (dict(layernorm=1, ln_eps=float("inf")), kt_mlp.KT_ERR_INVALID),
+    (dict(weight_layout=2), kt_mlp.KT_ERR_INVALID),
+    (dict(act=6), kt_mlp.KT_ERR_INVALID),
+    (dict(D=60), kt_mlp.KT_ERR_UNSUPPORTED),
+])
+def test_option_errors(lib, kw, status):
+    base = dict(M=8, D=64, F=64, act=0, dtype=0, bias=0, residual=0, layernorm=0, weight_layout=0, ln_eps=1e-5)
+    base.update(kw)
+    o = kt_mlp.kt_mlp_options(**base)
+    with pytest.raises(kt_mlp.KtError) as e:
+        kt_mlp.kt_mlp_plan_info_ex(o, SMS)
+    assert e.value.status == status
+    assert kt_mlp.kt_last_error()
+
+
+def test_options_are_reported_and_default_to_the_plain_plan(lib):
+    w = wl.WORKLOADS["sdxl_l2"]
+    plain = kt_mlp.kt_mlp_plan_info(w.M, w.D, w.F, w.act, w.dtype, w.bias, SMS)
+    same = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(w.M, w.D, w.F, w.act, w.dtype, w.bias), SMS)
+    assert same == plain
+    assert (plain["residual"], plain["layernorm"], plain["weight_layout"]) == (0, 0, 0)
+    ex = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(w.M, w.D, w.F, w.act, w.dtype, w.bias, residual=True,
+                                                   layernorm=True, ln_eps=1e-6), SMS)
+    assert (ex["residual"], ex["layernorm"]) == (1, 1)
+    assert ex["ln_eps"] == pytest.approx(1e-6)
+    assert ex["workspace_bytes"] == plain["workspace_bytes"] + 2 * w.M * w.D  # the normalised X
 
 
 def _check_gemm(g, M, N, K):
@@ -111,6 +148,33 @@ def test_planner_invariants_on_every_workload(lib, name):
     assert info["up"]["split_k"] == 1  # the activation is not linear: no split of the up projection
     if w.act == wl.ACT_GEGLU:
         assert info["up"]["BN"] <= 256
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+@pytest.mark.parametrize("act", [wl.ACT_GELU_SIGMOID, wl.ACT_SILU, None])
+def test_planner_invariants_with_pytorch_order_weights(lib, name, act):
+    w = wl.WORKLOADS[name]
+    a = w.act if act is None else act
+    o = kt_mlp.options(w.M, w.D, w.F, a, w.dtype, w.bias, weight_layout=kt_mlp.KT_W_OUT_IN)
+    info = kt_mlp.kt_mlp_plan_info_ex(o, SMS)
+    _check_gemm(info["up"], w.M, w.F, w.D)
+    _check_gemm(info["down"], w.M, w.D, w.F)
+    assert info["weight_layout"] == kt_mlp.KT_W_OUT_IN
+
+
+def test_pytorch_order_weights_need_no_column_padding_in_shared_memory(lib):
+    # a K-major B tile holds exactly BN / pair rows; the N-major one pads the columns
+    # of each CTA's share to whole 64-column boxes
+    for M, D, F, act in [(729, 1152, 4304, 1), (2048, 1280, 5120, 2), (8192, 640, 2560, 2)]:
+        for layout in (0, 1):
+            g = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, 0, False, weight_layout=layout), SMS)["up"]
+            pair = g["BM"] // 128
+            n_b = 2 if act == 2 else 1
+            share = g["BN"] // pair
+            b_cols = share if layout == 1 else -(-share // 64) * 64
+            stage = 128 * g["BK"] * 2 + n_b * b_cols * g["BK"] * 2
+            reserve = 8 * 32 * 32 * 2 + 2048
+            assert g["smem_bytes"] == g["stages"] * stage + reserve
 
 
 @pytest.mark.parametrize("M", [1, 33, 127, 128, 129, 729, 1000, 4097])

@@ -213,7 +213,7 @@ def test_plan_reports_its_choice():
     assert re.search(r"up: (128|256)x\d+", desc) and re.search(r"down: (128|256)x\d+", desc)
 
 
-@pytest.mark.parametrize("act", [wl.ACT_GELU_ERF, wl.ACT_GELU_TANH, wl.ACT_GEGLU])
+@pytest.mark.parametrize("act", [wl.ACT_GELU_ERF, wl.ACT_GELU_TANH, wl.ACT_GEGLU, wl.ACT_GELU_SIGMOID, wl.ACT_SILU])
 def test_device_activation_accuracy(act):
     # the epilogue's fp32 activations against the float64 oracle on a dense grid:
     # relative error <= 2e-5, over 10x below half an fp16 ulp (2.4e-4)
@@ -227,6 +227,8 @@ def test_device_activation_accuracy(act):
     zz = z.double().numpy()
     if act == wl.ACT_GEGLU:
         ref = zz * oracle.gelu(g.double().numpy(), oracle.GELU_ERF)
+    elif act in (wl.ACT_GELU_SIGMOID, wl.ACT_SILU):
+        ref = oracle.gelu(zz, act)
     else:
         ref = oracle.gelu(zz, oracle.GELU_TANH if act == wl.ACT_GELU_TANH else oracle.GELU_ERF)
     big = np.abs(ref) > 1e-30

@@ -31,7 +31,9 @@ enum Epi : int {
     EPI_GELU_TANH = 1,  // H = round(gelu_tanh(acc + b))
     EPI_GEGLU = 2,      // H = round((acc_v + b_v) * gelu_erf(acc_g + b_g))
     EPI_NONE = 3,       // H = round(acc + b)
-    EPI_DOWN = 4        // Y = round(sum_s partial_s + b)   (split-K when SK > 1)
+    EPI_DOWN = 4,       // Y = round(sum_s partial_s + b [+ R])   (split-K when SK > 1)
+    EPI_GELU_SIGMOID = 5,  // H = round(z * sigmoid(1.702 z)),  z = acc + b
+    EPI_SILU = 6           // H = round(z * sigmoid(z))
 };
 
 // Device error word values (first writer wins).
@@ -52,6 +54,7 @@ struct GemmConfig {
     int pair;              // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile (cta_group::2)
     int bk;                // k-block depth per pipeline stage: 64 or 128
     int cluster_sk;        // 1: split-K partials reduced inside a cluster (distributed smem)
+    int b_kmajor;          // 1: the weight is stored [N][K] (PyTorch order) and loaded K-major
     double useful_over_padded;
     double est_us;
 };
@@ -62,15 +65,23 @@ struct PlanChoice {
 
 // Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
 // 128 x 64) + n_b B tiles holding its share of the columns (BN, or BN/2 in a CTA
-// pair) in 64-column boxes of bk rows.
-inline int stage_bytes(int BN, int n_b, int pair, int bk) {
-    int chunks = (BN / pair + 63) / 64;
-    return kBM * bk * 2 + n_b * chunks * 64 * bk * 2;
+// pair): in 64-column boxes of bk rows for a [K][N] weight (N-major, padded to 64
+// columns), or in bk/64 atoms of (share) rows x 64 for a [N][K] weight (K-major).
+inline int b_tile_bytes(int BN, int pair, int bk, int b_kmajor) {
+    if (b_kmajor) return (BN / pair) * bk * 2;
+    return (BN / pair + 63) / 64 * 64 * bk * 2;
+}
+inline int stage_bytes(int BN, int n_b, int pair, int bk, int b_kmajor = 0) {
+    return kBM * bk * 2 + n_b * b_tile_bytes(BN, pair, bk, b_kmajor);
 }
 
 // Planner (host only, no GPU): returns KT_OK and fills `out`, or an error status.
+// w_layout: KT_W_IN_OUT ([in][out] weights, N-major B) or KT_W_OUT_IN ([out][in], K-major B).
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why, bool allow_cluster_sk = true);
+                      const char** why, bool allow_cluster_sk = true, int w_layout = KT_W_IN_OUT);
+
+// The up projection's epilogue kind for a kt_act.
+int up_epilogue(int act);
 
 // Fill the public description from a choice.
 void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* out);
@@ -83,12 +94,15 @@ struct GemmParams {
     int bk;                  // k-block depth per stage (64 or 128)
     int cluster_sk;          // 1: the split_k CTAs of a tile form a cluster and reduce on chip
     int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
-    int gate_col;            // GEGLU: first gate column in W_up (= F); else 0
+    int gate_col;            // GEGLU: first gate column (row, K-major) of W_up (= F); else 0
+    int b_kmajor;            // 1: B is [N][K] in memory, loaded in 64-deep K-major atoms
+    uint32_t b_atom_bytes;   // K-major B: bytes of one 64-deep atom of this CTA's column share
     uint32_t idesc;          // tcgen05 instruction descriptor
     uint32_t stage_bytes, a_bytes, b_bytes;  // per stage / A tile / one B operand tile
     uint32_t acc_bufs;       // accumulator buffers in TMEM (1 or 2)
     uint32_t gate_acc_off;   // TMEM column offset of the gate accumulator (GEGLU)
     const void* bias;        // b_up (GEGLU: value then gate halves) / b_down / null
+    const void* residual;    // down projection: R[M][N] added before the rounding, or null
     float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32
     int* counters;           // split-K: [tiles_m*tiles_n] arrival counters (zero between runs)
     int* error;              // device error word
@@ -126,6 +140,11 @@ constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const void* H, const void* W_down,
                             const void* b_down, void* Y, void* stream, const char** why);
 
+// LayerNorm of each row of X[M][D] into Xn[M][D] (kt_mlp_kernels.cu): fp32 statistics,
+// biased variance, one rounding to the dtype.  Launched as a programmatic dependent.
+kt_status launch_layernorm(int dtype, const void* X, const void* gamma, const void* beta, float eps, void* Xn,
+                           int64_t M, int64_t D, void* stream, const char** why);
+
 // Elementwise activation test kernel (kt_mlp_kernels.cu).
 kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
                             const char** why);
@@ -144,7 +163,7 @@ bool encode_tmap(void* tmap128, const void* base, int dtype, uint64_t rows, uint
                  uint32_t box_rows, uint32_t box_cols, int swizzle_bytes, const char** why);
 
 // tcgen05 instruction descriptor for kind::f16 with fp32 accumulation, A K-major,
-// B MN-major, M = m (128, or 256 for a CTA pair), N = n.
-uint32_t make_idesc(int dtype, int n, int m);
+// B MN-major (b_kmajor = 0) or K-major (1), M = m (128, or 256 for a CTA pair), N = n.
+uint32_t make_idesc(int dtype, int n, int m, int b_kmajor = 0);
 
 }  // namespace kt

@@ -1,12 +1,13 @@
 // kt_mlp_abi.cpp -- the extern "C" boundary: validation, plan ownership, launches.
 //
-// A plan binds a problem (M, D, F, act, dtype, bias) to the device current at
-// plan time, holds the planner's choice and owns the device workspace: the
-// intermediate H[M][F], the split-K fp32 partials, the split-K tile counters
-// and the device error word.  kt_mlp_run encodes (and caches, per pointer set)
-// the four TMA tensor maps and enqueues two kernels on the caller's stream:
-// the up projection with its fused epilogue, then the down projection as a
-// programmatic dependent launch.
+// A plan binds a problem (M, D, F, act, dtype, bias and the kt_mlp_options flags)
+// to the device current at plan time, holds the planner's choice and owns the
+// device workspace: the intermediate H[M][F], the split-K fp32 partials, the
+// split-K tile counters, the device error word and, with a LayerNorm prologue, the
+// normalised Xn[M][D].  A run encodes (and caches, per pointer set) the TMA tensor
+// maps and enqueues on the caller's stream: the LayerNorm kernel (if any), the up
+// projection with its fused epilogue, then the down projection, each a
+// programmatic dependent launch of the one before.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,16 +44,40 @@ const char* act_name(int a) {
         case KT_ACT_GELU_TANH: return "gelu_tanh";
         case KT_ACT_GEGLU: return "geglu";
         case KT_ACT_NONE: return "none";
+        case KT_ACT_GELU_SIGMOID: return "gelu_sigmoid";
+        case KT_ACT_SILU: return "silu";
     }
     return "?";
 }
 
 kt_status validate_problem(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias) {
     if (M < 1 || D < 1 || F < 1) return fail(KT_ERR_INVALID, "M, D and F must be positive");
-    if (act < KT_ACT_GELU_ERF || act > KT_ACT_NONE) return fail(KT_ERR_INVALID, "unknown activation");
+    if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) return fail(KT_ERR_INVALID, "unknown activation");
     if (dtype != KT_F16 && dtype != KT_BF16) return fail(KT_ERR_INVALID, "unknown dtype");
     if (bias != 0 && bias != 1) return fail(KT_ERR_INVALID, "bias must be 0 or 1");
     return KT_OK;
+}
+
+kt_status validate_options(const kt_mlp_options* o) {
+    if (!o) return fail(KT_ERR_INVALID, "options is NULL");
+    kt_status s = validate_problem(o->M, o->D, o->F, o->act, o->dtype, o->bias);
+    if (s != KT_OK) return s;
+    if ((o->residual != 0 && o->residual != 1) || (o->layernorm != 0 && o->layernorm != 1))
+        return fail(KT_ERR_INVALID, "residual and layernorm must be 0 or 1");
+    if (o->weight_layout != KT_W_IN_OUT && o->weight_layout != KT_W_OUT_IN)
+        return fail(KT_ERR_INVALID, "unknown weight layout");
+    if (o->layernorm && !(o->ln_eps > 0.0f && o->ln_eps < 3.0e38f))
+        return fail(KT_ERR_INVALID, "ln_eps must be positive and finite");
+    return KT_OK;
+}
+
+kt_mlp_options base_options(int64_t M, int64_t D, int64_t F, int act, int dtype, int bias) {
+    kt_mlp_options o;
+    std::memset(&o, 0, sizeof(o));
+    o.M = M; o.D = D; o.F = F;
+    o.act = act; o.dtype = dtype; o.bias = bias;
+    o.weight_layout = KT_W_IN_OUT;
+    return o;
 }
 
 }  // namespace
@@ -60,12 +85,15 @@ kt_status validate_problem(int64_t M, int64_t D, int64_t F, int act, int dtype, 
 struct kt_mlp_plan_s {
     int64_t M, D, F, F_up;
     int act, dtype, bias;
+    int residual = 0, layernorm = 0, w_layout = KT_W_IN_OUT;
+    float ln_eps = 0.0f;
     int device, num_sms;
     kt::PlanChoice choice;
     // device workspace (one allocation each)
     void* H = nullptr;          // [M][F]
     float* partials = nullptr;  // [SK][tiles_m*128][tiles_n*BN] when the down GEMM splits K
     int* flags = nullptr;       // [0] error word, [1..] split-K tile counters
+    void* xn = nullptr;         // [M][D] LayerNorm output (layernorm plans)
     void* x_stage = nullptr;    // [M][D] for kt_mlp_run_host
     void* y_stage = nullptr;    // [M][D]
     int64_t workspace_bytes = 0;
@@ -78,7 +106,7 @@ struct kt_mlp_plan_s {
     const void* c_y = nullptr;
     bool cache_valid = false;
     void* last_stream = nullptr;
-    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // kt_mlp_run_timed, created on first use
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // timed runs, created on first use
     int inject_stall = 0;
     int64_t stall_limit_us = 0;
     unsigned long long* trace_up = nullptr;    // caller-owned device buffers, or null
@@ -96,6 +124,7 @@ void free_plan(kt_mlp_plan_s* p) {
     for (cudaEvent_t e : p->ev)
         if (e) cudaEventDestroy(e);
     cudaFree(p->H);
+    cudaFree(p->xn);
     cudaFree(p->partials);
     cudaFree(p->flags);
     cudaFree(p->x_stage);
@@ -122,11 +151,13 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.kblocks_per_split = g.kblocks_per_split;
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
-    q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair);
+    q.b_kmajor = g.b_kmajor;
+    q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair, g.b_kmajor);
     q.bk = g.bk;
     q.a_bytes = kt::kBM * g.bk * 2;
-    q.b_bytes = (uint32_t)q.n_chunks * 64u * (uint32_t)g.bk * 2u;
-    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair, g.bk);
+    q.b_bytes = (uint32_t)kt::b_tile_bytes(g.BN, g.pair, g.bk, g.b_kmajor);
+    q.b_atom_bytes = g.b_kmajor ? (uint32_t)(g.BN / g.pair) * 128u : 0u;
+    q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair, g.bk, g.b_kmajor);
     q.acc_bufs = (epi == kt::EPI_GEGLU && g.BN > 128) ? 1u : 2u;
     q.gate_acc_off = epi == kt::EPI_GEGLU ? (g.BN <= 128 ? 128u : 256u) : 0u;
     q.error = P->flags;
@@ -135,67 +166,191 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     return q;
 }
 
-kt_status run_impl(kt_mlp_plan_t P, const void* X, const void* W_up, const void* W_down,
-                   const void* b_up, const void* b_down, void* Y, void* H, void* stream,
-                   bool timed = false) {
+kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stream, bool timed = false) {
     if (!P) return fail(KT_ERR_INVALID, "plan is NULL");
-    if (!X || !W_up || !W_down || !Y || !H) return fail(KT_ERR_INVALID, "X, W_up, W_down, Y (and H) must be non-NULL");
-    if (P->bias && (!b_up || !b_down)) return fail(KT_ERR_INVALID, "plan has bias = 1: b_up and b_down are required");
-    if (!aligned16(X) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(Y) || !aligned16(H) ||
-        (P->bias && (!aligned16(b_up) || !aligned16(b_down))))
+    if (!t.X || !t.W_up || !t.W_down || !t.Y || !H) return fail(KT_ERR_INVALID, "X, W_up, W_down, Y (and H) must be non-NULL");
+    if (P->bias && (!t.b_up || !t.b_down)) return fail(KT_ERR_INVALID, "plan has bias = 1: b_up and b_down are required");
+    if (!P->bias && (t.b_up || t.b_down)) return fail(KT_ERR_INVALID, "plan has bias = 0: b_up and b_down must be NULL");
+    if (P->residual != (t.R != nullptr)) return fail(KT_ERR_INVALID, "R must be given iff the plan has residual = 1");
+    if (P->layernorm != (t.ln_gamma != nullptr) || P->layernorm != (t.ln_beta != nullptr))
+        return fail(KT_ERR_INVALID, "ln_gamma and ln_beta must be given iff the plan has layernorm = 1");
+    if (!aligned16(t.X) || !aligned16(t.W_up) || !aligned16(t.W_down) || !aligned16(t.Y) || !aligned16(H) ||
+        !aligned16(t.b_up) || !aligned16(t.b_down) || !aligned16(t.R) || !aligned16(t.ln_gamma) ||
+        !aligned16(t.ln_beta))
         return fail(KT_ERR_INVALID, "device pointers must be 16-byte aligned");
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != P->device) return fail(KT_ERR_INVALID, "the current device is not the plan's device");
 
     const char* why = "";
-    if (!P->cache_valid || P->c_x != X || P->c_wu != W_up || P->c_h != H || P->c_wd != W_down || P->c_y != Y) {
+    const void* A_up = P->layernorm ? P->xn : t.X;
+    if (!P->cache_valid || P->c_x != A_up || P->c_wu != t.W_up || P->c_h != H || P->c_wd != t.W_down ||
+        P->c_y != t.Y) {
         // A operands: [rows][K] K-major, box 128 rows x 64 columns, 128-byte swizzle.
-        // B operands: [K][N] N-major, box bk rows (K) x 64 columns (N), 128-byte swizzle.
+        // B operands [K][N] (N-major): box bk rows (K) x 64 columns (N); [N][K] (K-major):
+        // box (BN / pair) rows (N) x 64 columns (K); 128-byte swizzle.
         // Stores of H and Y: box 32 rows x 32 columns, 64-byte swizzle.
-        if (!kt::encode_tmap(&P->tm_x, X, P->dtype, P->M, P->D, kt::kBM, kt::kAtomK, 128, &why) ||
-            !kt::encode_tmap(&P->tm_wu, W_up, P->dtype, P->D, P->F_up, P->choice.up.bk, 64, 128, &why) ||
-            !kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kAtomK, 128, &why) ||
-            !kt::encode_tmap(&P->tm_wd, W_down, P->dtype, P->F, P->D, P->choice.down.bk, 64, 128, &why) ||
-            !kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) ||
-            !kt::encode_tmap(&P->tm_ys, Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why)) {
+        const kt::GemmConfig& u = P->choice.up;
+        const kt::GemmConfig& d = P->choice.down;
+        const bool km = P->w_layout == KT_W_OUT_IN;
+        bool good =
+            kt::encode_tmap(&P->tm_x, A_up, P->dtype, P->M, P->D, kt::kBM, kt::kAtomK, 128, &why) &&
+            (km ? kt::encode_tmap(&P->tm_wu, t.W_up, P->dtype, P->F_up, P->D, u.BN / u.pair, 64, 128, &why)
+                : kt::encode_tmap(&P->tm_wu, t.W_up, P->dtype, P->D, P->F_up, u.bk, 64, 128, &why)) &&
+            kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kAtomK, 128, &why) &&
+            (km ? kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->D, P->F, d.BN / d.pair, 64, 128, &why)
+                : kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->F, P->D, d.bk, 64, 128, &why)) &&
+            kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) &&
+            kt::encode_tmap(&P->tm_ys, t.Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why);
+        if (!good) {
             P->cache_valid = false;
             return fail(KT_ERR_CUDA, std::string("tensor map: ") + why);
         }
-        P->c_x = X;
-        P->c_wu = W_up;
+        P->c_x = A_up;
+        P->c_wu = t.W_up;
         P->c_h = H;
-        P->c_wd = W_down;
-        P->c_y = Y;
+        P->c_wd = t.W_down;
+        P->c_y = t.Y;
         P->cache_valid = true;
     }
 
-    const int epi_up = P->act == KT_ACT_GELU_ERF ? kt::EPI_GELU_ERF
-                     : P->act == KT_ACT_GELU_TANH ? kt::EPI_GELU_TANH
-                     : P->act == KT_ACT_GEGLU ? kt::EPI_GEGLU : kt::EPI_NONE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (timed) cudaEventRecord(P->ev[0], st);
+    kt_status s;
+    if (P->layernorm) {
+        s = kt::launch_layernorm(P->dtype, t.X, t.ln_gamma, t.ln_beta, P->ln_eps, P->xn, P->M, P->D, stream, &why);
+        if (s != KT_OK) return fail(s, std::string("LayerNorm launch: ") + why);
+    }
+    if (timed) cudaEventRecord(P->ev[1], st);
+
+    const int epi_up = kt::up_epilogue(P->act);
     kt::GemmParams up = make_params(P, P->choice.up, epi_up);
-    up.bias = P->bias ? b_up : nullptr;
+    up.bias = P->bias ? t.b_up : nullptr;
     up.inject_stall = P->inject_stall;
     up.pdl_wait = 1;
     up.trace = P->trace_up;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (timed) cudaEventRecord(P->ev[0], st);
-    kt_status s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
-                                  P->choice.up.smem_bytes, stream, !timed, &why);
+    s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
+                        P->choice.up.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
 
     kt::GemmParams dn = make_params(P, P->choice.down, kt::EPI_DOWN);
-    dn.bias = P->bias ? b_down : nullptr;
+    dn.bias = P->bias ? t.b_down : nullptr;
+    dn.residual = t.R;
     dn.partials = P->partials;
     dn.counters = P->flags + 1;
     dn.pdl_wait = 1;
     dn.trace = P->trace_down;
-    if (timed) cudaEventRecord(P->ev[1], st);
+    if (timed) cudaEventRecord(P->ev[2], st);
     s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, &P->tm_ys, dn, P->choice.down.grid,
                         P->choice.down.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("down projection launch: ") + why);
-    if (timed) cudaEventRecord(P->ev[2], st);
+    if (timed) cudaEventRecord(P->ev[3], st);
     P->last_stream = stream;
+    return ok();
+}
+
+kt_mlp_tensors base_tensors(const void* X, const void* W_up, const void* W_down, const void* b_up,
+                            const void* b_down, void* Y) {
+    kt_mlp_tensors t;
+    std::memset(&t, 0, sizeof(t));
+    t.X = X; t.W_up = W_up; t.W_down = W_down; t.b_up = b_up; t.b_down = b_down; t.Y = Y;
+    return t;
+}
+
+kt_status timed_impl(kt_mlp_plan_t plan, const kt_mlp_tensors& t, void* stream, float* ms3) {
+    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
+    for (cudaEvent_t& e : plan->ev) {
+        if (!e) {
+            cudaError_t ce = cudaEventCreate(&e);
+            if (ce != cudaSuccess) return cuda_fail("cudaEventCreate", ce);
+        }
+    }
+    kt_status s = run_impl(plan, t, t.H_out ? t.H_out : plan->H, stream, true);
+    if (s != KT_OK) return s;
+    cudaError_t e = cudaEventSynchronize(plan->ev[3]);
+    if (e != cudaSuccess) return cuda_fail("cudaEventSynchronize", e);
+    for (int i = 0; i < 3; ++i) {
+        ms3[i] = 0.0f;
+        cudaEventElapsedTime(&ms3[i], plan->ev[i], plan->ev[i + 1]);
+    }
+    return ok();
+}
+
+kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDeviceProperties", e);
+    if (prop.major != 10 || prop.minor != 3) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf), "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
+                      prop.major, prop.minor);
+        return fail(KT_ERR_UNSUPPORTED, buf);
+    }
+    kt_mlp_plan_s* P = new (std::nothrow) kt_mlp_plan_s();
+    if (!P) return fail(KT_ERR_NOMEM, "host allocation of the plan failed");
+    const int64_t M = o.M, D = o.D, F = o.F;
+    P->M = M; P->D = D; P->F = F;
+    P->F_up = o.act == KT_ACT_GEGLU ? 2 * F : F;
+    P->act = o.act; P->dtype = o.dtype; P->bias = o.bias;
+    P->residual = o.residual; P->layernorm = o.layernorm; P->w_layout = o.weight_layout;
+    P->ln_eps = o.layernorm ? o.ln_eps : 0.0f;
+    P->device = dev;
+    P->num_sms = prop.multiProcessorCount;
+    const char* why = "";
+    kt_status s = kt::plan_choose(M, D, F, o.act, P->num_sms, &P->choice, &why, true, o.weight_layout);
+    if (s != KT_OK) {
+        delete P;
+        return fail(s, why);
+    }
+    const kt::GemmConfig& dn = P->choice.down;
+    size_t h_bytes = (size_t)M * (size_t)F * 2;
+    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
+    size_t flag_bytes = 4 * (1 + n_counters);
+    size_t part_bytes = dn.split_k > 1 && !dn.cluster_sk
+                            ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
+                            : 0;
+    size_t io_bytes = (size_t)M * (size_t)D * 2;
+    size_t xn_bytes = o.layernorm ? io_bytes : 0;
+    if ((e = cudaMalloc(&P->H, h_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&P->flags), flag_bytes)) != cudaSuccess ||
+        (part_bytes && (e = cudaMalloc(reinterpret_cast<void**>(&P->partials), part_bytes)) != cudaSuccess) ||
+        (xn_bytes && (e = cudaMalloc(&P->xn, xn_bytes)) != cudaSuccess) ||
+        (e = cudaMalloc(&P->x_stage, io_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(&P->y_stage, io_bytes)) != cudaSuccess) {
+        free_plan(P);
+        cudaGetLastError();
+        return fail(KT_ERR_NOMEM, std::string("workspace allocation: ") + cudaGetErrorString(e));
+    }
+    if ((e = cudaMemset(P->flags, 0, flag_bytes)) != cudaSuccess) {
+        free_plan(P);
+        return cuda_fail("cudaMemset", e);
+    }
+    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + part_bytes + xn_bytes + 2 * io_bytes);
+    *out = P;
+    return ok();
+}
+
+kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
+    kt::PlanChoice c;
+    const char* why = "";
+    kt_status s = kt::plan_choose(o.M, o.D, o.F, o.act, num_sms, &c, &why, true, o.weight_layout);
+    if (s != KT_OK) return fail(s, why);
+    std::memset(out, 0, sizeof(*out));
+    out->M = o.M; out->D = o.D; out->F = o.F;
+    out->act = o.act; out->dtype = o.dtype; out->bias = o.bias;
+    out->num_sms = num_sms;
+    out->residual = o.residual; out->layernorm = o.layernorm; out->weight_layout = o.weight_layout;
+    out->ln_eps = o.layernorm ? o.ln_eps : 0.0f;
+    kt::plan_fill_info(c.up, &out->up);
+    kt::plan_fill_info(c.down, &out->down);
+    int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * o.M * o.D;
+    if (c.down.split_k > 1 && !c.down.cluster_sk)
+        ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
+    if (o.layernorm) ws += 2 * o.M * o.D;
+    out->workspace_bytes = ws;
     return ok();
 }
 
@@ -212,21 +367,14 @@ kt_status kt_mlp_plan_info(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype
     if (!out) return fail(KT_ERR_INVALID, "out is NULL");
     kt_status s = validate_problem(M, D, F, act, dtype, bias);
     if (s != KT_OK) return s;
-    kt::PlanChoice c;
-    const char* why = "";
-    s = kt::plan_choose(M, D, F, act, num_sms, &c, &why);
-    if (s != KT_OK) return fail(s, why);
-    std::memset(out, 0, sizeof(*out));
-    out->M = M; out->D = D; out->F = F;
-    out->act = act; out->dtype = dtype; out->bias = bias;
-    out->num_sms = num_sms;
-    kt::plan_fill_info(c.up, &out->up);
-    kt::plan_fill_info(c.down, &out->down);
-    int64_t ws = M * F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * M * D;
-    if (c.down.split_k > 1 && !c.down.cluster_sk)
-        ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
-    out->workspace_bytes = ws;
-    return ok();
+    return info_impl(base_options(M, D, F, act, dtype, bias), num_sms, out);
+}
+
+kt_status kt_mlp_plan_info_ex(const kt_mlp_options* options, int num_sms, kt_plan_info* out) {
+    if (!out) return fail(KT_ERR_INVALID, "out is NULL");
+    kt_status s = validate_options(options);
+    if (s != KT_OK) return s;
+    return info_impl(*options, num_sms, out);
 }
 
 kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtype, int bias,
@@ -235,87 +383,46 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
     *out = nullptr;
     kt_status s = validate_problem(M, D, F, act, dtype, bias);
     if (s != KT_OK) return s;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
-    cudaDeviceProp prop;
-    e = cudaGetDeviceProperties(&prop, dev);
-    if (e != cudaSuccess) return cuda_fail("cudaGetDeviceProperties", e);
-    if (prop.major != 10 || prop.minor != 3) {
-        char buf[160];
-        std::snprintf(buf, sizeof(buf), "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
-                      prop.major, prop.minor);
-        return fail(KT_ERR_UNSUPPORTED, buf);
-    }
-    kt_mlp_plan_s* P = new (std::nothrow) kt_mlp_plan_s();
-    if (!P) return fail(KT_ERR_NOMEM, "host allocation of the plan failed");
-    P->M = M; P->D = D; P->F = F;
-    P->F_up = act == KT_ACT_GEGLU ? 2 * F : F;
-    P->act = act; P->dtype = dtype; P->bias = bias;
-    P->device = dev;
-    P->num_sms = prop.multiProcessorCount;
-    const char* why = "";
-    s = kt::plan_choose(M, D, F, act, P->num_sms, &P->choice, &why);
-    if (s != KT_OK) {
-        delete P;
-        return fail(s, why);
-    }
-    const kt::GemmConfig& dn = P->choice.down;
-    size_t h_bytes = (size_t)M * (size_t)F * 2;
-    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
-    size_t flag_bytes = 4 * (1 + n_counters);
-    size_t part_bytes = dn.split_k > 1 && !dn.cluster_sk
-                            ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
-                            : 0;
-    size_t io_bytes = (size_t)M * (size_t)D * 2;
-    if ((e = cudaMalloc(&P->H, h_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(reinterpret_cast<void**>(&P->flags), flag_bytes)) != cudaSuccess ||
-        (part_bytes && (e = cudaMalloc(reinterpret_cast<void**>(&P->partials), part_bytes)) != cudaSuccess) ||
-        (e = cudaMalloc(&P->x_stage, io_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(&P->y_stage, io_bytes)) != cudaSuccess) {
-        free_plan(P);
-        cudaGetLastError();
-        return fail(KT_ERR_NOMEM, std::string("workspace allocation: ") + cudaGetErrorString(e));
-    }
-    if ((e = cudaMemset(P->flags, 0, flag_bytes)) != cudaSuccess) {
-        free_plan(P);
-        return cuda_fail("cudaMemset", e);
-    }
-    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + part_bytes + 2 * io_bytes);
-    *out = P;
-    return ok();
+    return create_plan(base_options(M, D, F, act, dtype, bias), out);
+}
+
+kt_status kt_mlp_plan_ex(const kt_mlp_options* options, kt_mlp_plan_t* out) {
+    if (!out) return fail(KT_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    kt_status s = validate_options(options);
+    if (s != KT_OK) return s;
+    return create_plan(*options, out);
 }
 
 kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                      const void* b_up, const void* b_down, void* Y, void* stream) {
-    return run_impl(plan, X, W_up, W_down, b_up, b_down, Y, plan ? plan->H : nullptr, stream);
+    return run_impl(plan, base_tensors(X, W_up, W_down, b_up, b_down, Y), plan ? plan->H : nullptr, stream);
 }
 
 kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                             const void* b_up, const void* b_down, void* Y, void* H_out, void* stream) {
     if (!H_out) return fail(KT_ERR_INVALID, "H_out is NULL");
-    return run_impl(plan, X, W_up, W_down, b_up, b_down, Y, H_out, stream);
+    return run_impl(plan, base_tensors(X, W_up, W_down, b_up, b_down, Y), H_out, stream);
+}
+
+kt_status kt_mlp_run_ex(kt_mlp_plan_t plan, const kt_mlp_tensors* tensors, void* stream) {
+    if (!plan || !tensors) return fail(KT_ERR_INVALID, "plan and tensors must be non-NULL");
+    return run_impl(plan, *tensors, tensors->H_out ? tensors->H_out : plan->H, stream);
+}
+
+kt_status kt_mlp_run_ex_timed(kt_mlp_plan_t plan, const kt_mlp_tensors* tensors, void* stream, float* ms) {
+    if (!plan || !tensors || !ms) return fail(KT_ERR_INVALID, "plan, tensors and ms must be non-NULL");
+    return timed_impl(plan, *tensors, stream, ms);
 }
 
 kt_status kt_mlp_run_timed(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                            const void* b_up, const void* b_down, void* Y, void* stream,
                            float* ms_up, float* ms_down) {
-    if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
-    for (cudaEvent_t& e : plan->ev) {
-        if (!e) {
-            cudaError_t ce = cudaEventCreate(&e);
-            if (ce != cudaSuccess) return cuda_fail("cudaEventCreate", ce);
-        }
-    }
-    kt_status s = run_impl(plan, X, W_up, W_down, b_up, b_down, Y, plan->H, stream, true);
+    float ms[3] = {0.f, 0.f, 0.f};
+    kt_status s = timed_impl(plan, base_tensors(X, W_up, W_down, b_up, b_down, Y), stream, ms);
     if (s != KT_OK) return s;
-    cudaError_t e = cudaEventSynchronize(plan->ev[2]);
-    if (e != cudaSuccess) return cuda_fail("cudaEventSynchronize", e);
-    float a = 0.f, b = 0.f;
-    cudaEventElapsedTime(&a, plan->ev[0], plan->ev[1]);
-    cudaEventElapsedTime(&b, plan->ev[1], plan->ev[2]);
-    if (ms_up) *ms_up = a;
-    if (ms_down) *ms_down = b;
+    if (ms_up) *ms_up = ms[1];
+    if (ms_down) *ms_down = ms[2];
     return ok();
 }
 
@@ -323,11 +430,14 @@ kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_
                           const void* b_up, const void* b_down, void* Y_host, void* stream) {
     if (!plan) return fail(KT_ERR_INVALID, "plan is NULL");
     if (!X_host || !Y_host) return fail(KT_ERR_INVALID, "X_host and Y_host must be non-NULL");
+    if (plan->residual || plan->layernorm)
+        return fail(KT_ERR_INVALID, "kt_mlp_run_host takes plans without residual / layernorm");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     size_t bytes = (size_t)plan->M * (size_t)plan->D * 2;
     cudaError_t e = cudaMemcpyAsync(plan->x_stage, X_host, bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail("copy of X to the device", e);
-    kt_status s = run_impl(plan, plan->x_stage, W_up, W_down, b_up, b_down, plan->y_stage, plan->H, stream);
+    kt_status s = run_impl(plan, base_tensors(plan->x_stage, W_up, W_down, b_up, b_down, plan->y_stage), plan->H,
+                           stream);
     if (s != KT_OK) return s;
     e = cudaMemcpyAsync(Y_host, plan->y_stage, bytes, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail("copy of Y to the host", e);
@@ -370,6 +480,8 @@ kt_status kt_mlp_get_info(kt_mlp_plan_t plan, kt_plan_info* out) {
     out->M = plan->M; out->D = plan->D; out->F = plan->F;
     out->act = plan->act; out->dtype = plan->dtype; out->bias = plan->bias;
     out->num_sms = plan->num_sms;
+    out->residual = plan->residual; out->layernorm = plan->layernorm; out->weight_layout = plan->w_layout;
+    out->ln_eps = plan->ln_eps;
     kt::plan_fill_info(plan->choice.up, &out->up);
     kt::plan_fill_info(plan->choice.down, &out->down);
     out->workspace_bytes = plan->workspace_bytes;
@@ -381,11 +493,12 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
     const kt::GemmConfig& u = plan->choice.up;
     const kt::GemmConfig& d = plan->choice.down;
     std::snprintf(buf, len,
-                  "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d sms=%d | up: %dx%d tiles %dx%d (grid %d, %d "
+                  "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d residual=%d layernorm=%d weights=%s sms=%d | up: %dx%d tiles %dx%d (grid %d, %d "
                   "wave%s, %d stages, useful %.3f, model %.2f us) | down: %dx%d tiles %dx%d split_k %d (grid %d, "
                   "%d wave%s, %d stages, useful %.3f, model %.2f us) | workspace %lld B",
                   (long long)plan->M, (long long)plan->D, (long long)plan->F, act_name(plan->act),
-                  plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->num_sms, kt::kBM * u.pair, u.BN, u.tiles_m, u.tiles_n,
+                  plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->residual, plan->layernorm,
+                  plan->w_layout == KT_W_OUT_IN ? "out_in" : "in_out", plan->num_sms, kt::kBM * u.pair, u.BN, u.tiles_m, u.tiles_n,
                   u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, kt::kBM * d.pair, d.BN,
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
@@ -403,7 +516,7 @@ kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_dow
 
 kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, float* out, int64_t n,
                               void* stream) {
-    if (act < KT_ACT_GELU_ERF || act > KT_ACT_NONE) return fail(KT_ERR_INVALID, "unknown activation");
+    if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) return fail(KT_ERR_INVALID, "unknown activation");
     if (n < 0 || (n > 0 && (!z || !out || (act == KT_ACT_GEGLU && !gate))))
         return fail(KT_ERR_INVALID, "z and out (and gate for GEGLU) must be non-NULL, n >= 0");
     const char* why = "";

@@ -1,1029 +1,12 @@
-// kt_mlp_kernels.cu -- the sm_103a GEMM kernels of the fused MLP.
-//
-// One persistent, warp-specialised kernel template serves both projections:
-//
-//   warp 0      producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
-//               A tile (128 x 64, K-major) and the B tile(s) (64 x BN in 64-column
-//               boxes, N-major) into an S-stage shared-memory ring, one mbarrier
-//               pair (full / empty) per stage.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f16 (M=128, N=BN,
-//               K=16, fp32 accumulation in tensor memory), four per k-block, and
-//               tcgen05.commit hands the stage back to the producer.  Two TMEM
-//               accumulator buffers let tile i+1's main loop run under tile i's
-//               epilogue.  GEGLU issues a second MMA per step into a gate
-//               accumulator that shares the A tile (one X stream, two weights).
-//   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers
-//               (TMEM lane = tile row), adds the bias, applies the activation
-//               (GELU erf / tanh, GEGLU value*gelu(gate)), rounds ONCE to the I/O
-//               dtype, stages each warp's 32 x 32 block in swizzled shared memory
-//               and writes it with a TMA tensor store (coalesced, clipped at the
-//               ragged edges); the down projection adds b_down and stores Y, or,
-//               with split-K, writes an fp32 partial (warp-contiguous layout) and
-//               the last CTA to arrive on the tile sums the partials in split
-//               order (deterministic).
-//
-// Sources: "SDXL as a requirements inventory", section 1.3 (FeedForward: value =
-// first half, gate = second half) and 9.3 (erf GELU); "MLP layout sweep and
-// remaining representation limits" (the SigLIP MLP, tanh GELU, K-partitioned
-// down projection with a reduction); "The software stack", sections 2.2 (3-D grid,
-// split-K needs a reduction, every output element produced exactly once), 2.3
-// (epilogue folding; the accumulator is never a memory word) and 2.4 (B resident,
-// A double-buffered -> here a multi-stage ring).
-//
-// Every device-side wait is bounded by %globaltimer; on expiry the kernel records
-// an error code, raises a CTA-wide abort flag, drains its own in-flight copies and
-// MMAs (again bounded), frees tensor memory and returns.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
+// kt_mlp_kernels.cu -- host side of the sm_103a kernels: tensor-map encoding, the
+// instruction descriptor, the launch dispatch over the kernel instantiations (which
+// live in kt_gemm_act.cu, kt_gemm_geglu.cu and kt_gemm_down.cu), the allocation-free
+// down projection, and the small elementwise / test kernels.
+#include "kt_gemm.cuh"
 
-#include <algorithm>
-#include <atomic>
-#include <cstdio>
-#include <cstring>
-#include <mutex>
-
-#include "kt_internal.h"
+#include <climits>
 
 namespace kt {
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t sm_id() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void trace_mark(unsigned long long* tr, int slot) {
-    if (tr) tr[(size_t)blockIdx.x * kTraceSlots + slot] = global_ns();
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok;
-}
-
-// Wait for the phase of parity `parity` of barrier `bar` to complete.  Returns
-// false if the CTA is aborting or if `limit_ns` passed (then raises the abort
-// flag and records `code` in the error word, first writer wins).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int* err, int code, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > limit_ns) {
-                *abort_flag = 1;
-                atomicCAS(err, 0, code);
-                return false;
-            }
-        }
-    }
-}
-
-// Drain wait used on the abort path: ignores the abort flag, bounded by limit_ns.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return;
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x,
-                                            int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Tensor-memory allocation.  With PAIR = 2 (cta_group::2) one warp of each CTA of the
-// pair performs the allocation collectively; the same columns are allocated in both.
-template <int PAIR>
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    if constexpr (PAIR == 2) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-}
-
-template <int PAIR>
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    if constexpr (PAIR == 2)
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-    else
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// All threads of all CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address, in the cluster shared window, of the same shared variable in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier given by its cluster-window address (possibly in the peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// 16 bytes from a shared-memory address of any CTA of the cluster.
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-
-// TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int x,
-                                                 int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading-dimension and
-// stride-dimension byte offsets (all >> 4), descriptor version 1 (bits 46-48 =
-// 0b001), base offset 0 (tiles are 1024-byte aligned), 128-byte swizzle (= 2).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// M = 256 across the CTA pair: this CTA's smem holds A rows [0,128) and B columns
-// [0, N/2) of its half; the peer's the other halves (same offsets).
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive on the barrier at this offset in both CTAs of the pair once all prior MMAs finish.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"((unsigned short)3)
-        : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns; thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-// tcgen05.wait::ld, with the loaded registers threaded through so that no use
-// of them can be scheduled before the wait.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r)[16], uint32_t (&s)[16]) {
-    tmem_wait_ld(r);
-    asm volatile(""
-                 : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]),
-                   "+r"(s[6]), "+r"(s[7]), "+r"(s[8]), "+r"(s[9]), "+r"(s[10]), "+r"(s[11]),
-                   "+r"(s[12]), "+r"(s[13]), "+r"(s[14]), "+r"(s[15])
-                 :
-                 : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-// Pass 32 registers through an empty asm so that no use of them is scheduled
-// before the preceding tcgen05.wait::ld.
-__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                   "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-    asm volatile(""
-                 : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
-                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld_only() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// TMA tensor store of a box from shared memory (clipped at the tensor's bounds).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(tm)),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-}
-
-// Barrier over the epilogue warps that also ANDs a predicate across them, so that
-// all of them take the same branch after a bounded wait (no warp is left behind
-// at a later named barrier).
-__device__ __forceinline__ bool epi_all(bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok), "n"(kEpiWarps * 32)
-        : "memory");
-    return r != 0;
-}
-
-// ---------------------------------------------------------------------------
-// Epilogue arithmetic (fp32)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, hardware approximation (ftz)
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approximation (ftz)
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// gelu_erf(z) = z * Phi(z),  Phi(z) = erfc(-z / sqrt 2) / 2.
-// erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
-// 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), fractional error
-// below 1.2e-7 for every a >= 0; erfc(-a) = 2 - erfc(a).  Evaluated in fp32 with the
-// hardware exp2 and reciprocal: no cancellation for z < 0, no branches.
-__device__ __forceinline__ float gelu_erf_f(float z) {
-    const float a = fabsf(z) * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(0.5f, a, 1.0f));
-    float p = 0.17087277f;
-    p = fmaf(p, t, -0.82215223f);
-    p = fmaf(p, t, 1.48851587f);
-    p = fmaf(p, t, -1.13520398f);
-    p = fmaf(p, t, 0.27886807f);
-    p = fmaf(p, t, -0.18628806f);
-    p = fmaf(p, t, 0.09678418f);
-    p = fmaf(p, t, 0.37409196f);
-    p = fmaf(p, t, 1.00002368f);
-    p = fmaf(p, t, -1.26551223f);
-    const float e = t * ex2_approx((p - a * a) * 1.4426950408889634f);  // erfc(|z| / sqrt 2)
-    const float phi = z >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
-    return z * phi;
-}
-
-// gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
-// exp(-2u) = 2^(z (c1 + c2 z^2)), c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1.
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-    const float x = z * fmaf(-0.1029432395800235f, z * z, -2.302208198144325f);
-    return z * rcp_approx(1.0f + ex2_approx(x));
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    if constexpr (DT == KT_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    } else {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ void unpack8(const uint4& w, float* f) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if constexpr (DT == KT_BF16) {
-            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&u[i]);
-            float2 t = __bfloat1622float2(h);
-            f[2 * i] = t.x;
-            f[2 * i + 1] = t.y;
-        } else {
-            __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
-            float2 t = __half22float2(h);
-            f[2 * i] = t.x;
-            f[2 * i + 1] = t.y;
-        }
-    }
-}
-
-// 32 bias values starting at column `col` (groups of 8 at or past `limit` read as 0).
-template <int DT>
-__device__ __forceinline__ void load_bias32(const void* bias, int col, int limit, float* b) {
-    const uint16_t* ptr = reinterpret_cast<const uint16_t*>(bias) + col;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        if (col + 8 * g < limit) {
-            uint4 w = __ldg(reinterpret_cast<const uint4*>(ptr + 8 * g));
-            unpack8<DT>(w, b + 8 * g);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b[8 * g + i] = 0.0f;
-        }
-    }
-}
-
-// Round a warp's 32 x 32 block (this lane's row, 32 columns in v) to the I/O dtype,
-// stage it in the warp's 2 KB shared-memory buffer in the 64-byte swizzled layout
-// the output tensor map expects (16-byte chunk c of row r lands at chunk
-// c ^ ((r >> 1) & 3)), and store it with one TMA tensor store at (x, y).  Rows and
-// columns past the tensor's bounds are clipped by the TMA unit.
-template <int DT>
-__device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t stg, int lane, const float* v,
-                                                int x, int y) {
-    if (lane == 0) bulk_wait_read0();  // the previous store from this buffer has read it
-    __syncwarp();
-    const uint32_t row_base = stg + (uint32_t)lane * 64u;
-    const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        st_shared_v4(row_base + ((c ^ sw) << 4), pack2<DT>(v[8 * c + 0], v[8 * c + 1]),
-                     pack2<DT>(v[8 * c + 2], v[8 * c + 3]), pack2<DT>(v[8 * c + 4], v[8 * c + 5]),
-                     pack2<DT>(v[8 * c + 6], v[8 * c + 7]));
-    }
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        tma_store_2d(tmC, stg, x, y);
-        bulk_commit();
-    }
-}
-
-// The MMAs of one k-block: NK steps of K = 16 (4 for a 64-deep stage, 8 for 128).
-template <int EPI, int PAIR, int NK>
-__device__ __forceinline__ void issue_kblock(uint32_t d, uint32_t d_gate, uint64_t ad0, uint64_t bd0, uint64_t gd0,
-                                             uint32_t idesc, uint32_t acc0) {
-#pragma unroll
-    for (int k = 0; k < NK; ++k) {
-        const uint64_t ad = ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
-        const uint64_t bd = bd0 + (uint64_t)(k * 128);
-        const uint32_t acc = k == 0 ? acc0 : 1u;
-        if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, idesc, acc);
-        else mma_f16(d, ad, bd, idesc, acc);
-        if constexpr (EPI == EPI_GEGLU) {
-            const uint64_t gd = gd0 + (uint64_t)(k * 128);
-            if constexpr (PAIR == 2) mma_f16_pair(d_gate, ad, gd, idesc, acc);
-            else mma_f16(d_gate, ad, gd, idesc, acc);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// The kernel
-// ---------------------------------------------------------------------------
-
-struct TileCoord {
-    int split, tm, tn, mn;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
-    TileCoord c;
-    const int per_split = p.tiles_m * p.tiles_n;
-    if (p.cluster_sk) {  // the SK splits of one tile are one cluster of consecutive CTAs
-        c.split = t % p.split_k;
-        c.mn = t / p.split_k;
-    } else {
-        c.split = t / per_split;
-        c.mn = t - c.split * per_split;
-    }
-    c.tm = c.mn / p.tiles_n;
-    c.tn = c.mn - c.tm * p.tiles_n;
-    return c;
-}
-
-// PAIR = 1: one CTA per 128 x BN tile (cta_group::1).  PAIR = 2: a cluster pair per
-// 256 x BN tile (cta_group::2): each CTA loads its 128 rows of A and half of the B
-// columns; the even CTA (the leader) issues the MMAs, which write each CTA's 128
-// rows of the accumulator into that CTA's tensor memory; each CTA's epilogue stores
-// its own rows.
-template <int EPI, int DT, int PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
-    kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles want 1024-byte alignment
-    uint8_t* base_ptr = smem_raw + (base - raw);
-
-    const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
-    const uint32_t staging = base + tiles_bytes;  // kEpiWarps x 2 KB output staging buffers
-    const uint32_t bar_full = staging + (uint32_t)kStagingBytes;
-    const uint32_t bar_empty = bar_full + 8u * kMaxStages;
-    const uint32_t bar_accf = bar_empty + 8u * kMaxStages;
-    const uint32_t bar_acce = bar_accf + 16u;
-    const uint32_t bar_stall = bar_acce + 16u;
-    const uint32_t bar_drain = bar_stall + 8u;
-    const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partial is in smem
-    const uint32_t bar_rdone = bar_pready + 8u;  // cluster split-K: every CTA finished reading mine
-    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 8));
-    uint32_t* tmem_slot = slots;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    unsigned long long* const tr = p.trace;
-    if (threadIdx.x == 0) trace_mark(tr, TR_ENTRY);
-    const uint32_t rank = PAIR == 2 ? (cluster_ctarank() & 1u) : 0u;  // position in the CTA pair
-    const bool leader = rank == 0;
-    const int unit0 = (int)blockIdx.x / PAIR;        // first tile of this CTA (or pair)
-    const int unit_step = (int)gridDim.x / PAIR;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(bar_full + 8u * s, 1);
-            mbar_init(bar_empty + 8u * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar_accf + 8u * b, 1);
-            mbar_init(bar_acce + 8u * b, kEpiWarps * PAIR);  // both CTAs' epilogues (leader's copy)
-        }
-        mbar_init(bar_stall, 1);
-        mbar_init(bar_drain, 1);
-        mbar_init(bar_pready, (uint32_t)(p.split_k * kEpiWarps));
-        mbar_init(bar_rdone, (uint32_t)(p.split_k * kEpiWarps));
-        *abort_flag = 0;
-        *last_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        prefetch_tmap(&tmC);
-    }
-    if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    if (PAIR == 2 || p.cluster_sk) cluster_sync_all();  // peers' barriers initialised before any remote signal
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
-
-    // Programmatic dependent launch: let the next kernel in the stream get its CTAs
-    // resident (and through their set-up) as SMs free up; every kernel here waits for
-    // its predecessor's completion before its first global-memory access.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (p.pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
-
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            uint32_t armed = 0, armed_phase = 0;  // per-stage bits: loads issued / their phase
-            if (p.inject_stall) {
-                // failure injection: a barrier nobody arrives on, bounded wait
-                wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
-            }
-            for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step) {
-                const TileCoord c = decode_tile(t, p);
-                const int kb0 = c.split * p.kblocks_per_split;
-                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
-                // this CTA's rows of A and its share of the B columns
-                const int bcols = p.BN / PAIR;
-                auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
-                    m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
-                    nb_r = c.tn * p.BN + (int)r * bcols;
-                    chunks_r = 0;  // 64-column boxes of the share that start inside [0, N)
-                    for (int ch = 0; ch * 64 < bcols; ++ch)
-                        if (nb_r + 64 * ch < p.N) chunks_r = ch + 1;
-                    // boxes entirely past the tensor are not loaded: they would only feed
-                    // accumulator rows / columns that are never stored
-                    return (m_r < p.M ? p.a_bytes : 0u) + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * 128u);
-                };
-                int m_me, nb_me, chunks;
-                uint32_t tx = cta_share(rank, m_me, nb_me, chunks);
-                if (PAIR == 2) {  // the leader's full barrier counts the bytes of both CTAs
-                    int m_o, nb_o, ch_o;
-                    tx += cta_share(rank ^ 1u, m_o, nb_o, ch_o);
-                }
-                bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.error,
-                                    DEV_TIMEOUT_PRODUCER, p.wait_limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar_full + 8u * stage;
-                    const uint32_t sA = base + stage * p.stage_bytes;
-                    const uint32_t sB = sA + p.a_bytes;
-                    if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
-                    const int k0 = kb * p.bk;
-                    const uint32_t chunk_bytes = (uint32_t)p.bk * 128u;  // 64 columns x bk rows
-                    if constexpr (PAIR == 2) {
-                        const uint32_t fb_leader = mapa_rank(fb, 0);
-                        if (leader) mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M)
-                            for (int a = 0; a < p.bk / kAtomK; ++a)
-                                tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
-                        for (int ch = 0; ch < chunks; ++ch)
-                            tma_load_2d_pair(sB + chunk_bytes * ch, &tmB, fb_leader, nb_me + 64 * ch, k0);
-                        if (EPI == EPI_GEGLU) {
-                            for (int ch = 0; ch < chunks; ++ch)
-                                tma_load_2d_pair(sB + p.b_bytes + chunk_bytes * ch, &tmB, fb_leader,
-                                                 p.gate_col + nb_me + 64 * ch, k0);
-                        }
-                    } else {
-                        mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M)
-                            for (int a = 0; a < p.bk / kAtomK; ++a)
-                                tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
-                        for (int ch = 0; ch < chunks; ++ch)
-                            tma_load_2d(sB + chunk_bytes * ch, &tmB, fb, nb_me + 64 * ch, k0);
-                        if (EPI == EPI_GEGLU) {
-                            for (int ch = 0; ch < chunks; ++ch)
-                                tma_load_2d(sB + p.b_bytes + chunk_bytes * ch, &tmB, fb, p.gate_col + nb_me + 64 * ch,
-                                            k0);
-                        }
-                    }
-                    armed |= 1u << stage;
-                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == (uint32_t)p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-            }
-            if (*abort_flag && leader) {
-                // do not leave copies in flight into shared memory we are about to release
-                // (the leader's full barriers count the peer's copies too)
-                for (int s = 0; s < p.stages; ++s)
-                    if (armed & (1u << s)) wait_drain(bar_full + 8u * s, (armed_phase >> s) & 1u, 100000000ull);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ----------------------------
-        if (lane == 0 && leader) {
-            uint32_t stage = 0, phase = 0;
-            int local = 0;
-            bool issued_any = false;
-            for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
-                const TileCoord c = decode_tile(t, p);
-                const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
-                const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
-                if (!wait_phase(bar_acce + 8u * buf, (use & 1u) ^ 1u, abort_flag, p.error, DEV_TIMEOUT_MMA,
-                                p.wait_limit_ns))
-                    break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
-                const int kb0 = c.split * p.kblocks_per_split;
-                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
-                bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(bar_full + 8u * stage, phase, abort_flag, p.error, DEV_TIMEOUT_MMA,
-                                    p.wait_limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (tr && !issued_any) trace_mark(tr, TR_FIRST_FULL);
-                    const uint32_t sA = base + stage * p.stage_bytes;
-                    const uint32_t sB = sA + p.a_bytes;
-                    // Descriptors of this stage; the K steps only move the start address, by
-                    // constant offsets (in 16-byte units): A +32 bytes per 16-element step inside
-                    // a 128 x 64 swizzle atom and +16 KB per atom; B +2 KB per 16-row step.
-                    const uint64_t ad0 = smem_desc(sA, 16u, 1024u);
-                    const uint64_t bd0 = smem_desc(sB, (uint32_t)p.bk * 128u, 1024u);
-                    const uint64_t gd0 = smem_desc(sB + p.b_bytes, (uint32_t)p.bk * 128u, 1024u);
-                    const uint32_t acc0 = kb > kb0 ? 1u : 0u;
-                    if (p.bk == 64) {
-                        issue_kblock<EPI, PAIR, 4>(d, d + p.gate_acc_off, ad0, bd0, gd0, p.idesc, acc0);
-                    } else {
-                        issue_kblock<EPI, PAIR, 8>(d, d + p.gate_acc_off, ad0, bd0, gd0, p.idesc, acc0);
-                    }
-                    issued_any = true;
-                    // stage free (in both CTAs of a pair) once these MMAs completed
-                    if constexpr (PAIR == 2) mma_commit_pair(bar_empty + 8u * stage);
-                    else mma_commit(bar_empty + 8u * stage);
-                    if (++stage == (uint32_t)p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                // accumulator ready for the epilogue (of both CTAs of a pair)
-                if constexpr (PAIR == 2) mma_commit_pair(bar_accf + 8u * buf);
-                else mma_commit(bar_accf + 8u * buf);
-                if (tr) {
-                    if (local == 0) trace_mark(tr, TR_MAIN_DONE);
-                    trace_mark(tr, TR_LAST_MAIN);
-                    tr[(size_t)blockIdx.x * kTraceSlots + TR_TILES] = (unsigned long long)(local + 1);
-                }
-            }
-            if (*abort_flag && issued_any) {
-                if constexpr (PAIR == 2) mma_commit_pair(bar_drain);
-                else mma_commit(bar_drain);
-                wait_drain(bar_drain, 0u, 100000000ull);
-            }
-        }
-    } else {
-        // ------------------------------ epilogue ------------------------------
-        const int ew = warp - 2;
-        const int q = warp & 3;    // TMEM lane quadrant this warp may access
-        const int half = ew >> 2;  // which of the interleaved 32-column groups
-        const int row = q * 32 + lane;
-        const int ngroups = p.BN / 32;
-        const uint32_t stg = staging + (uint32_t)ew * 2048u;
-        const int tiles_mn = p.tiles_m * p.tiles_n;
-        const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
-        int local = 0;
-        for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
-            const TileCoord c = decode_tile(t, p);
-            const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
-            const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
-            // the accumulator-empty barrier lives in the leader CTA
-            const uint32_t acce = PAIR == 2 ? mapa_rank(bar_acce + 8u * buf, 0) : bar_acce + 8u * buf;
-            const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
-                                        DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
-            if (!epi_all(got)) break;
-            tc_fence_after();
-            const bool tr0 = tr && local == 0 && warp == 2 && lane == 0;
-            if (tr0) trace_mark(tr, TR_EPI_START);
-            const int m0 = c.tm * (kBM * PAIR) + (int)rank * kBM;  // this CTA's first row
-            const int y0 = m0 + q * 32;              // first row of this warp's block
-            const bool rows_live = y0 < p.M;         // warp-uniform
-            const int n0 = c.tn * p.BN;
-            const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)kAccSlot;
-
-            if (EPI != EPI_DOWN || p.split_k == 1) {
-                for (int g = half; g < ngroups; g += 2) {
-                    const int col = n0 + 32 * g;
-                    const bool mark = tr0 && g == half;
-                    uint32_t r[32];
-                    tmem_ld32(tq + 32u * g, r);
-                    float v[32];
-                    if constexpr (EPI == EPI_GEGLU) {
-                        uint32_t gr[32];
-                        tmem_ld32(tq + p.gate_acc_off + 32u * g, gr);
-                        tmem_wait_ld_only();
-                        reg_fence32(r);
-                        reg_fence32(gr);
-                        if (mark) trace_mark(tr, TR_EPI_LD);
-                        if (col < p.N && rows_live) {
-                            float bv[32], bg[32];
-                            if (p.bias) {
-                                load_bias32<DT>(p.bias, col, p.N, bv);
-                                load_bias32<DT>(p.bias, p.gate_col + col, p.gate_col + p.N, bg);
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) bv[i] = bg[i] = 0.0f;
-                            }
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(gr[i]) + bg[i]);
-                            if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
-                            if (mark) trace_mark(tr, TR_EPI_STORE);
-                        }
-                    } else {
-                        tmem_wait_ld_only();
-                        reg_fence32(r);
-                        if (mark) trace_mark(tr, TR_EPI_LD);
-                        if (col < p.N && rows_live) {
-                            float b[32];
-                            if (p.bias) {
-                                load_bias32<DT>(p.bias, col, p.N, b);
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) b[i] = 0.0f;
-                            }
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const float z = __uint_as_float(r[i]) + b[i];
-                                if (EPI == EPI_GELU_ERF) v[i] = gelu_erf_f(z);
-                                else if (EPI == EPI_GELU_TANH) v[i] = gelu_tanh_f(z);
-                                else v[i] = z;
-                            }
-                            if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
-                            if (mark) trace_mark(tr, TR_EPI_STORE);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
-                    else mbar_arrive(acce);
-                }
-            } else if (p.cluster_sk) {
-                // split-K inside a cluster: the SK CTAs of this tile hold their fp32 partials
-                // in their own (now idle) stage rings; each CTA reduces a share of the tile's
-                // 32 x 32 blocks by reading all SK partials through distributed shared memory,
-                // in split order, and stores them.  No global scratch, no atomics.
-                // partial layout [32-column group][16-byte chunk][row][4 floats]: a warp's access
-                // to one chunk of its 32 rows is 512 contiguous bytes, locally and remotely
-                for (int g = half; g < ngroups; g += 2) {
-                    uint32_t r[32];
-                    tmem_ld32(tq + 32u * g, r);
-                    tmem_wait_ld_only();
-                    reg_fence32(r);
-                    const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)row) * 16u;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        st_shared_v4(a + 2048u * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(acce);
-                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                    for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_pready, (uint32_t)s));
-                }
-                const bool ready = wait_phase(bar_pready, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
-                                              p.wait_limit_ns);
-                if (ready) {
-                    const int units = 4 * ngroups;  // 32-row blocks x 32-column groups of the tile
-                    int mine = 0;                   // index among this CTA's units
-                    for (int u = c.split; u < units; u += p.split_k, ++mine) {
-                        if ((mine & (kEpiWarps - 1)) != ew) continue;
-                        const int rb = u / ngroups, g = u - rb * ngroups;
-                        const int col = n0 + 32 * g;
-                        const int yb = m0 + 32 * rb;
-                        if (col >= p.N || yb >= p.M) continue;  // warp-uniform
-                        const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)(32 * rb + lane)) * 16u;
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                        for (int sp = 0; sp < p.split_k; ++sp) {  // split order: deterministic
-                            const uint32_t ra = mapa_rank(a, (uint32_t)sp);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                float4 x[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) x[i] = ld_cluster_v4(ra + 2048u * (4u * h + i));
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    v[16 * h + 4 * i] += x[i].x;
-                                    v[16 * h + 4 * i + 1] += x[i].y;
-                                    v[16 * h + 4 * i + 2] += x[i].z;
-                                    v[16 * h + 4 * i + 3] += x[i].w;
-                                }
-                            }
-                        }
-                        if (p.bias) {
-                            float b[32];
-                            load_bias32<DT>(p.bias, col, p.N, b);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += b[i];
-                        }
-                        stage_and_store<DT>(&tmC, stg, lane, v, col, yb);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                    for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_rdone, (uint32_t)s));
-                }
-                // no CTA leaves (and frees its shared memory) while a peer still reads it
-                wait_phase(bar_rdone, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
-            } else {
-                // split-K: this split's fp32 partial in a private layout in which every
-                // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]
-                const size_t half_tile = (size_t)c.mn * PAIR + rank;  // this CTA's 128-row half of the tile
-                float4* part = reinterpret_cast<float4*>(
-                    p.partials + (((size_t)c.split * tiles_mn) * PAIR + half_tile) * tile_elems);
-                for (int g = half; g < ngroups; g += 2) {
-                    uint32_t r[32];
-                    tmem_ld32(tq + 32u * g, r);
-                    tmem_wait_ld_only();
-                    reg_fence32(r);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float4* dst = part + (size_t)(2 * g + h) * 4 * kBM + row;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i * kBM] = make_float4(__uint_as_float(r[16 * h + 4 * i]), __uint_as_float(r[16 * h + 4 * i + 1]),
-                                                 __uint_as_float(r[16 * h + 4 * i + 2]),
-                                                 __uint_as_float(r[16 * h + 4 * i + 3]));
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
-                    else mbar_arrive(acce);
-                }
-                // the barrier orders every epilogue thread's partial stores before the
-                // arrival thread's gpu-scope release (fences are cumulative)
-                epi_bar_sync();
-                if (ew == 0 && lane == 0) {
-                    __threadfence();
-                    const int prev = atomicAdd(p.counters + half_tile, 1);
-                    const int last = (prev == p.split_k - 1);
-                    if (last) {
-                        atomicExch(p.counters + half_tile, 0);  // ready for the next run
-                        __threadfence();                   // acquire the other splits' partials
-                    }
-                    *last_flag = last;
-                }
-                epi_bar_sync();
-                if (*last_flag) {
-                    for (int g = half; g < ngroups; g += 2) {
-                        const int col = n0 + 32 * g;
-                        if (col >= p.N || !rows_live) continue;  // warp-uniform
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            // 16 columns of this row from every split: up to 4 splits' loads in
-                            // flight at once, summed in split order (deterministic)
-                            const size_t off = (size_t)(2 * g + h) * 4 * kBM + row;  // in float4
-                            for (int s0 = 0; s0 < p.split_k; s0 += 4) {
-                                float4 x[4][4];
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    if (s0 + j < p.split_k) {
-                                        const float4* src = reinterpret_cast<const float4*>(
-                                            p.partials + (((size_t)(s0 + j) * tiles_mn) * PAIR + half_tile) * tile_elems) + off;
-#pragma unroll
-                                        for (int i = 0; i < 4; ++i) x[j][i] = __ldcg(src + i * kBM);
-                                    }
-                                }
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    if (s0 + j < p.split_k) {
-#pragma unroll
-                                        for (int i = 0; i < 4; ++i) {
-                                            v[16 * h + 4 * i] += x[j][i].x;
-                                            v[16 * h + 4 * i + 1] += x[j][i].y;
-                                            v[16 * h + 4 * i + 2] += x[j][i].z;
-                                            v[16 * h + 4 * i + 3] += x[j][i].w;
-                                        }
-                                    }
-                                }
-                            }
-                        }
-                        if (p.bias) {
-                            float b[32];
-                            load_bias32<DT>(p.bias, col, p.N, b);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += b[i];
-                        }
-                        stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
-                    }
-                }
-                epi_bar_sync();  // last_flag is rewritten for the next tile
-            }
-            if (tr && warp == 2 && lane == 0) {
-                if (local == 0) trace_mark(tr, TR_EPI_DONE);
-                trace_mark(tr, TR_LAST_EPI);
-            }
-        }
-        // every TMA store of this warp has completed before the CTA may exit
-        if (lane == 0) bulk_wait0();
-        __syncwarp();
-        if (tr && warp == 2 && lane == 0) trace_mark(tr, TR_EPI_DRAIN);
-    }
-
-    // ------------------------------ teardown ------------------------------
-    tc_fence_before();
-    __syncthreads();
-    if (PAIR == 2 || p.cluster_sk) cluster_sync_all();  // no CTA leaves while a peer may still signal it
-    if (threadIdx.x == 0 && tr) {
-        trace_mark(tr, TR_EXIT);
-        tr[(size_t)blockIdx.x * kTraceSlots + TR_SMID] = sm_id();
-    }
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc<PAIR>(tmem_base, kTmemCols);
-    }
-}
 
 __global__ void kt_timestamp_kernel(unsigned long long* dst) { *dst = global_ns(); }
 
@@ -1036,8 +19,123 @@ __global__ void kt_activation_kernel(int act, const float* __restrict__ z, const
         if (act == KT_ACT_GELU_ERF) y = gelu_erf_f(x);
         else if (act == KT_ACT_GELU_TANH) y = gelu_tanh_f(x);
         else if (act == KT_ACT_GEGLU) y = x * gelu_erf_f(g[i]);
+        else if (act == KT_ACT_GELU_SIGMOID) y = gelu_sigmoid_f(x);
+        else if (act == KT_ACT_SILU) y = silu_f(x);
         else y = x;
         out[i] = y;
+    }
+}
+
+// LayerNorm prologue ("SDXL as a requirements inventory", section 1.3: the block's
+// feed-forward reads LayerNorm(x)).  One warp per row: the row is read once (kept in
+// registers as packed 16-bit vectors when D <= 2048, re-read from L1 / L2 beyond),
+// mean and biased variance over D in fp32 (two passes: the variance is a sum of
+// squared deviations from the mean, no cancellation), then (x - mean) / sqrt(var + eps) * gamma +
+// beta rounded once to the dtype.  HBM-bound: 2 * M * D * 2 bytes.
+constexpr int kLnWarps = 8;
+constexpr int kLnCache = 8;  // 16-byte vectors per lane kept in registers: D <= 32 * 8 * 8
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kLnWarps * 32) kt_layernorm_kernel(const uint4* __restrict__ X,
+                                                                      const uint4* __restrict__ gamma,
+                                                                      const uint4* __restrict__ beta, float eps,
+                                                                      uint4* __restrict__ Xn, int M, int D) {
+    // X may be the previous kernel's output: wait for it (no-op without a dependency)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int row = (int)blockIdx.x * kLnWarps + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const int nv = D >> 3;  // 16-byte vectors per row
+    const uint4* xr = X + (size_t)row * (size_t)nv;
+    const bool cached = nv <= 32 * kLnCache;
+    // Statistics of the deviations from the row's first element x0: x - x0 is exact in
+    // fp32 for 16-bit inputs, and the sums then carry rounding errors relative to the
+    // spread of the row rather than to its mean (a row far from zero with a small spread
+    // would otherwise lose the normalised value's low bits).
+    float x0;
+    {
+        float f[8];
+        unpack8<DT>(xr[0], f);
+        x0 = f[0];
+    }
+    uint4 c[kLnCache];
+    float s = 0.0f;
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kLnCache; ++i) {
+            const int j = lane + 32 * i;
+            if (j < nv) {
+                c[i] = xr[j];
+                float f[8];
+                unpack8<DT>(c[i], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s += f[e] - x0;
+            }
+        }
+    } else {
+        for (int j = lane; j < nv; j += 32) {
+            float f[8];
+            unpack8<DT>(xr[j], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s += f[e] - x0;
+        }
+    }
+    const float dmean = warp_sum(s) / (float)D;  // mean - x0
+    float q = 0.0f;
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kLnCache; ++i) {
+            if (lane + 32 * i < nv) {
+                float f[8];
+                unpack8<DT>(c[i], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float dv = (f[e] - x0) - dmean;
+                    q += dv * dv;
+                }
+            }
+        }
+    } else {
+        for (int j = lane; j < nv; j += 32) {
+            float f[8];
+            unpack8<DT>(xr[j], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float dv = (f[e] - x0) - dmean;
+                q += dv * dv;
+            }
+        }
+    }
+    const float var = warp_sum(q) / (float)D;
+    const float rstd = 1.0f / sqrtf(var + eps);
+    uint4* yr = Xn + (size_t)row * (size_t)nv;
+    auto emit = [&](int j, const uint4& w) {
+        float f[8], g[8], b[8], y[8];
+        unpack8<DT>(w, f);
+        unpack8<DT>(gamma[j], g);
+        unpack8<DT>(beta[j], b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = ((f[e] - x0) - dmean) * rstd * g[e] + b[e];
+        uint4 o;
+        o.x = pack2<DT>(y[0], y[1]);
+        o.y = pack2<DT>(y[2], y[3]);
+        o.z = pack2<DT>(y[4], y[5]);
+        o.w = pack2<DT>(y[6], y[7]);
+        yr[j] = o;
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kLnCache; ++i)
+            if (lane + 32 * i < nv) emit(lane + 32 * i, c[i]);
+    } else {
+        for (int j = lane; j < nv; j += 32) emit(j, xr[j]);
     }
 }
 
@@ -1045,13 +143,13 @@ __global__ void kt_activation_kernel(int act, const float* __restrict__ z, const
 // Host side
 // ---------------------------------------------------------------------------
 
-uint32_t make_idesc(int dtype, int n, int m) {
+uint32_t make_idesc(int dtype, int n, int m, int b_kmajor) {
     uint32_t d = 0;
     d |= 1u << 4;                                   // D (accumulator) format: f32
     d |= (dtype == KT_BF16 ? 1u : 0u) << 7;         // A format: f16 = 0, bf16 = 1
     d |= (dtype == KT_BF16 ? 1u : 0u) << 10;        // B format
     /* bit 15 = 0: A is K-major */
-    d |= 1u << 16;                                  // B is MN-major
+    d |= (b_kmajor ? 0u : 1u) << 16;                // B: MN-major (1) or K-major (0)
     d |= (uint32_t)(n >> 3) << 17;                  // N >> 3
     d |= (uint32_t)(m >> 4) << 24;                  // M >> 4 (256 for a CTA pair)
     return d;
@@ -1073,52 +171,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int EPI, int DT, int PAIR>
-kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmParams& p,
-                     int grid, int smem, void* stream, bool pdl, const char** why) {
-    auto kern = kt_gemm_kernel<EPI, DT, PAIR>;
-    // opt in to the shared memory this launch needs (idempotent, cheap after the first call)
-    static std::atomic<int> max_set[16];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 16 || max_set[dev].load(std::memory_order_relaxed) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) {
-            *why = cudaGetErrorString(e);
-            return KT_ERR_CUDA;
-        }
-        if (dev >= 0 && dev < 16) max_set[dev].store(kSmemBudget);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    if (PAIR == 2 || p.cluster_sk) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = PAIR == 2 ? 2 : (unsigned)p.split_k;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    cfg.attrs = na ? attr : nullptr;
-    cfg.numAttrs = na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
-    if (e != cudaSuccess) {
-        *why = cudaGetErrorString(e);
-        return KT_ERR_CUDA;
-    }
-    return KT_OK;
-}
-
 }  // namespace
+
 
 // ---------------------------------------------------------------------------
 // Allocation-free down projection (kt_down_proj_noalloc)
@@ -1261,6 +315,36 @@ kt_status launch_timestamp(void* dst, void* stream, const char** why) {
     return KT_OK;
 }
 
+kt_status launch_layernorm(int dtype, const void* X, const void* gamma, const void* beta, float eps, void* Xn,
+                           int64_t M, int64_t D, void* stream, const char** why) {
+    if (M < 1 || D < 8 || D % 8 != 0 || M > INT32_MAX || D > INT32_MAX) {
+        *why = "LayerNorm: M >= 1 and D a positive multiple of 8";
+        return KT_ERR_INVALID;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((M + kLnWarps - 1) / kLnWarps), 1, 1);
+    cfg.blockDim = dim3(kLnWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint4* x = static_cast<const uint4*>(X);
+    const uint4* g = static_cast<const uint4*>(gamma);
+    const uint4* b = static_cast<const uint4*>(beta);
+    uint4* y = static_cast<uint4*>(Xn);
+    cudaError_t e = dtype == KT_BF16
+                        ? cudaLaunchKernelEx(&cfg, kt_layernorm_kernel<KT_BF16>, x, g, b, eps, y, (int)M, (int)D)
+                        : cudaLaunchKernelEx(&cfg, kt_layernorm_kernel<KT_F16>, x, g, b, eps, y, (int)M, (int)D);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    return KT_OK;
+}
+
 kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
                             const char** why) {
     const int64_t blocks = n == 0 ? 0 : std::min<int64_t>((n + 255) / 256, 4096);
@@ -1312,27 +396,15 @@ kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, cons
         *why = "inconsistent cluster split-K launch";
         return KT_ERR_INVALID;
     }
-#define KT_LAUNCH(E, D)                                                                   \
-    return p.pair == 2 ? launch_one<E, D, 2>(a, b, c, p, grid, smem_bytes, stream, pdl, why) \
-                       : launch_one<E, D, 1>(a, b, c, p, grid, smem_bytes, stream, pdl, why)
-    if (dtype == KT_F16) {
-        switch (epi) {
-            case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_F16);
-            case EPI_GELU_TANH: KT_LAUNCH(EPI_GELU_TANH, KT_F16);
-            case EPI_GEGLU: KT_LAUNCH(EPI_GEGLU, KT_F16);
-            case EPI_NONE: KT_LAUNCH(EPI_NONE, KT_F16);
-            case EPI_DOWN: KT_LAUNCH(EPI_DOWN, KT_F16);
-        }
-    } else {
-        switch (epi) {
-            case EPI_GELU_ERF: KT_LAUNCH(EPI_GELU_ERF, KT_BF16);
-            case EPI_GELU_TANH: KT_LAUNCH(EPI_GELU_TANH, KT_BF16);
-            case EPI_GEGLU: KT_LAUNCH(EPI_GEGLU, KT_BF16);
-            case EPI_NONE: KT_LAUNCH(EPI_NONE, KT_BF16);
-            case EPI_DOWN: KT_LAUNCH(EPI_DOWN, KT_BF16);
-        }
+    switch (epi) {
+        case EPI_GELU_ERF:
+        case EPI_GELU_TANH:
+        case EPI_GELU_SIGMOID:
+        case EPI_SILU:
+        case EPI_NONE: return launch_gemm_act(epi, dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
+        case EPI_GEGLU: return launch_gemm_geglu(dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
+        case EPI_DOWN: return launch_gemm_down(dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
     }
-#undef KT_LAUNCH
     *why = "unknown epilogue kind";
     return KT_ERR_INVALID;
 }

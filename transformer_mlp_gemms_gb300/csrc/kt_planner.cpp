@@ -61,22 +61,24 @@ double epi_cost_per_elem(int epi) {      // seconds per output element per SM (m
         case EPI_GELU_TANH: return 0.07e-9;
         case EPI_GEGLU: return 0.13e-9;
         case EPI_NONE: return 0.03e-9;
+        case EPI_GELU_SIGMOID:
+        case EPI_SILU: return 0.07e-9;
         default: return 0.03e-9;
     }
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int max_stages(int BN, int n_b, int pair, int bk) {
-    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair, bk);
+int max_stages(int BN, int n_b, int pair, int bk, int kmaj) {
+    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair, bk, kmaj);
     return std::min(s, kMaxStages);
 }
 
 constexpr int kGpcs = 8;  // GB300: 152 SMs in 8 GPCs; a cluster must fit in one GPC
 
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
-              int bk, GemmConfig* g, bool cluster_sk = false) {
-    int stages = max_stages(BN, n_b, pair, bk);
+              int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0) {
+    int stages = max_stages(BN, n_b, pair, bk, kmaj);
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
     const int64_t bm = (int64_t)kBM * pair;  // rows per tile (a pair's tile spans two CTAs)
@@ -96,7 +98,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
         const int64_t per_gpc = (num_sms / kGpcs) / SK;
         if (epi != EPI_DOWN || pair != 1 || SK < 2 || SK > 8 || per_gpc < 1) return false;
         if (tm * tn > per_gpc * kGpcs) return false;
-        if ((int64_t)stages * stage_bytes(BN, n_b, pair, bk) < (int64_t)kBM * BN * 4) return false;
+        if ((int64_t)stages * stage_bytes(BN, n_b, pair, bk, kmaj) < (int64_t)kBM * BN * 4) return false;
         grid = ctas;
         waves = 1;
     }
@@ -106,7 +108,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     // operands, and the load latency the ring of `stages` k-blocks has to cover
     double t_mma = n_b * 2.0 * kBM * BN * bk / kRsm;
     double t_issue = kIssuePerStage + n_b * (bk / 16) * kIssuePerMma;
-    double bytes_kb = (double)stage_bytes(BN, n_b, pair, bk);
+    double bytes_kb = (double)stage_bytes(BN, n_b, pair, bk, kmaj);
     double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
     double t_kb = std::max(std::max(t_mma, t_issue), std::max(bytes_kb / feed, kLoadLatency / stages));
     double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0);
@@ -125,7 +127,8 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->tiles_m = (int)tm; g->tiles_n = (int)tn; g->kblocks = (int)kb;
     g->kblocks_per_split = (int)kps;
     g->grid = (int)grid; g->waves = (int)waves;
-    g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk) + kSmemReserve;
+    g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk, kmaj) + kSmemReserve;
+    g->b_kmajor = kmaj;
     g->n_b = n_b;
     g->pair = pair;
     g->bk = bk;
@@ -147,7 +150,7 @@ bool better(const GemmConfig& a, const GemmConfig& b) {
 }
 
 bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int num_sms,
-            GemmConfig* best, bool allow_cluster_sk) {
+            GemmConfig* best, bool allow_cluster_sk, int kmaj) {
     bool found = false;
     for (int pair = 1; pair <= 2; ++pair) {
         for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
@@ -156,7 +159,7 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
                 for (int SK = 1; SK <= max_sk; ++SK) {
                     for (int cl = 0; cl <= (allow_cluster_sk ? 1 : 0); ++cl) {
                         GemmConfig g;
-                        if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, bk, &g, cl == 1)) continue;
+                        if (!evaluate(M, N, K, BN, SK, n_b, epi, num_sms, pair, bk, &g, cl == 1, kmaj)) continue;
                         if (!found || better(g, *best)) {
                             *best = g;
                             found = true;
@@ -172,9 +175,11 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
 }  // namespace
 
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why, bool allow_cluster_sk) {
+                      const char** why, bool allow_cluster_sk, int w_layout) {
     if (M < 1 || D < 1 || F < 1) { *why = "M, D and F must be positive"; return KT_ERR_INVALID; }
-    if (act < 0 || act > 3) { *why = "unknown activation"; return KT_ERR_INVALID; }
+    if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) { *why = "unknown activation"; return KT_ERR_INVALID; }
+    if (w_layout != KT_W_IN_OUT && w_layout != KT_W_OUT_IN) { *why = "unknown weight layout"; return KT_ERR_INVALID; }
+    const int kmaj = w_layout == KT_W_OUT_IN ? 1 : 0;
     if (num_sms < 1) { *why = "num_sms must be positive"; return KT_ERR_INVALID; }
     if (D % 8 != 0 || F % 8 != 0) {
         *why = "D and F must be multiples of 8 (16-byte row pitch for TMA)";
@@ -187,15 +192,13 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         *why = "sizes beyond the supported index range";
         return KT_ERR_UNSUPPORTED;
     }
-    int epi_up = act == KT_ACT_GELU_ERF ? EPI_GELU_ERF
-               : act == KT_ACT_GELU_TANH ? EPI_GELU_TANH
-               : act == KT_ACT_GEGLU ? EPI_GEGLU : EPI_NONE;
+    int epi_up = up_epilogue(act);
     int n_b = act == KT_ACT_GEGLU ? 2 : 1;
-    if (!choose(M, F, D, n_b, epi_up, 1, num_sms, &out->up, false)) {
+    if (!choose(M, F, D, n_b, epi_up, 1, num_sms, &out->up, false, kmaj)) {
         *why = "no feasible tile for the up projection";
         return KT_ERR_UNSUPPORTED;
     }
-    if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down, allow_cluster_sk)) {
+    if (!choose(M, D, F, 1, EPI_DOWN, 16, num_sms, &out->down, allow_cluster_sk, kmaj)) {
         *why = "no feasible tile for the down projection";
         return KT_ERR_UNSUPPORTED;
     }
@@ -206,7 +209,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         GemmConfig g;
         int nf = std::sscanf(e, "%d,%d,%d", &bn, &pr, &bk);
         if (nf < 1 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
-            bn > 256 || !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, bk, &g)) {
+            bn > 256 || !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, bk, &g, false, kmaj)) {
             *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32, 64 for a pair; BK 64 or 128)";
             return KT_ERR_INVALID;
         }
@@ -218,13 +221,24 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         int nf = std::sscanf(e, "%d,%d,%d,%d,%d", &bn, &sk, &pr, &bk, &cl);
         if (nf < 2 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
             bn > 256 || sk < 1 || sk > 64 || (cl && !allow_cluster_sk) ||
-            !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g, cl != 0)) {
+            !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g, cl != 0, kmaj)) {
             *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR[,BK[,CLUSTER]]]\" (no empty split)";
             return KT_ERR_INVALID;
         }
         out->down = g;
     }
     return KT_OK;
+}
+
+int up_epilogue(int act) {
+    switch (act) {
+        case KT_ACT_GELU_ERF: return EPI_GELU_ERF;
+        case KT_ACT_GELU_TANH: return EPI_GELU_TANH;
+        case KT_ACT_GEGLU: return EPI_GEGLU;
+        case KT_ACT_GELU_SIGMOID: return EPI_GELU_SIGMOID;
+        case KT_ACT_SILU: return EPI_SILU;
+    }
+    return EPI_NONE;
 }
 
 void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* o) {

@@ -16,8 +16,9 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libkt_mlp.so")
 
-KT_ACT_GELU_ERF, KT_ACT_GELU_TANH, KT_ACT_GEGLU, KT_ACT_NONE = 0, 1, 2, 3
+KT_ACT_GELU_ERF, KT_ACT_GELU_TANH, KT_ACT_GEGLU, KT_ACT_NONE, KT_ACT_GELU_SIGMOID, KT_ACT_SILU = range(6)
 KT_F16, KT_BF16 = 0, 1
+KT_W_IN_OUT, KT_W_OUT_IN = 0, 1
 KT_OK, KT_ERR_INVALID, KT_ERR_UNSUPPORTED, KT_ERR_CUDA, KT_ERR_TIMEOUT, KT_ERR_NOMEM = range(6)
 STATUS_NAMES = {0: "KT_OK", 1: "KT_ERR_INVALID", 2: "KT_ERR_UNSUPPORTED", 3: "KT_ERR_CUDA",
                 4: "KT_ERR_TIMEOUT", 5: "KT_ERR_NOMEM"}
@@ -45,13 +46,39 @@ class kt_plan_info(ctypes.Structure):
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("bias", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32),
                 ("up", kt_gemm_plan_info), ("down", kt_gemm_plan_info),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64),
+                ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
+                ("ln_eps", ctypes.c_float)]
 
     def as_dict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_ if n not in ("up", "down")}
         d["up"] = self.up.as_dict()
         d["down"] = self.down.as_dict()
         return d
+
+
+class kt_mlp_options(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("F", ctypes.c_int64),
+                ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("bias", ctypes.c_int32),
+                ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
+                ("ln_eps", ctypes.c_float)]
+
+
+class kt_mlp_tensors(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("X", "W_up", "W_down", "b_up", "b_down", "R", "ln_gamma", "ln_beta", "Y", "H_out")]
+
+
+def options(M, D, F, act, dtype, bias=False, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
+            ln_eps=1e-5) -> kt_mlp_options:
+    return kt_mlp_options(M, D, F, act, dtype, int(bias), int(residual), int(layernorm), weight_layout,
+                          ln_eps if layernorm else 0.0)
+
+
+def tensors(X, W_up, W_down, Y, b_up=None, b_down=None, R=None, ln_gamma=None, ln_beta=None,
+            H_out=None) -> kt_mlp_tensors:
+    return kt_mlp_tensors(_ptr(X), _ptr(W_up), _ptr(W_down), _ptr(b_up), _ptr(b_down), _ptr(R), _ptr(ln_gamma),
+                          _ptr(ln_beta), _ptr(Y), _ptr(H_out))
 
 
 _lock = threading.Lock()
@@ -64,6 +91,10 @@ _I32 = ctypes.c_int
 SIGNATURES = {
     "kt_mlp_plan": ([_I64, _I64, _I64, _I32, _I32, _I32, ctypes.POINTER(_VP)], _I32),
     "kt_mlp_run": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "kt_mlp_plan_ex": ([ctypes.POINTER(kt_mlp_options), ctypes.POINTER(_VP)], _I32),
+    "kt_mlp_plan_info_ex": ([ctypes.POINTER(kt_mlp_options), _I32, ctypes.POINTER(kt_plan_info)], _I32),
+    "kt_mlp_run_ex": ([_VP, ctypes.POINTER(kt_mlp_tensors), _VP], _I32),
+    "kt_mlp_run_ex_timed": ([_VP, ctypes.POINTER(kt_mlp_tensors), _VP, ctypes.POINTER(ctypes.c_float)], _I32),
     "kt_mlp_run_with_h": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "kt_mlp_run_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "kt_mlp_run_timed": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_float),
@@ -137,6 +168,29 @@ def kt_mlp_plan(M: int, D: int, F: int, act: int, dtype: int, bias: bool) -> int
     out = _VP()
     _check(load().kt_mlp_plan(M, D, F, act, dtype, int(bias), ctypes.byref(out)), "kt_mlp_plan")
     return out.value
+
+
+def kt_mlp_plan_ex(opts: kt_mlp_options) -> int:
+    out = _VP()
+    _check(load().kt_mlp_plan_ex(ctypes.byref(opts), ctypes.byref(out)), "kt_mlp_plan_ex")
+    return out.value
+
+
+def kt_mlp_plan_info_ex(opts: kt_mlp_options, num_sms: int) -> dict:
+    info = kt_plan_info()
+    _check(load().kt_mlp_plan_info_ex(ctypes.byref(opts), num_sms, ctypes.byref(info)), "kt_mlp_plan_info_ex")
+    return info.as_dict()
+
+
+def kt_mlp_run_ex(plan: int, t: kt_mlp_tensors, stream=None) -> None:
+    _check(load().kt_mlp_run_ex(plan, ctypes.byref(t), _stream(stream)), "kt_mlp_run_ex")
+
+
+def kt_mlp_run_ex_timed(plan: int, t: kt_mlp_tensors, stream=None):
+    """Returns (ms_layernorm, ms_up, ms_down): device time of each kernel (CUDA events)."""
+    ms = (ctypes.c_float * 3)()
+    _check(load().kt_mlp_run_ex_timed(plan, ctypes.byref(t), _stream(stream), ms), "kt_mlp_run_ex_timed")
+    return ms[0], ms[1], ms[2]
 
 
 def kt_mlp_run(plan: int, X, W_up, W_down, b_up, b_down, Y, stream=None) -> None:
@@ -215,11 +269,28 @@ def kt_debug_timestamp(dst, stream=None) -> None:
 
 
 class Plan:
-    """Owning handle: ``Plan(M, D, F, act, dtype, bias)``; destroyed with the object."""
+    """Owning handle: ``Plan(M, D, F, act, dtype, bias)`` (kt_mlp_plan), or with any of
+    ``residual``, ``layernorm``, ``weight_layout``, ``ln_eps`` (kt_mlp_plan_ex);
+    destroyed with the object."""
 
-    def __init__(self, M, D, F, act, dtype, bias):
+    def __init__(self, M, D, F, act, dtype, bias, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
+                 ln_eps=1e-5):
         self.M, self.D, self.F, self.act, self.dtype, self.bias = M, D, F, act, dtype, bool(bias)
-        self.handle = kt_mlp_plan(M, D, F, act, dtype, bias)
+        self.residual, self.layernorm, self.weight_layout = bool(residual), bool(layernorm), weight_layout
+        if residual or layernorm or weight_layout != KT_W_IN_OUT:
+            self.handle = kt_mlp_plan_ex(options(M, D, F, act, dtype, bias, residual, layernorm, weight_layout,
+                                                 ln_eps))
+        else:
+            self.handle = kt_mlp_plan(M, D, F, act, dtype, bias)
+
+    def run_ex(self, X, W_up, W_down, Y, b_up=None, b_down=None, R=None, ln_gamma=None, ln_beta=None,
+               H_out=None, stream=None):
+        kt_mlp_run_ex(self.handle, tensors(X, W_up, W_down, Y, b_up, b_down, R, ln_gamma, ln_beta, H_out), stream)
+
+    def run_ex_timed(self, X, W_up, W_down, Y, b_up=None, b_down=None, R=None, ln_gamma=None, ln_beta=None,
+                     stream=None):
+        return kt_mlp_run_ex_timed(self.handle, tensors(X, W_up, W_down, Y, b_up, b_down, R, ln_gamma, ln_beta),
+                                   stream)
 
     def run(self, X, W_up, W_down, b_up, b_down, Y, stream=None):
         kt_mlp_run(self.handle, X, W_up, W_down, b_up, b_down, Y, stream)
