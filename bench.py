@@ -7,6 +7,12 @@ seeded synthetic input already resident in HBM.  The default workload is the F16
 SigLIP MLP X[1,729,1152] -> 4304 -> 1152 with tanh GELU and no biases.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl kt|reference]
+                    [--block ln,res] [--weights in_out|out_in]
+
+``--block`` runs the feed-forward as a transformer block applies it (LayerNorm
+prologue kernel and / or the residual add fused into the down projection);
+``--weights out_in`` passes the weights in PyTorch's nn.Linear order.  The
+FLOP count stays that of the two GEMMs.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
 device synchronize on both sides.  Each step's device time is taken with CUDA
@@ -52,6 +58,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="siglip")
+    ap.add_argument("--block", default="", help="comma list of block options: ln (LayerNorm prologue), "
+                                                 "res (residual add in the down epilogue)")
+    ap.add_argument("--weights", choices=["in_out", "out_in"], default="in_out")
     ap.add_argument("--impl", choices=["kt", "reference"], default="kt")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample (kt arm)")
@@ -78,9 +87,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("kt_gemm.cuh", "kt_gemm_act.cu", "kt_gemm_geglu.cu", "kt_gemm_down.cu", "kt_mlp_kernels.cu",
+                  "kt_internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("kt_mlp_kernels.cu", "kt_internal.h"):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "transformer_mlp_gemms_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -182,12 +195,30 @@ def oracle_baseline(w, t_bits, min_seconds: float, max_seconds: float = 30.0):
                       f"({done_rows * flops_row / 1e9:.1f} GFLOP in {t_total:.1f} s, float64, OpenMP over rows)"}
 
 
-def workload_config(w, l2):
+def block_options(args):
+    opts = {o for o in args.block.split(",") if o}
+    bad = opts - {"ln", "res"}
+    if bad:
+        raise SystemExit(f"unknown --block option(s): {sorted(bad)}")
+    return "ln" in opts, "res" in opts, args.weights == "out_in"
+
+
+def traffic_key(w, args) -> str:
+    ln, res, outin = block_options(args)
+    tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin)) if on]
+    return w.name + (f"[{','.join(tags)}]" if tags else "")
+
+
+def workload_config(w, l2, args=None):
     from transformer_mlp_gemms_gb300 import workloads as wl
-    return {"workload": f"{w.name}: X[{w.batch},{w.tokens},{w.D}] -> {w.F_up} -> {w.D}",
-            "M": w.M, "D": w.D, "F": w.F, "F_up": w.F_up, "act": wl.ACT_NAMES[w.act],
-            "io_dtype": wl.DT_NAMES[w.dtype], "bias": w.bias, "seed": w.seed,
-            "flops_per_call": w.flops, "l2": l2}
+    cfg = {"workload": f"{w.name}: X[{w.batch},{w.tokens},{w.D}] -> {w.F_up} -> {w.D}",
+           "M": w.M, "D": w.D, "F": w.F, "F_up": w.F_up, "act": wl.ACT_NAMES[w.act],
+           "io_dtype": wl.DT_NAMES[w.dtype], "bias": w.bias, "seed": w.seed,
+           "flops_per_call": w.flops, "l2": l2}
+    if args is not None:
+        ln, res, outin = block_options(args)
+        cfg["block"] = {"layernorm": ln, "residual": res, "weights": "out_in" if outin else "in_out"}
+    return cfg
 
 
 def emit(line, args):
@@ -265,15 +296,27 @@ def main():
         dist.barrier()
     kt_mlp.load()
 
-    t = wl.generate(w)
-    d = {k: v.cuda() for k, v in t.items()}
+    ln, res, outin = block_options(args)
+    plain = not (ln or res)
+    t = wl.generate(w, residual=res, layernorm=ln)
+    dev_t = wl.torch_order(t) if outin else t
+    d = {k: v.cuda() for k, v in dev_t.items()}
     tdt = wl.TORCH_DTYPES[w.dtype]
     Y = torch.empty((w.M, w.D), dtype=tdt, device="cuda")
-    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias, residual=res, layernorm=ln,
+                       weight_layout=kt_mlp.KT_W_OUT_IN if outin else kt_mlp.KT_W_IN_OUT)
     info = plan.info()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     args_run = (d["X"], d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Y)
+    ex_kw = dict(b_up=d.get("b_up"), b_down=d.get("b_down"), R=d.get("R"), ln_gamma=d.get("ln_gamma"),
+                 ln_beta=d.get("ln_beta"))
+
+    def run_once(X=d["X"], Yo=Y):
+        if plain:
+            plan.run(X, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yo)
+        else:
+            plan.run_ex(X, d["W_up"], d["W_down"], Yo, **ex_kw)
 
     props = torch.cuda.get_device_properties(local)
     gpu_id = str(local)
@@ -284,7 +327,7 @@ def main():
 
     for _ in range(args.warmup):
         flush.zero_()
-        plan.run(*args_run)
+        run_once()
     torch.cuda.synchronize()
     if plan.status() != kt_mlp.KT_OK:
         raise RuntimeError("device status after warm-up: " + kt_mlp.kt_last_error())
@@ -299,7 +342,7 @@ def main():
     for i in range(args.steps):
         flush.zero_()                 # L2 scrub, outside the step's events
         starts[i].record(stream)
-        plan.run(*args_run)
+        run_once()
         ends[i].record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -310,25 +353,44 @@ def main():
         raise RuntimeError("device status after the timed steps: " + kt_mlp.kt_last_error())
 
     # ---------------- per-kernel device time (same steps, events between the kernels) ----------------
-    ms_up, ms_dn = [], []
+    ms_ln, ms_up, ms_dn = [], [], []
     for _ in range(max(1, min(args.steps, 500))):
         flush.zero_()
-        a, b = plan.run_timed(*args_run)
+        if plain:
+            a, b = plan.run_timed(*args_run)
+            c0 = 0.0
+        else:
+            c0, a, b = plan.run_ex_timed(d["X"], d["W_up"], d["W_down"], Y, **ex_kw)
+        ms_ln.append(c0)
         ms_up.append(a)
         ms_dn.append(b)
 
     # ---------------- end to end through the C ABI with host buffers ----------------
     Xh = t["X"].pin_memory()
     Yh = torch.empty((w.M, w.D), dtype=tdt).pin_memory()
+    Xs = torch.empty_like(d["X"])
     e2e_steps = max(1, min(args.steps, 500))
+
+    def e2e_once():
+        if plain:  # the library's own host-buffer entry point
+            plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+        else:      # copies on the stream around kt_mlp_run_ex, read back before the clock stops
+            Xs.copy_(Xh, non_blocking=True)
+            kw = dict(ex_kw)
+            if res:
+                kw["R"] = Xs   # the block's residual is its own input: x = ff(LayerNorm(x)) + x
+            plan.run_ex(Xs, d["W_up"], d["W_down"], Y, **kw)
+            Yh.copy_(Y, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
     for _ in range(min(args.warmup, 5)):
-        plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+        e2e_once()
     e2e_s = 0.0
     for _ in range(e2e_steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+        e2e_once()
         e2e_s += time.perf_counter() - t0
     clocks = summarize_clocks(sampler.stop())
 
@@ -348,7 +410,7 @@ def main():
     e2e_value = world * e2e_steps * w.flops / e2e_s / 1e12
     up_flops = 2 * w.M * w.D * w.F_up
     dn_flops = 2 * w.M * w.F * w.D
-    mu, md = statistics.mean(ms_up), statistics.mean(ms_dn)
+    mu, md, ml = statistics.mean(ms_up), statistics.mean(ms_dn), statistics.mean(ms_ln)
     dominant = "up" if mu >= md else "down"
     k_ms, k_flops = (mu, up_flops) if dominant == "up" else (md, dn_flops)
     peak_tflops = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])  # fp16 : bf16 nominal 1 : 1
@@ -357,24 +419,29 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.DT_NAMES[w.dtype], "data": "synthetic",
-        "config": workload_config(w, l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"),
+        "config": workload_config(w, l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)", args=args),
         "us_per_call": ms_per_step * 1e3,
         "pct_of_peak": 100.0 * value / world / peak_tflops,
         "peak_tflops": peak_tflops, "peak_source": peak_src,
         "roofline": {"bound": "tensor", "kernel": f"kt_gemm_kernel ({dominant} projection)",
                      "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tflops, "traffic": ncu_traffic(w.name, dominant),
+                     "frac": achieved / peak_tflops, "traffic": ncu_traffic(traffic_key(w, args), dominant),
                      "algorithmic_flops_per_launch": k_flops, "ms_per_launch": k_ms,
                      "peak_note": (f"{peak_src} bf16 dense burst from MEASURED_PEAKS.json (fp16 has the "
                                    f"same nominal rate)") if peak_src == "measured" else "fallback"},
         "kernels_ms": {"up": mu, "down": md, "up_tflops": up_flops / (mu * 1e-3) / 1e12,
                        "down_tflops": dn_flops / (md * 1e-3) / 1e12},
-        "plan": {"up": {k: info["up"][k] for k in ("BN", "stages", "split_k", "grid", "waves")},
-                 "down": {k: info["down"][k] for k in ("BN", "stages", "split_k", "grid", "waves")}},
+        **({"layernorm_kernel": {"ms": ml, "bytes": 2 * w.M * w.D * 2 + 2 * w.D * 2,
+                                 "gbs": (2 * w.M * w.D * 2 + 2 * w.D * 2) / (ml * 1e-3) / 1e9 if ml > 0 else None}}
+           if ln else {}),
+        "plan": {"up": {k: info["up"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "grid", "waves")},
+                 "down": {k: info["down"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "cluster_sk", "grid",
+                                                       "waves")}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.D * 2,
                 "d2h_bytes_per_step": w.M * w.D * 2, "us_per_call": e2e_s / e2e_steps * 1e6,
-                "entry_point": "kt_mlp_run_host (pinned X in, Y out; weights resident)"},
-        "gpu_launches": 2 * args.steps,
+                "entry_point": ("kt_mlp_run_host (pinned X in, Y out; weights resident)" if plain else
+                                "kt_mlp_run_ex between a pinned X copy in and a Y copy out (weights resident)")},
+        "gpu_launches": (3 if ln else 2) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "gpu": props.name, "sms": props.multi_processor_count,

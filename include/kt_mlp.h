@@ -95,6 +95,10 @@ typedef struct {
     int32_t waves;             /* ceil(tiles_m * tiles_n * split_k / SMs)                 */
     int32_t smem_bytes;        /* dynamic shared memory per CTA                           */
     int32_t tmem_cols;         /* tensor-memory columns allocated per CTA                 */
+    int32_t cluster_sk;        /* 1: the split_k CTAs of a tile form a thread-block cluster and
+                                  reduce through distributed shared memory; 0: through global
+                                  memory (or no split)                                     */
+    int32_t b_kmajor;          /* 1: the weight operand is [N][K] (PyTorch order), K-major  */
     int64_t M, N, K;           /* the GEMM: [M,K] x [K,N]                                 */
     double useful_over_padded; /* M*N*K / (padded M * padded N * padded K)                */
     double est_us;             /* the planner's modelled time (a model, not a measurement) */

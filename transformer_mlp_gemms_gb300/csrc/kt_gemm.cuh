@@ -101,15 +101,31 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// As mbar_try_wait, acquiring at cluster scope: for barriers whose phase completes on
+// data written by other CTAs of the cluster (remote asynchronous stores).
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // Wait for the phase of parity `parity` of barrier `bar` to complete.  Returns
 // false if the CTA is aborting or if `limit_ns` passed (then raises the abort
 // flag and records `code` in the error word, first writer wins).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int* err, int code, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_wait()) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if ((i & 31u) == 0) {
             if (*abort_flag) return false;
             if (global_ns() - t0 > limit_ns) {
@@ -195,16 +211,6 @@ __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
 // Arrive on an mbarrier given by its cluster-window address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// 16 bytes from a shared-memory address of any CTA of the cluster.
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
 }
 
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
@@ -339,6 +345,11 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(tm)),
                  "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+// Untiled bulk copy of `bytes` (a multiple of 16) from shared to global memory.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -589,8 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_acce = bar_accf + 16u;
     const uint32_t bar_stall = bar_acce + 16u;
     const uint32_t bar_drain = bar_stall + 8u;
-    const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partial is in smem
-    const uint32_t bar_rdone = bar_pready + 8u;  // cluster split-K: every CTA finished reading mine
+    const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partials are written
     uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 8));
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
@@ -617,7 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_stall, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_pready, (uint32_t)(p.split_k * kEpiWarps));
-        mbar_init(bar_rdone, (uint32_t)(p.split_k * kEpiWarps));
         *abort_flag = 0;
         *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -898,58 +907,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else mbar_arrive(acce);
                 }
             } else if (p.cluster_sk) {
-                // split-K inside a cluster: the SK CTAs of this tile hold their fp32 partials
-                // in their own (now idle) stage rings; each CTA reduces a share of the tile's
-                // 32 x 32 blocks by reading all SK partials through distributed shared memory,
-                // in split order, and stores them.  No global scratch, no atomics.
-                // partial layout [32-column group][16-byte chunk][row][4 floats]: a warp's access
-                // to one chunk of its 32 rows is 512 contiguous bytes, locally and remotely
+                // split-K inside a cluster, reduce-scattered through L2: each 32 x 32 unit of
+                // the tile (row block q, column group g, u = q * ngroups + g) is owned by CTA
+                // u % SK of the cluster, and a unit is handled by the same warp in every CTA.
+                // Each CTA writes its fp32 partial of every unit it does not own to global
+                // scratch ([tile][unit][sender][16-byte chunk][row][4 floats]: 512 contiguous
+                // bytes per warp access), the cluster's epilogue warps signal one another on
+                // an mbarrier in every CTA (release / acquire at cluster scope), and each owner
+                // warp sums its units' SK partials (its own from tensor memory) in split
+                // order (deterministic) and stores them.
+                const uint32_t crank = (uint32_t)c.split;
+                float4* part = reinterpret_cast<float4*>(p.partials) + (size_t)c.mn * (size_t)(4 * ngroups) *
+                                                                           (size_t)p.split_k * 256u;
+                // (the partials go out as 4 KB bulk copies from the idle stage ring: the copy
+                // engine stores faster than per-thread stores do)
                 for (int g = half; g < ngroups; g += 2) {
+                    const int u = q * ngroups + g;
+                    if ((uint32_t)(u % p.split_k) == crank) continue;
                     uint32_t r[32];
                     tmem_ld32(tq + 32u * g, r);
                     tmem_wait_ld_only();
                     reg_fence32(r);
-                    const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)row) * 16u;
+                    const uint32_t slot = base + (uint32_t)u * 4096u;
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        st_shared_v4(a + 2048u * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                        st_shared_v4(slot + 512u * i + 16u * (uint32_t)lane, r[4 * i], r[4 * i + 1], r[4 * i + 2],
+                                     r[4 * i + 3]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) bulk_store(part + ((size_t)u * p.split_k + crank) * 256u, slot, 4096u);
                 }
-                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(acce);
+                    bulk_commit();
+                    bulk_wait0();  // the partials are in global memory
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     asm volatile("fence.acq_rel.cluster;" ::: "memory");
                     for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_pready, (uint32_t)s));
                 }
-                const bool ready = wait_phase(bar_pready, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
-                                              p.wait_limit_ns);
+                if (tr0) trace_mark(tr, TR_EPI_LD);  // (cluster split-K: partials written)
+                const bool ready = wait_phase<true>(bar_pready, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
+                                                    p.wait_limit_ns);
+                if (tr0) trace_mark(tr, TR_EPI_MATH);  // (cluster split-K: every partial written)
                 if (ready) {
-                    const int units = 4 * ngroups;  // 32-row blocks x 32-column groups of the tile
-                    int mine = 0;                   // index among this CTA's units
-                    for (int u = c.split; u < units; u += p.split_k, ++mine) {
-                        if ((mine & (kEpiWarps - 1)) != ew) continue;
-                        const int rb = u / ngroups, g = u - rb * ngroups;
+                    for (int g = half; g < ngroups; g += 2) {
+                        const int u = q * ngroups + g;
+                        if ((uint32_t)(u % p.split_k) != crank) continue;
                         const int col = n0 + 32 * g;
-                        const int yb = m0 + 32 * rb;
-                        if (col >= p.N || yb >= p.M) continue;  // warp-uniform
-                        const uint32_t a = base + ((uint32_t)g * 8u * 128u + (uint32_t)(32 * rb + lane)) * 16u;
+                        if (col >= p.N || !rows_live) continue;  // warp-uniform
+                        uint32_t r[32];
+                        tmem_ld32(tq + 32u * g, r);
+                        tmem_wait_ld_only();
+                        reg_fence32(r);
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        const float4* src = part + (size_t)u * p.split_k * 256u + lane;
                         for (int sp = 0; sp < p.split_k; ++sp) {  // split order: deterministic
-                            const uint32_t ra = mapa_rank(a, (uint32_t)sp);
+                            if ((uint32_t)sp == crank) {
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                float4 x[4];
+                                for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(r[i]);
+                                continue;
+                            }
+                            float4 x[8];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) x[i] = ld_cluster_v4(ra + 2048u * (4u * h + i));
+                            for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + (size_t)sp * 256u + 32 * i);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    v[16 * h + 4 * i] += x[i].x;
-                                    v[16 * h + 4 * i + 1] += x[i].y;
-                                    v[16 * h + 4 * i + 2] += x[i].z;
-                                    v[16 * h + 4 * i + 3] += x[i].w;
-                                }
+                            for (int i = 0; i < 8; ++i) {
+                                v[4 * i] += x[i].x;
+                                v[4 * i + 1] += x[i].y;
+                                v[4 * i + 2] += x[i].z;
+                                v[4 * i + 3] += x[i].w;
                             }
                         }
                         if (p.bias) {
@@ -958,17 +986,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
-                        if (p.residual) add_residual32<DT>(p.residual, yb + lane, p.M, col, p.N, v);
-                        stage_and_store<DT>(&tmC, stg, lane, v, col, yb);
+                        if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
+                        stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
                     }
                 }
+                if (tr0) trace_mark(tr, TR_EPI_STORE);  // (cluster split-K: my units stored)
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                    for (int s = 0; s < p.split_k; ++s) mbar_arrive_cluster(mapa_rank(bar_rdone, (uint32_t)s));
-                }
-                // no CTA leaves (and frees its shared memory) while a peer still reads it
-                wait_phase(bar_rdone, 0u, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
+                if (lane == 0) mbar_arrive(acce);
             } else {
                 // split-K: this split's fp32 partial in a private layout in which every
                 // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]

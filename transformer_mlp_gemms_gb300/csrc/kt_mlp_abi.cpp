@@ -309,7 +309,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
     size_t flag_bytes = 4 * (1 + n_counters);
-    size_t part_bytes = dn.split_k > 1 && !dn.cluster_sk
+    size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
                             : 0;
     size_t io_bytes = (size_t)M * (size_t)D * 2;
@@ -347,7 +347,7 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * o.M * o.D;
-    if (c.down.split_k > 1 && !c.down.cluster_sk)
+    if (c.down.split_k > 1)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
     if (o.layernorm) ws += 2 * o.M * o.D;
     out->workspace_bytes = ws;
@@ -495,12 +495,13 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
     std::snprintf(buf, len,
                   "M=%lld D=%lld F=%lld act=%s dtype=%s bias=%d residual=%d layernorm=%d weights=%s sms=%d | up: %dx%d tiles %dx%d (grid %d, %d "
                   "wave%s, %d stages, useful %.3f, model %.2f us) | down: %dx%d tiles %dx%d split_k %d (grid %d, "
-                  "%d wave%s, %d stages, useful %.3f, model %.2f us) | workspace %lld B",
+                  "%d wave%s, %d stages, %s, useful %.3f, model %.2f us) | workspace %lld B",
                   (long long)plan->M, (long long)plan->D, (long long)plan->F, act_name(plan->act),
                   plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->residual, plan->layernorm,
                   plan->w_layout == KT_W_OUT_IN ? "out_in" : "in_out", plan->num_sms, kt::kBM * u.pair, u.BN, u.tiles_m, u.tiles_n,
                   u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, kt::kBM * d.pair, d.BN,
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
+                  d.split_k == 1 ? "no reduction" : d.cluster_sk ? "cluster reduction" : "global reduction",
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
     return ok();
 }

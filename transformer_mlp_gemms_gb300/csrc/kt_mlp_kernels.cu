@@ -392,7 +392,8 @@ kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, cons
         return KT_ERR_INVALID;
     }
     if (p.cluster_sk && (p.pair != 1 || epi != EPI_DOWN || p.split_k < 2 || p.split_k > 8 ||
-                         grid != p.num_tiles || grid % p.split_k != 0)) {
+                         grid != p.num_tiles || grid % p.split_k != 0 ||
+                         (uint64_t)p.stages * p.stage_bytes < (uint64_t)kBM * (uint64_t)p.BN * 4u)) {
         *why = "inconsistent cluster split-K launch";
         return KT_ERR_INVALID;
     }

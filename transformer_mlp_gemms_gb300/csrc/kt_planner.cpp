@@ -94,7 +94,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     int64_t waves = cdiv(ctas, slots);
     if (cluster_sk) {
         // the SK CTAs of a tile form a cluster: one tile per CTA, all clusters resident at
-        // once, and the stage ring must hold the padded fp32 partial of the tile
+        // once, and the idle stage ring stages the tile's fp32 partial for its bulk copies
         const int64_t per_gpc = (num_sms / kGpcs) / SK;
         if (epi != EPI_DOWN || pair != 1 || SK < 2 || SK > 8 || per_gpc < 1) return false;
         if (tm * tn > per_gpc * kGpcs) return false;
@@ -115,7 +115,8 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
     // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
     // all SK partials, both latency-bound at a few tens of GB/s per SM; in a cluster: the
-    // partial to shared memory, two cluster-wide handshakes, the distributed-smem reads
+    // (SK-1)/SK of the partial other CTAs own written, a cluster-wide handshake, the
+    // owner's reads of its 1/SK of the tile from every other split
     if (SK > 1 && !cluster_sk) t_epi += kBM * BN * 4.0 / 25e9 + SK * (kBM * BN * 4.0) / 60e9;
     if (SK > 1 && cluster_sk) t_epi += 1.0e-6 + kBM * BN * 4.0 / 150e9;
     bool two_bufs = !(n_b == 2 && BN > 128);
@@ -247,6 +248,7 @@ void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* o) {
     o->tiles_m = g.tiles_m; o->tiles_n = g.tiles_n; o->kblocks = g.kblocks;
     o->grid = g.grid; o->waves = g.waves;
     o->smem_bytes = g.smem_bytes; o->tmem_cols = kTmemCols;
+    o->cluster_sk = g.cluster_sk; o->b_kmajor = g.b_kmajor;
     o->M = g.M; o->N = g.N; o->K = g.K;
     o->useful_over_padded = g.useful_over_padded;
     o->est_us = g.est_us;

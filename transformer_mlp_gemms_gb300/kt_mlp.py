@@ -33,7 +33,7 @@ class KtError(RuntimeError):
 class kt_gemm_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("BM", "BN", "BK", "stages", "split_k", "tiles_m", "tiles_n", "kblocks", "grid", "waves",
-                 "smem_bytes", "tmem_cols")] + \
+                 "smem_bytes", "tmem_cols", "cluster_sk", "b_kmajor")] + \
                [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("useful_over_padded", ctypes.c_double), ("est_us", ctypes.c_double)]
 
