@@ -137,6 +137,31 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// Wait until the counter at `ctr` reaches `target` (wrap-around compare), acquiring at
+// GPU scope.  Gives up, with the abort flag raised, when the error word shows that an
+// earlier kernel failed, when this CTA aborts, or after limit_ns (error code recorded).
+__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned target, volatile int* abort_flag, int* err,
+                                             unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if ((int)(v - target) >= 0) return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_flag || *reinterpret_cast<volatile int*>(err) != 0) {
+                *abort_flag = 1;
+                return false;
+            }
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, DEV_TIMEOUT_PRODUCER);
+                return false;
+            }
+        }
+        __nanosleep(32);
+    }
+}
+
 // Drain wait used on the abort path: ignores the abort flag, bounded by limit_ns.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     const unsigned long long t0 = global_ns();
@@ -649,7 +674,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // resident (and through their set-up) as SMs free up; every kernel here waits for
     // its predecessor's completion before its first global-memory access.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (p.pdl_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // With row-block readiness counters (down projection after the up projection), only
+    // the epilogue waits for the predecessor grid to complete (before it reads the bias
+    // or the residual and writes Y); the producer waits on the counters of the rows of H
+    // it reads, and the MMA warp touches no global memory.
+    const bool ready_mode = EPI == EPI_DOWN && p.ready != nullptr;
+    if (p.pdl_wait && (!ready_mode || warp >= 2)) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
 
@@ -688,6 +718,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (PAIR == 2) {  // the leader's full barrier counts the bytes of both CTAs
                     int m_o, nb_o, ch_o;
                     tx += cta_share(rank ^ 1u, m_o, nb_o, ch_o);
+                }
+                if (ready_mode && m_me < p.M) {
+                    // the up projection's row blocks that hold this CTA's 128 rows of H
+                    const int r1 = min(m_me + kBM, p.M) - 1;
+                    bool got = true;
+                    for (int rb = m_me / p.ready_rows; rb <= r1 / p.ready_rows && got; ++rb)
+                        got = wait_counter(p.ready + rb, p.ready_target, abort_flag, p.error, p.wait_limit_ns);
+                    if (!got) break;
+                    asm volatile("fence.proxy.async.global;" ::: "memory");  // H was written by TMA stores
                 }
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -905,6 +944,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
                     else mbar_arrive(acce);
+                }
+                if (EPI != EPI_DOWN && p.ready != nullptr) {
+                    // this CTA's rows of the tile are in global memory: count them for the
+                    // down projection's producer (release after every epilogue warp's stores)
+                    if (lane == 0) {
+                        bulk_wait0();
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                    __syncwarp();
+                    epi_bar_sync();
+                    if (ew == 0 && lane == 0) {
+                        __threadfence();
+                        atomicAdd(p.ready + c.tm, 1u);
+                    }
                 }
             } else if (p.cluster_sk) {
                 // split-K inside a cluster, reduce-scattered through L2: each 32 x 32 unit of

@@ -109,7 +109,11 @@ struct GemmParams {
     int inject_stall;        // failure-injection hook (producer waits on a silent barrier)
     unsigned long long wait_limit_ns;   // bound of every device-side wait
     unsigned long long stall_limit_ns;  // bound of the injected wait
-    int pdl_wait;            // 1: griddepcontrol.wait before reading the A operand
+    int pdl_wait;            // 1: griddepcontrol.wait before the first global access (see ready)
+    unsigned* ready;         // up: per row-block counters of stored tiles (incremented per CTA tile);
+                             // down: the same counters, waited on before loading rows of H; or null
+    unsigned ready_target;   // down: counter value meaning "every tile of this row block stored"
+    int ready_rows;          // down: rows per up-projection row block (128 x its CTA pairing)
     unsigned long long* trace;  // optional per-CTA timeline (kTraceSlots u64 per CTA) or null
 };
 

@@ -92,7 +92,10 @@ struct kt_mlp_plan_s {
     // device workspace (one allocation each)
     void* H = nullptr;          // [M][F]
     float* partials = nullptr;  // [SK][tiles_m*128][tiles_n*BN] when the down GEMM splits K
-    int* flags = nullptr;       // [0] error word, [1..] split-K tile counters
+    int* flags = nullptr;       // [0] error word, [1..] split-K tile counters, then row-block counters
+    unsigned* ready = nullptr;  // per up-projection row block: CTA tiles of H stored (inside flags)
+    size_t flag_bytes = 0;
+    unsigned epoch = 0;         // runs since the counters were last zero
     void* xn = nullptr;         // [M][D] LayerNorm output (layernorm plans)
     void* x_stage = nullptr;    // [M][D] for kt_mlp_run_host
     void* y_stage = nullptr;    // [M][D]
@@ -224,11 +227,16 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     if (timed) cudaEventRecord(P->ev[1], st);
 
     const int epi_up = kt::up_epilogue(P->act);
+    // the down projection's producer waits on per-row-block counters of stored H tiles
+    // (instead of the whole up grid); each run raises the target by one row block's tiles
+    const unsigned per_block = (unsigned)(P->choice.up.tiles_n * P->choice.up.pair);
+    ++P->epoch;
     kt::GemmParams up = make_params(P, P->choice.up, epi_up);
     up.bias = P->bias ? t.b_up : nullptr;
     up.inject_stall = P->inject_stall;
     up.pdl_wait = 1;
     up.trace = P->trace_up;
+    up.ready = P->ready;
     s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
                         P->choice.up.smem_bytes, stream, !timed, &why);
     if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
@@ -240,6 +248,9 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.counters = P->flags + 1;
     dn.pdl_wait = 1;
     dn.trace = P->trace_down;
+    dn.ready = P->ready;
+    dn.ready_target = P->epoch * per_block;
+    dn.ready_rows = kt::kBM * P->choice.up.pair;
     if (timed) cudaEventRecord(P->ev[2], st);
     s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, &P->tm_ys, dn, P->choice.down.grid,
                         P->choice.down.smem_bytes, stream, !timed, &why);
@@ -308,7 +319,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     const kt::GemmConfig& dn = P->choice.down;
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
-    size_t flag_bytes = 4 * (1 + n_counters);
+    size_t n_ready = (size_t)P->choice.up.tiles_m;                     // one per up row block
+    size_t flag_bytes = 4 * (1 + n_counters + n_ready);
     size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
                             : 0;
@@ -328,6 +340,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
         free_plan(P);
         return cuda_fail("cudaMemset", e);
     }
+    P->ready = reinterpret_cast<unsigned*>(P->flags + 1 + n_counters);
+    P->flag_bytes = flag_bytes;
     P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + part_bytes + xn_bytes + 2 * io_bytes);
     *out = P;
     return ok();
@@ -454,11 +468,10 @@ kt_status kt_mlp_status(kt_mlp_plan_t plan) {
     e = cudaMemcpy(&word, plan->flags, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail("reading the error word", e);
     if (word != kt::DEV_OK) {
-        // clear the word and the split-K counters an aborted run may have left behind
-        const kt::GemmConfig& dn = plan->choice.down;
-        size_t flag_bytes = 4 * (1 + (size_t)dn.tiles_m * dn.tiles_n * dn.pair);
-        cudaMemset(plan->flags, 0, flag_bytes);
+        // clear the word and the counters an aborted run may have left behind
+        cudaMemset(plan->flags, 0, plan->flag_bytes);
         cudaDeviceSynchronize();
+        plan->epoch = 0;
         const char* where = word == kt::DEV_TIMEOUT_PRODUCER ? "producer"
                           : word == kt::DEV_TIMEOUT_MMA ? "MMA issuer"
                           : word == kt::DEV_TIMEOUT_EPILOGUE ? "epilogue"
