@@ -46,14 +46,37 @@ constexpr double kTFill = 0.35e-6;        // pipeline fill + drain latency per t
 // Load latency a stage ring must cover (calibrated on GB300 with a measured sweep of
 // tile shapes: the main loop runs at about max(MMA, issue, 2.0 us / (K depth in flight))).
 constexpr double kLoadLatency = 2.0e-6;
-// Launch, set-up, first loads and drain of one kernel (calibrated; shifts every
-// candidate equally, so it does not change the ranking).
-constexpr double kKernelOverhead = 4.0e-6;
+// Launch, set-up, first loads and drain of one kernel, as CUDA events around a single
+// launch see them (calibrated; shifts every candidate equally, so it does not change
+// the ranking).
+constexpr double kKernelOverhead = 8.5e-6;
+// Split-K exchange rates of one SM (measured on GB300 with a probe of 120 CTAs moving
+// 96 KB each): stores out of the SM ~40-50 GB/s (per-thread or bulk copies), reads of
+// L2-resident data ~70 GB/s; a partial is written once and read once.
+constexpr double kSmStoreRate = 32e9;
+constexpr double kSmReadRate = 70e9;
+// Clusters of SK CTAs that can be resident at once on a 152-SM GB300 (measured with
+// cudaOccupancyMaxActiveClusters at one CTA per SM); sizes not listed are not used.
+int max_active_clusters(int size, int num_sms) {
+    int cap = 0;
+    switch (size) {
+        case 2: cap = 76; break;
+        case 3: cap = 46; break;
+        case 4: cap = 36; break;
+        case 6: cap = 23; break;
+        case 8: cap = 15; break;
+        default: return 0;
+    }
+    return (int)((int64_t)cap * num_sms / 152);
+}
 // Extra cost of a CTA pair (calibrated): once per kernel for cluster launch, paired
 // tensor-memory allocation and cluster barriers, and per tile for the cross-CTA
 // barrier traffic of the main loop and epilogue.
 constexpr double kPairKernelCost = 3.0e-6;
 constexpr double kPairTileCost = 0.3e-6;
+// A GEGLU tile on a CTA pair (two MMAs per step for both CTAs' rows) measured about
+// 13 ns per tile column slower than the model above (calibrated on the SDXL shapes).
+constexpr double kPairGegluPerCol = 13e-9;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -74,8 +97,6 @@ int max_stages(int BN, int n_b, int pair, int bk, int kmaj) {
     return std::min(s, kMaxStages);
 }
 
-constexpr int kGpcs = 8;  // GB300: 152 SMs in 8 GPCs; a cluster must fit in one GPC
-
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
               int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0) {
     int stages = max_stages(BN, n_b, pair, bk, kmaj);
@@ -95,9 +116,8 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     if (cluster_sk) {
         // the SK CTAs of a tile form a cluster: one tile per CTA, all clusters resident at
         // once, and the idle stage ring stages the tile's fp32 partial for its bulk copies
-        const int64_t per_gpc = (num_sms / kGpcs) / SK;
-        if (epi != EPI_DOWN || pair != 1 || SK < 2 || SK > 8 || per_gpc < 1) return false;
-        if (tm * tn > per_gpc * kGpcs) return false;
+        if (epi != EPI_DOWN || pair != 1 || SK < 2 || SK > 8) return false;
+        if (tm * tn > max_active_clusters(SK, num_sms)) return false;
         if ((int64_t)stages * stage_bytes(BN, n_b, pair, bk, kmaj) < (int64_t)kBM * BN * 4) return false;
         grid = ctas;
         waves = 1;
@@ -111,14 +131,16 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     double bytes_kb = (double)stage_bytes(BN, n_b, pair, bk, kmaj);
     double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
     double t_kb = std::max(std::max(t_mma, t_issue), std::max(bytes_kb / feed, kLoadLatency / stages));
-    double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0);
+    double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0) +
+                    (pair == 2 && n_b == 2 ? kPairGegluPerCol * BN : 0.0);
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
     // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
     // all SK partials, both latency-bound at a few tens of GB/s per SM; in a cluster: the
     // (SK-1)/SK of the partial other CTAs own written, a cluster-wide handshake, the
     // owner's reads of its 1/SK of the tile from every other split
-    if (SK > 1 && !cluster_sk) t_epi += kBM * BN * 4.0 / 25e9 + SK * (kBM * BN * 4.0) / 60e9;
-    if (SK > 1 && cluster_sk) t_epi += 1.0e-6 + kBM * BN * 4.0 / 150e9;
+    const double part = kBM * BN * 4.0;  // one fp32 partial tile
+    if (SK > 1 && !cluster_sk) t_epi += part / kSmStoreRate + SK * part / kSmReadRate;
+    if (SK > 1 && cluster_sk) t_epi += 0.5e-6 + (SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate);
     bool two_bufs = !(n_b == 2 && BN > 128);
     double t_cta = two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
                             : waves * (t_main + t_epi);
