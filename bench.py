@@ -61,6 +61,11 @@ def parse_args():
     ap.add_argument("--block", default="", help="comma list of block options: ln (LayerNorm prologue), "
                                                  "res (residual add in the down epilogue)")
     ap.add_argument("--weights", choices=["in_out", "out_in"], default="in_out")
+    ap.add_argument("--h-path", choices=["memory", "on_chip", "auto"], default="memory",
+                    help="where H lives between the projections (on_chip: the fused kernel, D <= 256)")
+    ap.add_argument("--shape", default=None,
+                    help="a custom workload instead of --workload: M,D,F,act,dtype,bias with act one of "
+                         "gelu_erf|gelu_tanh|geglu|none|gelu_sigmoid|silu and dtype f16|bf16")
     ap.add_argument("--impl", choices=["kt", "reference"], default="kt")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample (kt arm)")
@@ -203,9 +208,26 @@ def block_options(args):
     return "ln" in opts, "res" in opts, args.weights == "out_in"
 
 
+def h_path_code(args):
+    from transformer_mlp_gemms_gb300 import kt_mlp
+    return {"memory": kt_mlp.KT_H_MEMORY, "on_chip": kt_mlp.KT_H_ON_CHIP, "auto": kt_mlp.KT_H_AUTO}[args.h_path]
+
+
+def pick_workload(args):
+    from transformer_mlp_gemms_gb300 import workloads as wl
+    if not args.shape:
+        return wl.WORKLOADS[args.workload]
+    M, D, F, act, dt, bias = args.shape.split(",")
+    acts = {v: k for k, v in wl.ACT_NAMES.items()}
+    dts = {v: k for k, v in wl.DT_NAMES.items()}
+    return wl.custom(int(M), int(D), int(F), acts[act], dts[dt], bias in ("1", "true", "yes"), seed=11,
+                     name=f"custom_{M}x{D}x{F}")
+
+
 def traffic_key(w, args) -> str:
     ln, res, outin = block_options(args)
-    tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin)) if on]
+    tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin), ("h_on_chip", args.h_path != "memory"))
+            if on]
     return w.name + (f"[{','.join(tags)}]" if tags else "")
 
 
@@ -217,7 +239,8 @@ def workload_config(w, l2, args=None):
            "flops_per_call": w.flops, "l2": l2}
     if args is not None:
         ln, res, outin = block_options(args)
-        cfg["block"] = {"layernorm": ln, "residual": res, "weights": "out_in" if outin else "in_out"}
+        cfg["block"] = {"layernorm": ln, "residual": res, "weights": "out_in" if outin else "in_out",
+                        "h_path": args.h_path}
     return cfg
 
 
@@ -277,7 +300,7 @@ def main():
     args = parse_args()
     rank, world, local = dist_env()
     from transformer_mlp_gemms_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.workload]
+    w = pick_workload(args)
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
 
@@ -297,14 +320,14 @@ def main():
     kt_mlp.load()
 
     ln, res, outin = block_options(args)
-    plain = not (ln or res)
+    plain = not (ln or res) and args.h_path == "memory"
     t = wl.generate(w, residual=res, layernorm=ln)
     dev_t = wl.torch_order(t) if outin else t
     d = {k: v.cuda() for k, v in dev_t.items()}
     tdt = wl.TORCH_DTYPES[w.dtype]
     Y = torch.empty((w.M, w.D), dtype=tdt, device="cuda")
     plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias, residual=res, layernorm=ln,
-                       weight_layout=kt_mlp.KT_W_OUT_IN if outin else kt_mlp.KT_W_IN_OUT)
+                       weight_layout=kt_mlp.KT_W_OUT_IN if outin else kt_mlp.KT_W_IN_OUT, h_path=h_path_code(args))
     info = plan.info()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -411,8 +434,9 @@ def main():
     up_flops = 2 * w.M * w.D * w.F_up
     dn_flops = 2 * w.M * w.F * w.D
     mu, md, ml = statistics.mean(ms_up), statistics.mean(ms_dn), statistics.mean(ms_ln)
-    dominant = "up" if mu >= md else "down"
-    k_ms, k_flops = (mu, up_flops) if dominant == "up" else (md, dn_flops)
+    fused = bool(info.get("h_on_chip"))
+    dominant = "fused" if fused else ("up" if mu >= md else "down")
+    k_ms, k_flops = {"fused": (mu, w.flops), "up": (mu, up_flops), "down": (md, dn_flops)}[dominant]
     peak_tflops = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])  # fp16 : bf16 nominal 1 : 1
     achieved = k_flops / (k_ms * 1e-3) / 1e12
     line = {
@@ -423,25 +447,29 @@ def main():
         "us_per_call": ms_per_step * 1e3,
         "pct_of_peak": 100.0 * value / world / peak_tflops,
         "peak_tflops": peak_tflops, "peak_source": peak_src,
-        "roofline": {"bound": "tensor", "kernel": f"kt_gemm_kernel ({dominant} projection)",
+        "roofline": {"bound": "tensor", "kernel": ("kt_fused_kernel (both projections, H on chip)" if fused else
+                                                   f"kt_gemm_kernel ({dominant} projection)"),
                      "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": ncu_traffic(traffic_key(w, args), dominant),
                      "algorithmic_flops_per_launch": k_flops, "ms_per_launch": k_ms,
                      "peak_note": (f"{peak_src} bf16 dense burst from MEASURED_PEAKS.json (fp16 has the "
                                    f"same nominal rate)") if peak_src == "measured" else "fallback"},
-        "kernels_ms": {"up": mu, "down": md, "up_tflops": up_flops / (mu * 1e-3) / 1e12,
-                       "down_tflops": dn_flops / (md * 1e-3) / 1e12},
+        "kernels_ms": ({"fused": mu, "fused_tflops": w.flops / (mu * 1e-3) / 1e12} if fused else
+                       {"up": mu, "down": md, "up_tflops": up_flops / (mu * 1e-3) / 1e12,
+                        "down_tflops": dn_flops / (md * 1e-3) / 1e12}),
         **({"layernorm_kernel": {"ms": ml, "bytes": 2 * w.M * w.D * 2 + 2 * w.D * 2,
                                  "gbs": (2 * w.M * w.D * 2 + 2 * w.D * 2) / (ml * 1e-3) / 1e9 if ml > 0 else None}}
            if ln else {}),
         "plan": {"up": {k: info["up"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "grid", "waves")},
                  "down": {k: info["down"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "cluster_sk", "grid",
-                                                       "waves")}},
+                                                       "waves")},
+                 "h_on_chip": int(fused),
+                 **({"fused": {"grid": info["fused_grid"], "stages": info["fused_stages"]}} if fused else {})},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.D * 2,
                 "d2h_bytes_per_step": w.M * w.D * 2, "us_per_call": e2e_s / e2e_steps * 1e6,
                 "entry_point": ("kt_mlp_run_host (pinned X in, Y out; weights resident)" if plain else
                                 "kt_mlp_run_ex between a pinned X copy in and a Y copy out (weights resident)")},
-        "gpu_launches": (3 if ln else 2) * args.steps,
+        "gpu_launches": ((1 if fused else 2) + (1 if ln else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "gpu": props.name, "sms": props.multi_processor_count,

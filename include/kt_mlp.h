@@ -64,6 +64,16 @@ typedef enum {
     KT_ACT_SILU = 5       /* z * sigmoid(z) (SiLU / swish)                                      */
 } kt_act;
 
+/*
+ * Where the intermediate H lives.  KT_H_MEMORY: two kernels, H written once (to L2 /
+ * HBM) by the up projection and read by the down projection.  KT_H_ON_CHIP: one kernel
+ * that keeps H in shared memory, one 64-column slice at a time, and accumulates Y in
+ * tensor memory; it applies only where Y[128 x D] fits tensor memory beside the slices
+ * (D <= 256, D <= 192 for GEGLU) and to [in][out] weights.  KT_H_AUTO: the planner's
+ * choice between the two.  kt_mlp_plan uses KT_H_MEMORY.
+ */
+typedef enum { KT_H_AUTO = 0, KT_H_MEMORY = 1, KT_H_ON_CHIP = 2 } kt_h_path;
+
 /* Memory order of W_up and W_down. */
 typedef enum {
     KT_W_IN_OUT = 0, /* W_up[D][F_up], W_down[F][D]: the layer computes X . W               */
@@ -113,6 +123,10 @@ typedef struct {
     int64_t workspace_bytes;   /* device bytes the plan owns (H, split-K partials, flags) */
     int32_t residual, layernorm, weight_layout;  /* the kt_mlp_options of the plan (0 for kt_mlp_plan) */
     float ln_eps;
+    int32_t h_on_chip;         /* 1: the fused H-on-chip kernel runs (up / down describe the
+                                  two-kernel alternative); its tile facts follow           */
+    int32_t fused_grid, fused_stages, fused_smem_bytes;
+    double fused_est_us;
 } kt_plan_info;
 
 /*
@@ -132,6 +146,7 @@ typedef struct {
                                and biased variance over D in fp32, rounded once to dtype     */
     int32_t weight_layout;  /* kt_weight_layout                                              */
     float ln_eps;           /* LayerNorm epsilon (> 0; PyTorch's default is 1e-5)            */
+    int32_t h_path;         /* kt_h_path: where H lives between the two projections          */
 } kt_mlp_options;
 
 /*
@@ -150,7 +165,7 @@ typedef struct {
     const void* ln_beta;    /* [D], iff layernorm                                            */
     void* Y;                /* [M][D]; may equal X and / or R, must not partially overlap them */
     void* H_out;            /* [M][F] to receive the rounded intermediate, or NULL (the plan's
-                               workspace is used)                                            */
+                               workspace is used); must be NULL for an H-on-chip plan        */
 } kt_mlp_tensors;
 
 /*
@@ -182,10 +197,11 @@ kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const 
 
 /*
  * kt_mlp_plan_ex -- kt_mlp_plan for a problem with the options of kt_mlp_options: a
- * LayerNorm prologue, a residual add, the sigmoid GELU / SiLU activations and the
- * [out][in] weight order.  A layernorm plan also owns a workspace Xn[M][D] for the
- * normalised X.  Errors as kt_mlp_plan, plus INVALID for a flag outside {0, 1}, an
- * unknown weight layout or ln_eps <= 0 (or not finite) with layernorm = 1.
+ * LayerNorm prologue, a residual add, the sigmoid GELU / SiLU activations, the
+ * [out][in] weight order and the H path.  A layernorm plan also owns a workspace
+ * Xn[M][D] for the normalised X.  Errors as kt_mlp_plan, plus INVALID for a flag
+ * outside {0, 1}, an unknown weight layout or H path, or ln_eps <= 0 (or not finite)
+ * with layernorm = 1; UNSUPPORTED for KT_H_ON_CHIP where it does not apply.
  */
 kt_status kt_mlp_plan_ex(const kt_mlp_options* options, kt_mlp_plan_t* out);
 

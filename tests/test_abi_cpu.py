@@ -206,3 +206,27 @@ def test_planner_uses_split_k_for_a_deep_narrow_down_projection(lib):
     # so only split-K can occupy more than one SM
     info = kt_mlp.kt_mlp_plan_info(128, 128, 16384, 3, 0, False, SMS)
     assert info["down"]["split_k"] > 1
+
+
+def test_h_path_planning(lib):
+    on = kt_mlp.KT_H_ON_CHIP
+    # the tiny workload's shape fits the fused kernel and the model prefers it
+    i = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(33, 64, 176, 0, 0, False, h_path=kt_mlp.KT_H_AUTO), SMS)
+    assert i["h_on_chip"] == 1 and i["fused_grid"] == 1 and 2 <= i["fused_stages"] <= 8
+    assert i["fused_smem_bytes"] <= 227 * 1024
+    # the default path and kt_mlp_plan write H
+    assert kt_mlp.kt_mlp_plan_info(33, 64, 176, 0, 0, False, SMS)["h_on_chip"] == 0
+    assert kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(33, 64, 176, 0, 0, False), SMS)["h_on_chip"] == 0
+    # where it does not fit: SigLIP's D, GEGLU beyond D = 192, [out][in] weights
+    for args, kw in [((729, 1152, 4304, 1, 0, False), {}), ((64, 256, 128, 2, 1, True), {}),
+                     ((64, 64, 128, 0, 0, False), {"weight_layout": kt_mlp.KT_W_OUT_IN})]:
+        assert kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(*args, h_path=kt_mlp.KT_H_AUTO, **kw), SMS)["h_on_chip"] == 0
+        with pytest.raises(kt_mlp.KtError) as e:
+            kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(*args, h_path=on, **kw), SMS)
+        assert e.value.status == kt_mlp.KT_ERR_UNSUPPORTED
+    with pytest.raises(kt_mlp.KtError) as e:
+        kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(33, 64, 176, 0, 0, False, h_path=3), SMS)
+    assert e.value.status == kt_mlp.KT_ERR_INVALID
+    # a wide-D shape with few row blocks stays on the two-kernel path
+    assert kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(8192, 256, 1024, 1, 0, False, h_path=kt_mlp.KT_H_AUTO),
+                                      SMS)["h_on_chip"] == 0

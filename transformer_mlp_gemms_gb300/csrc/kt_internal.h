@@ -59,8 +59,23 @@ struct GemmConfig {
     double est_us;
 };
 
+// The H-on-chip variant (kt_fused.cu): both projections in one kernel, H in shared
+// memory one 64-column slice at a time; applies for D <= 256 with [in][out] weights.
+constexpr int kFusedSlice = 64;
+struct FusedConfig {
+    int Dk;                // D rounded up to 64: K of the up GEMM, N of the down GEMM
+    int n_b;               // up-projection B boxes per slice (2 for GEGLU)
+    int n_slices;          // ceil(F / 64)
+    int tiles_m;           // ceil(M / 128)
+    int grid, waves, stages, smem_bytes;
+    uint32_t x_bytes, stage_bytes, wup_bytes, wdn_bytes;
+    double est_us;
+};
+
 struct PlanChoice {
     GemmConfig up, down;
+    int h_on_chip;         // 1: run the fused kernel (`fused`) instead of up + down
+    FusedConfig fused;
 };
 
 // Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
@@ -77,8 +92,12 @@ inline int stage_bytes(int BN, int n_b, int pair, int bk, int b_kmajor = 0) {
 
 // Planner (host only, no GPU): returns KT_OK and fills `out`, or an error status.
 // w_layout: KT_W_IN_OUT ([in][out] weights, N-major B) or KT_W_OUT_IN ([out][in], K-major B).
+// h_path: KT_H_AUTO (the fused H-on-chip kernel where it applies and the model prefers
+// it), KT_H_MEMORY (always two kernels) or KT_H_ON_CHIP (the fused kernel, or
+// KT_ERR_UNSUPPORTED where it does not apply).
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why, bool allow_cluster_sk = true, int w_layout = KT_W_IN_OUT);
+                      const char** why, bool allow_cluster_sk = true, int w_layout = KT_W_IN_OUT,
+                      int h_path = KT_H_MEMORY);
 
 // The up projection's epilogue kind for a kt_act.
 int up_epilogue(int act);
@@ -137,6 +156,25 @@ enum TraceSlot : int {
     TR_EPI_DRAIN = 15,   //   ... all its stores complete
     kTraceSlots = 16
 };
+
+// Launch parameters of the fused kernel.
+struct FusedParams {
+    int M, D, F, Dk, n_slices, tiles_m, stages;
+    int gate_col;            // GEGLU: F (first gate column of W_up); else 0
+    uint32_t idesc_up, idesc_dn;
+    uint32_t x_bytes, stage_bytes, wup_bytes, wdn_bytes;
+    const void* bias_up;
+    const void* bias_dn;
+    const void* residual;
+    int* error;
+    unsigned long long wait_limit_ns;
+    int pdl_wait;
+};
+
+// tx: X [M][D] (box 128 x 64); twu: W_up [D][F_up] (box Dk rows x 64); twd: W_down [F][D]
+// (box 64 x 64); ty: Y store map (box 32 x 32).
+kt_status launch_fused(int epi, int dtype, const void* tx, const void* twu, const void* twd, const void* ty,
+                       const FusedParams& p, int grid, int smem, void* stream, bool pdl, const char** why);
 
 // Allocation-free down projection (kt_mlp_kernels.cu): its split-K partials, tile
 // counters and error word live in a static device array of this many bytes.

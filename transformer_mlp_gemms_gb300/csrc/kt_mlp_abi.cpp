@@ -68,6 +68,8 @@ kt_status validate_options(const kt_mlp_options* o) {
         return fail(KT_ERR_INVALID, "unknown weight layout");
     if (o->layernorm && !(o->ln_eps > 0.0f && o->ln_eps < 3.0e38f))
         return fail(KT_ERR_INVALID, "ln_eps must be positive and finite");
+    if (o->h_path != KT_H_AUTO && o->h_path != KT_H_MEMORY && o->h_path != KT_H_ON_CHIP)
+        return fail(KT_ERR_INVALID, "unknown H path");
     return KT_OK;
 }
 
@@ -77,6 +79,7 @@ kt_mlp_options base_options(int64_t M, int64_t D, int64_t F, int act, int dtype,
     o.M = M; o.D = D; o.F = F;
     o.act = act; o.dtype = dtype; o.bias = bias;
     o.weight_layout = KT_W_IN_OUT;
+    o.h_path = KT_H_MEMORY;
     return o;
 }
 
@@ -102,6 +105,7 @@ struct kt_mlp_plan_s {
     int64_t workspace_bytes = 0;
     // tensor maps, cached by pointer set
     alignas(64) CUtensorMap tm_x, tm_wu, tm_h, tm_wd, tm_hs, tm_ys;  // loads, then H / Y stores
+    alignas(64) CUtensorMap tm_fwu, tm_fwd;  // the fused kernel's weight maps (H-on-chip plans)
     const void* c_x = nullptr;
     const void* c_wu = nullptr;
     const void* c_h = nullptr;
@@ -186,6 +190,8 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     if (cur != P->device) return fail(KT_ERR_INVALID, "the current device is not the plan's device");
 
     const char* why = "";
+    if (P->choice.h_on_chip && t.H_out)
+        return fail(KT_ERR_INVALID, "an H-on-chip plan keeps H on chip: H_out must be NULL");
     const void* A_up = P->layernorm ? P->xn : t.X;
     if (!P->cache_valid || P->c_x != A_up || P->c_wu != t.W_up || P->c_h != H || P->c_wd != t.W_down ||
         P->c_y != t.Y) {
@@ -204,7 +210,10 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
             (km ? kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->D, P->F, d.BN / d.pair, 64, 128, &why)
                 : kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->F, P->D, d.bk, 64, 128, &why)) &&
             kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) &&
-            kt::encode_tmap(&P->tm_ys, t.Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why);
+            kt::encode_tmap(&P->tm_ys, t.Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why) &&
+            (!P->choice.h_on_chip ||
+             (kt::encode_tmap(&P->tm_fwu, t.W_up, P->dtype, P->D, P->F_up, P->choice.fused.Dk, 64, 128, &why) &&
+              kt::encode_tmap(&P->tm_fwd, t.W_down, P->dtype, P->F, P->D, kt::kFusedSlice, 64, 128, &why)));
         if (!good) {
             P->cache_valid = false;
             return fail(KT_ERR_CUDA, std::string("tensor map: ") + why);
@@ -227,6 +236,33 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     if (timed) cudaEventRecord(P->ev[1], st);
 
     const int epi_up = kt::up_epilogue(P->act);
+    if (P->choice.h_on_chip) {
+        // one kernel: H stays on chip
+        const kt::FusedConfig& f = P->choice.fused;
+        kt::FusedParams fp;
+        std::memset(&fp, 0, sizeof(fp));
+        fp.M = (int)P->M; fp.D = (int)P->D; fp.F = (int)P->F;
+        fp.Dk = f.Dk; fp.n_slices = f.n_slices; fp.tiles_m = f.tiles_m; fp.stages = f.stages;
+        fp.gate_col = P->act == KT_ACT_GEGLU ? (int)P->F : 0;
+        fp.idesc_up = kt::make_idesc(P->dtype, kt::kFusedSlice, kt::kBM, 0);
+        fp.idesc_dn = kt::make_idesc(P->dtype, f.Dk, kt::kBM, 0);
+        fp.x_bytes = f.x_bytes; fp.stage_bytes = f.stage_bytes; fp.wup_bytes = f.wup_bytes; fp.wdn_bytes = f.wdn_bytes;
+        fp.bias_up = P->bias ? t.b_up : nullptr;
+        fp.bias_dn = P->bias ? t.b_down : nullptr;
+        fp.residual = t.R;
+        fp.error = P->flags;
+        fp.wait_limit_ns = 4000000000ull;
+        fp.pdl_wait = 1;
+        s = kt::launch_fused(epi_up, P->dtype, &P->tm_x, &P->tm_fwu, &P->tm_fwd, &P->tm_ys, fp, f.grid, f.smem_bytes,
+                             stream, !timed, &why);
+        if (s != KT_OK) return fail(s, std::string("fused launch: ") + why);
+        if (timed) {
+            cudaEventRecord(P->ev[2], st);
+            cudaEventRecord(P->ev[3], st);
+        }
+        P->last_stream = stream;
+        return ok();
+    }
     // the down projection's producer waits on per-row-block counters of stored H tiles
     // (instead of the whole up grid); each run raises the target by one row block's tiles
     const unsigned per_block = (unsigned)(P->choice.up.tiles_n * P->choice.up.pair);
@@ -311,7 +347,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     P->device = dev;
     P->num_sms = prop.multiProcessorCount;
     const char* why = "";
-    kt_status s = kt::plan_choose(M, D, F, o.act, P->num_sms, &P->choice, &why, true, o.weight_layout);
+    kt_status s = kt::plan_choose(M, D, F, o.act, P->num_sms, &P->choice, &why, true, o.weight_layout, o.h_path);
     if (s != KT_OK) {
         delete P;
         return fail(s, why);
@@ -350,7 +386,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
 kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     kt::PlanChoice c;
     const char* why = "";
-    kt_status s = kt::plan_choose(o.M, o.D, o.F, o.act, num_sms, &c, &why, true, o.weight_layout);
+    kt_status s = kt::plan_choose(o.M, o.D, o.F, o.act, num_sms, &c, &why, true, o.weight_layout, o.h_path);
     if (s != KT_OK) return fail(s, why);
     std::memset(out, 0, sizeof(*out));
     out->M = o.M; out->D = o.D; out->F = o.F;
@@ -358,6 +394,13 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     out->num_sms = num_sms;
     out->residual = o.residual; out->layernorm = o.layernorm; out->weight_layout = o.weight_layout;
     out->ln_eps = o.layernorm ? o.ln_eps : 0.0f;
+    out->h_on_chip = c.h_on_chip;
+    if (c.h_on_chip) {
+        out->fused_grid = c.fused.grid;
+        out->fused_stages = c.fused.stages;
+        out->fused_smem_bytes = c.fused.smem_bytes;
+        out->fused_est_us = c.fused.est_us;
+    }
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * o.M * o.D;
@@ -495,6 +538,13 @@ kt_status kt_mlp_get_info(kt_mlp_plan_t plan, kt_plan_info* out) {
     out->num_sms = plan->num_sms;
     out->residual = plan->residual; out->layernorm = plan->layernorm; out->weight_layout = plan->w_layout;
     out->ln_eps = plan->ln_eps;
+    out->h_on_chip = plan->choice.h_on_chip;
+    if (plan->choice.h_on_chip) {
+        out->fused_grid = plan->choice.fused.grid;
+        out->fused_stages = plan->choice.fused.stages;
+        out->fused_smem_bytes = plan->choice.fused.smem_bytes;
+        out->fused_est_us = plan->choice.fused.est_us;
+    }
     kt::plan_fill_info(plan->choice.up, &out->up);
     kt::plan_fill_info(plan->choice.down, &out->down);
     out->workspace_bytes = plan->workspace_bytes;
@@ -516,6 +566,13 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.split_k == 1 ? "no reduction" : d.cluster_sk ? "cluster reduction" : "global reduction",
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
+    if (plan->choice.h_on_chip) {
+        const kt::FusedConfig& f = plan->choice.fused;
+        const size_t used = std::strlen(buf);
+        std::snprintf(buf + used, len - used,
+                      " | RUNS H on chip: one kernel, 128-row blocks x %d slices of 64 (grid %d, %d stages, model %.2f us)",
+                      f.n_slices, f.grid, f.stages, f.est_us);
+    }
     return ok();
 }
 

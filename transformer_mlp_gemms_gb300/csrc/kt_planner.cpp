@@ -197,11 +197,60 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
 
 }  // namespace
 
+// The fused H-on-chip kernel: feasibility (tensor memory: Y[128 x Dk] beside two slice
+// accumulators; shared memory: X tile, two H slices and a ring of >= 2 weight stages) and
+// its modelled time.  Per CTA and row block, each 64-column slice costs the larger of its
+// MMAs (up and down), its weight bytes at the SM's load rate, its epilogue and the load
+// latency its two ring stages must cover; the slices pipeline, so the row block costs
+// n_slices of those plus one X load and the Y epilogue.
+static bool plan_fused(int64_t M, int64_t D, int64_t F, int act, int num_sms, FusedConfig* f) {
+    const int n_b = act == KT_ACT_GEGLU ? 2 : 1;
+    if (D < 1 || D > 256 || num_sms < 1) return false;
+    const int Dk = (int)((D + 63) / 64 * 64);
+    if (Dk + 2 * n_b * kFusedSlice > kTmemCols) return false;
+    const uint32_t x_bytes = (uint32_t)(Dk / 64) * 16384u;
+    const uint32_t wup = (uint32_t)(n_b * Dk) * 128u, wdn = (uint32_t)Dk * 128u;
+    const uint32_t stage = std::max(wup, wdn);
+    const int fixed = (int)x_bytes + 2 * 16384 + kSmemReserve;
+    const int stages = std::min(kMaxStages, (kSmemBudget - fixed) / (int)stage);
+    if (stages < 2) return false;
+    const int64_t tiles_m = cdiv(M, kBM);
+    const int64_t n_slices = cdiv(F, kFusedSlice);
+    if (tiles_m > ((int64_t)1 << 29) || n_slices > ((int64_t)1 << 20)) return false;
+    f->Dk = Dk;
+    f->n_b = n_b;
+    f->n_slices = (int)n_slices;
+    f->tiles_m = (int)tiles_m;
+    f->grid = (int)std::min<int64_t>(tiles_m, num_sms);
+    f->waves = (int)cdiv(tiles_m, num_sms);
+    f->stages = stages;
+    f->smem_bytes = fixed + stages * (int)stage;
+    f->x_bytes = x_bytes;
+    f->stage_bytes = stage;
+    f->wup_bytes = wup;
+    f->wdn_bytes = wdn;
+    const double t_mma = (n_b + 1) * 2.0 * kBM * kFusedSlice * Dk / kRsm;
+    const double t_load = (double)(wup + wdn) / 100e9;
+    const double t_epi = (double)kBM * kFusedSlice * epi_cost_per_elem(up_epilogue(act));
+    // each slice takes two ring stages (its W_up and its W_down slices): the ring must
+    // cover the load latency as in the two-kernel main loop
+    const double t_lat = 2.0 * kLoadLatency / stages;
+    const double t_slice = std::max(std::max(t_mma, t_load), std::max(t_epi, t_lat));
+    const double t_rb = (double)n_slices * t_slice + kLoadLatency / 2 + (double)kBM * Dk * epi_cost_per_elem(EPI_DOWN);
+    f->est_us = ((double)f->waves * t_rb + kKernelOverhead) * 1e6;
+    return true;
+}
+
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why, bool allow_cluster_sk, int w_layout) {
+                      const char** why, bool allow_cluster_sk, int w_layout, int h_path) {
     if (M < 1 || D < 1 || F < 1) { *why = "M, D and F must be positive"; return KT_ERR_INVALID; }
     if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) { *why = "unknown activation"; return KT_ERR_INVALID; }
     if (w_layout != KT_W_IN_OUT && w_layout != KT_W_OUT_IN) { *why = "unknown weight layout"; return KT_ERR_INVALID; }
+    if (h_path != KT_H_AUTO && h_path != KT_H_MEMORY && h_path != KT_H_ON_CHIP) {
+        *why = "unknown H path";
+        return KT_ERR_INVALID;
+    }
+    out->h_on_chip = 0;
     const int kmaj = w_layout == KT_W_OUT_IN ? 1 : 0;
     if (num_sms < 1) { *why = "num_sms must be positive"; return KT_ERR_INVALID; }
     if (D % 8 != 0 || F % 8 != 0) {
@@ -249,6 +298,17 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
             return KT_ERR_INVALID;
         }
         out->down = g;
+    }
+    // the H path: the fused kernel where it applies ([in][out] weights, D small enough)
+    // and is asked for, or, in KT_H_AUTO, where the model prefers it to two kernels
+    if (h_path != KT_H_MEMORY) {
+        const bool fits = w_layout == KT_W_IN_OUT && plan_fused(M, D, F, act, num_sms, &out->fused);
+        if (h_path == KT_H_ON_CHIP && !fits) {
+            *why = "the H-on-chip kernel needs [in][out] weights and D <= 256 (<= 192 for GEGLU)";
+            return KT_ERR_UNSUPPORTED;
+        }
+        if (fits && (h_path == KT_H_ON_CHIP || out->fused.est_us < out->up.est_us + out->down.est_us))
+            out->h_on_chip = 1;
     }
     return KT_OK;
 }

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libkt_mlp.so")
 KT_ACT_GELU_ERF, KT_ACT_GELU_TANH, KT_ACT_GEGLU, KT_ACT_NONE, KT_ACT_GELU_SIGMOID, KT_ACT_SILU = range(6)
 KT_F16, KT_BF16 = 0, 1
 KT_W_IN_OUT, KT_W_OUT_IN = 0, 1
+KT_H_AUTO, KT_H_MEMORY, KT_H_ON_CHIP = 0, 1, 2
 KT_OK, KT_ERR_INVALID, KT_ERR_UNSUPPORTED, KT_ERR_CUDA, KT_ERR_TIMEOUT, KT_ERR_NOMEM = range(6)
 STATUS_NAMES = {0: "KT_OK", 1: "KT_ERR_INVALID", 2: "KT_ERR_UNSUPPORTED", 3: "KT_ERR_CUDA",
                 4: "KT_ERR_TIMEOUT", 5: "KT_ERR_NOMEM"}
@@ -48,7 +49,8 @@ class kt_plan_info(ctypes.Structure):
                 ("up", kt_gemm_plan_info), ("down", kt_gemm_plan_info),
                 ("workspace_bytes", ctypes.c_int64),
                 ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
-                ("ln_eps", ctypes.c_float)]
+                ("ln_eps", ctypes.c_float), ("h_on_chip", ctypes.c_int32), ("fused_grid", ctypes.c_int32),
+                ("fused_stages", ctypes.c_int32), ("fused_smem_bytes", ctypes.c_int32), ("fused_est_us", ctypes.c_double)]
 
     def as_dict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_ if n not in ("up", "down")}
@@ -61,7 +63,7 @@ class kt_mlp_options(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("F", ctypes.c_int64),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("bias", ctypes.c_int32),
                 ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
-                ("ln_eps", ctypes.c_float)]
+                ("ln_eps", ctypes.c_float), ("h_path", ctypes.c_int32)]
 
 
 class kt_mlp_tensors(ctypes.Structure):
@@ -70,9 +72,9 @@ class kt_mlp_tensors(ctypes.Structure):
 
 
 def options(M, D, F, act, dtype, bias=False, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
-            ln_eps=1e-5) -> kt_mlp_options:
+            ln_eps=1e-5, h_path=KT_H_MEMORY) -> kt_mlp_options:
     return kt_mlp_options(M, D, F, act, dtype, int(bias), int(residual), int(layernorm), weight_layout,
-                          ln_eps if layernorm else 0.0)
+                          ln_eps if layernorm else 0.0, h_path)
 
 
 def tensors(X, W_up, W_down, Y, b_up=None, b_down=None, R=None, ln_gamma=None, ln_beta=None,
@@ -274,12 +276,12 @@ class Plan:
     destroyed with the object."""
 
     def __init__(self, M, D, F, act, dtype, bias, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
-                 ln_eps=1e-5):
+                 ln_eps=1e-5, h_path=KT_H_MEMORY):
         self.M, self.D, self.F, self.act, self.dtype, self.bias = M, D, F, act, dtype, bool(bias)
         self.residual, self.layernorm, self.weight_layout = bool(residual), bool(layernorm), weight_layout
-        if residual or layernorm or weight_layout != KT_W_IN_OUT:
+        if residual or layernorm or weight_layout != KT_W_IN_OUT or h_path != KT_H_MEMORY:
             self.handle = kt_mlp_plan_ex(options(M, D, F, act, dtype, bias, residual, layernorm, weight_layout,
-                                                 ln_eps))
+                                                 ln_eps, h_path))
         else:
             self.handle = kt_mlp_plan(M, D, F, act, dtype, bias)
 
