@@ -83,6 +83,19 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest rank's times)."""
+    import torch
+    v = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(v, op=dist.ReduceOp.MAX)
+    return [float(x) for x in v]
+
+
+def job_value(world: int, steps: int, flops_per_step: float, seconds: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank (weak scaling) over the slowest rank's time."""
+    return world * steps * flops_per_step / seconds / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -418,9 +431,7 @@ def main():
     clocks = summarize_clocks(sampler.stop())
 
     if dist is not None:
-        v = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        total_ms, e2e_s = float(v[0]), float(v[1])
+        total_ms, e2e_s = reduce_max([total_ms, e2e_s], dist, "cuda")
     if rank != 0:
         plan.close()
         if dist is not None:
@@ -428,9 +439,9 @@ def main():
         return 0
 
     peaks, peak_src = load_peaks()
-    value = world * args.steps * w.flops / (total_ms * 1e-3) / 1e12
+    value = job_value(world, args.steps, w.flops, total_ms * 1e-3)
     ms_per_step = total_ms / args.steps
-    e2e_value = world * e2e_steps * w.flops / e2e_s / 1e12
+    e2e_value = job_value(world, e2e_steps, w.flops, e2e_s)
     up_flops = 2 * w.M * w.D * w.F_up
     dn_flops = 2 * w.M * w.F * w.D
     mu, md, ml = statistics.mean(ms_up), statistics.mean(ms_dn), statistics.mean(ms_ln)
