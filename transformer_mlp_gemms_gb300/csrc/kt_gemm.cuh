@@ -424,17 +424,18 @@ __device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approxi
 __device__ __forceinline__ float gelu_erf_f(float z) {
     const float a = fabsf(z) * 0.70710678118654752f;
     const float t = rcp_approx(fmaf(0.5f, a, 1.0f));
-    float p = 0.17087277f;
-    p = fmaf(p, t, -0.82215223f);
-    p = fmaf(p, t, 1.48851587f);
-    p = fmaf(p, t, -1.13520398f);
-    p = fmaf(p, t, 0.27886807f);
-    p = fmaf(p, t, -0.18628806f);
-    p = fmaf(p, t, 0.09678418f);
-    p = fmaf(p, t, 0.37409196f);
-    p = fmaf(p, t, 1.00002368f);
-    p = fmaf(p, t, -1.26551223f);
-    const float e = t * ex2_approx((p - a * a) * 1.4426950408889634f);  // erfc(|z| / sqrt 2)
+    // the fit's degree-9 polynomial in t by Estrin's scheme (pairs, then t^2, t^4, t^8):
+    // the same coefficients as Horner's rule with a dependency chain of 4 instead of 9
+    const float t2 = t * t, t4 = t2 * t2, t8 = t4 * t4;
+    const float q01 = fmaf(1.00002368f, t, -1.26551223f);
+    const float q23 = fmaf(0.09678418f, t, 0.37409196f);
+    const float q45 = fmaf(0.27886807f, t, -0.18628806f);
+    const float q67 = fmaf(1.48851587f, t, -1.13520398f);
+    const float q89 = fmaf(0.17087277f, t, -0.82215223f);
+    const float r0 = fmaf(q23, t2, q01);
+    const float r1 = fmaf(q67, t2, q45);
+    const float p = fmaf(q89, t8, fmaf(r1, t4, r0));
+    const float e = t * ex2_approx(fmaf(-a, a, p) * 1.4426950408889634f);  // erfc(|z| / sqrt 2)
     const float phi = z >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
     return z * phi;
 }
@@ -508,6 +509,21 @@ __device__ __forceinline__ void load_bias32(const void* bias, int col, int limit
 #pragma unroll
             for (int i = 0; i < 8; ++i) b[8 * g + i] = 0.0f;
         }
+    }
+}
+
+// 32 bias values from the tile's bias slice staged in shared memory (bsm: the slice's
+// first column; columns past N were staged as zeros).  Every lane reads the same
+// addresses: broadcast reads.
+template <int DT>
+__device__ __forceinline__ void bias32_smem(uint32_t bsm, float* b) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 w;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(bsm + 16u * g));
+        unpack8<DT>(w, b + 8 * g);
     }
 }
 
@@ -627,6 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_drain = bar_stall + 8u;
     const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partials are written
     uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 8));
+    // the epilogue's bias slices, two tiles deep: [2][value 256 | gate 256] in the I/O dtype
+    const uint32_t bias_smem = staging + (uint32_t)kStagingBytes + kBarrierBytes;
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
@@ -875,6 +893,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
             // the accumulator-empty barrier lives in the leader CTA
             const uint32_t acce = PAIR == 2 ? mapa_rank(bar_acce + 8u * buf, 0) : bar_acce + 8u * buf;
+            // Stage this tile's bias slice (value and, for GEGLU, gate columns) in shared
+            // memory while the MMAs run; the barrier after the accumulator wait publishes
+            // it to every epilogue warp (two buffers: a warp can only reach tile + 2 after
+            // every warp has finished tile).
+            const uint32_t bsm = bias_smem + (uint32_t)(local & 1) * 1024u;
+            if (p.bias) {
+                const int per = p.BN / 8;  // 16-byte chunks per operand
+                const int nb0 = c.tn * p.BN;
+                for (int i = ew * 32 + lane; i < n_b * per; i += kEpiWarps * 32) {
+                    const int op = i >= per ? 1 : 0;
+                    const int col = nb0 + 8 * (i - op * per);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (col < p.N)
+                        v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.bias) +
+                                                                 (op ? p.gate_col : 0) + col));
+                    st_shared_v4(bsm + (uint32_t)op * 512u + (uint32_t)(i - op * per) * 16u, v.x, v.y, v.z, v.w);
+                }
+            }
             const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             if (!epi_all(got)) break;
@@ -891,40 +927,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = half; g < ngroups; g += 2) {
                     const int col = n0 + 32 * g;
                     const bool mark = tr0 && g == half;
-                    uint32_t r[32];
-                    tmem_ld32(tq + 32u * g, r);
                     float v[32];
                     if constexpr (EPI == EPI_GEGLU) {
-                        uint32_t gr[32];
-                        tmem_ld32(tq + p.gate_acc_off + 32u * g, gr);
-                        tmem_wait_ld_only();
-                        reg_fence32(r);
-                        reg_fence32(gr);
-                        if (mark) trace_mark(tr, TR_EPI_LD);
+                        // in two halves of 16 columns: value, gate and bias of one half live at
+                        // a time, which leaves registers for more independent GELU chains
                         if (col < p.N && rows_live) {
-                            float bv[32], bg[32];
-                            if (p.bias) {
-                                load_bias32<DT>(p.bias, col, p.N, bv);
-                                load_bias32<DT>(p.bias, p.gate_col + col, p.gate_col + p.N, bg);
-                            } else {
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) bv[i] = bg[i] = 0.0f;
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t rv[16], rg[16];
+                                tmem_ld16(tq + 32u * g + 16u * h, rv);
+                                tmem_ld16(tq + p.gate_acc_off + 32u * g + 16u * h, rg);
+                                tmem_wait_ld2(rv, rg);
+                                if (mark && h == 0) trace_mark(tr, TR_EPI_LD);
+                                float bv[16], bg[16];
+                                if (p.bias) {
+                                    const uint32_t o = 64u * (uint32_t)g + 32u * (uint32_t)h;
+#pragma unroll
+                                    for (int q2 = 0; q2 < 2; ++q2) {
+                                        uint4 wv, wg;
+                                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                                     : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w)
+                                                     : "r"(bsm + o + 16u * q2));
+                                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                                     : "=r"(wg.x), "=r"(wg.y), "=r"(wg.z), "=r"(wg.w)
+                                                     : "r"(bsm + 512u + o + 16u * q2));
+                                        unpack8<DT>(wv, bv + 8 * q2);
+                                        unpack8<DT>(wg, bg + 8 * q2);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) bv[i] = bg[i] = 0.0f;
+                                }
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[16 * h + i] = (__uint_as_float(rv[i]) + bv[i]) *
+                                                    gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
                             }
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(gr[i]) + bg[i]);
                             if (mark) trace_mark(tr, TR_EPI_MATH);
                             stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
                             if (mark) trace_mark(tr, TR_EPI_STORE);
                         }
                     } else {
+                        uint32_t r[32];
+                        tmem_ld32(tq + 32u * g, r);
                         tmem_wait_ld_only();
                         reg_fence32(r);
                         if (mark) trace_mark(tr, TR_EPI_LD);
                         if (col < p.N && rows_live) {
                             float b[32];
                             if (p.bias) {
-                                load_bias32<DT>(p.bias, col, p.N, b);
+                                bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) b[i] = 0.0f;
@@ -1035,7 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (p.bias) {
                             float b[32];
-                            load_bias32<DT>(p.bias, col, p.N, b);
+                            bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
@@ -1127,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (p.bias) {
                             float b[32];
-                            load_bias32<DT>(p.bias, col, p.N, b);
+                            bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }

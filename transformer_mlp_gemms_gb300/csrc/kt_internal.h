@@ -21,8 +21,11 @@ constexpr int kSmemBudget = 227 * 1024;  // opt-in dynamic shared memory per CTA
 // guard band past the ring so that no descriptor stride can reach beyond the allocation
 constexpr int kStoreCols = 32;    // columns per epilogue TMA store box (32 rows x 32 columns)
 constexpr int kStagingBytes = kEpiWarps * 32 * kStoreCols * 2;  // one 2 KB buffer per epilogue warp
-// output staging, barriers / TMEM slot / flags (1 KB) and 1024-byte alignment slack (1 KB)
-constexpr int kSmemReserve = kStagingBytes + 2048;
+// output staging, barriers / TMEM slot / flags, the epilogue's two bias slices (2 KB)
+// and 1024-byte alignment slack (1 KB)
+constexpr int kBarrierBytes = 512;
+constexpr int kBiasSmemBytes = 2048;
+constexpr int kSmemReserve = kStagingBytes + kBarrierBytes + kBiasSmemBytes + 1024;
 constexpr int kMaxStages = 8;
 
 // Epilogue kinds (one kernel instantiation each, times two dtypes).
