@@ -229,6 +229,7 @@ kt_status kt_mlp_run_ex_timed(kt_mlp_plan_t plan, const kt_mlp_tensors* tensors,
  * kt_mlp_run_with_h -- as kt_mlp_run, but the rounded intermediate H[M][F] is
  * written to the caller's device buffer H_out (16-byte aligned) instead of the
  * plan's workspace, so that it can be inspected.  Same kernels, same results.
+ * INVALID for an H-on-chip plan (it never writes H).
  */
 kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                             const void* b_up, const void* b_down, void* Y, void* H_out, void* stream);

@@ -105,4 +105,15 @@ def test_h_on_chip_plan_errors():
     with pytest.raises(kt_mlp.KtError) as e:
         plan.run_ex(d["X"], d["W_up"], d["W_down"], Y, H_out=H)
     assert e.value.status == kt_mlp.KT_ERR_INVALID
+    with pytest.raises(kt_mlp.KtError) as e:
+        plan.run_with_h(d["X"], d["W_up"], d["W_down"], None, None, Y, H)
+    assert e.value.status == kt_mlp.KT_ERR_INVALID
+    # the host-buffer entry point runs the fused kernel like any other plan
+    Xh = d["X"].cpu().pin_memory()
+    Yh = torch.empty((w.M, w.D), dtype=torch.float16).pin_memory()
+    plan.run_host(Xh, d["W_up"], d["W_down"], None, None, Yh)
+    Yd = torch.empty_like(Y)
+    plan.run_ex(d["X"], d["W_up"], d["W_down"], Yd)
+    torch.cuda.synchronize()
+    assert torch.equal(Yh.view(torch.int16), Yd.cpu().view(torch.int16))
     plan.close()

@@ -1,28 +1,35 @@
 // kt_gemm.cuh -- the sm_103a GEMM kernel template of the fused MLP (device code
 // and its launch helper), included by the translation units that instantiate it.
 //
-//
-// One persistent, warp-specialised kernel template serves both projections:
+// One persistent, warp-specialised kernel template serves both projections, on one
+// CTA per 128-row tile (PAIR = 1) or on a CTA pair per 256-row tile (PAIR = 2,
+// tcgen05 cta_group::2: each CTA loads its 128 rows of A and half of the B columns):
 //
 //   warp 0      producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
-//               A tile (128 x 64, K-major) and the B tile(s) (64 x BN in 64-column
-//               boxes, N-major) into an S-stage shared-memory ring, one mbarrier
-//               pair (full / empty) per stage.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f16 (M=128, N=BN,
-//               K=16, fp32 accumulation in tensor memory), four per k-block, and
-//               tcgen05.commit hands the stage back to the producer.  Two TMEM
-//               accumulator buffers let tile i+1's main loop run under tile i's
+//               A tile (128 x 64 K-major boxes, one per 64-deep atom of a BK = 64 or
+//               128 k-block) and the B tile(s) -- 64-column N-major boxes of an
+//               [in][out] weight, or (BN / PAIR)-row K-major boxes of an [out][in]
+//               weight -- into an S-stage shared-memory ring, one mbarrier pair
+//               (full / empty) per stage.  The down projection's producer first waits
+//               for the up projection's per-row-block counters of stored H tiles.
+//   warp 1      MMA issuer: one thread of the leader CTA issues tcgen05.mma kind::f16
+//               (M = 128 or 256, N = BN, K = 16, fp32 accumulation in tensor memory),
+//               BK / 16 per k-block, and tcgen05.commit hands the stage back.  Two
+//               TMEM accumulator buffers let tile i+1's main loop run under tile i's
 //               epilogue.  GEGLU issues a second MMA per step into a gate
 //               accumulator that shares the A tile (one X stream, two weights).
-//   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers
-//               (TMEM lane = tile row), adds the bias, applies the activation
-//               (GELU erf / tanh, GEGLU value*gelu(gate)), rounds ONCE to the I/O
-//               dtype, stages each warp's 32 x 32 block in swizzled shared memory
-//               and writes it with a TMA tensor store (coalesced, clipped at the
-//               ragged edges); the down projection adds b_down and stores Y, or,
-//               with split-K, writes an fp32 partial (warp-contiguous layout) and
-//               the last CTA to arrive on the tile sums the partials in split
-//               order (deterministic).
+//   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers (TMEM
+//               lane = tile row), adds the bias (staged per tile in shared memory),
+//               applies the activation (GELU erf / tanh / sigmoid, SiLU, GEGLU
+//               value * gelu(gate)), rounds ONCE to the I/O dtype, stages each warp's
+//               32 x 32 block in swizzled shared memory and writes it with a TMA
+//               tensor store (clipped at the ragged edges).  The up projection then
+//               counts the stored tile for the down projection.  The down projection
+//               adds b_down and the residual and stores Y; with split-K its CTAs
+//               either reduce-scatter their fp32 partials through L2 inside a
+//               cluster (each 32 x 32 unit summed by its owner CTA, its own partial
+//               still in TMEM) or write them to global memory for the last CTA to
+//               arrive on the tile; partials are always summed in split order.
 //
 // Sources: "SDXL as a requirements inventory", section 1.3 (FeedForward: value =
 // first half, gate = second half) and 9.3 (erf GELU); "MLP layout sweep and

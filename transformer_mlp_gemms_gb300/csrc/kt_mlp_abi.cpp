@@ -459,6 +459,8 @@ kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const 
 kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,
                             const void* b_up, const void* b_down, void* Y, void* H_out, void* stream) {
     if (!H_out) return fail(KT_ERR_INVALID, "H_out is NULL");
+    if (plan && plan->choice.h_on_chip)
+        return fail(KT_ERR_INVALID, "an H-on-chip plan keeps H on chip: it cannot return H");
     return run_impl(plan, base_tensors(X, W_up, W_down, b_up, b_down, Y), H_out, stream);
 }
 
