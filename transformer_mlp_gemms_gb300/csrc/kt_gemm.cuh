@@ -388,13 +388,15 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+template <int NEPI = kEpiWarps>
 __device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NEPI * 32) : "memory");
 }
 
 // Barrier over the epilogue warps that also ANDs a predicate across them, so that
 // all of them take the same branch after a bounded wait (no warp is left behind
 // at a later named barrier).
+template <int NEPI = kEpiWarps>
 __device__ __forceinline__ bool epi_all(bool ok) {
     uint32_t r;
     asm volatile(
@@ -403,7 +405,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
         "bar.red.and.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)ok), "n"(kEpiWarps * 32)
+        : "r"((uint32_t)ok), "n"(NEPI * 32)
         : "memory");
     return r != 0;
 }
@@ -632,7 +634,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
 // rows of the accumulator into that CTA's tensor memory; each CTA's epilogue stores
 // its own rows.
 template <int EPI, int DT, int PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -641,17 +643,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
 
     const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
-    const uint32_t staging = base + tiles_bytes;  // kEpiWarps x 2 KB output staging buffers
-    const uint32_t bar_full = staging + (uint32_t)kStagingBytes;
+    constexpr int NEPI = epi_warps(EPI);   // epilogue warps
+    constexpr int NPART = NEPI / 4;        // epilogue warps per TMEM lane quadrant
+    constexpr uint32_t kStaging = (uint32_t)NEPI * 2048u;
+    const uint32_t staging = base + tiles_bytes;  // NEPI x 2 KB output staging buffers
+    const uint32_t bar_full = staging + kStaging;
     const uint32_t bar_empty = bar_full + 8u * kMaxStages;
     const uint32_t bar_accf = bar_empty + 8u * kMaxStages;
     const uint32_t bar_acce = bar_accf + 16u;
     const uint32_t bar_stall = bar_acce + 16u;
     const uint32_t bar_drain = bar_stall + 8u;
     const uint32_t bar_pready = bar_drain + 8u;  // cluster split-K: every CTA's partials are written
-    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStagingBytes + 8u * (2 * kMaxStages + 8));
+    uint32_t* slots = reinterpret_cast<uint32_t*>(base_ptr + tiles_bytes + kStaging + 8u * (2 * kMaxStages + 8));
     // the epilogue's bias slices, two tiles deep: [2][value 256 | gate 256] in the I/O dtype
-    const uint32_t bias_smem = staging + (uint32_t)kStagingBytes + kBarrierBytes;
+    const uint32_t bias_smem = staging + kStaging + kBarrierBytes;
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
@@ -672,11 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accf + 8u * b, 1);
-            mbar_init(bar_acce + 8u * b, kEpiWarps * PAIR);  // both CTAs' epilogues (leader's copy)
+            mbar_init(bar_acce + 8u * b, NEPI * PAIR);  // both CTAs' epilogues (leader's copy)
         }
         mbar_init(bar_stall, 1);
         mbar_init(bar_drain, 1);
-        mbar_init(bar_pready, (uint32_t)(p.split_k * kEpiWarps));
+        mbar_init(bar_pready, (uint32_t)(p.split_k * NEPI));
         *abort_flag = 0;
         *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -887,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - 2;
         const int q = warp & 3;    // TMEM lane quadrant this warp may access
-        const int half = ew >> 2;  // which of the interleaved 32-column groups
+        const int half = ew >> 2;  // which of the NPART interleaved 32-column groups
         const int row = q * 32 + lane;
         const int ngroups = p.BN / 32;
         const uint32_t stg = staging + (uint32_t)ew * 2048u;
@@ -908,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.bias) {
                 const int per = p.BN / 8;  // 16-byte chunks per operand
                 const int nb0 = c.tn * p.BN;
-                for (int i = ew * 32 + lane; i < n_b * per; i += kEpiWarps * 32) {
+                for (int i = ew * 32 + lane; i < n_b * per; i += NEPI * 32) {
                     const int op = i >= per ? 1 : 0;
                     const int col = nb0 + 8 * (i - op * per);
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -920,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
-            if (!epi_all(got)) break;
+            if (!epi_all<NEPI>(got)) break;
             tc_fence_after();
             const bool tr0 = tr && local == 0 && warp == 2 && lane == 0;
             if (tr0) trace_mark(tr, TR_EPI_START);
@@ -931,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)kAccSlot;
 
             if (EPI != EPI_DOWN || p.split_k == 1) {
-                for (int g = half; g < ngroups; g += 2) {
+                for (int g = half; g < ngroups; g += NPART) {
                     const int col = n0 + 32 * g;
                     const bool mark = tr0 && g == half;
                     float v[32];
@@ -1012,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         asm volatile("fence.proxy.async.global;" ::: "memory");
                     }
                     __syncwarp();
-                    epi_bar_sync();
+                    epi_bar_sync<NEPI>();
                     if (ew == 0 && lane == 0) {
                         __threadfence();
                         atomicAdd(p.ready + c.tm, 1u);
@@ -1033,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                            (size_t)p.split_k * 256u;
                 // (the partials go out as 4 KB bulk copies from the idle stage ring: the copy
                 // engine stores faster than per-thread stores do)
-                for (int g = half; g < ngroups; g += 2) {
+                for (int g = half; g < ngroups; g += NPART) {
                     const int u = q * ngroups + g;
                     if ((uint32_t)(u % p.split_k) == crank) continue;
                     uint32_t r[32];
@@ -1062,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     p.wait_limit_ns);
                 if (tr0) trace_mark(tr, TR_EPI_MATH);  // (cluster split-K: every partial written)
                 if (ready) {
-                    for (int g = half; g < ngroups; g += 2) {
+                    for (int g = half; g < ngroups; g += NPART) {
                         const int u = q * ngroups + g;
                         if ((uint32_t)(u % p.split_k) != crank) continue;
                         const int col = n0 + 32 * g;
@@ -1112,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t half_tile = (size_t)c.mn * PAIR + rank;  // this CTA's 128-row half of the tile
                 float4* part = reinterpret_cast<float4*>(
                     p.partials + (((size_t)c.split * tiles_mn) * PAIR + half_tile) * tile_elems);
-                for (int g = half; g < ngroups; g += 2) {
+                for (int g = half; g < ngroups; g += NPART) {
                     uint32_t r[32];
                     tmem_ld32(tq + 32u * g, r);
                     tmem_wait_ld_only();
@@ -1135,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // the barrier orders every epilogue thread's partial stores before the
                 // arrival thread's gpu-scope release (fences are cumulative)
-                epi_bar_sync();
+                epi_bar_sync<NEPI>();
                 if (ew == 0 && lane == 0) {
                     __threadfence();
                     const int prev = atomicAdd(p.counters + half_tile, 1);
@@ -1146,9 +1151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     *last_flag = last;
                 }
-                epi_bar_sync();
+                epi_bar_sync<NEPI>();
                 if (*last_flag) {
-                    for (int g = half; g < ngroups; g += 2) {
+                    for (int g = half; g < ngroups; g += NPART) {
                         const int col = n0 + 32 * g;
                         if (col >= p.N || !rows_live) continue;  // warp-uniform
                         float v[32];
@@ -1194,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
                     }
                 }
-                epi_bar_sync();  // last_flag is rewritten for the next tile
+                epi_bar_sync<NEPI>();  // last_flag is rewritten for the next tile
             }
             if (tr && warp == 2 && lane == 0) {
                 if (local == 0) trace_mark(tr, TR_EPI_DONE);
@@ -1242,7 +1247,7 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)((2 + epi_warps(EPI)) * 32), 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];

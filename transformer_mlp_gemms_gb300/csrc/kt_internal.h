@@ -26,6 +26,13 @@ constexpr int kStagingBytes = kEpiWarps * 32 * kStoreCols * 2;  // one 2 KB buff
 constexpr int kBarrierBytes = 512;
 constexpr int kBiasSmemBytes = 2048;
 constexpr int kSmemReserve = kStagingBytes + kBarrierBytes + kBiasSmemBytes + 1024;
+
+// Epilogue warps per kernel kind: GEGLU's fp32 erf-GELU epilogue is latency-bound with
+// two warps per SM sub-partition and gets three (12 warps); the others keep 8.
+constexpr int epi_warps(int epi) { return epi == 2 /* EPI_GEGLU */ ? 12 : kEpiWarps; }
+constexpr int smem_reserve(int epi) {
+    return epi_warps(epi) * 32 * kStoreCols * 2 + kBarrierBytes + kBiasSmemBytes + 1024;
+}
 constexpr int kMaxStages = 8;
 
 // Epilogue kinds (one kernel instantiation each, times two dtypes).

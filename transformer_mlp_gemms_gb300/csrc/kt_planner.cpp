@@ -92,14 +92,14 @@ double epi_cost_per_elem(int epi) {      // seconds per output element per SM (m
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int max_stages(int BN, int n_b, int pair, int bk, int kmaj) {
-    int s = (kSmemBudget - kSmemReserve) / stage_bytes(BN, n_b, pair, bk, kmaj);
+int max_stages(int BN, int n_b, int pair, int bk, int kmaj, int epi) {
+    int s = (kSmemBudget - smem_reserve(epi)) / stage_bytes(BN, n_b, pair, bk, kmaj);
     return std::min(s, kMaxStages);
 }
 
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
               int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0) {
-    int stages = max_stages(BN, n_b, pair, bk, kmaj);
+    int stages = max_stages(BN, n_b, pair, bk, kmaj, epi);
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
     const int64_t bm = (int64_t)kBM * pair;  // rows per tile (a pair's tile spans two CTAs)
@@ -150,7 +150,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->tiles_m = (int)tm; g->tiles_n = (int)tn; g->kblocks = (int)kb;
     g->kblocks_per_split = (int)kps;
     g->grid = (int)grid; g->waves = (int)waves;
-    g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk, kmaj) + kSmemReserve;
+    g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk, kmaj) + smem_reserve(epi);
     g->b_kmajor = kmaj;
     g->n_b = n_b;
     g->pair = pair;
