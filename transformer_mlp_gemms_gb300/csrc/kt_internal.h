@@ -118,7 +118,7 @@ void plan_fill_info(const GemmConfig& g, kt_gemm_plan_info* out);
 // Launch parameters shared by host and device.
 struct GemmParams {
     int M, N, K;
-    int BN, n_chunks, stages, split_k;  // n_chunks: 64-column B boxes per CTA
+    int BN, stages, split_k;
     int pair;                // 1 or 2 (CTA pair, tiles of 256 rows); tiles_m counts pair-tiles
     int bk;                  // k-block depth per stage (64 or 128)
     int cluster_sk;          // 1: the split_k CTAs of a tile form a cluster and reduce on chip

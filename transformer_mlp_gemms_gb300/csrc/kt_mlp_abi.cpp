@@ -149,7 +149,6 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.BN = g.BN;
     q.pair = g.pair;
     q.cluster_sk = g.cluster_sk;
-    q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.stages = g.stages;
     q.split_k = g.split_k;
     q.tiles_m = g.tiles_m;

@@ -280,7 +280,6 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.N = (int)D;
     q.K = (int)F;
     q.BN = g.BN;
-    q.n_chunks = (g.BN + 63) / 64;
     q.stages = g.stages;
     q.split_k = g.split_k;
     q.tiles_m = g.tiles_m;
@@ -290,11 +289,10 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.pair = g.pair;
     q.cluster_sk = 0;
-    q.n_chunks = (g.BN / g.pair + 63) / 64;
     q.idesc = make_idesc(dtype, g.BN, kBM * g.pair);
     q.bk = g.bk;
     q.a_bytes = kBM * g.bk * 2;
-    q.b_bytes = (uint32_t)q.n_chunks * 64u * (uint32_t)g.bk * 2u;
+    q.b_bytes = (uint32_t)b_tile_bytes(g.BN, g.pair, g.bk, 0);
     q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1, g.pair, g.bk);
     q.acc_bufs = 2u;
     q.bias = b_down;
