@@ -138,12 +138,16 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     // all SK partials, both latency-bound at a few tens of GB/s per SM; in a cluster: the
     // (SK-1)/SK of the partial other CTAs own written, a cluster-wide handshake, the
     // owner's reads of its 1/SK of the tile from every other split
+    // The exchange moves partials through the same SM ports the main loop loads through,
+    // so it does not hide under the next tile's main loop: it is paid once per wave.
     const double part = kBM * BN * 4.0;  // one fp32 partial tile
-    if (SK > 1 && !cluster_sk) t_epi += part / kSmStoreRate + SK * part / kSmReadRate;
-    if (SK > 1 && cluster_sk) t_epi += 0.5e-6 + (SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate);
+    double t_x = 0.0;
+    if (SK > 1 && !cluster_sk) t_x = part / kSmStoreRate + SK * part / kSmReadRate;
+    if (SK > 1 && cluster_sk) t_x = 0.5e-6 + (SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate);
     bool two_bufs = !(n_b == 2 && BN > 128);
-    double t_cta = two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
-                            : waves * (t_main + t_epi);
+    double t_cta = (two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
+                             : waves * (t_main + t_epi)) +
+                   waves * t_x;
 
     g->M = M; g->N = N; g->K = K;
     g->BN = BN; g->stages = stages; g->split_k = SK;
