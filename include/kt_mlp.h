@@ -190,6 +190,9 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
  * caller, 16-byte aligned, laid out as described at the top of this file.  b_up /
  * b_down must be non-NULL iff the plan has bias = 1.  Asynchronous: returns after
  * enqueueing.  A plan must not run concurrently on two streams (one workspace).
+ * Every launch parameter is the same from call to call, so the call may be captured
+ * into a CUDA graph (stream capture) and replayed; replays read and write the
+ * captured pointers.  The same holds for kt_mlp_run_ex.
  * Errors: INVALID (null / misaligned pointer, bias mismatch), CUDA (launch failed).
  */
 kt_status kt_mlp_run(kt_mlp_plan_t plan, const void* X, const void* W_up, const void* W_down,

@@ -753,8 +753,17 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     // the up projection's row blocks that hold this CTA's 128 rows of H
                     const int r1 = min(m_me + kBM, p.M) - 1;
                     bool got = true;
-                    for (int rb = m_me / p.ready_rows; rb <= r1 / p.ready_rows && got; ++rb)
+                    for (int rb = m_me / p.ready_rows; rb <= r1 / p.ready_rows && got; ++rb) {
                         got = wait_counter(p.ready + rb, p.ready_target, abort_flag, p.error, p.wait_limit_ns);
+                        // the last of this run's waits on the row block resets its counters
+                        // for the next run (whose up projection starts only after this grid
+                        // has completed): every launch parameter stays the same from run to
+                        // run, so a captured CUDA graph can replay the pair of kernels
+                        if (got && atomicAdd(p.ready_readers + rb, 1u) == p.ready_expect[rb] - 1u) {
+                            atomicExch(p.ready + rb, 0u);
+                            atomicExch(p.ready_readers + rb, 0u);
+                        }
+                    }
                     if (!got) break;
                     asm volatile("fence.proxy.async.global;" ::: "memory");  // H was written by TMA stores
                 }

@@ -141,6 +141,8 @@ struct GemmParams {
     int pdl_wait;            // 1: griddepcontrol.wait before the first global access (see ready)
     unsigned* ready;         // up: per row-block counters of stored tiles (incremented per CTA tile);
                              // down: the same counters, waited on before loading rows of H; or null
+    unsigned* ready_readers; // down: per row block, how many of this run's waits on it are done
+    const unsigned* ready_expect;  // down: per row block, how many waits this run makes on it
     unsigned ready_target;   // down: counter value meaning "every tile of this row block stored"
     int ready_rows;          // down: rows per up-projection row block (128 x its CTA pairing)
     unsigned long long* trace;  // optional per-CTA timeline (kTraceSlots u64 per CTA) or null

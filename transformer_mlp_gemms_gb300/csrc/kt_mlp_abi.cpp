@@ -12,9 +12,11 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "kt_internal.h"
 
@@ -97,8 +99,9 @@ struct kt_mlp_plan_s {
     float* partials = nullptr;  // [SK][tiles_m*128][tiles_n*BN] when the down GEMM splits K
     int* flags = nullptr;       // [0] error word, [1..] split-K tile counters, then row-block counters
     unsigned* ready = nullptr;  // per up-projection row block: CTA tiles of H stored (inside flags)
+    unsigned* readers = nullptr;  // per row block: the down projection's waits done this run (inside flags)
+    unsigned* ready_expect = nullptr;  // per row block: the down projection's waits per run (own allocation)
     size_t flag_bytes = 0;
-    unsigned epoch = 0;         // runs since the counters were last zero
     void* xn = nullptr;         // [M][D] LayerNorm output (layernorm plans)
     void* x_stage = nullptr;    // [M][D] for kt_mlp_run_host
     void* y_stage = nullptr;    // [M][D]
@@ -132,6 +135,7 @@ void free_plan(kt_mlp_plan_s* p) {
         if (e) cudaEventDestroy(e);
     cudaFree(p->H);
     cudaFree(p->xn);
+    cudaFree(p->ready_expect);
     cudaFree(p->partials);
     cudaFree(p->flags);
     cudaFree(p->x_stage);
@@ -263,9 +267,8 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
         return ok();
     }
     // the down projection's producer waits on per-row-block counters of stored H tiles
-    // (instead of the whole up grid); each run raises the target by one row block's tiles
+    // (instead of the whole up grid); its last reader of a row block resets them
     const unsigned per_block = (unsigned)(P->choice.up.tiles_n * P->choice.up.pair);
-    ++P->epoch;
     kt::GemmParams up = make_params(P, P->choice.up, epi_up);
     up.bias = P->bias ? t.b_up : nullptr;
     up.inject_stall = P->inject_stall;
@@ -284,7 +287,9 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.pdl_wait = 1;
     dn.trace = P->trace_down;
     dn.ready = P->ready;
-    dn.ready_target = P->epoch * per_block;
+    dn.ready_readers = P->readers;
+    dn.ready_expect = P->ready_expect;
+    dn.ready_target = per_block;
     dn.ready_rows = kt::kBM * P->choice.up.pair;
     if (timed) cudaEventRecord(P->ev[2], st);
     s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, &P->tm_ys, dn, P->choice.down.grid,
@@ -355,7 +360,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
     size_t n_ready = (size_t)P->choice.up.tiles_m;                     // one per up row block
-    size_t flag_bytes = 4 * (1 + n_counters + n_ready);
+    size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready);
     size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
                             : 0;
@@ -376,8 +381,29 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
         return cuda_fail("cudaMemset", e);
     }
     P->ready = reinterpret_cast<unsigned*>(P->flags + 1 + n_counters);
+    P->readers = P->ready + n_ready;
     P->flag_bytes = flag_bytes;
-    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + part_bytes + xn_bytes + 2 * io_bytes);
+    {
+        // how many times this plan's down projection waits on each up row block per run:
+        // every tile (and split) of a 128-row CTA share waits on the row blocks it covers
+        std::vector<unsigned> expect(n_ready, 0u);
+        const int64_t rows_up = (int64_t)kt::kBM * P->choice.up.pair;
+        for (int64_t tm = 0; tm < dn.tiles_m; ++tm)
+            for (int r = 0; r < dn.pair; ++r) {
+                const int64_t m0 = tm * kt::kBM * dn.pair + (int64_t)r * kt::kBM;
+                if (m0 >= M) continue;
+                const int64_t m1 = std::min<int64_t>(m0 + kt::kBM, M) - 1;
+                for (int64_t rb = m0 / rows_up; rb <= m1 / rows_up; ++rb)
+                    expect[(size_t)rb] += (unsigned)(dn.tiles_n * dn.split_k);
+            }
+        if ((e = cudaMalloc(reinterpret_cast<void**>(&P->ready_expect), 4 * n_ready)) != cudaSuccess ||
+            (e = cudaMemcpy(P->ready_expect, expect.data(), 4 * n_ready, cudaMemcpyHostToDevice)) != cudaSuccess) {
+            free_plan(P);
+            cudaGetLastError();
+            return fail(KT_ERR_NOMEM, std::string("workspace allocation: ") + cudaGetErrorString(e));
+        }
+    }
+    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + 4 * n_ready + part_bytes + xn_bytes + 2 * io_bytes);
     *out = P;
     return ok();
 }
@@ -402,7 +428,9 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     }
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
-    int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) + 2 * 2 * o.M * o.D;
+    // H, error word and split-K counters, three words per up row block, host staging
+    int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
+                 4 * 3 * (int64_t)c.up.tiles_m + 2 * 2 * o.M * o.D;
     if (c.down.split_k > 1)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
     if (o.layernorm) ws += 2 * o.M * o.D;
@@ -515,7 +543,6 @@ kt_status kt_mlp_status(kt_mlp_plan_t plan) {
         // clear the word and the counters an aborted run may have left behind
         cudaMemset(plan->flags, 0, plan->flag_bytes);
         cudaDeviceSynchronize();
-        plan->epoch = 0;
         const char* where = word == kt::DEV_TIMEOUT_PRODUCER ? "producer"
                           : word == kt::DEV_TIMEOUT_MMA ? "MMA issuer"
                           : word == kt::DEV_TIMEOUT_EPILOGUE ? "epilogue"
