@@ -563,8 +563,13 @@ __device__ __forceinline__ void add_residual32(const void* R, int row, int M, in
 // columns past the tensor's bounds are clipped by the TMA unit.
 template <int DT>
 __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t stg, int lane, const float* v,
-                                                int x, int y) {
-    if (lane == 0) bulk_wait_read0();  // the previous store from this buffer has read it
+                                                int x, int y, bool two_buffers = false) {
+    // the previous store from this buffer has read it (with two buffers per warp, the
+    // store from the other buffer may still be reading)
+    if (lane == 0) {
+        if (two_buffers) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else bulk_wait_read0();
+    }
     __syncwarp();
     const uint32_t row_base = stg + (uint32_t)lane * 64u;
     const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
@@ -645,8 +650,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
     constexpr int NEPI = epi_warps(EPI);   // epilogue warps
     constexpr int NPART = NEPI / 4;        // epilogue warps per TMEM lane quadrant
-    constexpr uint32_t kStaging = (uint32_t)NEPI * 2048u;
-    const uint32_t staging = base + tiles_bytes;  // NEPI x 2 KB output staging buffers
+    // NEPI x 2 KB output staging buffers, twice over when the plan has room for a second set
+    const uint32_t kStaging = (uint32_t)NEPI * 2048u * (p.dbl_staging ? 2u : 1u);
+    const uint32_t staging = base + tiles_bytes;
     const uint32_t bar_full = staging + kStaging;
     const uint32_t bar_empty = bar_full + 8u * kMaxStages;
     const uint32_t bar_accf = bar_empty + 8u * kMaxStages;
@@ -904,7 +910,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         const int half = ew >> 2;  // which of the NPART interleaved 32-column groups
         const int row = q * 32 + lane;
         const int ngroups = p.BN / 32;
-        const uint32_t stg = staging + (uint32_t)ew * 2048u;
+        const uint32_t stg0 = staging + (uint32_t)ew * 2048u;
+        const uint32_t stg_alt = (uint32_t)NEPI * 2048u;  // offset of the second buffer set
+        const bool dbl = p.dbl_staging != 0;
+        uint32_t nstores = 0;  // this warp's stores so far: picks the buffer
         const int tiles_mn = p.tiles_m * p.tiles_n;
         const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
         int local = 0;
@@ -985,7 +994,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                                     gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
                             }
                             if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                            stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
                             if (mark) trace_mark(tr, TR_EPI_STORE);
                         }
                     } else {
@@ -1007,7 +1016,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             if constexpr (EPI == EPI_DOWN)
                                 if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
                             if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                            stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
                             if (mark) trace_mark(tr, TR_EPI_STORE);
                         }
                     }
@@ -1113,7 +1122,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
                         if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
-                        stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                        stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
                     }
                 }
                 if (tr0) trace_mark(tr, TR_EPI_STORE);  // (cluster split-K: my units stored)
@@ -1205,7 +1214,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
                         if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
-                        stage_and_store<DT>(&tmC, stg, lane, v, col, y0);
+                        stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
                     }
                 }
                 epi_bar_sync<NEPI>();  // last_flag is rewritten for the next tile

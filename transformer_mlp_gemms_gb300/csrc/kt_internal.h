@@ -65,6 +65,7 @@ struct GemmConfig {
     int bk;                // k-block depth per pipeline stage: 64 or 128
     int cluster_sk;        // 1: split-K partials reduced inside a cluster (distributed smem)
     int b_kmajor;          // 1: the weight is stored [N][K] (PyTorch order) and loaded K-major
+    int dbl_staging;       // 1: shared memory left over for a second set of output staging buffers
     double useful_over_padded;
     double est_us;
 };
@@ -139,6 +140,7 @@ struct GemmParams {
     unsigned long long wait_limit_ns;   // bound of every device-side wait
     unsigned long long stall_limit_ns;  // bound of the injected wait
     int pdl_wait;            // 1: griddepcontrol.wait before the first global access (see ready)
+    int dbl_staging;         // 1: two output staging buffers per epilogue warp
     unsigned* ready;         // up: per row-block counters of stored tiles (incremented per CTA tile);
                              // down: the same counters, waited on before loading rows of H; or null
     unsigned* ready_readers; // down: per row block, how many of this run's waits on it are done

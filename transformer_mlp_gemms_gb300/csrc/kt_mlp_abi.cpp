@@ -162,6 +162,7 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.num_tiles = g.tiles_m * g.tiles_n * g.split_k;
     q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
     q.b_kmajor = g.b_kmajor;
+    q.dbl_staging = g.dbl_staging;
     q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair, g.b_kmajor);
     q.bk = g.bk;
     q.a_bytes = kt::kBM * g.bk * 2;

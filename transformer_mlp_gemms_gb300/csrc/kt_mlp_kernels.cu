@@ -291,6 +291,7 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.cluster_sk = 0;
     q.idesc = make_idesc(dtype, g.BN, kBM * g.pair);
     q.bk = g.bk;
+    q.dbl_staging = g.dbl_staging;
     q.a_bytes = kBM * g.bk * 2;
     q.b_bytes = (uint32_t)b_tile_bytes(g.BN, g.pair, g.bk, 0);
     q.stage_bytes = (uint32_t)stage_bytes(g.BN, 1, g.pair, g.bk);

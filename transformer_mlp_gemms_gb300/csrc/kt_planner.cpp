@@ -155,6 +155,10 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->kblocks_per_split = (int)kps;
     g->grid = (int)grid; g->waves = (int)waves;
     g->smem_bytes = stages * stage_bytes(BN, n_b, pair, bk, kmaj) + smem_reserve(epi);
+    // a second set of output staging buffers where it costs no pipeline stage: a warp's
+    // next store then need not wait for its previous one to be read out
+    g->dbl_staging = g->smem_bytes + epi_warps(epi) * 2048 <= kSmemBudget ? 1 : 0;
+    if (g->dbl_staging) g->smem_bytes += epi_warps(epi) * 2048;
     g->b_kmajor = kmaj;
     g->n_b = n_b;
     g->pair = pair;
