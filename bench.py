@@ -237,6 +237,20 @@ def pick_workload(args):
                      name=f"custom_{M}x{D}x{F}")
 
 
+def kernel_bytes(w, kernel: str, residual: bool) -> int:
+    """Algorithmic DRAM bytes of one launch: every operand read once, every result written once."""
+    e = 2
+    x, y, h = w.M * w.D * e, w.M * w.D * e, w.M * w.F * e
+    wu, wd = w.D * w.F_up * e, w.F * w.D * e
+    bu, bd = (w.F_up * e, w.D * e) if w.bias else (0, 0)
+    r = y if residual else 0
+    if kernel == "up":
+        return x + wu + bu + h
+    if kernel == "down":
+        return h + wd + bd + r + y
+    return x + wu + bu + wd + bd + r + y  # both projections in one kernel, H on chip
+
+
 def traffic_key(w, args) -> str:
     ln, res, outin = block_options(args)
     tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin), ("h_on_chip", args.h_path != "memory"))
@@ -449,7 +463,15 @@ def main():
     dominant = "fused" if fused else ("up" if mu >= md else "down")
     k_ms, k_flops = {"fused": (mu, w.flops), "up": (mu, up_flops), "down": (md, dn_flops)}[dominant]
     peak_tflops = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])  # fp16 : bf16 nominal 1 : 1
+    peak_gbs = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     achieved = k_flops / (k_ms * 1e-3) / 1e12
+    # the dominant kernel's algorithmic bytes (each operand read once, each result written
+    # once) and the roofline that binds: the larger of its FLOP floor and its byte floor
+    k_bytes = kernel_bytes(w, dominant, res)
+    t_tensor = k_flops / (peak_tflops * 1e12)
+    t_hbm = k_bytes / (peak_gbs * 1e9)
+    achieved_gbs = k_bytes / (k_ms * 1e-3) / 1e9
+    hbm_bound = t_hbm > t_tensor
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -458,11 +480,17 @@ def main():
         "us_per_call": ms_per_step * 1e3,
         "pct_of_peak": 100.0 * value / world / peak_tflops,
         "peak_tflops": peak_tflops, "peak_source": peak_src,
-        "roofline": {"bound": "tensor", "kernel": ("kt_fused_kernel (both projections, H on chip)" if fused else
-                                                   f"kt_gemm_kernel ({dominant} projection)"),
-                     "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tflops, "traffic": ncu_traffic(traffic_key(w, args), dominant),
-                     "algorithmic_flops_per_launch": k_flops, "ms_per_launch": k_ms,
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor",
+                     "kernel": ("kt_fused_kernel (both projections, H on chip)" if fused else
+                                f"kt_gemm_kernel ({dominant} projection)"),
+                     "achieved": achieved_gbs if hbm_bound else achieved,
+                     "peak": peak_gbs if hbm_bound else peak_tflops,
+                     "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                     "frac": achieved_gbs / peak_gbs if hbm_bound else achieved / peak_tflops,
+                     "traffic": ncu_traffic(traffic_key(w, args), dominant),
+                     "algorithmic_flops_per_launch": k_flops, "algorithmic_bytes_per_launch": k_bytes,
+                     "tensor_frac": achieved / peak_tflops, "hbm_frac": achieved_gbs / peak_gbs,
+                     "hbm_peak_gbs": peak_gbs, "ms_per_launch": k_ms,
                      "peak_note": (f"{peak_src} bf16 dense burst from MEASURED_PEAKS.json (fp16 has the "
                                    f"same nominal rate)") if peak_src == "measured" else "fallback"},
         "kernels_ms": ({"fused": mu, "fused_tflops": w.flops / (mu * 1e-3) / 1e12} if fused else
