@@ -295,12 +295,13 @@ kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us);
 /*
  * kt_mlp_debug_trace -- timeline tracing for tests and profiling.  With non-NULL
  * device buffers, the next runs of this plan write, per CTA of the up / down kernel,
- * 16 uint64 slots: %globaltimer (ns) at CTA entry, set-up done, first copy issued,
+ * 32 uint64 slots: %globaltimer (ns) at CTA entry, set-up done, first copy issued,
  * first stage landed, first tile's main loop done, epilogue start / done, exit;
  * then the SM id, the number of tiles, the last tile's main-loop / epilogue end,
- * and four epilogue sub-phase marks of the first epilogue warp.  Each buffer must
- * hold 16 * grid uint64 (grid from kt_mlp_get_info); the caller owns them.  NULL
- * buffers switch tracing off.
+ * four epilogue sub-phase marks of the first epilogue warp, and ten marks of the
+ * CTA's second tile (epilogue sub-phases, its main loop's start and end, its first
+ * copy); slots 26-31 are unused.  Each buffer must hold 32 * grid uint64 (grid from
+ * kt_mlp_get_info); the caller owns them.  NULL buffers switch tracing off.
  */
 kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_down);
 

@@ -147,7 +147,7 @@ def test_planner_invariants_on_every_workload(lib, name):
     _check_gemm(info["down"], w.M, w.D, w.F)
     assert info["up"]["split_k"] == 1  # the activation is not linear: no split of the up projection
     if w.act == wl.ACT_GEGLU:
-        assert info["up"]["BN"] <= 256
+        assert info["up"]["BN"] <= 128  # value and gate columns: one MMA of N = 2 BN <= 256
 
 
 @pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
@@ -173,7 +173,7 @@ def test_pytorch_order_weights_need_no_column_padding_in_shared_memory(lib):
             share = g["BN"] // pair
             b_cols = share if layout == 1 else -(-share // 64) * 64
             stage = 128 * g["BK"] * 2 + n_b * b_cols * g["BK"] * 2
-            reserve = (12 if act == 2 else 8) * 2048 + 512 + 2048 + 1024  # staging, barriers, bias, alignment
+            reserve = 8 * 2048 + 512 + 2048 + 1024  # staging, barriers, bias, alignment
             assert g["smem_bytes"] == g["stages"] * stage + reserve
 
 

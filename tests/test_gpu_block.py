@@ -84,11 +84,15 @@ CASES = [
     ("erf_outin_bk128_splitk", (257, 1152, 4304, wl.ACT_GELU_ERF, wl.DT_F16, False), 1, 1, 1, "192,1,128",
      "96,4,1,128,0"),
     ("none_outin_cluster_sk", (130, 72, 4104, wl.ACT_NONE, wl.DT_F16, True), 1, 0, 1, None, "96,4,1,64,1"),
-    ("geglu_outin_pair_bn256", (64, 320, 640, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 0, 1, "256,2,64", None),
+    ("geglu_outin_pair_bn128", (64, 320, 640, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 0, 1, "128,2,64", None),
+    ("geglu_outin_pair_share32", (300, 136, 200, wl.ACT_GEGLU, wl.DT_F16, True), 1, 0, 1, "64,2,128", None),
+    ("geglu_inout_pair_bk128", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128", None),
+    ("geglu_inout_bn64", (129, 200, 136, wl.ACT_GEGLU, wl.DT_F16, False), 1, 0, 0, "64,1,64", None),
     ("geglu_outin_bn96_bk128", (77, 128, 136, wl.ACT_GEGLU, wl.DT_F16, False), 1, 0, 1, "96,1,128", "32,2,1,128,0"),
     ("silu_pair_splitk_res", (384, 1280, 512, wl.ACT_SILU, wl.DT_BF16, True), 1, 1, 0, "128,2,128",
      "128,2,2,64,0"),
     ("tiny_everything", (5, 8, 8, wl.ACT_GELU_SIGMOID, wl.DT_F16, True), 1, 1, 1, None, None),
+    ("geglu_pair_ln_bk128", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128", None),
     ("wide_ln_reread", (40, 4096, 64, wl.ACT_GELU_ERF, wl.DT_BF16, False), 1, 1, 1, None, None),
 ]
 

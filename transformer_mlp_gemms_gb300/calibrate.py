@@ -140,7 +140,9 @@ def evaluate(names, in_dir: str, num_sms: int = 152) -> float:
             pick = kt_mlp.kt_mlp_plan_info(w.M, w.D, w.F, w.act, w.dtype, w.bias, num_sms)[gemm]
             hit = [r for r in keep if (r["BM"], r["BN"], r["BK"], r["SK"], r["CL"]) ==
                    (pick["BM"], pick["BN"], pick["BK"], pick["split_k"], pick["cluster_sk"])]
-            best = min(meas) if meas else float("nan")
+            if not meas:
+                continue
+            best = min(meas)
             pm = hit[0]["us_mean"] if hit else float("nan")
             regret = pm - best
             if regret == regret:

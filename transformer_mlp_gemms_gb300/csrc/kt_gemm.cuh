@@ -16,8 +16,8 @@
 //               (M = 128 or 256, N = BN, K = 16, fp32 accumulation in tensor memory),
 //               BK / 16 per k-block, and tcgen05.commit hands the stage back.  Two
 //               TMEM accumulator buffers let tile i+1's main loop run under tile i's
-//               epilogue.  GEGLU issues a second MMA per step into a gate
-//               accumulator that shares the A tile (one X stream, two weights).
+//               epilogue.  GEGLU loads the value and the gate columns of its tile as
+//               one B operand, so one MMA of N = 2 BN fills both accumulators.
 //   warps 2-9   epilogue: tcgen05.ld moves the fp32 accumulator to registers (TMEM
 //               lane = tile row), adds the bias (staged per tile in shared memory),
 //               applies the activation (GELU erf / tanh / sigmoid, SiLU, GEGLU
@@ -312,7 +312,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // tcgen05.wait::ld, with the loaded registers threaded through so that no use
-// of them can be scheduled before the wait.
+// of them can be scheduled before the wait.  (tmem_f16cols below: 16 columns as fp32.)
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
@@ -329,6 +329,15 @@ __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r)[16], uint32_t (&s)[1
                    "+r"(s[12]), "+r"(s[13]), "+r"(s[14]), "+r"(s[15])
                  :
                  : "memory");
+}
+
+// 16 consecutive fp32 accumulator columns of this lane's row (TMEM lane), waited for.
+__device__ __forceinline__ void tmem_f16cols(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld(r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 32 lanes x 32 consecutive 32-bit columns.
@@ -425,28 +434,41 @@ __device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approxi
     return y;
 }
 
-// gelu_erf(z) = z * Phi(z),  Phi(z) = erfc(-z / sqrt 2) / 2.
+// gelu_erf(z) = z * Phi(z), and Phi(-|z|) = erfc(a) / 2 with a = |z| / sqrt 2.
 // erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
-// 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), fractional error
-// below 1.2e-7 for every a >= 0; erfc(-a) = 2 - erfc(a).  Evaluated in fp32 with the
-// hardware exp2 and reciprocal: no cancellation for z < 0, no branches.
+// 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), P of degree 9,
+// fractional error below 1.2e-7 for every a >= 0.  Evaluated in fp32 with the hardware
+// exp2 and reciprocal, constants folded: with t' = t / 2 = 1 / (2 + a) and
+// u = a sqrt(log2 e),  erfc(a) / 2 = t' * 2^(Q(t') - u^2),  Q(t') = log2(e) P(2 t')
+// (coefficient i of the fit times 2^i log2 e; Horner's rule).  Then gelu = z Phi(-|z|)
+// for z < 0 and z - z Phi(-|z|) for z >= 0: no cancellation for z < 0, no branches.
+namespace erfc_fit {
+constexpr double kL = 1.4426950408889634;  // log2(e)
+constexpr float kQ9 = (float)(0.17087277 * 512.0 * kL), kQ8 = (float)(-0.82215223 * 256.0 * kL);
+constexpr float kQ7 = (float)(1.48851587 * 128.0 * kL), kQ6 = (float)(-1.13520398 * 64.0 * kL);
+constexpr float kQ5 = (float)(0.27886807 * 32.0 * kL), kQ4 = (float)(-0.18628806 * 16.0 * kL);
+constexpr float kQ3 = (float)(0.09678418 * 8.0 * kL), kQ2 = (float)(0.37409196 * 4.0 * kL);
+constexpr float kQ1 = (float)(1.00002368 * 2.0 * kL), kQ0 = (float)(-1.26551223 * kL);
+constexpr float kU = 0.84932180028801907f;  // sqrt(log2(e) / 2): u = |z| kU
+constexpr float kA = 0.83255461115769776f;  // 1 / sqrt(log2 e):  a = u kA
+}  // namespace erfc_fit
+
 __device__ __forceinline__ float gelu_erf_f(float z) {
-    const float a = fabsf(z) * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(0.5f, a, 1.0f));
-    // the fit's degree-9 polynomial in t by Estrin's scheme (pairs, then t^2, t^4, t^8):
-    // the same coefficients as Horner's rule with a dependency chain of 4 instead of 9
-    const float t2 = t * t, t4 = t2 * t2, t8 = t4 * t4;
-    const float q01 = fmaf(1.00002368f, t, -1.26551223f);
-    const float q23 = fmaf(0.09678418f, t, 0.37409196f);
-    const float q45 = fmaf(0.27886807f, t, -0.18628806f);
-    const float q67 = fmaf(1.48851587f, t, -1.13520398f);
-    const float q89 = fmaf(0.17087277f, t, -0.82215223f);
-    const float r0 = fmaf(q23, t2, q01);
-    const float r1 = fmaf(q67, t2, q45);
-    const float p = fmaf(q89, t8, fmaf(r1, t4, r0));
-    const float e = t * ex2_approx(fmaf(-a, a, p) * 1.4426950408889634f);  // erfc(|z| / sqrt 2)
-    const float phi = z >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
-    return z * phi;
+    using namespace erfc_fit;
+    const float u = fabsf(z) * kU;
+    const float tp = rcp_approx(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
+    float q = fmaf(kQ9, tp, kQ8);
+    q = fmaf(q, tp, kQ7);
+    q = fmaf(q, tp, kQ6);
+    q = fmaf(q, tp, kQ5);
+    q = fmaf(q, tp, kQ4);
+    q = fmaf(q, tp, kQ3);
+    q = fmaf(q, tp, kQ2);
+    q = fmaf(q, tp, kQ1);
+    q = fmaf(q, tp, kQ0);
+    const float h = tp * ex2_approx(fmaf(-u, u, q));  // Phi(-|z|)
+    const float zh = z * h;
+    return z >= 0.0f ? z - zh : zh;
 }
 
 // gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
@@ -521,31 +543,28 @@ __device__ __forceinline__ void load_bias32(const void* bias, int col, int limit
     }
 }
 
-// 32 bias values from the tile's bias slice staged in shared memory (bsm: the slice's
-// first column; columns past N were staged as zeros).  Every lane reads the same
-// addresses: broadcast reads.
-template <int DT>
-__device__ __forceinline__ void bias32_smem(uint32_t bsm, float* b) {
+// n (a multiple of 4) fp32 bias values from the tile's bias slice staged in shared
+// memory (bsm: the first of them; columns past N were staged as zeros).  Every lane
+// reads the same addresses: broadcast reads.
+template <int n>
+__device__ __forceinline__ void bias_from_smem(uint32_t bsm, float* b) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        uint4 w;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+    for (int g = 0; g < n / 4; ++g)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b[4 * g]), "=f"(b[4 * g + 1]), "=f"(b[4 * g + 2]), "=f"(b[4 * g + 3])
                      : "r"(bsm + 16u * g));
-        unpack8<DT>(w, b + 8 * g);
-    }
 }
 
-// Add 32 values of row `row` of the residual R[M][N], starting at column `col`, to v
-// (rows past M and groups of 8 at or past N are skipped: those results are never
-// stored).  Plain loads: R may be the output Y itself, whose other blocks other
+// Add n (16 or 32) values of row `row` of the residual R[M][N], starting at column
+// `col`, to v (rows past M and groups of 8 at or past N are skipped: those results are
+// never stored).  Plain loads: R may be the output Y itself, whose other blocks other
 // threads are writing meanwhile.
-template <int DT>
+template <int DT, int n = 32>
 __device__ __forceinline__ void add_residual32(const void* R, int row, int M, int col, int N, float* v) {
     if (row >= M) return;
     const uint16_t* ptr = reinterpret_cast<const uint16_t*>(R) + (size_t)row * (size_t)N + col;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < n / 8; ++g) {
         if (col + 8 * g < N) {
             const uint4 w = *reinterpret_cast<const uint4*>(ptr + 8 * g);
             float f[8];
@@ -556,14 +575,13 @@ __device__ __forceinline__ void add_residual32(const void* R, int row, int M, in
     }
 }
 
-// Round a warp's 32 x 32 block (this lane's row, 32 columns in v) to the I/O dtype,
-// stage it in the warp's 2 KB shared-memory buffer in the 64-byte swizzled layout
-// the output tensor map expects (16-byte chunk c of row r lands at chunk
-// c ^ ((r >> 1) & 3)), and store it with one TMA tensor store at (x, y).  Rows and
-// columns past the tensor's bounds are clipped by the TMA unit.
-template <int DT>
-__device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t stg, int lane, const float* v,
-                                                int x, int y, bool two_buffers = false) {
+// Stage a warp's 32 x 32 block, already rounded to the I/O dtype (this lane's row: 32
+// values packed in pairs in w), in the warp's 2 KB shared-memory buffer in the 64-byte
+// swizzled layout the output tensor map expects (16-byte chunk c of row r lands at
+// chunk c ^ ((r >> 1) & 3)), and store it with one TMA tensor store at (x, y).  Rows
+// and columns past the tensor's bounds are clipped by the TMA unit.
+__device__ __forceinline__ void stage_and_store_packed(const CUtensorMap* tmC, uint32_t stg, int lane,
+                                                       const uint32_t* w, int x, int y, bool two_buffers = false) {
     // the previous store from this buffer has read it (with two buffers per warp, the
     // store from the other buffer may still be reading)
     if (lane == 0) {
@@ -574,11 +592,8 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t
     const uint32_t row_base = stg + (uint32_t)lane * 64u;
     const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        st_shared_v4(row_base + ((c ^ sw) << 4), pack2<DT>(v[8 * c + 0], v[8 * c + 1]),
-                     pack2<DT>(v[8 * c + 2], v[8 * c + 3]), pack2<DT>(v[8 * c + 4], v[8 * c + 5]),
-                     pack2<DT>(v[8 * c + 6], v[8 * c + 7]));
-    }
+    for (int c = 0; c < 4; ++c)
+        st_shared_v4(row_base + ((c ^ sw) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -587,13 +602,25 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t
     }
 }
 
+// As stage_and_store_packed, rounding 32 fp32 values (round to nearest even) first.
+template <int DT>
+__device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t stg, int lane, const float* v,
+                                                int x, int y, bool two_buffers = false) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack2<DT>(v[2 * i], v[2 * i + 1]);
+    stage_and_store_packed(tmC, stg, lane, w, x, y, two_buffers);
+}
+
 // The MMAs of one k-block: NK steps of K = 16 (4 for a 64-deep stage, 8 for 128).
 // Descriptor start addresses move in 16-byte units.  A (K-major): +32 bytes per step
 // inside a 64-deep swizzle atom, +16 KB per atom.  B N-major (KB = 0): +2 KB per step
 // (16 rows of 128 bytes).  B K-major (KB = 1): as A, with atoms of b_atom16 units.
-template <int EPI, int PAIR, int NK, int KB>
-__device__ __forceinline__ void issue_kblock(uint32_t d, uint32_t d_gate, uint64_t ad0, uint64_t bd0, uint64_t gd0,
-                                             uint32_t idesc, uint32_t acc0, uint32_t b_atom16) {
+// GEGLU needs no second MMA: its B operand holds the value and the gate columns of
+// the tile side by side, so one MMA of N = 2 BN fills both accumulators.
+template <int PAIR, int NK, int KB>
+__device__ __forceinline__ void issue_kblock(uint32_t d, uint64_t ad0, uint64_t bd0, uint32_t idesc, uint32_t acc0,
+                                             uint32_t b_atom16) {
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const uint64_t ad = ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
@@ -602,11 +629,6 @@ __device__ __forceinline__ void issue_kblock(uint32_t d, uint32_t d_gate, uint64
         const uint32_t acc = k == 0 ? acc0 : 1u;
         if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, idesc, acc);
         else mma_f16(d, ad, bd, idesc, acc);
-        if constexpr (EPI == EPI_GEGLU) {
-            const uint64_t gd = gd0 + boff;
-            if constexpr (PAIR == 2) mma_f16_pair(d_gate, ad, gd, idesc, acc);
-            else mma_f16(d_gate, ad, gd, idesc, acc);
-        }
     }
 }
 
@@ -614,14 +636,18 @@ __device__ __forceinline__ void issue_kblock(uint32_t d, uint32_t d_gate, uint64
 // The kernel
 // ---------------------------------------------------------------------------
 
+// The t-th work item of the kernel: a tile, which of its split_k partial sums this CTA
+// accumulates (`split`) and that split's k-blocks [kb0, kb1).  The SK splits of one tile
+// are consecutive CTAs of a cluster with the cluster reduction, otherwise split-major.
 struct TileCoord {
     int split, tm, tn, mn;
+    int kb0, kb1;
 };
 
 __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     TileCoord c;
     const int per_split = p.tiles_m * p.tiles_n;
-    if (p.cluster_sk) {  // the SK splits of one tile are one cluster of consecutive CTAs
+    if (p.cluster_sk) {
         c.split = t % p.split_k;
         c.mn = t / p.split_k;
     } else {
@@ -630,6 +656,8 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     }
     c.tm = c.mn / p.tiles_n;
     c.tn = c.mn - c.tm * p.tiles_n;
+    c.kb0 = c.split * p.kblocks_per_split;
+    c.kb1 = min(c.kb0 + p.kblocks_per_split, p.kblocks);
     return c;
 }
 
@@ -728,10 +756,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 // failure injection: a barrier nobody arrives on, bounded wait
                 wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
             }
-            for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step) {
+            int local = 0;
+            for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step, ++local) {
                 const TileCoord c = decode_tile(t, p);
-                const int kb0 = c.split * p.kblocks_per_split;
-                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
+                const int kb0 = c.kb0, kb1 = c.kb1;
                 // this CTA's rows of A and its share of the B columns
                 const int bcols = p.BN / PAIR;
                 auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
@@ -784,11 +812,19 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
                     if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
+                    if (tr && kb == kb0 && local == 1) trace_mark(tr, TR_S_LD0);
                     const int k0 = kb * p.bk;
                     // N-major B: box j is 64 columns x bk rows at column nb + 64 j, row k0.
                     // K-major B: box j is bcols rows x 64 at row nb, column k0 + 64 j.
                     const uint32_t box_bytes = p.b_kmajor ? p.b_atom_bytes : (uint32_t)p.bk * 128u;
                     const int nbox = p.b_kmajor ? (chunks ? p.bk / kAtomK : 0) : chunks;
+                    // shared-memory slots of value box j and gate box j: N-major, the gate
+                    // chunks follow all value chunks at the same pitch; K-major, each 64-deep
+                    // atom holds this CTA's value rows, then its gate rows
+                    auto vslot = [&](int j) { return sB + box_bytes * (uint32_t)(p.b_kmajor ? n_b * j : j); };
+                    auto gslot = [&](int j) {
+                        return p.b_kmajor ? sB + box_bytes * (uint32_t)(2 * j + 1) : sB + p.b_bytes + box_bytes * (uint32_t)j;
+                    };
                     auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + 64 * j; };
                     auto by = [&](int j, int row0) { return p.b_kmajor ? row0 + nb_me : k0; };
                     auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + 64 * j; };
@@ -799,11 +835,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             for (int a = 0; a < p.bk / kAtomK; ++a)
                                 tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_pair(sB + box_bytes * j, &tmB, fb_leader, bx(j), by(j, 0));
+                            tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
                         if (EPI == EPI_GEGLU) {
                             for (int j = 0; j < nbox; ++j)
-                                tma_load_2d_pair(sB + p.b_bytes + box_bytes * j, &tmB, fb_leader, gx(j),
-                                                 by(j, p.gate_col));
+                                tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
                         }
                     } else {
                         mbar_arrive_expect_tx(fb, tx);
@@ -811,10 +846,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             for (int a = 0; a < p.bk / kAtomK; ++a)
                                 tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d(sB + box_bytes * j, &tmB, fb, bx(j), by(j, 0));
+                            tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
                         if (EPI == EPI_GEGLU) {
                             for (int j = 0; j < nbox; ++j)
-                                tma_load_2d(sB + p.b_bytes + box_bytes * j, &tmB, fb, gx(j), by(j, p.gate_col));
+                                tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
                         }
                     }
                     armed |= 1u << stage;
@@ -847,9 +882,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                 p.wait_limit_ns))
                     break;
                 tc_fence_after();
+                if (tr && local == 1) trace_mark(tr, TR_S_MMA0);
                 const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
-                const int kb0 = c.split * p.kblocks_per_split;
-                const int kb1 = min(kb0 + p.kblocks_per_split, p.kblocks);
+                const int kb0 = c.kb0, kb1 = c.kb1;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(bar_full + 8u * stage, phase, abort_flag, p.error, DEV_TIMEOUT_MMA,
@@ -864,19 +899,19 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     // Descriptors of this stage; the K steps only move the start address by
                     // constant offsets (issue_kblock).  128-byte swizzle, 8-row groups 1 KB
                     // apart; N-major B: 64-column chunks bk x 128 bytes apart.
+                    // GEGLU: the gate chunks follow the value chunks (N-major: at the same
+                    // chunk pitch; K-major: inside every 64-deep atom), one operand of 2 BN.
                     const uint64_t ad0 = smem_desc(sA, 16u, 1024u);
                     const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * 128u;
                     const uint64_t bd0 = smem_desc(sB, b_lbo, 1024u);
-                    const uint64_t gd0 = smem_desc(sB + p.b_bytes, b_lbo, 1024u);
                     const uint32_t acc0 = kb > kb0 ? 1u : 0u;
-                    const uint32_t batom16 = p.b_atom_bytes >> 4;
-                    const uint32_t dg = d + p.gate_acc_off;
+                    const uint32_t batom16 = (p.b_atom_bytes * (uint32_t)n_b) >> 4;
                     if (p.b_kmajor) {
-                        if (p.bk == 64) issue_kblock<EPI, PAIR, 4, 1>(d, dg, ad0, bd0, gd0, p.idesc, acc0, batom16);
-                        else issue_kblock<EPI, PAIR, 8, 1>(d, dg, ad0, bd0, gd0, p.idesc, acc0, batom16);
+                        if (p.bk == 64) issue_kblock<PAIR, 4, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
+                        else issue_kblock<PAIR, 8, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
                     } else {
-                        if (p.bk == 64) issue_kblock<EPI, PAIR, 4, 0>(d, dg, ad0, bd0, gd0, p.idesc, acc0, 0u);
-                        else issue_kblock<EPI, PAIR, 8, 0>(d, dg, ad0, bd0, gd0, p.idesc, acc0, 0u);
+                        if (p.bk == 64) issue_kblock<PAIR, 4, 0>(d, ad0, bd0, p.idesc, acc0, 0u);
+                        else issue_kblock<PAIR, 8, 0>(d, ad0, bd0, p.idesc, acc0, 0u);
                     }
                     issued_any = true;
                     // stage free (in both CTAs of a pair) once these MMAs completed
@@ -893,6 +928,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 else mma_commit(bar_accf + 8u * buf);
                 if (tr) {
                     if (local == 0) trace_mark(tr, TR_MAIN_DONE);
+                    if (local == 1) trace_mark(tr, TR_S_MMA1);
                     trace_mark(tr, TR_LAST_MAIN);
                     tr[(size_t)blockIdx.x * kTraceSlots + TR_TILES] = (unsigned long long)(local + 1);
                 }
@@ -916,6 +952,24 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         uint32_t nstores = 0;  // this warp's stores so far: picks the buffer
         const int tiles_mn = p.tiles_m * p.tiles_n;
         const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
+        // Up projection: this CTA's rows of a stored tile are counted for the down
+        // projection's producer once every epilogue warp's TMA stores of the tile have
+        // completed.  The count of tile i is raised after tile i + 1's accumulator wait
+        // (or after the last tile), when those stores have long completed, so that the
+        // wait for their completion is off the epilogue's path.
+        int pending_rows = -1;
+        auto signal_ready = [&](int tm) {
+            if (lane == 0) {
+                bulk_wait0();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            __syncwarp();
+            epi_bar_sync<NEPI>();  // every epilogue warp's stores of the tile completed
+            if (ew == 0 && lane == 0) {
+                __threadfence();
+                atomicAdd(p.ready + tm, 1u);
+            }
+        };
         int local = 0;
         for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
             const TileCoord c = decode_tile(t, p);
@@ -927,9 +981,11 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
             // memory while the MMAs run; the barrier after the accumulator wait publishes
             // it to every epilogue warp (two buffers: a warp can only reach tile + 2 after
             // every warp has finished tile).
+            // Staged in fp32 (1 KB per tile: up to 256 columns, or GEGLU's 128 value
+            // columns at +0 and 128 gate columns at +512 bytes).
             const uint32_t bsm = bias_smem + (uint32_t)(local & 1) * 1024u;
             if (p.bias) {
-                const int per = p.BN / 8;  // 16-byte chunks per operand
+                const int per = p.BN / 8;  // 8-column chunks per operand
                 const int nb0 = c.tn * p.BN;
                 for (int i = ew * 32 + lane; i < n_b * per; i += NEPI * 32) {
                     const int op = i >= per ? 1 : 0;
@@ -938,13 +994,27 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     if (col < p.N)
                         v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.bias) +
                                                                  (op ? p.gate_col : 0) + col));
-                    st_shared_v4(bsm + (uint32_t)op * 512u + (uint32_t)(i - op * per) * 16u, v.x, v.y, v.z, v.w);
+                    float f[8];
+                    unpack8<DT>(v, f);
+                    const uint32_t dst = bsm + (uint32_t)op * 512u + (uint32_t)(i - op * per) * 32u;
+                    st_shared_v4(dst, __float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                 __float_as_uint(f[3]));
+                    st_shared_v4(dst + 16u, __float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                                 __float_as_uint(f[7]));
                 }
             }
             const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
             if (!epi_all<NEPI>(got)) break;
             tc_fence_after();
+            const bool tr1 = tr && local == 1 && warp == 2 && lane == 0;  // steady-state marks
+            if (tr1) trace_mark(tr, TR_S_ACC);
+            if (EPI != EPI_DOWN && pending_rows >= 0) {  // the previous tile's rows (see above)
+                signal_ready(pending_rows);
+                pending_rows = -1;
+            }
+            if (tr1) trace_mark(tr, TR_S_SIG);
+            int gi = 0;  // this warp's column groups of the tile so far (trace marks)
             const bool tr0 = tr && local == 0 && warp == 2 && lane == 0;
             if (tr0) trace_mark(tr, TR_EPI_START);
             const int m0 = c.tm * (kBM * PAIR) + (int)rank * kBM;  // this CTA's first row
@@ -957,67 +1027,83 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 for (int g = half; g < ngroups; g += NPART) {
                     const int col = n0 + 32 * g;
                     const bool mark = tr0 && g == half;
-                    float v[32];
                     if constexpr (EPI == EPI_GEGLU) {
-                        // in two halves of 16 columns: value, gate and bias of one half live at
-                        // a time, which leaves registers for more independent GELU chains
+                        // Accumulator columns: PAIR runs of [value share | gate share], one
+                        // per CTA's B share (share = BN / PAIR columns of H).  In two halves
+                        // of 16 columns: value, gate and bias of one half live at a time,
+                        // which leaves registers for more independent GELU chains.
+                        const uint32_t share = p.geglu_share;
+                        const uint32_t c32 = 32u * (uint32_t)g;
+                        const uint32_t vcol = (c32 / share) * 2u * share + c32 % share;
                         if (col < p.N && rows_live) {
+                            uint32_t w[16];  // the group's 32 results, rounded and packed in pairs
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 uint32_t rv[16], rg[16];
-                                tmem_ld16(tq + 32u * g + 16u * h, rv);
-                                tmem_ld16(tq + p.gate_acc_off + 32u * g + 16u * h, rg);
+                                tmem_ld16(tq + vcol + 16u * h, rv);
+                                tmem_ld16(tq + vcol + share + 16u * h, rg);
                                 tmem_wait_ld2(rv, rg);
                                 if (mark && h == 0) trace_mark(tr, TR_EPI_LD);
                                 float bv[16], bg[16];
                                 if (p.bias) {
-                                    const uint32_t o = 64u * (uint32_t)g + 32u * (uint32_t)h;
-#pragma unroll
-                                    for (int q2 = 0; q2 < 2; ++q2) {
-                                        uint4 wv, wg;
-                                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                                     : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w)
-                                                     : "r"(bsm + o + 16u * q2));
-                                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                                     : "=r"(wg.x), "=r"(wg.y), "=r"(wg.z), "=r"(wg.w)
-                                                     : "r"(bsm + 512u + o + 16u * q2));
-                                        unpack8<DT>(wv, bv + 8 * q2);
-                                        unpack8<DT>(wg, bg + 8 * q2);
-                                    }
+                                    const uint32_t o = 128u * (uint32_t)g + 64u * (uint32_t)h;
+                                    bias_from_smem<16>(bsm + o, bv);
+                                    bias_from_smem<16>(bsm + 512u + o, bg);
                                 } else {
 #pragma unroll
                                     for (int i = 0; i < 16; ++i) bv[i] = bg[i] = 0.0f;
                                 }
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[16 * h + i] = (__uint_as_float(rv[i]) + bv[i]) *
-                                                    gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
+                                for (int i = 0; i < 16; i += 2) {
+                                    const float y0v = (__uint_as_float(rv[i]) + bv[i]) *
+                                                      gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
+                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) *
+                                                      gelu_erf_f(__uint_as_float(rg[i + 1]) + bg[i + 1]);
+                                    w[8 * h + i / 2] = pack2<DT>(y0v, y1v);
+                                }
                             }
                             if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
+                            if (tr1 && gi < 2) trace_mark(tr, gi == 0 ? TR_S_G0M : TR_S_G1M);
+                            stage_and_store_packed(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, w, col,
+                                                   y0, dbl);
                             if (mark) trace_mark(tr, TR_EPI_STORE);
+                            if (tr1 && gi < 2) trace_mark(tr, gi == 0 ? TR_S_G0S : TR_S_G1S);
+                            ++gi;
                         }
                     } else {
-                        uint32_t r[32];
-                        tmem_ld32(tq + 32u * g, r);
-                        tmem_wait_ld_only();
-                        reg_fence32(r);
-                        if (mark) trace_mark(tr, TR_EPI_LD);
                         if (col < p.N && rows_live) {
-                            float b[32];
-                            if (p.bias) {
-                                bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
-                            } else {
+                            uint32_t r[32];
+                            tmem_ld32(tq + 32u * g, r);
+                            tmem_wait_ld_only();
+                            reg_fence32(r);
+                            if (mark) trace_mark(tr, TR_EPI_LD);
+                            uint32_t w[16];  // the group's 32 results, rounded and packed in pairs
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) b[i] = 0.0f;
+                            for (int h = 0; h < 2; ++h) {  // in 16-column slices
+                                float v[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[16 * h + i]);
+                                if (p.bias) {
+                                    float b[16];
+                                    bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) v[i] += b[i];
+                                }
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = act_f<EPI>(v[i]);
+                                if constexpr (EPI == EPI_DOWN)
+                                    if (p.residual)
+                                        add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) w[8 * h + i] = pack2<DT>(v[2 * i], v[2 * i + 1]);
                             }
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = act_f<EPI>(__uint_as_float(r[i]) + b[i]);
-                            if constexpr (EPI == EPI_DOWN)
-                                if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
                             if (mark) trace_mark(tr, TR_EPI_MATH);
-                            stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
+                            if (tr1 && gi < 2) trace_mark(tr, gi == 0 ? TR_S_G0M : TR_S_G1M);
+                            stage_and_store_packed(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, w, col,
+                                                   y0, dbl);
                             if (mark) trace_mark(tr, TR_EPI_STORE);
+                            if (tr1 && gi < 2) trace_mark(tr, gi == 0 ? TR_S_G0S : TR_S_G1S);
+                            ++gi;
                         }
                     }
                 }
@@ -1027,21 +1113,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
                     else mbar_arrive(acce);
                 }
-                if (EPI != EPI_DOWN && p.ready != nullptr) {
-                    // this CTA's rows of the tile are in global memory: count them for the
-                    // down projection's producer (release after every epilogue warp's stores)
-                    if (lane == 0) {
-                        bulk_wait0();
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                    }
-                    __syncwarp();
-                    epi_bar_sync<NEPI>();
-                    if (ew == 0 && lane == 0) {
-                        __threadfence();
-                        atomicAdd(p.ready + c.tm, 1u);
-                    }
-                }
-            } else if (p.cluster_sk) {
+                if (tr1) trace_mark(tr, TR_S_ARR);
+                if (EPI != EPI_DOWN && p.ready != nullptr) pending_rows = c.tm;  // counted later
+            } else if constexpr (EPI == EPI_DOWN) {
+              if (p.cluster_sk) {
                 // split-K inside a cluster, reduce-scattered through L2: each 32 x 32 unit of
                 // the tile (row block q, column group g, u = q * ngroups + g) is owned by CTA
                 // u % SK of the cluster, and a unit is handled by the same warp in every CTA.
@@ -1090,39 +1165,44 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                         if ((uint32_t)(u % p.split_k) != crank) continue;
                         const int col = n0 + 32 * g;
                         if (col >= p.N || !rows_live) continue;  // warp-uniform
-                        uint32_t r[32];
-                        tmem_ld32(tq + 32u * g, r);
-                        tmem_wait_ld_only();
-                        reg_fence32(r);
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
                         const float4* src = part + (size_t)u * p.split_k * 256u + lane;
-                        for (int sp = 0; sp < p.split_k; ++sp) {  // split order: deterministic
-                            if ((uint32_t)sp == crank) {
+                        uint32_t w[16];  // the unit's 32 results, rounded and packed in pairs
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(r[i]);
-                                continue;
+                        for (int h = 0; h < 2; ++h) {  // in 16-column slices
+                            float v[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                            for (int sp = 0; sp < p.split_k; ++sp) {  // split order: deterministic
+                                if ((uint32_t)sp == crank) {
+                                    float a[16];
+                                    tmem_f16cols(tq + 32u * g + 16u * h, a);
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) v[i] += a[i];
+                                    continue;
+                                }
+                                float4 x[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) x[i] = __ldcg(src + (size_t)sp * 256u + 32 * (4 * h + i));
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    v[4 * i] += x[i].x;
+                                    v[4 * i + 1] += x[i].y;
+                                    v[4 * i + 2] += x[i].z;
+                                    v[4 * i + 3] += x[i].w;
+                                }
                             }
-                            float4 x[8];
+                            if (p.bias) {
+                                float b[16];
+                                bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + (size_t)sp * 256u + 32 * i);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                v[4 * i] += x[i].x;
-                                v[4 * i + 1] += x[i].y;
-                                v[4 * i + 2] += x[i].z;
-                                v[4 * i + 3] += x[i].w;
+                                for (int i = 0; i < 16; ++i) v[i] += b[i];
                             }
-                        }
-                        if (p.bias) {
-                            float b[32];
-                            bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
+                            if (p.residual) add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += b[i];
+                            for (int i = 0; i < 8; ++i) w[8 * h + i] = pack2<DT>(v[2 * i], v[2 * i + 1]);
                         }
-                        if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
-                        stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
+                        stage_and_store_packed(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, w, col, y0,
+                                               dbl);
                     }
                 }
                 if (tr0) trace_mark(tr, TR_EPI_STORE);  // (cluster split-K: my units stored)
@@ -1174,13 +1254,14 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     for (int g = half; g < ngroups; g += NPART) {
                         const int col = n0 + 32 * g;
                         if (col >= p.N || !rows_live) continue;  // warp-uniform
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        uint32_t w[16];  // the group's 32 results, rounded and packed in pairs
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             // 16 columns of this row from every split: up to 4 splits' loads in
                             // flight at once, summed in split order (deterministic)
+                            float v[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
                             const size_t off = (size_t)(2 * g + h) * 4 * kBM + row;  // in float4
                             for (int s0 = 0; s0 < p.split_k; s0 += 4) {
                                 float4 x[4][4];
@@ -1198,32 +1279,37 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                     if (s0 + j < p.split_k) {
 #pragma unroll
                                         for (int i = 0; i < 4; ++i) {
-                                            v[16 * h + 4 * i] += x[j][i].x;
-                                            v[16 * h + 4 * i + 1] += x[j][i].y;
-                                            v[16 * h + 4 * i + 2] += x[j][i].z;
-                                            v[16 * h + 4 * i + 3] += x[j][i].w;
+                                            v[4 * i] += x[j][i].x;
+                                            v[4 * i + 1] += x[j][i].y;
+                                            v[4 * i + 2] += x[j][i].z;
+                                            v[4 * i + 3] += x[j][i].w;
                                         }
                                     }
                                 }
                             }
-                        }
-                        if (p.bias) {
-                            float b[32];
-                            bias32_smem<DT>(bsm + 64u * (uint32_t)g, b);
+                            if (p.bias) {
+                                float b[16];
+                                bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += b[i];
+                                for (int i = 0; i < 16; ++i) v[i] += b[i];
+                            }
+                            if (p.residual) add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) w[8 * h + i] = pack2<DT>(v[2 * i], v[2 * i + 1]);
                         }
-                        if (p.residual) add_residual32<DT>(p.residual, y0 + lane, p.M, col, p.N, v);
-                        stage_and_store<DT>(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, v, col, y0, dbl);
+                        stage_and_store_packed(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, w, col, y0,
+                                               dbl);
                     }
                 }
                 epi_bar_sync<NEPI>();  // last_flag is rewritten for the next tile
+              }
             }
             if (tr && warp == 2 && lane == 0) {
                 if (local == 0) trace_mark(tr, TR_EPI_DONE);
                 trace_mark(tr, TR_LAST_EPI);
             }
         }
+        if (EPI != EPI_DOWN && pending_rows >= 0) signal_ready(pending_rows);  // the last tile's rows
         // every TMA store of this warp has completed before the CTA may exit
         if (lane == 0) bulk_wait0();
         __syncwarp();

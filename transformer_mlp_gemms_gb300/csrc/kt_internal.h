@@ -27,9 +27,10 @@ constexpr int kBarrierBytes = 512;
 constexpr int kBiasSmemBytes = 2048;
 constexpr int kSmemReserve = kStagingBytes + kBarrierBytes + kBiasSmemBytes + 1024;
 
-// Epilogue warps per kernel kind: GEGLU's fp32 erf-GELU epilogue is latency-bound with
-// two warps per SM sub-partition and gets three (12 warps); the others keep 8.
-constexpr int epi_warps(int epi) { return epi == 2 /* EPI_GEGLU */ ? 12 : kEpiWarps; }
+// Epilogue warps per kernel kind: 8 for every kind (two per TMEM lane quadrant).  GEGLU's
+// 128-column tiles split into 4 column groups evenly over 8 warps; 12 warps measured no
+// faster and cost a third more output staging.
+constexpr int epi_warps(int epi) { return epi == 2 /* EPI_GEGLU */ ? 8 : kEpiWarps; }
 constexpr int smem_reserve(int epi) {
     return epi_warps(epi) * 32 * kStoreCols * 2 + kBarrierBytes + kBiasSmemBytes + 1024;
 }
@@ -53,7 +54,7 @@ enum DevError : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2,
 // One GEMM's launch configuration, chosen by the planner.
 struct GemmConfig {
     int64_t M, N, K;       // output rows, output columns, reduction length
-    int BN;                // N tile, multiple of 32, 32..256
+    int BN;                // N tile (H columns for GEGLU, whose MMA N is 2 BN), multiple of 32, 32..256
     int stages;
     int split_k;
     int tiles_m, tiles_n, kblocks, kblocks_per_split;
@@ -130,11 +131,12 @@ struct GemmParams {
     uint32_t idesc;          // tcgen05 instruction descriptor
     uint32_t stage_bytes, a_bytes, b_bytes;  // per stage / A tile / one B operand tile
     uint32_t acc_bufs;       // accumulator buffers in TMEM (1 or 2)
-    uint32_t gate_acc_off;   // TMEM column offset of the gate accumulator (GEGLU)
+    uint32_t geglu_share;    // GEGLU: H columns per CTA share (BN / pair); the accumulator holds,
+                             // per share, its value columns then its gate columns
     const void* bias;        // b_up (GEGLU: value then gate halves) / b_down / null
     const void* residual;    // down projection: R[M][N] added before the rounding, or null
     float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32
-    int* counters;           // split-K: [tiles_m*tiles_n] arrival counters (zero between runs)
+    int* counters;           // split-K: per 128-row half tile, arrival counters (zero between runs)
     int* error;              // device error word
     int inject_stall;        // failure-injection hook (producer waits on a silent barrier)
     unsigned long long wait_limit_ns;   // bound of every device-side wait
@@ -168,7 +170,18 @@ enum TraceSlot : int {
     TR_EPI_MATH = 13,    //   ... its bias / activation done
     TR_EPI_STORE = 14,   //   ... its first store issued
     TR_EPI_DRAIN = 15,   //   ... all its stores complete
-    kTraceSlots = 16
+    // steady state: the CTA's second tile
+    TR_S_ACC = 16,       // first epilogue warp: accumulator ready
+    TR_S_SIG = 17,       //   ... the previous tile's rows counted (up projection)
+    TR_S_G0M = 18,       //   ... its first column group computed
+    TR_S_G0S = 19,       //   ... its first column group's store issued
+    TR_S_G1M = 20,       //   ... its second column group computed
+    TR_S_G1S = 21,       //   ... its second column group's store issued
+    TR_S_ARR = 22,       //   ... accumulator released
+    TR_S_MMA0 = 23,      // MMA issuer: the tile's accumulator free, main loop starts
+    TR_S_MMA1 = 24,      // MMA issuer: the tile's last k-block committed
+    TR_S_LD0 = 25,       // producer: the tile's first copy issued
+    kTraceSlots = 32
 };
 
 // Launch parameters of the fused kernel.

@@ -163,14 +163,14 @@ kt::GemmParams make_params(const kt_mlp_plan_s* P, const kt::GemmConfig& g, int 
     q.gate_col = epi == kt::EPI_GEGLU ? (int)P->F : 0;
     q.b_kmajor = g.b_kmajor;
     q.dbl_staging = g.dbl_staging;
-    q.idesc = kt::make_idesc(P->dtype, g.BN, kt::kBM * g.pair, g.b_kmajor);
+    q.idesc = kt::make_idesc(P->dtype, g.BN * g.n_b, kt::kBM * g.pair, g.b_kmajor);  // GEGLU: N = 2 BN
     q.bk = g.bk;
     q.a_bytes = kt::kBM * g.bk * 2;
     q.b_bytes = (uint32_t)kt::b_tile_bytes(g.BN, g.pair, g.bk, g.b_kmajor);
     q.b_atom_bytes = g.b_kmajor ? (uint32_t)(g.BN / g.pair) * 128u : 0u;
     q.stage_bytes = (uint32_t)kt::stage_bytes(g.BN, g.n_b, g.pair, g.bk, g.b_kmajor);
-    q.acc_bufs = (epi == kt::EPI_GEGLU && g.BN > 128) ? 1u : 2u;
-    q.gate_acc_off = epi == kt::EPI_GEGLU ? (g.BN <= 128 ? 128u : 256u) : 0u;
+    q.acc_bufs = 2u;
+    q.geglu_share = epi == kt::EPI_GEGLU ? (uint32_t)(g.BN / g.pair) : 0u;
     q.error = P->flags;
     q.wait_limit_ns = 4000000000ull;  // 4 s: far beyond any legitimate wait
     q.stall_limit_ns = (unsigned long long)P->stall_limit_us * 1000ull;
@@ -358,9 +358,10 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
         return fail(s, why);
     }
     const kt::GemmConfig& dn = P->choice.down;
+    const kt::GemmConfig& up = P->choice.up;
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
-    size_t n_ready = (size_t)P->choice.up.tiles_m;                     // one per up row block
+    size_t n_ready = (size_t)up.tiles_m;                               // one per up row block
     size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready);
     size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
@@ -388,7 +389,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
         // how many times this plan's down projection waits on each up row block per run:
         // every tile (and split) of a 128-row CTA share waits on the row blocks it covers
         std::vector<unsigned> expect(n_ready, 0u);
-        const int64_t rows_up = (int64_t)kt::kBM * P->choice.up.pair;
+        const int64_t rows_up = (int64_t)kt::kBM * up.pair;
         for (int64_t tm = 0; tm < dn.tiles_m; ++tm)
             for (int r = 0; r < dn.pair; ++r) {
                 const int64_t m0 = tm * kt::kBM * dn.pair + (int64_t)r * kt::kBM;
@@ -404,7 +405,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
             return fail(KT_ERR_NOMEM, std::string("workspace allocation: ") + cudaGetErrorString(e));
         }
     }
-    P->workspace_bytes = (int64_t)(h_bytes + flag_bytes + 4 * n_ready + part_bytes + xn_bytes + 2 * io_bytes);
+    P->workspace_bytes =
+        (int64_t)(h_bytes + flag_bytes + 4 * n_ready + part_bytes + xn_bytes + 2 * io_bytes);
     *out = P;
     return ok();
 }
@@ -591,7 +593,8 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
                   (long long)plan->M, (long long)plan->D, (long long)plan->F, act_name(plan->act),
                   plan->dtype == KT_BF16 ? "bf16" : "f16", plan->bias, plan->residual, plan->layernorm,
                   plan->w_layout == KT_W_OUT_IN ? "out_in" : "in_out", plan->num_sms, kt::kBM * u.pair, u.BN, u.tiles_m, u.tiles_n,
-                  u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us, kt::kBM * d.pair, d.BN,
+                  u.grid, u.waves, u.waves == 1 ? "" : "s", u.stages, u.useful_over_padded, u.est_us,
+                  kt::kBM * d.pair, d.BN,
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.split_k == 1 ? "no reduction" : d.cluster_sk ? "cluster reduction" : "global reduction",
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);

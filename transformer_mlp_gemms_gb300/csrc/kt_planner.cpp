@@ -19,7 +19,6 @@
 //   t_epi   = 128 * BN * c_epi          (per-element epilogue cost of the kind)
 //           + (SK > 1) the fp32 partial write and the last CTA's read of SK partials
 //   t_cta   = t_main + (waves-1) * max(t_main, t_epi) + t_epi   (two TMEM buffers)
-//           = waves * (t_main + t_epi)                           (one buffer)
 // and the candidate with the smallest t_cta wins; ties go to the larger
 // tile (fewer, more intense tiles).  All constants are a model; est_us is never
 // reported as a measurement.
@@ -43,9 +42,16 @@ constexpr double kIssuePerStage = 200.0 / kClk;
 constexpr double kL2Feed = 20e12;         // aggregate L2 -> SM bytes/s (model)
 constexpr double kSmFeedMax = 240e9;      // one SM's fill bandwidth (model)
 constexpr double kTFill = 0.35e-6;        // pipeline fill + drain latency per tile (model)
-// Load latency a stage ring must cover (calibrated on GB300 with a measured sweep of
-// tile shapes: the main loop runs at about max(MMA, issue, 2.0 us / (K depth in flight))).
-constexpr double kLoadLatency = 2.0e-6;
+// Load latency that the stages in flight must cover (all but the one the MMAs read), and
+// a fixed cost per k-block that nothing overlaps (calibrated on GB300 with a measured
+// sweep of tile shapes: the main loop runs at about max(MMA, issue, feed,
+// 1.2 us / (stages - 1)) + 0.17 us per k-block, so that deep k-blocks of large TMA
+// boxes beat more, shallower stages holding the same bytes, given three stages or more).
+constexpr double kLoadLatency = 1.2e-6;
+constexpr double kStageCost = 0.17e-6;
+// The fused H-on-chip kernel's ring (two stages per 64-column slice) was calibrated
+// against the two-kernel path with a load latency of 2.0 us per ring pass.
+constexpr double kFusedLoadLatency = 2.0e-6;
 // Launch, set-up, first loads and drain of one kernel, as CUDA events around a single
 // launch see them (calibrated; shifts every candidate equally, so it does not change
 // the ranking).
@@ -74,9 +80,6 @@ int max_active_clusters(int size, int num_sms) {
 // barrier traffic of the main loop and epilogue.
 constexpr double kPairKernelCost = 3.0e-6;
 constexpr double kPairTileCost = 0.3e-6;
-// A GEGLU tile on a CTA pair (two MMAs per step for both CTAs' rows) measured about
-// 13 ns per tile column slower than the model above (calibrated on the SDXL shapes).
-constexpr double kPairGegluPerCol = 13e-9;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -99,6 +102,9 @@ int max_stages(int BN, int n_b, int pair, int bk, int kmaj, int epi) {
 
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
               int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0) {
+    // GEGLU: value and gate columns form one MMA operand of N = 2 BN (at most 256, one
+    // accumulator buffer of tensor memory); an N-major share must be whole 64-column boxes
+    if (n_b == 2 && (n_b * BN > kAccSlot || (!kmaj && (BN / pair) % 64 != 0))) return false;
     int stages = max_stages(BN, n_b, pair, bk, kmaj, epi);
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
@@ -127,12 +133,12 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     // thread (in a pair it issues for both CTAs), the time to stream its share of the
     // operands, and the load latency the ring of `stages` k-blocks has to cover
     double t_mma = n_b * 2.0 * kBM * BN * bk / kRsm;
-    double t_issue = kIssuePerStage + n_b * (bk / 16) * kIssuePerMma;
+    double t_issue = kIssuePerStage + (bk / 16) * kIssuePerMma;
     double bytes_kb = (double)stage_bytes(BN, n_b, pair, bk, kmaj);
     double feed = std::min(kSmFeedMax, kL2Feed / (double)grid);
-    double t_kb = std::max(std::max(t_mma, t_issue), std::max(bytes_kb / feed, kLoadLatency / stages));
-    double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0) +
-                    (pair == 2 && n_b == 2 ? kPairGegluPerCol * BN : 0.0);
+    double t_kb = std::max(std::max(t_mma, t_issue), std::max(bytes_kb / feed, kLoadLatency / (stages - 1))) +
+                  kStageCost;
+    double t_main = (double)kps * t_kb + kTFill + (pair == 2 ? kPairTileCost : 0.0);
     double t_epi = (double)kBM * BN * epi_cost_per_elem(epi);
     // split-K (calibrated on GB300): writing the fp32 partial, then the last CTA reading
     // all SK partials, both latency-bound at a few tens of GB/s per SM; in a cluster: the
@@ -144,10 +150,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     double t_x = 0.0;
     if (SK > 1 && !cluster_sk) t_x = part / kSmStoreRate + SK * part / kSmReadRate;
     if (SK > 1 && cluster_sk) t_x = 0.5e-6 + (SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate);
-    bool two_bufs = !(n_b == 2 && BN > 128);
-    double t_cta = (two_bufs ? t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi
-                             : waves * (t_main + t_epi)) +
-                   waves * t_x;
+    double t_cta = t_main + (waves - 1) * std::max(t_main, t_epi) + t_epi + waves * t_x;
 
     g->M = M; g->N = N; g->K = K;
     g->BN = BN; g->stages = stages; g->split_k = SK;
@@ -242,9 +245,10 @@ static bool plan_fused(int64_t M, int64_t D, int64_t F, int act, int num_sms, Fu
     const double t_epi = (double)kBM * kFusedSlice * epi_cost_per_elem(up_epilogue(act));
     // each slice takes two ring stages (its W_up and its W_down slices): the ring must
     // cover the load latency as in the two-kernel main loop
-    const double t_lat = 2.0 * kLoadLatency / stages;
+    const double t_lat = 2.0 * kFusedLoadLatency / stages;
     const double t_slice = std::max(std::max(t_mma, t_load), std::max(t_epi, t_lat));
-    const double t_rb = (double)n_slices * t_slice + kLoadLatency / 2 + (double)kBM * Dk * epi_cost_per_elem(EPI_DOWN);
+    const double t_rb =
+        (double)n_slices * t_slice + kFusedLoadLatency / 2 + (double)kBM * Dk * epi_cost_per_elem(EPI_DOWN);
     f->est_us = ((double)f->waves * t_rb + kKernelOverhead) * 1e6;
     return true;
 }
@@ -283,14 +287,15 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         return KT_ERR_UNSUPPORTED;
     }
     // Measurement overrides (planner calibration sweeps): KT_FORCE_UP="BN[,PAIR[,BK]]" and
-    // KT_FORCE_DOWN="BN,SK[,PAIR[,BK]]".  An infeasible override is an error, never ignored.
+    // KT_FORCE_DOWN="BN,SK[,PAIR[,BK[,CLUSTER]]]".  An infeasible override is an error, never ignored.
     if (const char* e = std::getenv("KT_FORCE_UP")) {
         int bn = 0, pr = 1, bk = 64;
         GemmConfig g;
         int nf = std::sscanf(e, "%d,%d,%d", &bn, &pr, &bk);
         if (nf < 1 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
             bn > 256 || !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, bk, &g, false, kmaj)) {
-            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32, 64 for a pair; BK 64 or 128)";
+            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32, 64 for a pair; BK 64 or "
+                   "128; GEGLU: BN <= 128, and BN / PAIR a multiple of 64 for [in][out] weights)";
             return KT_ERR_INVALID;
         }
         out->up = g;
