@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--weights", choices=["in_out", "out_in"], default="in_out")
     ap.add_argument("--h-path", choices=["memory", "on_chip", "auto"], default="memory",
                     help="where H lives between the projections (on_chip: the fused kernel, D <= 256)")
+    ap.add_argument("--launches", choices=["auto", "one", "two"], default="auto",
+                    help="both projections in one persistent launch (one) or two launches (two; auto: the "
+                         "planner's choice)")
     ap.add_argument("--shape", default=None,
                     help="a custom workload instead of --workload: M,D,F,act,dtype,bias with act one of "
                          "gelu_erf|gelu_tanh|geglu|none|gelu_sigmoid|silu and dtype f16|bf16")
@@ -226,6 +229,12 @@ def h_path_code(args):
     return {"memory": kt_mlp.KT_H_MEMORY, "on_chip": kt_mlp.KT_H_ON_CHIP, "auto": kt_mlp.KT_H_AUTO}[args.h_path]
 
 
+def launches_code(args):
+    from transformer_mlp_gemms_gb300 import kt_mlp
+    return {"auto": kt_mlp.KT_LAUNCH_AUTO, "one": kt_mlp.KT_LAUNCH_ONE, "two": kt_mlp.KT_LAUNCH_TWO}[
+        getattr(args, "launches", "auto")]
+
+
 def pick_workload(args):
     from transformer_mlp_gemms_gb300 import workloads as wl
     if not args.shape:
@@ -248,13 +257,15 @@ def kernel_bytes(w, kernel: str, residual: bool) -> int:
         return x + wu + bu + h
     if kernel == "down":
         return h + wd + bd + r + y
+    if kernel == "one":  # both projections in one kernel, H through memory
+        return x + wu + bu + 2 * h + wd + bd + r + y
     return x + wu + bu + wd + bd + r + y  # both projections in one kernel, H on chip
 
 
 def traffic_key(w, args) -> str:
     ln, res, outin = block_options(args)
-    tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin), ("h_on_chip", args.h_path != "memory"))
-            if on]
+    tags = [t for t, on in (("ln", ln), ("res", res), ("out_in", outin), ("h_on_chip", args.h_path != "memory"),
+                            ("one_launch", getattr(args, "launches", "auto") == "one")) if on]
     return w.name + (f"[{','.join(tags)}]" if tags else "")
 
 
@@ -267,7 +278,7 @@ def workload_config(w, l2, args=None):
     if args is not None:
         ln, res, outin = block_options(args)
         cfg["block"] = {"layernorm": ln, "residual": res, "weights": "out_in" if outin else "in_out",
-                        "h_path": args.h_path}
+                        "h_path": args.h_path, "launches": getattr(args, "launches", "auto")}
     return cfg
 
 
@@ -354,7 +365,8 @@ def main():
     tdt = wl.TORCH_DTYPES[w.dtype]
     Y = torch.empty((w.M, w.D), dtype=tdt, device="cuda")
     plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias, residual=res, layernorm=ln,
-                       weight_layout=kt_mlp.KT_W_OUT_IN if outin else kt_mlp.KT_W_IN_OUT, h_path=h_path_code(args))
+                       weight_layout=kt_mlp.KT_W_OUT_IN if outin else kt_mlp.KT_W_IN_OUT, h_path=h_path_code(args),
+                       launches=launches_code(args))
     info = plan.info()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -460,8 +472,10 @@ def main():
     dn_flops = 2 * w.M * w.F * w.D
     mu, md, ml = statistics.mean(ms_up), statistics.mean(ms_dn), statistics.mean(ms_ln)
     fused = bool(info.get("h_on_chip"))
-    dominant = "fused" if fused else ("up" if mu >= md else "down")
-    k_ms, k_flops = {"fused": (mu, w.flops), "up": (mu, up_flops), "down": (md, dn_flops)}[dominant]
+    one = bool(info.get("one_launch"))
+    dominant = "fused" if fused else "one" if one else ("up" if mu >= md else "down")
+    k_ms, k_flops = {"fused": (mu, w.flops), "one": (mu, w.flops), "up": (mu, up_flops),
+                     "down": (md, dn_flops)}[dominant]
     peak_tflops = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])  # fp16 : bf16 nominal 1 : 1
     peak_gbs = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     achieved = k_flops / (k_ms * 1e-3) / 1e12
@@ -482,6 +496,7 @@ def main():
         "peak_tflops": peak_tflops, "peak_source": peak_src,
         "roofline": {"bound": "hbm" if hbm_bound else "tensor",
                      "kernel": ("kt_fused_kernel (both projections, H on chip)" if fused else
+                                "kt_gemm_kernel (both projections in one launch)" if one else
                                 f"kt_gemm_kernel ({dominant} projection)"),
                      "achieved": achieved_gbs if hbm_bound else achieved,
                      "peak": peak_gbs if hbm_bound else peak_tflops,
@@ -494,6 +509,7 @@ def main():
                      "peak_note": (f"{peak_src} bf16 dense burst from MEASURED_PEAKS.json (fp16 has the "
                                    f"same nominal rate)") if peak_src == "measured" else "fallback"},
         "kernels_ms": ({"fused": mu, "fused_tflops": w.flops / (mu * 1e-3) / 1e12} if fused else
+                       {"one_launch": mu, "one_launch_tflops": w.flops / (mu * 1e-3) / 1e12} if one else
                        {"up": mu, "down": md, "up_tflops": up_flops / (mu * 1e-3) / 1e12,
                         "down_tflops": dn_flops / (md * 1e-3) / 1e12}),
         **({"layernorm_kernel": {"ms": ml, "bytes": 2 * w.M * w.D * 2 + 2 * w.D * 2,
@@ -502,13 +518,13 @@ def main():
         "plan": {"up": {k: info["up"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "grid", "waves")},
                  "down": {k: info["down"][k] for k in ("BM", "BN", "BK", "stages", "split_k", "cluster_sk", "grid",
                                                        "waves")},
-                 "h_on_chip": int(fused),
+                 "h_on_chip": int(fused), "one_launch": int(one),
                  **({"fused": {"grid": info["fused_grid"], "stages": info["fused_stages"]}} if fused else {})},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.D * 2,
                 "d2h_bytes_per_step": w.M * w.D * 2, "us_per_call": e2e_s / e2e_steps * 1e6,
                 "entry_point": ("kt_mlp_run_host (pinned X in, Y out; weights resident)" if plain else
                                 "kt_mlp_run_ex between a pinned X copy in and a Y copy out (weights resident)")},
-        "gpu_launches": ((1 if fused else 2) + (1 if ln else 0)) * args.steps,
+        "gpu_launches": ((1 if fused or one else 2) + (1 if ln else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "gpu": props.name, "sms": props.multi_processor_count,

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define KT_MLP_ABI_VERSION 2
+#define KT_MLP_ABI_VERSION 3
 
 typedef enum {
     KT_ACT_GELU_ERF = 0,  /* gelu(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2))                 */
@@ -73,6 +73,15 @@ typedef enum {
  * choice between the two.  kt_mlp_plan uses KT_H_MEMORY.
  */
 typedef enum { KT_H_AUTO = 0, KT_H_MEMORY = 1, KT_H_ON_CHIP = 2 } kt_h_path;
+
+/* How the two projections are launched when H goes through memory.  KT_LAUNCH_TWO: two
+ * persistent kernels, the down projection's CTAs starting as the up projection's finish
+ * (programmatic dependent launch) and loading rows of H as they are stored.  KT_LAUNCH_ONE:
+ * one persistent kernel that takes up tiles, then down tiles, from one work queue (a down
+ * tile once its rows of H are stored); no split-K for the down projection.  KT_LAUNCH_AUTO
+ * is the planner's choice: two launches, which measured as fast or faster on all but one
+ * of the benchmark shapes. */
+typedef enum { KT_LAUNCH_AUTO = 0, KT_LAUNCH_ONE = 1, KT_LAUNCH_TWO = 2 } kt_launches;
 
 /* Memory order of W_up and W_down. */
 typedef enum {
@@ -127,6 +136,12 @@ typedef struct {
                                   two-kernel alternative); its tile facts follow           */
     int32_t fused_grid, fused_stages, fused_smem_bytes;
     double fused_est_us;
+    int32_t one_launch;        /* 1: both projections run in ONE persistent launch: up and down
+                                  tiles taken from one work queue (up tiles first), a down tile
+                                  as soon as its rows of H are stored; up / down describe the
+                                  two GEMMs in it, sharing one shared-memory ring            */
+    int32_t one_launch_grid, one_launch_stages, one_launch_smem_bytes;
+    double one_launch_est_us;
 } kt_plan_info;
 
 /*
@@ -147,6 +162,7 @@ typedef struct {
     int32_t weight_layout;  /* kt_weight_layout                                              */
     float ln_eps;           /* LayerNorm epsilon (> 0; PyTorch's default is 1e-5)            */
     int32_t h_path;         /* kt_h_path: where H lives between the two projections          */
+    int32_t launches;       /* kt_launches: one or two kernel launches (H through memory)    */
 } kt_mlp_options;
 
 /*

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
     # and the binding wraps each of them under the same name
     assert set(names) <= set(kt_mlp.SIGNATURES)
-    assert lib.kt_mlp_abi_version() == 2
+    assert lib.kt_mlp_abi_version() == 3
 
 
 def test_plan_without_a_gpu_fails_cleanly(lib):
@@ -139,12 +139,29 @@ def _check_gemm(g, M, N, K):
     assert g["est_us"] > 0
 
 
+def _check_one_launch(info):
+    # both projections in one persistent launch: whole down tiles, one CTA pairing, one
+    # shared-memory ring, at most one unit per resident CTA (pair), never more units than tiles
+    if not info["one_launch"]:
+        return
+    up, dn = info["up"], info["down"]
+    pair = up["BM"] // 128
+    assert dn["BM"] == up["BM"] and dn["split_k"] == 1 and dn["cluster_sk"] == 0 and info["h_on_chip"] == 0
+    assert up["stages"] == dn["stages"] == info["one_launch_stages"] >= 2
+    assert up["smem_bytes"] == dn["smem_bytes"] == info["one_launch_smem_bytes"] <= 227 * 1024
+    g = info["one_launch_grid"]
+    assert g % pair == 0 and g <= (SMS // pair) * pair
+    assert g // pair <= up["tiles_m"] * up["tiles_n"] + dn["tiles_m"] * dn["tiles_n"]
+    assert info["one_launch_est_us"] > 0
+
+
 @pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
 def test_planner_invariants_on_every_workload(lib, name):
     w = wl.WORKLOADS[name]
     info = kt_mlp.kt_mlp_plan_info(w.M, w.D, w.F, w.act, w.dtype, w.bias, SMS)
     _check_gemm(info["up"], w.M, w.F, w.D)
     _check_gemm(info["down"], w.M, w.D, w.F)
+    _check_one_launch(info)
     assert info["up"]["split_k"] == 1  # the activation is not linear: no split of the up projection
     if w.act == wl.ACT_GEGLU:
         assert info["up"]["BN"] <= 128  # value and gate columns: one MMA of N = 2 BN <= 256
@@ -162,9 +179,10 @@ def test_planner_invariants_with_pytorch_order_weights(lib, name, act):
     assert info["weight_layout"] == kt_mlp.KT_W_OUT_IN
 
 
-def test_pytorch_order_weights_need_no_column_padding_in_shared_memory(lib):
+def test_pytorch_order_weights_need_no_column_padding_in_shared_memory(lib, monkeypatch):
     # a K-major B tile holds exactly BN / pair rows; the N-major one pads the columns
-    # of each CTA's share to whole 64-column boxes
+    # of each CTA's share to whole 64-column boxes (the up projection's own ring: two launches)
+    monkeypatch.setenv("KT_FORCE_LAUNCHES", "2")
     for M, D, F, act in [(729, 1152, 4304, 1), (2048, 1280, 5120, 2), (8192, 640, 2560, 2)]:
         for layout in (0, 1):
             g = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, 0, False, weight_layout=layout), SMS)["up"]

@@ -34,11 +34,11 @@ def _lib():
     kt_mlp.load()
 
 
-def _run_block(w, d, residual, layernorm, layout, plan=None, Y=None):
+def _run_block(w, d, residual, layernorm, layout, plan=None, Y=None, launches=kt_mlp.KT_LAUNCH_AUTO):
     own = plan is None
     if own:
         plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias, residual=residual, layernorm=layernorm,
-                           weight_layout=layout, ln_eps=EPS)
+                           weight_layout=layout, ln_eps=EPS, launches=launches)
     if Y is None:
         Y = torch.full((w.M, w.D), float("nan"), dtype=TDT[w.dtype], device="cuda")
     H = torch.full((w.M, w.F), float("nan"), dtype=TDT[w.dtype], device="cuda")
@@ -219,3 +219,34 @@ def test_timed_block_reports_three_kernels():
     assert plan.status() == kt_mlp.KT_OK
     plan.close()
     assert all(0 < m < 5.0 for m in ms), ms
+
+
+# Both projections in one persistent launch (tiles from one work queue) against two launches,
+# each element by element against the oracle: CTA pairs and single CTAs, GEGLU and elementwise
+# activations, both weight orders, LayerNorm and residual.
+ONE_LAUNCH_CASES = [
+    ("geglu_pair", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128"),
+    ("erf_outin_ln_res", (700, 320, 1000, wl.ACT_GELU_ERF, wl.DT_F16, False), 1, 1, 1, None),
+    ("tanh_single_cta", (300, 256, 1000, wl.ACT_GELU_TANH, wl.DT_F16, True), 1, 0, 0, "128,1,64"),
+    ("silu_many_tiles", (1500, 136, 776, wl.ACT_SILU, wl.DT_BF16, True), 0, 0, 0, None),
+    ("tiny", (33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), 0, 0, 0, None),
+]
+
+
+@pytest.mark.parametrize("cid,shape,residual,layernorm,layout,fu", ONE_LAUNCH_CASES,
+                         ids=[c[0] for c in ONE_LAUNCH_CASES])
+@pytest.mark.parametrize("launches", [kt_mlp.KT_LAUNCH_ONE, kt_mlp.KT_LAUNCH_TWO])
+def test_one_launch_and_two_launches_match_the_oracle(monkeypatch, cid, shape, residual, layernorm, layout, fu,
+                                                      launches):
+    if fu:
+        monkeypatch.setenv("KT_FORCE_UP", fu)
+    M, D, F, act, dt, bias = shape
+    w = wl.custom(M, D, F, act, dt, bias, seed=5000 + M + D + F + act)
+    info = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, dt, bias, residual, layernorm, layout,
+                                                     launches=launches), 152)
+    assert info["one_launch"] == (launches == kt_mlp.KT_LAUNCH_ONE)
+    t, d = _inputs(w, residual, layernorm, layout)
+    Y, H = _run_block(w, d, residual, layernorm, layout, launches=launches)
+    Ho, Yx, bound = _oracle(w, t, layout)
+    parity.check_y(wl.bits(Y), Yx, w.dtype)
+    parity.check_h(wl.bits(H), Ho, bound, w.dtype)

@@ -39,7 +39,10 @@ CASES = [
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_noalloc_down_projection_matches_the_regular_entry_point(w):
+def test_noalloc_down_projection_matches_the_regular_entry_point(monkeypatch, w):
+    # the regular path as two launches, whose down projection the allocation-free entry
+    # point runs (with the split-K reduction through global memory)
+    monkeypatch.setenv("KT_FORCE_LAUNCHES", "2")
     t = wl.generate(w)
     d = {k: v.cuda() for k, v in t.items()}
     tdt = wl.TORCH_DTYPES[w.dtype]

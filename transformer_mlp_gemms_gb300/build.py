@@ -21,8 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkt_mlp.so")
 
-SOURCES = ["kt_gemm_act.cu", "kt_gemm_geglu.cu", "kt_gemm_down.cu", "kt_fused.cu", "kt_mlp_kernels.cu",
-           "kt_mlp_abi.cpp", "kt_planner.cpp"]
+SOURCES = ["kt_gemm_act.cu", "kt_gemm_geglu.cu", "kt_gemm_down.cu", "kt_mlp_two_act_f16.cu", "kt_mlp_two_act_bf16.cu",
+           "kt_mlp_two_geglu.cu", "kt_fused.cu", "kt_mlp_kernels.cu", "kt_mlp_abi.cpp", "kt_planner.cpp"]
 HEADERS = [os.path.join(CSRC, "kt_internal.h"), os.path.join(CSRC, "kt_gemm.cuh"), os.path.join(INCLUDE, "kt_mlp.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

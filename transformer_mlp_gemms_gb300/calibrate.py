@@ -36,6 +36,13 @@ ENV = ("KT_FORCE_UP", "KT_FORCE_DOWN")
 def _clear_env():
     for k in ENV:
         os.environ.pop(k, None)
+    # each GEMM is measured and modelled on its own: two launches, never the one-launch schedule
+    os.environ["KT_FORCE_LAUNCHES"] = "2"
+
+
+def _restore_env():
+    for k in ENV + ("KT_FORCE_LAUNCHES",):
+        os.environ.pop(k, None)
 
 
 def _configs():
@@ -87,7 +94,7 @@ def sweep(name: str, out_dir: str, calls: int = 40, warm: int = 5) -> list:
              "model_us": g["est_us"], "us_mean": statistics.mean(ms), "us_median": statistics.median(ms)}
         rows.append(r)
         print(json.dumps(r), flush=True)
-    _clear_env()
+    _restore_env()
     with open(os.path.join(out_dir, f"calib_{name}.json"), "w") as f:
         json.dump(rows, f)
     return rows
@@ -150,6 +157,7 @@ def evaluate(names, in_dir: str, num_sms: int = 152) -> float:
             tag = f"{pick['BM']}x{pick['BN']}x{pick['BK']} SK {pick['split_k']}" + (" cluster" if pick["cluster_sk"] else "")
             print(f"| {name} | {gemm} | {len(keep)} | {_spearman(mod, meas):.2f} | {tag} | {pm:.2f} | {best:.2f} | "
                   f"{regret:.2f} |")
+    _restore_env()
     print(f"\ntotal regret {total:.2f} µs")
     return total
 

@@ -54,6 +54,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "kt_internal.h"
 
@@ -666,10 +667,12 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
 // columns; the even CTA (the leader) issues the MMAs, which write each CTA's 128
 // rows of the accumulator into that CTA's tensor memory; each CTA's epilogue stores
 // its own rows.
-template <int EPI, int DT, int PAIR>
+template <int EPI, int DT, int PAIR, bool TWO>
 __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ GemmParams p2) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles want 1024-byte alignment
@@ -694,6 +697,11 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
+    // TWO (both projections in one launch): the work-item ring, kItemRing deep: item
+    // indices and their full / empty barriers (in the barrier area, past the slots)
+    const uint32_t item_idx = staging + kStaging + 256u;
+    const uint32_t item_full = item_idx + 16u;
+    const uint32_t item_empty = item_full + 8u * kItemRing;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -716,6 +724,14 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         mbar_init(bar_stall, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_pready, (uint32_t)(p.split_k * NEPI));
+        if constexpr (TWO) {
+            // consumers of an item: the MMA issuer and the epilogue warps of the leader CTA,
+            // and the producer and the epilogue warps of its peer
+            for (int i = 0; i < kItemRing; ++i) {
+                mbar_init(item_full + 8u * i, 1);
+                mbar_init(item_empty + 8u * i, PAIR == 2 ? 2 + 2 * NEPI : 1 + NEPI);
+            }
+        }
         *abort_flag = 0;
         *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -725,6 +741,11 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
+        if constexpr (TWO) {
+            prefetch_tmap(&tmA2);
+            prefetch_tmap(&tmB2);
+            prefetch_tmap(&tmC2);
+        }
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
@@ -747,6 +768,46 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
 
     const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
 
+    // Work items.  One projection: tiles unit0, unit0 + unit_step, ... (static).  TWO: items
+    // 0 .. p.num_tiles - 1 are up-projection tiles, the next p2.num_tiles down-projection
+    // tiles (whole tiles), handed out dynamically: the leader CTA's producer takes the next
+    // index from a global counter and publishes it in the item ring of both CTAs of the
+    // pair; every role consumes the same sequence.  All up tiles are taken before any down
+    // tile, and up tiles wait on nothing, so a down tile waiting for its rows of H always
+    // waits on work in progress.
+    const int total = p.num_tiles + (TWO ? p2.num_tiles : 0);
+    // While up tiles remain for every unit, the leader's producer takes each index one item
+    // ahead (the counter's round trip then overlaps the previous item's loads); down tiles
+    // are taken on demand, so that none waits on a unit still busy with an earlier tile.
+    int next_idx = -1;
+    auto publish = [&](uint32_t k) -> int {  // leader CTA's producer
+        const uint32_t slot = k % kItemRing, par = (k / kItemRing) & 1u;
+        if (!wait_phase(item_empty + 8u * slot, par ^ 1u, abort_flag, p.error, DEV_TIMEOUT_PRODUCER,
+                        p.wait_limit_ns))
+            return INT_MAX;
+        const int idx = next_idx >= 0 ? next_idx : atomicAdd(p.sched, 1);
+        next_idx = idx + 2 * (int)(gridDim.x / PAIR) < p.num_tiles ? atomicAdd(p.sched, 1) : -1;
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(item_idx + 4u * slot), "r"(idx) : "memory");
+        if constexpr (PAIR == 2) {
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa_rank(item_idx + 4u * slot, 1)), "r"(idx)
+                         : "memory");
+            mbar_arrive_cluster(mapa_rank(item_full + 8u * slot, 1));
+        }
+        mbar_arrive(item_full + 8u * slot);
+        return idx;
+    };
+    auto consume = [&](uint32_t k) -> int {  // one thread per consuming warp
+        const uint32_t slot = k % kItemRing, par = (k / kItemRing) & 1u;
+        if (!wait_phase<PAIR == 2>(item_full + 8u * slot, par, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
+                                   p.wait_limit_ns))
+            return INT_MAX;
+        int idx;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(idx) : "r"(item_idx + 4u * slot) : "memory");
+        if constexpr (PAIR == 2) mbar_arrive_cluster(mapa_rank(item_empty + 8u * slot, 0));
+        else mbar_arrive(item_empty + 8u * slot);
+        return idx;
+    };
+
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
@@ -756,8 +817,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 // failure injection: a barrier nobody arrives on, bounded wait
                 wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
             }
-            int local = 0;
-            for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step, ++local) {
+            // one work item of one projection (p: its parameters, tmA / tmB: its operands)
+            auto produce = [&](const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, const int n_b,
+                               const bool ready_mode, const int t, const int local) -> bool {
                 const TileCoord c = decode_tile(t, p);
                 const int kb0 = c.kb0, kb1 = c.kb1;
                 // this CTA's rows of A and its share of the B columns
@@ -798,8 +860,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                             atomicExch(p.ready_readers + rb, 0u);
                         }
                     }
-                    if (!got) break;
+                    if (!got) return false;
                     asm volatile("fence.proxy.async.global;" ::: "memory");  // H was written by TMA stores
+                    if (TWO && tr && local >= 0 && tr[(size_t)blockIdx.x * kTraceSlots + TR_T_DN_READY] == 0)
+                        trace_mark(tr, TR_T_DN_READY);
                 }
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -836,7 +900,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                 tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
                         for (int j = 0; j < nbox; ++j)
                             tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
-                        if (EPI == EPI_GEGLU) {
+                        if (n_b == 2) {
                             for (int j = 0; j < nbox; ++j)
                                 tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
                         }
@@ -847,7 +911,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                 tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
                         for (int j = 0; j < nbox; ++j)
                             tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
-                        if (EPI == EPI_GEGLU) {
+                        if (n_b == 2) {
                             for (int j = 0; j < nbox; ++j)
                                 tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
                         }
@@ -859,7 +923,35 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
+                return ok;
+            };
+            if constexpr (TWO) {
+                bool done = false;  // this unit took the end-of-work index
+                for (uint32_t k = 0; !*abort_flag; ++k) {
+                    const int idx = leader ? publish(k) : consume(k);
+                    if (idx >= total) {
+                        done = idx != INT_MAX;
+                        break;
+                    }
+                    if (tr && idx == p.num_tiles + (int)blockIdx.x / PAIR) trace_mark(tr, TR_T_DN_TAKEN);
+                    const bool ok = idx >= p.num_tiles
+                                        ? produce(p2, tmA2, tmB2, 1, p2.ready != nullptr, idx - p.num_tiles, (int)k)
+                                        : produce(p, tmA, tmB, n_b, false, idx, (int)k);
+                    if (!ok) break;
+                }
+                if (done && leader) {
+                    // the last unit to finish resets the counter for the next run
+                    __threadfence();
+                    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x / PAIR - 1) {
+                        __threadfence();
+                        atomicExch(p.sched, 0);
+                        atomicExch(p.sched + 1, 0);
+                    }
+                }
+            } else {
+                int local = 0;
+                for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step, ++local)
+                    if (!produce(p, tmA, tmB, n_b, ready_mode, t, local)) break;
             }
             if (*abort_flag && leader) {
                 // do not leave copies in flight into shared memory we are about to release
@@ -872,15 +964,15 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         // ------------------------------ MMA issuer ----------------------------
         if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0;
-            int local = 0;
             bool issued_any = false;
-            for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
+            // one work item of one projection (p: its parameters)
+            auto mma_item = [&](const GemmParams& p, const int n_b, const int t, const int local) -> bool {
                 const TileCoord c = decode_tile(t, p);
                 const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
                 const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
                 if (!wait_phase(bar_acce + 8u * buf, (use & 1u) ^ 1u, abort_flag, p.error, DEV_TIMEOUT_MMA,
                                 p.wait_limit_ns))
-                    break;
+                    return false;
                 tc_fence_after();
                 if (tr && local == 1) trace_mark(tr, TR_S_MMA0);
                 const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
@@ -922,7 +1014,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
+                if (!ok) return false;
                 // accumulator ready for the epilogue (of both CTAs of a pair)
                 if constexpr (PAIR == 2) mma_commit_pair(bar_accf + 8u * buf);
                 else mma_commit(bar_accf + 8u * buf);
@@ -932,6 +1024,30 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     trace_mark(tr, TR_LAST_MAIN);
                     tr[(size_t)blockIdx.x * kTraceSlots + TR_TILES] = (unsigned long long)(local + 1);
                 }
+                return true;
+            };
+            if constexpr (TWO) {
+                unsigned long long n_up = 0, n_dn = 0;
+                for (uint32_t k = 0;; ++k) {
+                    const int idx = consume(k);
+                    if (idx >= total) break;
+                    const bool dn = idx >= p.num_tiles;
+                    const bool ok = dn ? mma_item(p2, 1, idx - p.num_tiles, (int)k) : mma_item(p, n_b, idx, (int)k);
+                    if (!ok) break;
+                    if (tr) {
+                        if (dn) ++n_dn;
+                        else {
+                            ++n_up;
+                            trace_mark(tr, TR_T_LAST_UP);
+                        }
+                        tr[(size_t)blockIdx.x * kTraceSlots + TR_T_UP_ITEMS] = n_up;
+                        tr[(size_t)blockIdx.x * kTraceSlots + TR_T_DN_ITEMS] = n_dn;
+                    }
+                }
+            } else {
+                int local = 0;
+                for (int t = unit0; t < p.num_tiles; t += unit_step, ++local)
+                    if (!mma_item(p, n_b, t, local)) break;
             }
             if (*abort_flag && issued_any) {
                 if constexpr (PAIR == 2) mma_commit_pair(bar_drain);
@@ -945,13 +1061,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         const int q = warp & 3;    // TMEM lane quadrant this warp may access
         const int half = ew >> 2;  // which of the NPART interleaved 32-column groups
         const int row = q * 32 + lane;
-        const int ngroups = p.BN / 32;
         const uint32_t stg0 = staging + (uint32_t)ew * 2048u;
         const uint32_t stg_alt = (uint32_t)NEPI * 2048u;  // offset of the second buffer set
         const bool dbl = p.dbl_staging != 0;
         uint32_t nstores = 0;  // this warp's stores so far: picks the buffer
-        const int tiles_mn = p.tiles_m * p.tiles_n;
-        const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
         // Up projection: this CTA's rows of a stored tile are counted for the down
         // projection's producer once every epilogue warp's TMA stores of the tile have
         // completed.  The count of tile i is raised after tile i + 1's accumulator wait
@@ -970,8 +1083,16 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 atomicAdd(p.ready + tm, 1u);
             }
         };
-        int local = 0;
-        for (int t = unit0; t < p.num_tiles; t += unit_step, ++local) {
+        // One work item of one projection: `kind` carries its epilogue (the up projection's
+        // activation or EPI_DOWN), p its parameters, tmC its output store map.  Returns false
+        // when the kernel aborts (uniformly across the epilogue warps).
+        auto epi_item = [&](auto kind, const GemmParams& p, const CUtensorMap& tmC, const int t,
+                            const int local) -> bool {
+            constexpr int EPI = decltype(kind)::value;
+            const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
+            const int ngroups = p.BN / 32;
+            const int tiles_mn = p.tiles_m * p.tiles_n;
+            const size_t tile_elems = (size_t)kBM * (size_t)p.BN;
             const TileCoord c = decode_tile(t, p);
             const uint32_t buf = p.acc_bufs == 2 ? (uint32_t)(local & 1) : 0u;
             const uint32_t use = p.acc_bufs == 2 ? (uint32_t)(local >> 1) : (uint32_t)local;
@@ -1005,7 +1126,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
             }
             const bool got = wait_phase(bar_accf + 8u * buf, use & 1u, abort_flag, p.error,
                                         DEV_TIMEOUT_EPILOGUE, p.wait_limit_ns);
-            if (!epi_all<NEPI>(got)) break;
+            if (!epi_all<NEPI>(got)) return false;
             tc_fence_after();
             const bool tr1 = tr && local == 1 && warp == 2 && lane == 0;  // steady-state marks
             if (tr1) trace_mark(tr, TR_S_ACC);
@@ -1115,7 +1236,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 }
                 if (tr1) trace_mark(tr, TR_S_ARR);
                 if (EPI != EPI_DOWN && p.ready != nullptr) pending_rows = c.tm;  // counted later
-            } else if constexpr (EPI == EPI_DOWN) {
+            } else if constexpr (EPI == EPI_DOWN && !TWO) {
               if (p.cluster_sk) {
                 // split-K inside a cluster, reduce-scattered through L2: each 32 x 32 unit of
                 // the tile (row block q, column group g, u = q * ngroups + g) is owned by CTA
@@ -1308,8 +1429,31 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 if (local == 0) trace_mark(tr, TR_EPI_DONE);
                 trace_mark(tr, TR_LAST_EPI);
             }
+            return true;
+        };
+        if constexpr (TWO) {
+            for (uint32_t k = 0;; ++k) {
+                int idx = 0;
+                if (lane == 0) idx = consume(k);
+                idx = __shfl_sync(0xffffffffu, idx, 0);
+                // every epilogue warp took the same item, unless the kernel is aborting
+                if (!epi_all<NEPI>(idx < total)) break;
+                const bool dn = idx >= p.num_tiles;
+                if (dn && pending_rows >= 0) {  // before a down tile waits: its rows may be these
+                    signal_ready(pending_rows);
+                    pending_rows = -1;
+                }
+                const bool ok = dn ? epi_item(std::integral_constant<int, EPI_DOWN>{}, p2, tmC2, idx - p.num_tiles,
+                                              (int)k)
+                                   : epi_item(std::integral_constant<int, EPI>{}, p, tmC, idx, (int)k);
+                if (!ok) break;
+            }
+        } else {
+            int local = 0;
+            for (int t = unit0; t < p.num_tiles; t += unit_step, ++local)
+                if (!epi_item(std::integral_constant<int, EPI>{}, p, tmC, t, local)) break;
         }
-        if (EPI != EPI_DOWN && pending_rows >= 0) signal_ready(pending_rows);  // the last tile's rows
+        if (EPI != EPI_DOWN && pending_rows >= 0) signal_ready(pending_rows);  // the last up tile's rows
         // every TMA store of this warp has completed before the CTA may exit
         if (lane == 0) bulk_wait0();
         __syncwarp();
@@ -1332,11 +1476,13 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
 }
 
 // Launch one instantiation (cluster and programmatic-dependent-launch attributes as
-// the parameters ask).
-template <int EPI, int DT, int PAIR>
+// the parameters ask).  TWO: both projections in one launch (tmA2 / tmB2 / tmC2 / p2: the
+// down projection); otherwise the second set repeats the first and is not read.
+template <int EPI, int DT, int PAIR, bool TWO>
 kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmParams& p,
+                     const CUtensorMap* tmA2, const CUtensorMap* tmB2, const CUtensorMap* tmC2, const GemmParams& p2,
                      int grid, int smem, void* stream, bool pdl, const char** why) {
-    auto kern = kt_gemm_kernel<EPI, DT, PAIR>;
+    auto kern = kt_gemm_kernel<EPI, DT, PAIR, TWO>;
     // opt in to the shared memory this launch needs (idempotent, cheap after the first call)
     static std::atomic<int> max_set[16];
     int dev = 0;
@@ -1370,12 +1516,18 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
     }
     cfg.attrs = na ? attr : nullptr;
     cfg.numAttrs = na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p, *tmA2, *tmB2, *tmC2, p2);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return KT_ERR_CUDA;
     }
     return KT_OK;
+}
+
+template <int EPI, int DT, int PAIR>
+kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmParams& p,
+                     int grid, int smem, void* stream, bool pdl, const char** why) {
+    return launch_one<EPI, DT, PAIR, false>(tmA, tmB, tmC, p, tmA, tmB, tmC, p, grid, smem, stream, pdl, why);
 }
 
 // Launch dispatch per group of epilogues (one translation unit each, compiled in parallel).
@@ -1385,5 +1537,13 @@ kt_status launch_gemm_geglu(int dtype, const CUtensorMap* a, const CUtensorMap* 
                             const GemmParams& p, int grid, int smem, void* stream, bool pdl, const char** why);
 kt_status launch_gemm_down(int dtype, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                            const GemmParams& p, int grid, int smem, void* stream, bool pdl, const char** why);
+// Both projections in one launch (the up projection's epilogue `epi`; CTA pairs as up.pair);
+// maps: the up projection's A, B and output maps, then the down projection's.
+kt_status launch_mlp_two_act_f16(int epi, const CUtensorMap* const* maps, const GemmParams& up, const GemmParams& down,
+                                 int grid, int smem, void* stream, bool pdl, const char** why);
+kt_status launch_mlp_two_act_bf16(int epi, const CUtensorMap* const* maps, const GemmParams& up,
+                                  const GemmParams& down, int grid, int smem, void* stream, bool pdl, const char** why);
+kt_status launch_mlp_two_geglu(int dtype, const CUtensorMap* const* maps, const GemmParams& up, const GemmParams& down,
+                               int grid, int smem, void* stream, bool pdl, const char** why);
 
 }  // namespace kt

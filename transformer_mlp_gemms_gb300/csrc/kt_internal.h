@@ -35,6 +35,7 @@ constexpr int smem_reserve(int epi) {
     return epi_warps(epi) * 32 * kStoreCols * 2 + kBarrierBytes + kBiasSmemBytes + 1024;
 }
 constexpr int kMaxStages = 8;
+constexpr int kItemRing = 4;  // work items published ahead when both projections run in one launch
 
 // Epilogue kinds (one kernel instantiation each, times two dtypes).
 enum Epi : int {
@@ -69,6 +70,8 @@ struct GemmConfig {
     int dbl_staging;       // 1: shared memory left over for a second set of output staging buffers
     double useful_over_padded;
     double est_us;
+    double t_tile_us;      // model: one tile's main loop on one CTA (pair), and its epilogue
+    double t_epi_us;
 };
 
 // The H-on-chip variant (kt_fused.cu): both projections in one kernel, H in shared
@@ -88,6 +91,13 @@ struct PlanChoice {
     GemmConfig up, down;
     int h_on_chip;         // 1: run the fused kernel (`fused`) instead of up + down
     FusedConfig fused;
+    // 1: both projections in one persistent launch (kt_gemm_kernel<..., TWO = true>): up and
+    // down tiles from one dynamic work queue, down tiles as soon as their rows of H are
+    // stored; one shared-memory ring of `one_stages` stages of `one_slot` bytes
+    int one_launch;
+    int one_grid, one_stages, one_slot, one_smem, one_dbl;
+    double one_est_us;
+    GemmConfig one_up, one_down;  // the two GEMMs' configurations in that launch
 };
 
 // Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
@@ -109,7 +119,7 @@ inline int stage_bytes(int BN, int n_b, int pair, int bk, int b_kmajor = 0) {
 // KT_ERR_UNSUPPORTED where it does not apply).
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
                       const char** why, bool allow_cluster_sk = true, int w_layout = KT_W_IN_OUT,
-                      int h_path = KT_H_MEMORY);
+                      int h_path = KT_H_MEMORY, bool allow_one_launch = true, int launches = KT_LAUNCH_AUTO);
 
 // The up projection's epilogue kind for a kt_act.
 int up_epilogue(int act);
@@ -150,6 +160,8 @@ struct GemmParams {
     unsigned ready_target;   // down: counter value meaning "every tile of this row block stored"
     int ready_rows;          // down: rows per up-projection row block (128 x its CTA pairing)
     unsigned long long* trace;  // optional per-CTA timeline (kTraceSlots u64 per CTA) or null
+    int* sched;              // both projections in one launch: [0] next work item, [1] units done
+                             // (zero between runs; the last unit to finish resets both)
 };
 
 // Per-CTA trace slots (globaltimer ns unless noted), written when GemmParams::trace is set.
@@ -181,6 +193,12 @@ enum TraceSlot : int {
     TR_S_MMA0 = 23,      // MMA issuer: the tile's accumulator free, main loop starts
     TR_S_MMA1 = 24,      // MMA issuer: the tile's last k-block committed
     TR_S_LD0 = 25,       // producer: the tile's first copy issued
+    // both projections in one launch
+    TR_T_DN_TAKEN = 26,  // producer: first down-projection tile taken
+    TR_T_DN_READY = 27,  // producer: its rows of H stored (readiness wait done)
+    TR_T_UP_ITEMS = 28,  // MMA issuer: up-projection tiles processed (a count)
+    TR_T_DN_ITEMS = 29,  // MMA issuer: down-projection tiles processed (a count)
+    TR_T_LAST_UP = 30,   // MMA issuer: last up-projection tile's main loop committed
     kTraceSlots = 32
 };
 
@@ -225,6 +243,11 @@ kt_status launch_timestamp(void* dst, void* stream, const char** why);
 // CUtensorMaps: the A operand, the B operand and the output (H or Y) store map.
 kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const void* tmC, const GemmParams& p,
                       int grid, int smem_bytes, void* stream, bool pdl, const char** why);
+
+// Both projections in one launch: maps[0..2] the up projection's A, B and H store maps,
+// maps[3..5] the down projection's; up.stages / stage_bytes / dbl_staging equal down's.
+kt_status launch_mlp_two(int epi, int dtype, const void* const* maps, const GemmParams& up, const GemmParams& down,
+                         int grid, int smem_bytes, void* stream, bool pdl, const char** why);
 
 // Encode a 2-D tiled tensor map over a row-major [rows][cols] 16-bit matrix with a
 // box of box_cols x box_rows and a 128- or 64-byte swizzle.  Returns false on failure.

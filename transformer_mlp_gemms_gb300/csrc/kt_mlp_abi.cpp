@@ -70,6 +70,8 @@ kt_status validate_options(const kt_mlp_options* o) {
         return fail(KT_ERR_INVALID, "unknown weight layout");
     if (o->layernorm && !(o->ln_eps > 0.0f && o->ln_eps < 3.0e38f))
         return fail(KT_ERR_INVALID, "ln_eps must be positive and finite");
+    if (o->launches != KT_LAUNCH_AUTO && o->launches != KT_LAUNCH_ONE && o->launches != KT_LAUNCH_TWO)
+        return fail(KT_ERR_INVALID, "launches must be KT_LAUNCH_AUTO, KT_LAUNCH_ONE or KT_LAUNCH_TWO");
     if (o->h_path != KT_H_AUTO && o->h_path != KT_H_MEMORY && o->h_path != KT_H_ON_CHIP)
         return fail(KT_ERR_INVALID, "unknown H path");
     return KT_OK;
@@ -101,6 +103,7 @@ struct kt_mlp_plan_s {
     unsigned* ready = nullptr;  // per up-projection row block: CTA tiles of H stored (inside flags)
     unsigned* readers = nullptr;  // per row block: the down projection's waits done this run (inside flags)
     unsigned* ready_expect = nullptr;  // per row block: the down projection's waits per run (own allocation)
+    int* sched = nullptr;       // one-launch plans: the work-item counters (inside flags)
     size_t flag_bytes = 0;
     void* xn = nullptr;         // [M][D] LayerNorm output (layernorm plans)
     void* x_stage = nullptr;    // [M][D] for kt_mlp_run_host
@@ -276,9 +279,6 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     up.pdl_wait = 1;
     up.trace = P->trace_up;
     up.ready = P->ready;
-    s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
-                        P->choice.up.smem_bytes, stream, !timed, &why);
-    if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
 
     kt::GemmParams dn = make_params(P, P->choice.down, kt::EPI_DOWN);
     dn.bias = P->bias ? t.b_down : nullptr;
@@ -292,6 +292,25 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.ready_expect = P->ready_expect;
     dn.ready_target = per_block;
     dn.ready_rows = kt::kBM * P->choice.up.pair;
+    if (P->choice.one_launch) {
+        // both projections in one launch: one shared-memory ring, tiles from one queue
+        up.stage_bytes = dn.stage_bytes = (uint32_t)P->choice.one_slot;
+        up.sched = dn.sched = P->sched;
+        up.pdl_wait = dn.pdl_wait = 1;
+        const void* maps[6] = {&P->tm_x, &P->tm_wu, &P->tm_hs, &P->tm_h, &P->tm_wd, &P->tm_ys};
+        s = kt::launch_mlp_two(epi_up, P->dtype, maps, up, dn, P->choice.one_grid, P->choice.one_smem, stream, !timed,
+                               &why);
+        if (s != KT_OK) return fail(s, std::string("one-launch MLP: ") + why);
+        if (timed) {
+            cudaEventRecord(P->ev[2], st);
+            cudaEventRecord(P->ev[3], st);
+        }
+        P->last_stream = stream;
+        return ok();
+    }
+    s = kt::launch_gemm(epi_up, P->dtype, &P->tm_x, &P->tm_wu, &P->tm_hs, up, P->choice.up.grid,
+                        P->choice.up.smem_bytes, stream, !timed, &why);
+    if (s != KT_OK) return fail(s, std::string("up projection launch: ") + why);
     if (timed) cudaEventRecord(P->ev[2], st);
     s = kt::launch_gemm(kt::EPI_DOWN, P->dtype, &P->tm_h, &P->tm_wd, &P->tm_ys, dn, P->choice.down.grid,
                         P->choice.down.smem_bytes, stream, !timed, &why);
@@ -352,7 +371,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     P->device = dev;
     P->num_sms = prop.multiProcessorCount;
     const char* why = "";
-    kt_status s = kt::plan_choose(M, D, F, o.act, P->num_sms, &P->choice, &why, true, o.weight_layout, o.h_path);
+    kt_status s = kt::plan_choose(M, D, F, o.act, P->num_sms, &P->choice, &why, true, o.weight_layout, o.h_path,
+                                  true, o.launches);
     if (s != KT_OK) {
         delete P;
         return fail(s, why);
@@ -362,7 +382,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     size_t h_bytes = (size_t)M * (size_t)F * 2;
     size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
     size_t n_ready = (size_t)up.tiles_m;                               // one per up row block
-    size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready);
+    size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready + 2);
     size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
                             : 0;
@@ -384,6 +404,7 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     }
     P->ready = reinterpret_cast<unsigned*>(P->flags + 1 + n_counters);
     P->readers = P->ready + n_ready;
+    P->sched = P->flags + 1 + n_counters + 2 * n_ready;
     P->flag_bytes = flag_bytes;
     {
         // how many times this plan's down projection waits on each up row block per run:
@@ -411,10 +432,21 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     return ok();
 }
 
+void fill_one_launch(const kt::PlanChoice& c, kt_plan_info* out) {
+    out->one_launch = c.one_launch;
+    if (c.one_launch) {
+        out->one_launch_grid = c.one_grid;
+        out->one_launch_stages = c.one_stages;
+        out->one_launch_smem_bytes = c.one_smem;
+        out->one_launch_est_us = c.one_est_us;
+    }
+}
+
 kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     kt::PlanChoice c;
     const char* why = "";
-    kt_status s = kt::plan_choose(o.M, o.D, o.F, o.act, num_sms, &c, &why, true, o.weight_layout, o.h_path);
+    kt_status s = kt::plan_choose(o.M, o.D, o.F, o.act, num_sms, &c, &why, true, o.weight_layout, o.h_path, true,
+                                  o.launches);
     if (s != KT_OK) return fail(s, why);
     std::memset(out, 0, sizeof(*out));
     out->M = o.M; out->D = o.D; out->F = o.F;
@@ -429,11 +461,12 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
         out->fused_smem_bytes = c.fused.smem_bytes;
         out->fused_est_us = c.fused.est_us;
     }
+    fill_one_launch(c, out);
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     // H, error word and split-K counters, three words per up row block, host staging
     int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
-                 4 * 3 * (int64_t)c.up.tiles_m + 2 * 2 * o.M * o.D;
+                 4 * 3 * (int64_t)c.up.tiles_m + 8 + 2 * 2 * o.M * o.D;
     if (c.down.split_k > 1)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;
     if (o.layernorm) ws += 2 * o.M * o.D;
@@ -576,6 +609,7 @@ kt_status kt_mlp_get_info(kt_mlp_plan_t plan, kt_plan_info* out) {
         out->fused_smem_bytes = plan->choice.fused.smem_bytes;
         out->fused_est_us = plan->choice.fused.est_us;
     }
+    fill_one_launch(plan->choice, out);
     kt::plan_fill_info(plan->choice.up, &out->up);
     kt::plan_fill_info(plan->choice.down, &out->down);
     out->workspace_bytes = plan->workspace_bytes;
@@ -598,6 +632,12 @@ kt_status kt_mlp_describe(kt_mlp_plan_t plan, char* buf, size_t len) {
                   d.tiles_m, d.tiles_n, d.split_k, d.grid, d.waves, d.waves == 1 ? "" : "s", d.stages,
                   d.split_k == 1 ? "no reduction" : d.cluster_sk ? "cluster reduction" : "global reduction",
                   d.useful_over_padded, d.est_us, (long long)plan->workspace_bytes);
+    if (plan->choice.one_launch) {
+        const size_t used = std::strlen(buf);
+        std::snprintf(buf + used, len - used,
+                      " | RUNS both in one launch (grid %d, %d shared stages of %d B, model %.2f us)",
+                      plan->choice.one_grid, plan->choice.one_stages, plan->choice.one_slot, plan->choice.one_est_us);
+    }
     if (plan->choice.h_on_chip) {
         const kt::FusedConfig& f = plan->choice.fused;
         const size_t used = std::strlen(buf);

@@ -249,7 +249,8 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     // the tile plan of the MLP's down projection, with the split-K reduction through this
     // entry point's scratch (not through a cluster's shared memory)
     PlanChoice pc;
-    kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why, /*allow_cluster_sk=*/false);
+    kt_status st = plan_choose(M, D, F, KT_ACT_NONE, sms, &pc, why, /*allow_cluster_sk=*/false, KT_W_IN_OUT,
+                               KT_H_MEMORY, /*allow_one_launch=*/false);
     if (st != KT_OK) return st;
     const GemmConfig& g = pc.down;
     const size_t n_counters = (size_t)g.tiles_m * (size_t)g.tiles_n * (size_t)g.pair;
@@ -404,6 +405,30 @@ kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, cons
         case EPI_NONE: return launch_gemm_act(epi, dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
         case EPI_GEGLU: return launch_gemm_geglu(dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
         case EPI_DOWN: return launch_gemm_down(dtype, a, b, c, p, grid, smem_bytes, stream, pdl, why);
+    }
+    *why = "unknown epilogue kind";
+    return KT_ERR_INVALID;
+}
+
+kt_status launch_mlp_two(int epi, int dtype, const void* const* maps, const GemmParams& up, const GemmParams& down,
+                         int grid, int smem_bytes, void* stream, bool pdl, const char** why) {
+    const CUtensorMap* m[6];
+    for (int i = 0; i < 6; ++i) m[i] = reinterpret_cast<const CUtensorMap*>(maps[i]);
+    if (up.pair != down.pair || (up.pair == 2 && grid % 2 != 0) || down.split_k != 1 || up.split_k != 1 ||
+        up.cluster_sk || down.cluster_sk || up.stages != down.stages || up.stage_bytes != down.stage_bytes ||
+        up.dbl_staging != down.dbl_staging || up.sched == nullptr || grid / up.pair > up.num_tiles + down.num_tiles) {
+        *why = "inconsistent one-launch configuration";
+        return KT_ERR_INVALID;
+    }
+    switch (epi) {
+        case EPI_GEGLU: return launch_mlp_two_geglu(dtype, m, up, down, grid, smem_bytes, stream, pdl, why);
+        case EPI_GELU_ERF:
+        case EPI_GELU_TANH:
+        case EPI_GELU_SIGMOID:
+        case EPI_SILU:
+        case EPI_NONE:
+            return dtype == KT_F16 ? launch_mlp_two_act_f16(epi, m, up, down, grid, smem_bytes, stream, pdl, why)
+                                   : launch_mlp_two_act_bf16(epi, m, up, down, grid, smem_bytes, stream, pdl, why);
     }
     *why = "unknown epilogue kind";
     return KT_ERR_INVALID;

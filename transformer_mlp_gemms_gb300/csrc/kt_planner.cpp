@@ -101,11 +101,15 @@ int max_stages(int BN, int n_b, int pair, int bk, int kmaj, int epi) {
 }
 
 bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi, int num_sms, int pair,
-              int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0) {
+              int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0, int force_stages = 0) {
     // GEGLU: value and gate columns form one MMA operand of N = 2 BN (at most 256, one
     // accumulator buffer of tensor memory); an N-major share must be whole 64-column boxes
     if (n_b == 2 && (n_b * BN > kAccSlot || (!kmaj && (BN / pair) % 64 != 0))) return false;
     int stages = max_stages(BN, n_b, pair, bk, kmaj, epi);
+    if (force_stages > 0) {  // a ring shared with another GEMM (one launch for both projections)
+        if (force_stages > stages) return false;
+        stages = force_stages;
+    }
     if (stages < 2) return false;
     if (pair == 2 && num_sms < 2) return false;
     const int64_t bm = (int64_t)kBM * pair;  // rows per tile (a pair's tile spans two CTAs)
@@ -170,6 +174,8 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->useful_over_padded = (double)M * N * K /
                             ((double)(tm * bm) * (double)(tn * BN) * (double)(kb * bk));
     g->est_us = (t_cta + kKernelOverhead + (pair == 2 ? kPairKernelCost : 0.0)) * 1e6;
+    g->t_tile_us = t_main * 1e6;
+    g->t_epi_us = t_epi * 1e6;
     return true;
 }
 
@@ -253,8 +259,66 @@ static bool plan_fused(int64_t M, int64_t D, int64_t F, int act, int num_sms, Fu
     return true;
 }
 
+// Both projections in one persistent launch, tiles from one dynamic queue (up tiles first):
+// the down projection's whole-tile candidates with the up projection's CTA pairing, the two
+// GEMMs sharing one shared-memory ring (its stage the larger of their k-blocks).  Modelled
+// time: the up tiles spread over the units, then the down tiles in whole rounds of one
+// tile per unit (a down tile is long: a round a few tiles short of the units' count still
+// costs a full tile), at least the total work spread over the units, plus an epilogue and
+// the launch.
+static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sms, int kmaj, PlanChoice* out,
+                            const GemmConfig* forced_down) {
+    out->one_launch = 0;
+    out->one_est_us = 0.0;
+    const GemmConfig& u0 = out->up;
+    const int pair = u0.pair;
+    const int epi_up = up_epilogue(act);
+    const int n_b = act == KT_ACT_GEGLU ? 2 : 1;
+    const int units = num_sms / pair;
+    bool found = false;
+    for (int BN = 32 * pair; BN <= 256; BN += 32 * pair) {
+        for (int bk = 64; bk <= 128; bk += 64) {
+            if (forced_down && (forced_down->BN != BN || forced_down->bk != bk || forced_down->pair != pair ||
+                                forced_down->split_k != 1))
+                continue;
+            GemmConfig d0;
+            if (!evaluate(M, D, F, BN, 1, 1, EPI_DOWN, num_sms, pair, bk, &d0, false, kmaj)) continue;
+            const int slot = std::max(stage_bytes(u0.BN, n_b, pair, u0.bk, kmaj), stage_bytes(BN, 1, pair, bk, kmaj));
+            const int stages = std::min((kSmemBudget - smem_reserve(epi_up)) / slot, kMaxStages);
+            GemmConfig u, d;
+            if (stages < 2 || !evaluate(M, F, D, u0.BN, 1, n_b, epi_up, num_sms, pair, u0.bk, &u, false, kmaj, stages) ||
+                !evaluate(M, D, F, BN, 1, 1, EPI_DOWN, num_sms, pair, bk, &d, false, kmaj, stages))
+                continue;
+            const double up_tiles = (double)u.tiles_m * u.tiles_n, dn_tiles = (double)d.tiles_m * d.tiles_n;
+            const int grid = (int)std::min<int64_t>((int64_t)units, (int64_t)(up_tiles + dn_tiles)) * pair;
+            const double n = grid / pair;
+            const double work = (up_tiles * u.t_tile_us + dn_tiles * d.t_tile_us) / n;
+            const double rounds = up_tiles * u.t_tile_us / n + std::ceil(dn_tiles / n) * d.t_tile_us;
+            const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us) + kKernelOverhead * 1e6 +
+                             (pair == 2 ? kPairKernelCost * 1e6 : 0.0);
+            if (!found || t < out->one_est_us) {
+                found = true;
+                out->one_est_us = t;
+                out->one_grid = grid;
+                out->one_stages = stages;
+                out->one_slot = slot;
+                const int smem = stages * slot + smem_reserve(epi_up);
+                out->one_dbl = smem + epi_warps(epi_up) * 2048 <= kSmemBudget ? 1 : 0;
+                out->one_smem = smem + (out->one_dbl ? epi_warps(epi_up) * 2048 : 0);
+                u.dbl_staging = d.dbl_staging = out->one_dbl;
+                u.stages = d.stages = stages;
+                u.smem_bytes = d.smem_bytes = out->one_smem;
+                out->one_up = u;
+                out->one_down = d;
+            }
+        }
+    }
+    if (found) out->one_launch = 1;
+}
+
 kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, PlanChoice* out,
-                      const char** why, bool allow_cluster_sk, int w_layout, int h_path) {
+                      const char** why, bool allow_cluster_sk, int w_layout, int h_path, bool allow_one_launch,
+                      int launches) {
     if (M < 1 || D < 1 || F < 1) { *why = "M, D and F must be positive"; return KT_ERR_INVALID; }
     if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) { *why = "unknown activation"; return KT_ERR_INVALID; }
     if (w_layout != KT_W_IN_OUT && w_layout != KT_W_OUT_IN) { *why = "unknown weight layout"; return KT_ERR_INVALID; }
@@ -322,6 +386,37 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         }
         if (fits && (h_path == KT_H_ON_CHIP || out->fused.est_us < out->up.est_us + out->down.est_us))
             out->h_on_chip = 1;
+    }
+    // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory; the
+    // planner's own choice (KT_LAUNCH_AUTO) is two launches: one launch measured slower
+    // than two on every benchmark shape but one (SigLIP's 729 tokens, 7 % faster), and the
+    // model does not tell that case apart.  Measurement override: KT_FORCE_LAUNCHES=1|2.
+    out->one_launch = 0;
+    if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
+        *why = "unknown launches option";
+        return KT_ERR_INVALID;
+    }
+    const char* fl = std::getenv("KT_FORCE_LAUNCHES");
+    if (fl) {
+        const int v = std::atoi(fl);
+        if (v != 1 && v != 2) {
+            *why = "KT_FORCE_LAUNCHES must be 1 or 2";
+            return KT_ERR_INVALID;
+        }
+        launches = v == 1 ? KT_LAUNCH_ONE : KT_LAUNCH_TWO;
+    }
+    const int force_launches = launches == KT_LAUNCH_ONE ? 1 : 2;
+    const bool forced_dn = std::getenv("KT_FORCE_DOWN") != nullptr;
+    if (allow_one_launch && !out->h_on_chip && force_launches == 1) {
+        plan_one_launch(M, D, F, act, num_sms, kmaj, out, forced_dn ? &out->down : nullptr);
+        if (out->one_launch) {  // the configurations that launch runs
+            out->up = out->one_up;
+            out->down = out->one_down;
+        }
+    }
+    if (allow_one_launch && force_launches == 1 && !out->one_launch) {
+        *why = "one launch: no configuration applies (H stays on chip, or no whole-tile down projection fits)";
+        return KT_ERR_UNSUPPORTED;
     }
     return KT_OK;
 }

@@ -20,6 +20,7 @@ KT_ACT_GELU_ERF, KT_ACT_GELU_TANH, KT_ACT_GEGLU, KT_ACT_NONE, KT_ACT_GELU_SIGMOI
 KT_F16, KT_BF16 = 0, 1
 KT_W_IN_OUT, KT_W_OUT_IN = 0, 1
 KT_H_AUTO, KT_H_MEMORY, KT_H_ON_CHIP = 0, 1, 2
+KT_LAUNCH_AUTO, KT_LAUNCH_ONE, KT_LAUNCH_TWO = 0, 1, 2
 KT_OK, KT_ERR_INVALID, KT_ERR_UNSUPPORTED, KT_ERR_CUDA, KT_ERR_TIMEOUT, KT_ERR_NOMEM = range(6)
 STATUS_NAMES = {0: "KT_OK", 1: "KT_ERR_INVALID", 2: "KT_ERR_UNSUPPORTED", 3: "KT_ERR_CUDA",
                 4: "KT_ERR_TIMEOUT", 5: "KT_ERR_NOMEM"}
@@ -50,7 +51,10 @@ class kt_plan_info(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64),
                 ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
                 ("ln_eps", ctypes.c_float), ("h_on_chip", ctypes.c_int32), ("fused_grid", ctypes.c_int32),
-                ("fused_stages", ctypes.c_int32), ("fused_smem_bytes", ctypes.c_int32), ("fused_est_us", ctypes.c_double)]
+                ("fused_stages", ctypes.c_int32), ("fused_smem_bytes", ctypes.c_int32), ("fused_est_us", ctypes.c_double),
+                ("one_launch", ctypes.c_int32), ("one_launch_grid", ctypes.c_int32),
+                ("one_launch_stages", ctypes.c_int32), ("one_launch_smem_bytes", ctypes.c_int32),
+                ("one_launch_est_us", ctypes.c_double)]
 
     def as_dict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_ if n not in ("up", "down")}
@@ -63,7 +67,7 @@ class kt_mlp_options(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("F", ctypes.c_int64),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("bias", ctypes.c_int32),
                 ("residual", ctypes.c_int32), ("layernorm", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
-                ("ln_eps", ctypes.c_float), ("h_path", ctypes.c_int32)]
+                ("ln_eps", ctypes.c_float), ("h_path", ctypes.c_int32), ("launches", ctypes.c_int32)]
 
 
 class kt_mlp_tensors(ctypes.Structure):
@@ -72,9 +76,9 @@ class kt_mlp_tensors(ctypes.Structure):
 
 
 def options(M, D, F, act, dtype, bias=False, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
-            ln_eps=1e-5, h_path=KT_H_MEMORY) -> kt_mlp_options:
+            ln_eps=1e-5, h_path=KT_H_MEMORY, launches=KT_LAUNCH_AUTO) -> kt_mlp_options:
     return kt_mlp_options(M, D, F, act, dtype, int(bias), int(residual), int(layernorm), weight_layout,
-                          ln_eps if layernorm else 0.0, h_path)
+                          ln_eps if layernorm else 0.0, h_path, launches)
 
 
 def tensors(X, W_up, W_down, Y, b_up=None, b_down=None, R=None, ln_gamma=None, ln_beta=None,
@@ -272,16 +276,16 @@ def kt_debug_timestamp(dst, stream=None) -> None:
 
 class Plan:
     """Owning handle: ``Plan(M, D, F, act, dtype, bias)`` (kt_mlp_plan), or with any of
-    ``residual``, ``layernorm``, ``weight_layout``, ``ln_eps`` (kt_mlp_plan_ex);
-    destroyed with the object."""
+    ``residual``, ``layernorm``, ``weight_layout``, ``ln_eps``, ``h_path``, ``launches``
+    (kt_mlp_plan_ex); destroyed with the object."""
 
     def __init__(self, M, D, F, act, dtype, bias, residual=False, layernorm=False, weight_layout=KT_W_IN_OUT,
-                 ln_eps=1e-5, h_path=KT_H_MEMORY):
+                 ln_eps=1e-5, h_path=KT_H_MEMORY, launches=KT_LAUNCH_AUTO):
         self.M, self.D, self.F, self.act, self.dtype, self.bias = M, D, F, act, dtype, bool(bias)
         self.residual, self.layernorm, self.weight_layout = bool(residual), bool(layernorm), weight_layout
-        if residual or layernorm or weight_layout != KT_W_IN_OUT or h_path != KT_H_MEMORY:
+        if residual or layernorm or weight_layout != KT_W_IN_OUT or h_path != KT_H_MEMORY or launches:
             self.handle = kt_mlp_plan_ex(options(M, D, F, act, dtype, bias, residual, layernorm, weight_layout,
-                                                 ln_eps, h_path))
+                                                 ln_eps, h_path, launches))
         else:
             self.handle = kt_mlp_plan(M, D, F, act, dtype, bias)
 
