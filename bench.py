@@ -108,7 +108,8 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("kt_gemm.cuh", "kt_gemm_act.cu", "kt_gemm_geglu.cu", "kt_gemm_down.cu", "kt_mlp_kernels.cu",
+KERNEL_SOURCES = ("kt_gemm.cuh", "kt_gemm_act.cu", "kt_gemm_geglu.cu", "kt_gemm_down.cu", "kt_mlp_two_act_f16.cu",
+                  "kt_mlp_two_act_bf16.cu", "kt_mlp_two_geglu.cu", "kt_mlp_kernels.cu",
                   "kt_internal.h")
 
 
