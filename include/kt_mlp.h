@@ -79,8 +79,9 @@ typedef enum { KT_H_AUTO = 0, KT_H_MEMORY = 1, KT_H_ON_CHIP = 2 } kt_h_path;
  * (programmatic dependent launch) and loading rows of H as they are stored.  KT_LAUNCH_ONE:
  * one persistent kernel that takes up tiles, then down tiles, from one work queue (a down
  * tile once its rows of H are stored); no split-K for the down projection.  KT_LAUNCH_AUTO
- * is the planner's choice: two launches, which measured as fast or faster on all but one
- * of the benchmark shapes. */
+ * is the planner's choice: one launch when the up projection is a single wave, the
+ * two-launch down projection would split K and the model prefers one launch (SigLIP's
+ * 729 tokens), two launches otherwise. */
 typedef enum { KT_LAUNCH_AUTO = 0, KT_LAUNCH_ONE = 1, KT_LAUNCH_TWO = 2 } kt_launches;
 
 /* Memory order of W_up and W_down. */

@@ -139,6 +139,16 @@ def _check_gemm(g, M, N, K):
     assert g["est_us"] > 0
 
 
+def test_launch_policy_on_the_benchmark_shapes(lib):
+    # the planner's own choice between one and two launches, as measured on GB300: one
+    # launch only for SigLIP's single-wave up projection with a split-K down projection
+    expect = {"siglip": 1, "sweep_M729": 1, "tiny": 0, "sweep_M256": 0, "sweep_M1000": 0, "sweep_M4096": 0,
+              "sweep_M16384": 0, "sdxl_l2": 0, "sdxl_l1": 0}
+    for name, one in expect.items():
+        w = wl.WORKLOADS[name]
+        assert kt_mlp.kt_mlp_plan_info(w.M, w.D, w.F, w.act, w.dtype, w.bias, SMS)["one_launch"] == one, name
+
+
 def _check_one_launch(info):
     # both projections in one persistent launch: whole down tiles, one CTA pairing, one
     # shared-memory ring, at most one unit per resident CTA (pair), never more units than tiles

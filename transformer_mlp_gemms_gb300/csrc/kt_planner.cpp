@@ -387,10 +387,15 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         if (fits && (h_path == KT_H_ON_CHIP || out->fused.est_us < out->up.est_us + out->down.est_us))
             out->h_on_chip = 1;
     }
-    // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory; the
-    // planner's own choice (KT_LAUNCH_AUTO) is two launches: one launch measured slower
-    // than two on every benchmark shape but one (SigLIP's 729 tokens, 7 % faster), and the
-    // model does not tell that case apart.  Measurement override: KT_FORCE_LAUNCHES=1|2.
+    // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory.  The
+    // planner's own choice (KT_LAUNCH_AUTO): one launch when the up projection is a single
+    // wave (all of H is stored at about the same time, so the second kernel's launch and
+    // set-up sit on the critical path), the two-launch down projection would split K (its
+    // exchange sits there too; the one-launch kernel takes whole down tiles instead), and the
+    // model prefers one launch; otherwise two.  This rule reproduces the measured winner on
+    // all eight benchmark shapes (one launch: SigLIP, 37.0 against 39.7 us; two launches: the
+    // tiny case, M = 256 and 1000, which split the down projection but lose more parallelism
+    // than they gain, and the multi-wave SDXL and sweep shapes).  Override: KT_FORCE_LAUNCHES=1|2.
     out->one_launch = 0;
     if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
         *why = "unknown launches option";
@@ -405,10 +410,13 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         }
         launches = v == 1 ? KT_LAUNCH_ONE : KT_LAUNCH_TWO;
     }
-    const int force_launches = launches == KT_LAUNCH_ONE ? 1 : 2;
     const bool forced_dn = std::getenv("KT_FORCE_DOWN") != nullptr;
-    if (allow_one_launch && !out->h_on_chip && force_launches == 1) {
+    const bool auto_one = launches == KT_LAUNCH_AUTO && out->up.waves == 1 && out->down.split_k > 1 && !forced_dn;
+    const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
+    if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
+        const double t_two = out->up.est_us + out->down.est_us;
         plan_one_launch(M, D, F, act, num_sms, kmaj, out, forced_dn ? &out->down : nullptr);
+        if (force_launches == 0 && out->one_launch && out->one_est_us >= t_two) out->one_launch = 0;
         if (out->one_launch) {  // the configurations that launch runs
             out->up = out->one_up;
             out->down = out->one_down;
