@@ -258,8 +258,10 @@ kt_status kt_mlp_run_with_h(kt_mlp_plan_t plan, const void* X, const void* W_up,
  * kt_mlp_run_host -- end-to-end call with HOST activations: copies X_host[M][D] to
  * the device (plan-owned staging), runs the MLP, copies Y back into Y_host[M][D]
  * and synchronises `stream`.  Weights and biases stay device pointers (resident
- * model parameters).  Pinned host memory gives asynchronous copies; pageable memory
- * works but is slower.  Returns after Y_host is filled.
+ * model parameters).  Pinned host memory (mapped into the device's address space) is
+ * moved by two copy kernels chained to the MLP by programmatic dependent launch;
+ * any other host memory by cudaMemcpyAsync, which works but is slower.  Returns after
+ * Y_host is filled.
  */
 kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_up,
                           const void* W_down, const void* b_up, const void* b_down,

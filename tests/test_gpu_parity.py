@@ -137,18 +137,25 @@ def test_runs_are_bitwise_deterministic_and_h_is_not_needed():
     assert torch.equal(Y2.view(torch.int16), Y3.view(torch.int16))
 
 
-def test_host_buffer_entry_point_matches_device_path():
-    w = wl.WORKLOADS["sdxl_l2"]
+@pytest.mark.parametrize("name", ["sdxl_l2", "siglip", "tiny"])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned_copy_kernels", "pageable_memcpy"])
+def test_host_buffer_entry_point_matches_device_path(name, pinned):
+    # pinned host buffers move through the copy kernels, pageable ones through
+    # cudaMemcpyAsync; both calls twice in a row, bit-identical to the device path
+    w = wl.WORKLOADS[name]
     t = wl.generate(w)
     d = _to_dev(t)
     plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
     Yd, _ = _run(w, d, with_h=False, plan=plan)
-    Xh = t["X"].pin_memory()
-    Yh = torch.empty((w.M, w.D), dtype=TDT[w.dtype]).pin_memory()
-    plan.run_host(Xh, d["W_up"], d["W_down"], d["b_up"], d["b_down"], Yh)
-    assert plan.status() == kt_mlp.KT_OK
+    Xh = t["X"].pin_memory() if pinned else t["X"].clone()
+    for _ in range(2):
+        Yh = torch.full((w.M, w.D), float("nan"), dtype=TDT[w.dtype])
+        if pinned:
+            Yh = Yh.pin_memory()
+        plan.run_host(Xh, d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Yh)
+        assert plan.status() == kt_mlp.KT_OK
+        assert torch.equal(Yd.view(torch.int16), Yh.view(torch.int16))
     plan.close()
-    assert torch.equal(Yd.view(torch.int16), Yh.view(torch.int16))
 
 
 def test_overflow_rounds_to_infinity_like_the_oracle():

@@ -239,6 +239,11 @@ kt_status launch_activation(int act, const float* z, const float* g, float* out,
 // One-thread kernel writing %globaltimer to dst (kt_mlp_kernels.cu).
 kt_status launch_timestamp(void* dst, void* stream, const char** why);
 
+// Copy `bytes` (a multiple of 16, both pointers 16-byte aligned; device memory or mapped
+// pinned host memory) with `grid` CTAs, as a programmatic dependent of the previous kernel
+// on `stream` (kt_mlp_kernels.cu).
+kt_status launch_copy16(const void* src, void* dst, size_t bytes, int grid, void* stream, const char** why);
+
 // Host launch wrappers (kt_mlp_kernels.cu).  tmA / tmB / tmC point to 128-byte
 // CUtensorMaps: the A operand, the B operand and the output (H or Y) store map.
 kt_status launch_gemm(int epi, int dtype, const void* tmA, const void* tmB, const void* tmC, const GemmParams& p,

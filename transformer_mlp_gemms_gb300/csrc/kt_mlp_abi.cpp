@@ -556,13 +556,44 @@ kt_status kt_mlp_run_host(kt_mlp_plan_t plan, const void* X_host, const void* W_
         return fail(KT_ERR_INVALID, "kt_mlp_run_host takes plans without residual / layernorm");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     size_t bytes = (size_t)plan->M * (size_t)plan->D * 2;
-    cudaError_t e = cudaMemcpyAsync(plan->x_stage, X_host, bytes, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail("copy of X to the device", e);
+    // Pinned host buffers mapped into the device's address space are moved by copy
+    // kernels (SM loads and stores over the CPU-GPU link, chained to the MLP's kernels by
+    // programmatic dependent launch: no copy-engine submission on the path); any other host
+    // memory goes through cudaMemcpyAsync.
+    const void* x_dev = nullptr;
+    void* y_dev = nullptr;
+    auto mapped = [](const void* h) -> const void* {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+        return a.devicePointer;
+    };
+    x_dev = mapped(X_host);
+    y_dev = const_cast<void*>(mapped(Y_host));
+    const bool by_kernel = x_dev && y_dev && bytes % 16 == 0 && aligned16(x_dev) && aligned16(y_dev);
+    const int copy_grid = std::max(1, std::min(plan->num_sms, (int)((bytes / 16 + 1023) / 1024)));
+    const char* why = "";
+    cudaError_t e = cudaSuccess;
+    if (by_kernel) {
+        kt_status s = kt::launch_copy16(x_dev, plan->x_stage, bytes, copy_grid, stream, &why);
+        if (s != KT_OK) return fail(s, std::string("copy of X to the device: ") + why);
+    } else {
+        e = cudaMemcpyAsync(plan->x_stage, X_host, bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail("copy of X to the device", e);
+    }
     kt_status s = run_impl(plan, base_tensors(plan->x_stage, W_up, W_down, b_up, b_down, plan->y_stage), plan->H,
                            stream);
     if (s != KT_OK) return s;
-    e = cudaMemcpyAsync(Y_host, plan->y_stage, bytes, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_fail("copy of Y to the host", e);
+    if (by_kernel) {
+        s = kt::launch_copy16(plan->y_stage, y_dev, bytes, copy_grid, stream, &why);
+        if (s != KT_OK) return fail(s, std::string("copy of Y to the host: ") + why);
+    } else {
+        e = cudaMemcpyAsync(Y_host, plan->y_stage, bytes, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail("copy of Y to the host", e);
+    }
     e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     return ok();

@@ -10,6 +10,28 @@ namespace kt {
 
 __global__ void kt_timestamp_kernel(unsigned long long* dst) { *dst = global_ns(); }
 
+// Copy n16 16-byte words from src to dst (either may be pinned host memory mapped into the
+// device's address space: the host-buffer entry point moves X in and Y out with SM loads
+// and stores over the CPU-GPU link instead of copy-engine transfers).  A programmatic
+// dependent of the previous kernel: lets its own dependent start at once, and waits for
+// the previous kernel to complete before it reads.
+__global__ void __launch_bounds__(256) kt_copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                        size_t n16) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // four independent 16-byte loads in flight per thread
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride) dst[i] = src[i];
+}
+
 // Elementwise evaluation of the epilogue's fp32 activations (test hook).
 __global__ void kt_activation_kernel(int act, const float* __restrict__ z, const float* __restrict__ g,
                                      float* __restrict__ out, int64_t n) {
@@ -303,6 +325,31 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     q.partials = reinterpret_cast<float*>(scratch + 256 + counter_bytes);
     q.wait_limit_ns = 4000000000ull;
     return launch_gemm(EPI_DOWN, dtype, &tmA, &tmB, &tmC, q, g.grid, g.smem_bytes, stream, false, why);
+}
+
+kt_status launch_copy16(const void* src, void* dst, size_t bytes, int grid, void* stream, const char** why) {
+    if (bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(src) & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u)) {
+        *why = "copy: 16-byte aligned pointers and a multiple of 16 bytes";
+        return KT_ERR_INVALID;
+    }
+    if (bytes == 0) return KT_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::max(1, grid), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kt_copy16_kernel, reinterpret_cast<const uint4*>(src),
+                                       reinterpret_cast<uint4*>(dst), bytes / 16);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return KT_ERR_CUDA;
+    }
+    return KT_OK;
 }
 
 kt_status launch_timestamp(void* dst, void* stream, const char** why) {
