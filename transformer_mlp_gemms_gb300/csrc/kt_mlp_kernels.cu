@@ -73,28 +73,42 @@ __global__ void __launch_bounds__(kLnWarps * 32) kt_layernorm_kernel(const uint4
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int row = (int)blockIdx.x * kLnWarps + (threadIdx.x >> 5);
-    if (row >= M) return;
     const int nv = D >> 3;  // 16-byte vectors per row
-    const uint4* xr = X + (size_t)row * (size_t)nv;
     const bool cached = nv <= 32 * kLnCache;
+    // gamma and beta, shared by the CTA's rows, staged once in shared memory (rows that fit
+    // in registers); the loads overlap the rows' own
+    __shared__ uint4 s_gamma[32 * kLnCache], s_beta[32 * kLnCache];
+    if (cached) {
+        for (int j = threadIdx.x; j < nv; j += kLnWarps * 32) {
+            s_gamma[j] = gamma[j];
+            s_beta[j] = beta[j];
+        }
+    }
+    const uint4* xr = X + (size_t)(row < M ? row : 0) * (size_t)nv;
     // Statistics of the deviations from the row's first element x0: x - x0 is exact in
     // fp32 for 16-bit inputs, and the sums then carry rounding errors relative to the
     // spread of the row rather than to its mean (a row far from zero with a small spread
-    // would otherwise lose the normalised value's low bits).
-    float x0;
-    {
-        float f[8];
-        unpack8<DT>(xr[0], f);
-        x0 = f[0];
-    }
+    // would otherwise lose the normalised value's low bits).  A row that fits in
+    // registers is loaded in one go; x0 comes from lane 0's first vector.
+    float x0 = 0.0f;
     uint4 c[kLnCache];
     float s = 0.0f;
     if (cached) {
 #pragma unroll
         for (int i = 0; i < kLnCache; ++i) {
             const int j = lane + 32 * i;
-            if (j < nv) {
-                c[i] = xr[j];
+            if (j < nv && row < M) c[i] = xr[j];
+        }
+        __syncthreads();  // gamma and beta staged (every thread of the CTA reaches this)
+        if (row >= M) return;
+        {
+            float f[8];
+            unpack8<DT>(c[0], f);
+            x0 = __shfl_sync(0xffffffffu, f[0], 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kLnCache; ++i) {
+            if (lane + 32 * i < nv) {
                 float f[8];
                 unpack8<DT>(c[i], f);
 #pragma unroll
@@ -102,6 +116,12 @@ __global__ void __launch_bounds__(kLnWarps * 32) kt_layernorm_kernel(const uint4
             }
         }
     } else {
+        if (row >= M) return;
+        {
+            float f[8];
+            unpack8<DT>(xr[0], f);
+            x0 = f[0];
+        }
         for (int j = lane; j < nv; j += 32) {
             float f[8];
             unpack8<DT>(xr[j], f);
@@ -138,11 +158,11 @@ __global__ void __launch_bounds__(kLnWarps * 32) kt_layernorm_kernel(const uint4
     const float var = warp_sum(q) / (float)D;
     const float rstd = 1.0f / sqrtf(var + eps);
     uint4* yr = Xn + (size_t)row * (size_t)nv;
-    auto emit = [&](int j, const uint4& w) {
+    auto emit = [&](int j, const uint4& w, const uint4& gw, const uint4& bw) {
         float f[8], g[8], b[8], y[8];
         unpack8<DT>(w, f);
-        unpack8<DT>(gamma[j], g);
-        unpack8<DT>(beta[j], b);
+        unpack8<DT>(gw, g);
+        unpack8<DT>(bw, b);
 #pragma unroll
         for (int e = 0; e < 8; ++e) y[e] = ((f[e] - x0) - dmean) * rstd * g[e] + b[e];
         uint4 o;
@@ -155,9 +175,9 @@ __global__ void __launch_bounds__(kLnWarps * 32) kt_layernorm_kernel(const uint4
     if (cached) {
 #pragma unroll
         for (int i = 0; i < kLnCache; ++i)
-            if (lane + 32 * i < nv) emit(lane + 32 * i, c[i]);
+            if (lane + 32 * i < nv) emit(lane + 32 * i, c[i], s_gamma[lane + 32 * i], s_beta[lane + 32 * i]);
     } else {
-        for (int j = lane; j < nv; j += 32) emit(j, xr[j]);
+        for (int j = lane; j < nv; j += 32) emit(j, xr[j], gamma[j], beta[j]);
     }
 }
 
