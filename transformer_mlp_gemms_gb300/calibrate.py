@@ -12,7 +12,7 @@ model's pick):
 ``sweep`` (needs the GPU) forces every feasible configuration of each GEMM of a
 workload through the planner's override variables (``KT_FORCE_UP`` =
 ``BN,PAIR,BK``; ``KT_FORCE_DOWN`` = ``BN,SK,PAIR,BK,CLUSTER``), skips those of more
-than 8 waves, and times each with ``kt_mlp_run_timed`` (CUDA events around each
+than 10 waves, and times each with ``kt_mlp_run_timed`` (CUDA events around each
 kernel, 256 MiB L2 scrub before each call, mean of the calls after warm-up).  It
 writes ``calib_<workload>.json``.  ``evaluate`` (host only) recomputes the model's
 estimate of every measured configuration with the current library, and prints per
@@ -76,7 +76,7 @@ def sweep(name: str, out_dir: str, calls: int = 40, warm: int = 5) -> list:
         except kt_mlp.KtError:
             continue  # infeasible: the planner rejects the override
         g = p.info()[gemm]
-        if g["waves"] > 8:
+        if g["waves"] > 10:
             p.close()
             continue
         ms = []
