@@ -31,6 +31,13 @@
 //               still in TMEM) or write them to global memory for the last CTA to
 //               arrive on the tile; partials are always summed in split order.
 //
+// TWO = true runs both projections in one launch: the up projection's tiles, then the
+// down projection's (whole tiles), taken from one global work counter by the leader
+// CTA's producer and published to every role of the CTA (pair) through a small ring of
+// item indices in shared memory; a down tile's producer waits for the counters of its
+// rows of H as above.  Each role's per-tile work is a lambda over one projection's
+// parameters (the epilogue's also over its epilogue kind), shared by both modes.
+//
 // Sources: "SDXL as a requirements inventory", section 1.3 (FeedForward: value =
 // first half, gate = second half) and 9.3 (erf GELU); "MLP layout sweep and
 // remaining representation limits" (the SigLIP MLP, tanh GELU, K-partitioned
