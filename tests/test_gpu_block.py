@@ -223,28 +223,38 @@ def test_timed_block_reports_three_kernels():
 
 # Both projections in one persistent launch (tiles from one work queue) against two launches,
 # each element by element against the oracle: CTA pairs and single CTAs, GEGLU and elementwise
-# activations, both weight orders, LayerNorm and residual.
+# activations, both weight orders, LayerNorm and residual, whole down tiles and down tiles
+# split along K (the last CTA to finish a tile sums the partials; ragged tiles and splits).
 ONE_LAUNCH_CASES = [
-    ("geglu_pair", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128"),
-    ("erf_outin_ln_res", (700, 320, 1000, wl.ACT_GELU_ERF, wl.DT_F16, False), 1, 1, 1, None),
-    ("tanh_single_cta", (300, 256, 1000, wl.ACT_GELU_TANH, wl.DT_F16, True), 1, 0, 0, "128,1,64"),
-    ("silu_many_tiles", (1500, 136, 776, wl.ACT_SILU, wl.DT_BF16, True), 0, 0, 0, None),
-    ("tiny", (33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), 0, 0, 0, None),
+    # id, (M, D, F, act, dtype, bias), residual, layernorm, layout, KT_FORCE_UP, KT_FORCE_DOWN
+    ("geglu_pair_whole", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128", "64,1,2,128"),
+    ("geglu_pair_split3", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 1, 0, 0, "128,2,128", "128,3,2,128"),
+    ("erf_outin_ln_res", (700, 320, 1000, wl.ACT_GELU_ERF, wl.DT_F16, False), 1, 1, 1, None, None),
+    ("erf_outin_split2", (700, 320, 1000, wl.ACT_GELU_ERF, wl.DT_F16, True), 1, 0, 1, "128,1,64", "64,2,1,64"),
+    ("tanh_single_cta", (300, 256, 1000, wl.ACT_GELU_TANH, wl.DT_F16, True), 1, 0, 0, "128,1,64", None),
+    ("tanh_split4_ragged", (729, 192, 1000, wl.ACT_GELU_TANH, wl.DT_F16, False), 0, 0, 0, "192,1,64",
+     "192,4,1,64"),
+    ("silu_many_tiles", (1500, 136, 776, wl.ACT_SILU, wl.DT_BF16, True), 0, 0, 0, None, None),
+    ("tiny", (33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), 0, 0, 0, None, None),
 ]
 
 
-@pytest.mark.parametrize("cid,shape,residual,layernorm,layout,fu", ONE_LAUNCH_CASES,
+@pytest.mark.parametrize("cid,shape,residual,layernorm,layout,fu,fd", ONE_LAUNCH_CASES,
                          ids=[c[0] for c in ONE_LAUNCH_CASES])
 @pytest.mark.parametrize("launches", [kt_mlp.KT_LAUNCH_ONE, kt_mlp.KT_LAUNCH_TWO])
-def test_one_launch_and_two_launches_match_the_oracle(monkeypatch, cid, shape, residual, layernorm, layout, fu,
+def test_one_launch_and_two_launches_match_the_oracle(monkeypatch, cid, shape, residual, layernorm, layout, fu, fd,
                                                       launches):
     if fu:
         monkeypatch.setenv("KT_FORCE_UP", fu)
+    if fd:
+        monkeypatch.setenv("KT_FORCE_DOWN", fd)
     M, D, F, act, dt, bias = shape
     w = wl.custom(M, D, F, act, dt, bias, seed=5000 + M + D + F + act)
     info = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, dt, bias, residual, layernorm, layout,
                                                      launches=launches), 152)
     assert info["one_launch"] == (launches == kt_mlp.KT_LAUNCH_ONE)
+    if fd:
+        assert info["down"]["split_k"] == int(fd.split(",")[1]) and info["down"]["cluster_sk"] == 0
     t, d = _inputs(w, residual, layernorm, layout)
     Y, H = _run_block(w, d, residual, layernorm, layout, launches=launches)
     Ho, Yx, bound = _oracle(w, t, layout)

@@ -23,23 +23,27 @@ def _lib():
     kt_mlp.load()
 
 
+SIGLIP = (729, 1152, 4304, wl.ACT_GELU_TANH, wl.DT_F16, False)
 CASES = [
-    # (M, D, F, act, dtype, bias), block options, h_path
-    ((729, 1152, 4304, wl.ACT_GELU_TANH, wl.DT_F16, False), {}, kt_mlp.KT_H_MEMORY),   # SigLIP: cluster split-K
-    ((2048, 1280, 5120, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY),      # SDXL level 2: CTA pairs
-    ((300, 256, 1000, wl.ACT_SILU, wl.DT_F16, True), {"residual": True, "layernorm": True}, kt_mlp.KT_H_MEMORY),
-    ((33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), {}, kt_mlp.KT_H_ON_CHIP),        # the fused kernel
+    # (M, D, F, act, dtype, bias), block options, h_path, launches
+    (SIGLIP, {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_ONE),   # one launch, down tiles split along K
+    (SIGLIP, {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_TWO),   # two launches, cluster split-K
+    ((2048, 1280, 5120, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_AUTO),  # pairs
+    ((300, 256, 1000, wl.ACT_SILU, wl.DT_F16, True), {"residual": True, "layernorm": True}, kt_mlp.KT_H_MEMORY,
+     kt_mlp.KT_LAUNCH_AUTO),
+    ((33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), {}, kt_mlp.KT_H_ON_CHIP, kt_mlp.KT_LAUNCH_AUTO),  # fused
 ]
 
 
-@pytest.mark.parametrize("shape,opts,h_path", CASES, ids=["siglip", "sdxl_l2", "block", "h_on_chip"])
-def test_graph_replay_matches_eager_runs(shape, opts, h_path):
+@pytest.mark.parametrize("shape,opts,h_path,launches", CASES,
+                         ids=["siglip_one", "siglip_two", "sdxl_l2", "block", "h_on_chip"])
+def test_graph_replay_matches_eager_runs(shape, opts, h_path, launches):
     M, D, F, act, dt, bias = shape
     res, ln = opts.get("residual", False), opts.get("layernorm", False)
     w = wl.custom(M, D, F, act, dt, bias, seed=123)
     t = wl.generate(w, residual=res, layernorm=ln)
     d = {k: v.cuda() for k, v in t.items()}
-    plan = kt_mlp.Plan(M, D, F, act, dt, bias, residual=res, layernorm=ln, h_path=h_path)
+    plan = kt_mlp.Plan(M, D, F, act, dt, bias, residual=res, layernorm=ln, h_path=h_path, launches=launches)
     tdt = wl.TORCH_DTYPES[dt]
     X = torch.empty_like(d["X"])
     Y = torch.empty((M, D), dtype=tdt, device="cuda")

@@ -32,7 +32,8 @@
 //               arrive on the tile; partials are always summed in split order.
 //
 // TWO = true runs both projections in one launch: the up projection's tiles, then the
-// down projection's (whole tiles), taken from one global work counter by the leader
+// down projection's (whole tiles, or K splits whose partials the last CTA to finish a
+// tile sums through global memory), taken from one global work counter by the leader
 // CTA's producer and published to every role of the CTA (pair) through a small ring of
 // item indices in shared memory; a down tile's producer waits for the counters of its
 // rows of H as above.  Each role's per-tile work is a lambda over one projection's
@@ -777,11 +778,12 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
 
     // Work items.  One projection: tiles unit0, unit0 + unit_step, ... (static).  TWO: items
     // 0 .. p.num_tiles - 1 are up-projection tiles, the next p2.num_tiles down-projection
-    // tiles (whole tiles), handed out dynamically: the leader CTA's producer takes the next
-    // index from a global counter and publishes it in the item ring of both CTAs of the
-    // pair; every role consumes the same sequence.  All up tiles are taken before any down
-    // tile, and up tiles wait on nothing, so a down tile waiting for its rows of H always
-    // waits on work in progress.
+    // items (tiles, or K splits of tiles), handed out dynamically: the leader CTA's
+    // producer takes the next index from a global counter and publishes it in the item
+    // ring of both CTAs of the pair; every role consumes the same sequence.  All up tiles
+    // are taken before any down item, and up tiles wait on nothing, so a down item waiting
+    // for its rows of H always waits on work in progress (the split-K reduction waits on
+    // nothing: the last CTA to finish a tile sums it).
     const int total = p.num_tiles + (TWO ? p2.num_tiles : 0);
     // While up tiles remain for every unit, the leader's producer takes each index one item
     // ahead (the counter's round trip then overlaps the previous item's loads); down tiles
@@ -1243,8 +1245,8 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 }
                 if (tr1) trace_mark(tr, TR_S_ARR);
                 if (EPI != EPI_DOWN && p.ready != nullptr) pending_rows = c.tm;  // counted later
-            } else if constexpr (EPI == EPI_DOWN && !TWO) {
-              if (p.cluster_sk) {
+            } else if constexpr (EPI == EPI_DOWN) {
+              if (!TWO && p.cluster_sk) {  // (one launch for both projections: never a cluster)
                 // split-K inside a cluster, reduce-scattered through L2: each 32 x 32 unit of
                 // the tile (row block q, column group g, u = q * ngroups + g) is owned by CTA
                 // u % SK of the cluster, and a unit is handled by the same warp in every CTA.

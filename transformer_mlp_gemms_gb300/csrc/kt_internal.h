@@ -65,13 +65,14 @@ struct GemmConfig {
     int n_b;               // B operand tiles per stage: 1, or 2 for GEGLU (value + gate)
     int pair;              // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile (cta_group::2)
     int bk;                // k-block depth per pipeline stage: 64 or 128
-    int cluster_sk;        // 1: split-K partials reduced inside a cluster (distributed smem)
+    int cluster_sk;        // 1: split-K partials reduce-scattered through L2 inside a cluster
     int b_kmajor;          // 1: the weight is stored [N][K] (PyTorch order) and loaded K-major
     int dbl_staging;       // 1: shared memory left over for a second set of output staging buffers
     double useful_over_padded;
     double est_us;
     double t_tile_us;      // model: one tile's main loop on one CTA (pair), and its epilogue
     double t_epi_us;
+    double t_x_us;         // model: the split-K exchange of one tile (0 without split-K)
 };
 
 // The H-on-chip variant (kt_fused.cu): both projections in one kernel, H in shared

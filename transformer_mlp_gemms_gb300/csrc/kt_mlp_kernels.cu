@@ -481,7 +481,10 @@ kt_status launch_mlp_two(int epi, int dtype, const void* const* maps, const Gemm
                          int grid, int smem_bytes, void* stream, bool pdl, const char** why) {
     const CUtensorMap* m[6];
     for (int i = 0; i < 6; ++i) m[i] = reinterpret_cast<const CUtensorMap*>(maps[i]);
-    if (up.pair != down.pair || (up.pair == 2 && grid % 2 != 0) || down.split_k != 1 || up.split_k != 1 ||
+    // the down projection's K splits (if any) are summed by the last CTA of each tile
+    // through the partials and tile counters
+    if (up.pair != down.pair || (up.pair == 2 && grid % 2 != 0) || down.split_k < 1 || up.split_k != 1 ||
+        (down.split_k > 1 && (down.partials == nullptr || down.counters == nullptr)) ||
         up.cluster_sk || down.cluster_sk || up.stages != down.stages || up.stage_bytes != down.stage_bytes ||
         up.dbl_staging != down.dbl_staging || up.sched == nullptr || grid / up.pair > up.num_tiles + down.num_tiles) {
         *why = "inconsistent one-launch configuration";

@@ -80,6 +80,12 @@ int max_active_clusters(int size, int num_sms) {
 // barrier traffic of the main loop and epilogue.
 constexpr double kPairKernelCost = 3.0e-6;
 constexpr double kPairTileCost = 0.3e-6;
+// Splits along K of the one-launch down projection's tiles considered by the planner, and
+// the extra cost of a split there over the exchange modelled above (calibrated on GB300
+// against whole tiles: SigLIP's MLP with six down configurations in one launch, and three
+// more shapes, ran 5-10 us slower than modelled with split-K and 3.5 us faster without).
+constexpr int kOneLaunchMaxSplit = 4;
+constexpr double kOneLaunchSplitCost = 7.0e-6;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -176,6 +182,7 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     g->est_us = (t_cta + kKernelOverhead + (pair == 2 ? kPairKernelCost : 0.0)) * 1e6;
     g->t_tile_us = t_main * 1e6;
     g->t_epi_us = t_epi * 1e6;
+    g->t_x_us = t_x * 1e6;
     return true;
 }
 
@@ -260,12 +267,13 @@ static bool plan_fused(int64_t M, int64_t D, int64_t F, int act, int num_sms, Fu
 }
 
 // Both projections in one persistent launch, tiles from one dynamic queue (up tiles first):
-// the down projection's whole-tile candidates with the up projection's CTA pairing, the two
-// GEMMs sharing one shared-memory ring (its stage the larger of their k-blocks).  Modelled
-// time: the up tiles spread over the units, then the down tiles in whole rounds of one
-// tile per unit (a down tile is long: a round a few tiles short of the units' count still
-// costs a full tile), at least the total work spread over the units, plus an epilogue and
-// the launch.
+// the down projection's candidates with the up projection's CTA pairing, whole tiles or
+// split along K (each split a work item; the last CTA to finish a tile sums the partials
+// through global memory), the two GEMMs sharing one shared-memory ring (its stage the
+// larger of their k-blocks).  Modelled time: the up tiles spread over the units, then the
+// down items in whole rounds of one item per unit (a down item is long: a round a few
+// items short of the units' count still costs a full item), at least the total work spread
+// over the units, plus the last epilogue (with the split-K exchange) and the launch.
 static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sms, int kmaj, PlanChoice* out,
                             const GemmConfig* forced_down) {
     out->one_launch = 0;
@@ -276,26 +284,31 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
     const int n_b = act == KT_ACT_GEGLU ? 2 : 1;
     const int units = num_sms / pair;
     bool found = false;
-    for (int BN = 32 * pair; BN <= 256; BN += 32 * pair) {
-        for (int bk = 64; bk <= 128; bk += 64) {
+    for (int BN = 32 * pair; BN <= 256; BN += 32 * pair)
+      for (int bk = 64; bk <= 128; bk += 64)
+        for (int SK = 1; SK <= kOneLaunchMaxSplit; ++SK) {
             if (forced_down && (forced_down->BN != BN || forced_down->bk != bk || forced_down->pair != pair ||
-                                forced_down->split_k != 1))
+                                forced_down->split_k != SK || forced_down->cluster_sk))
                 continue;
             GemmConfig d0;
-            if (!evaluate(M, D, F, BN, 1, 1, EPI_DOWN, num_sms, pair, bk, &d0, false, kmaj)) continue;
+            if (!evaluate(M, D, F, BN, SK, 1, EPI_DOWN, num_sms, pair, bk, &d0, false, kmaj)) continue;
             const int slot = std::max(stage_bytes(u0.BN, n_b, pair, u0.bk, kmaj), stage_bytes(BN, 1, pair, bk, kmaj));
             const int stages = std::min((kSmemBudget - smem_reserve(epi_up)) / slot, kMaxStages);
             GemmConfig u, d;
             if (stages < 2 || !evaluate(M, F, D, u0.BN, 1, n_b, epi_up, num_sms, pair, u0.bk, &u, false, kmaj, stages) ||
-                !evaluate(M, D, F, BN, 1, 1, EPI_DOWN, num_sms, pair, bk, &d, false, kmaj, stages))
+                !evaluate(M, D, F, BN, SK, 1, EPI_DOWN, num_sms, pair, bk, &d, false, kmaj, stages))
                 continue;
-            const double up_tiles = (double)u.tiles_m * u.tiles_n, dn_tiles = (double)d.tiles_m * d.tiles_n;
-            const int grid = (int)std::min<int64_t>((int64_t)units, (int64_t)(up_tiles + dn_tiles)) * pair;
+            const double up_tiles = (double)u.tiles_m * u.tiles_n;
+            const double dn_items = (double)d.tiles_m * d.tiles_n * SK;
+            // a split is worth its exchange only while all the items run in one round
+            if (SK > 1 && !forced_down && dn_items > units) continue;
+            const int grid = (int)std::min<int64_t>((int64_t)units, (int64_t)(up_tiles + dn_items)) * pair;
             const double n = grid / pair;
-            const double work = (up_tiles * u.t_tile_us + dn_tiles * d.t_tile_us) / n;
-            const double rounds = up_tiles * u.t_tile_us / n + std::ceil(dn_tiles / n) * d.t_tile_us;
-            const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us) + kKernelOverhead * 1e6 +
-                             (pair == 2 ? kPairKernelCost * 1e6 : 0.0);
+            const double work = (up_tiles * u.t_tile_us + dn_items * d.t_tile_us) / n;
+            const double rounds = up_tiles * u.t_tile_us / n + std::ceil(dn_items / n) * d.t_tile_us;
+            const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us + d.t_x_us) +
+                             kKernelOverhead * 1e6 + (pair == 2 ? kPairKernelCost * 1e6 : 0.0) +
+                             (SK > 1 ? kOneLaunchSplitCost * 1e6 : 0.0);
             if (!found || t < out->one_est_us) {
                 found = true;
                 out->one_est_us = t;
@@ -312,7 +325,6 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
                 out->one_down = d;
             }
         }
-    }
     if (found) out->one_launch = 1;
 }
 
@@ -389,13 +401,14 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     }
     // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory.  The
     // planner's own choice (KT_LAUNCH_AUTO): one launch when the up projection is a single
-    // wave (all of H is stored at about the same time, so the second kernel's launch and
-    // set-up sit on the critical path), the two-launch down projection would split K (its
-    // exchange sits there too; the one-launch kernel takes whole down tiles instead), and the
-    // model prefers one launch; otherwise two.  This rule reproduces the measured winner on
-    // all eight benchmark shapes (one launch: SigLIP, 37.0 against 39.7 us; two launches: the
-    // tiny case, M = 256 and 1000, which split the down projection but lose more parallelism
-    // than they gain, and the multi-wave SDXL and sweep shapes).  Override: KT_FORCE_LAUNCHES=1|2.
+    // wave of single-CTA tiles (all of H is stored at about the same time, so the second
+    // kernel's launch and set-up sit on the critical path), the two-launch down projection
+    // would split K (its cluster exchange sits there too), and the model prefers one launch;
+    // otherwise two.  This rule reproduces the measured winner on all eight benchmark shapes
+    // (one launch: SigLIP, whole down tiles, 36.8 against 40.0 us, and M = 256, down tiles
+    // split four ways, 26.3 against 28.9 us; two launches: the tiny case, M = 1000, whose
+    // CTA-pair tiles ran 42.5 against 39.2 us in one launch, and the multi-wave SDXL and
+    // sweep shapes).  Override: KT_FORCE_LAUNCHES=1|2.
     out->one_launch = 0;
     if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
         *why = "unknown launches option";
@@ -411,7 +424,8 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         launches = v == 1 ? KT_LAUNCH_ONE : KT_LAUNCH_TWO;
     }
     const bool forced_dn = std::getenv("KT_FORCE_DOWN") != nullptr;
-    const bool auto_one = launches == KT_LAUNCH_AUTO && out->up.waves == 1 && out->down.split_k > 1 && !forced_dn;
+    const bool auto_one = launches == KT_LAUNCH_AUTO && out->up.waves == 1 && out->up.pair == 1 &&
+                          out->down.split_k > 1 && !forced_dn;
     const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
     if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
         const double t_two = out->up.est_us + out->down.est_us;
