@@ -319,7 +319,10 @@ kt_status kt_mlp_debug_stall(kt_mlp_plan_t plan, int enable, int64_t limit_us);
  * then the SM id, the number of tiles, the last tile's main-loop / epilogue end,
  * four epilogue sub-phase marks of the first epilogue warp, and ten marks of the
  * CTA's second tile (epilogue sub-phases, its main loop's start and end, its first
- * copy); slots 26-31 are unused.  Each buffer must hold 32 * grid uint64 (grid from
+ * copy); with both projections in one launch (trace_up then holds the one kernel's
+ * CTAs), slots 26-30: first down item taken, its rows of H stored, up and down items
+ * processed (counts), last up tile's main loop done; slot 31: past the wait for the
+ * previous kernel in the stream.  Each buffer must hold 32 * grid uint64 (grid from
  * kt_mlp_get_info); the caller owns them.  NULL buffers switch tracing off.
  */
 kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_down);

@@ -773,17 +773,20 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     // it reads, and the MMA warp touches no global memory.
     const bool ready_mode = EPI == EPI_DOWN && p.ready != nullptr;
     if (p.pdl_wait && (!ready_mode || warp >= 2)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) trace_mark(tr, TR_PDL);
 
     const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
 
     // Work items.  One projection: tiles unit0, unit0 + unit_step, ... (static).  TWO: items
     // 0 .. p.num_tiles - 1 are up-projection tiles, the next p2.num_tiles down-projection
-    // items (tiles, or K splits of tiles), handed out dynamically: the leader CTA's
-    // producer takes the next index from a global counter and publishes it in the item
-    // ring of both CTAs of the pair; every role consumes the same sequence.  All up tiles
-    // are taken before any down item, and up tiles wait on nothing, so a down item waiting
-    // for its rows of H always waits on work in progress (the split-K reduction waits on
-    // nothing: the last CTA to finish a tile sums it).
+    // items (tiles, or K splits of tiles).  Unit u's first item is item u; the rest are
+    // handed out dynamically: the leader CTA's producer takes the next index (unit_step +
+    // a global counter) and publishes it in the item ring of both CTAs of the pair; every
+    // role consumes the same sequence.  Indices go out in increasing order and up tiles
+    // wait on nothing, so a down item waiting for its rows of H always waits on up tiles
+    // held by units that run or will run once the SMs the previous kernel holds are free
+    // (the grid fits the GPU); the split-K reduction waits on nothing: the last CTA to
+    // finish a tile sums it.
     const int total = p.num_tiles + (TWO ? p2.num_tiles : 0);
     // While up tiles remain for every unit, the leader's producer takes each index one item
     // ahead (the counter's round trip then overlaps the previous item's loads); down tiles
@@ -794,8 +797,8 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         if (!wait_phase(item_empty + 8u * slot, par ^ 1u, abort_flag, p.error, DEV_TIMEOUT_PRODUCER,
                         p.wait_limit_ns))
             return INT_MAX;
-        const int idx = next_idx >= 0 ? next_idx : atomicAdd(p.sched, 1);
-        next_idx = idx + 2 * (int)(gridDim.x / PAIR) < p.num_tiles ? atomicAdd(p.sched, 1) : -1;
+        const int idx = k == 0 ? unit0 : next_idx >= 0 ? next_idx : unit_step + atomicAdd(p.sched, 1);
+        next_idx = idx + 2 * unit_step < p.num_tiles ? unit_step + atomicAdd(p.sched, 1) : -1;
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(item_idx + 4u * slot), "r"(idx) : "memory");
         if constexpr (PAIR == 2) {
             asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa_rank(item_idx + 4u * slot, 1)), "r"(idx)

@@ -200,6 +200,7 @@ enum TraceSlot : int {
     TR_T_UP_ITEMS = 28,  // MMA issuer: up-projection tiles processed (a count)
     TR_T_DN_ITEMS = 29,  // MMA issuer: down-projection tiles processed (a count)
     TR_T_LAST_UP = 30,   // MMA issuer: last up-projection tile's main loop committed
+    TR_PDL = 31,         // thread 0 past the wait for the predecessor grid
     kTraceSlots = 32
 };
 
