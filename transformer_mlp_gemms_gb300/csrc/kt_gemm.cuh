@@ -266,10 +266,11 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading-dimension and
 // stride-dimension byte offsets (all >> 4), descriptor version 1 (bits 46-48 =
-// 0b001), base offset 0 (tiles are 1024-byte aligned), 128-byte swizzle (= 2).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// 0b001), base offset 0 (tiles are 1024-byte aligned), swizzle mode in bits 61-63:
+// 128-byte swizzle (= 2) by default, 64-byte swizzle (= 4).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz = 2u) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -623,17 +624,18 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t
 
 // The MMAs of one k-block: NK steps of K = 16 (4 for a 64-deep stage, 8 for 128).
 // Descriptor start addresses move in 16-byte units.  A (K-major): +32 bytes per step
-// inside a 64-deep swizzle atom, +16 KB per atom.  B N-major (KB = 0): +2 KB per step
-// (16 rows of 128 bytes).  B K-major (KB = 1): as A, with atoms of b_atom16 units.
+// inside a 64-deep swizzle atom, +16 KB per atom.  B N-major (KB = 0): +16 rows per
+// step, b_step16 units (2 KB for 128-byte rows, 1 KB for 64-byte rows).  B K-major
+// (KB = 1): as A, with atoms of b_atom16 units.
 // GEGLU needs no second MMA: its B operand holds the value and the gate columns of
 // the tile side by side, so one MMA of N = 2 BN fills both accumulators.
 template <int PAIR, int NK, int KB>
 __device__ __forceinline__ void issue_kblock(uint32_t d, uint64_t ad0, uint64_t bd0, uint32_t idesc, uint32_t acc0,
-                                             uint32_t b_atom16) {
+                                             uint32_t b_atom16, uint32_t b_step16 = 128u) {
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const uint64_t ad = ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
-        const uint64_t boff = KB ? (uint64_t)((k >> 2) * b_atom16 + (k & 3) * 2) : (uint64_t)(k * 128);
+        const uint64_t boff = KB ? (uint64_t)((k >> 2) * b_atom16 + (k & 3) * 2) : (uint64_t)(k * b_step16);
         const uint64_t bd = bd0 + boff;
         const uint32_t acc = k == 0 ? acc0 : 1u;
         if constexpr (PAIR == 2) mma_f16_pair(d, ad, bd, idesc, acc);
@@ -834,8 +836,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                                const bool ready_mode, const int t, const int local) -> bool {
                 const TileCoord c = decode_tile(t, p);
                 const int kb0 = c.kb0, kb1 = c.kb1;
-                // this CTA's rows of A and its share of the B columns
+                // this CTA's rows of A and its share of the B columns (N-major B: in boxes of
+                // bw columns, 64 or 32; 32 only for shares that are odd multiples of 32)
                 const int bcols = p.BN / PAIR;
+                const int bw = bcols % 64 == 0 ? 64 : 32;
                 auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
                     m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
                     nb_r = c.tn * p.BN + (int)r * bcols;
@@ -846,10 +850,10 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                         chunks_r = nb_r < p.N ? 1 : 0;
                         return a_b + (uint32_t)(n_b * chunks_r) * p.b_bytes;
                     }
-                    chunks_r = 0;  // 64-column boxes of the share that start inside [0, N)
-                    for (int ch = 0; ch * 64 < bcols; ++ch)
-                        if (nb_r + 64 * ch < p.N) chunks_r = ch + 1;
-                    return a_b + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * 128u);
+                    chunks_r = 0;  // boxes of the share that start inside [0, N)
+                    for (int ch = 0; ch * bw < bcols; ++ch)
+                        if (nb_r + bw * ch < p.N) chunks_r = ch + 1;
+                    return a_b + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * (uint32_t)bw * 2u);
                 };
                 int m_me, nb_me, chunks;
                 uint32_t tx = cta_share(rank, m_me, nb_me, chunks);
@@ -890,9 +894,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
                     if (tr && kb == kb0 && local == 1) trace_mark(tr, TR_S_LD0);
                     const int k0 = kb * p.bk;
-                    // N-major B: box j is 64 columns x bk rows at column nb + 64 j, row k0.
+                    // N-major B: box j is bw columns x bk rows at column nb + bw j, row k0.
                     // K-major B: box j is bcols rows x 64 at row nb, column k0 + 64 j.
-                    const uint32_t box_bytes = p.b_kmajor ? p.b_atom_bytes : (uint32_t)p.bk * 128u;
+                    const uint32_t box_bytes = p.b_kmajor ? p.b_atom_bytes : (uint32_t)p.bk * (uint32_t)bw * 2u;
                     const int nbox = p.b_kmajor ? (chunks ? p.bk / kAtomK : 0) : chunks;
                     // shared-memory slots of value box j and gate box j: N-major, the gate
                     // chunks follow all value chunks at the same pitch; K-major, each 64-deep
@@ -901,9 +905,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     auto gslot = [&](int j) {
                         return p.b_kmajor ? sB + box_bytes * (uint32_t)(2 * j + 1) : sB + p.b_bytes + box_bytes * (uint32_t)j;
                     };
-                    auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + 64 * j; };
+                    auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + bw * j; };
                     auto by = [&](int j, int row0) { return p.b_kmajor ? row0 + nb_me : k0; };
-                    auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + 64 * j; };
+                    auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + bw * j; };
                     if constexpr (PAIR == 2) {
                         const uint32_t fb_leader = mapa_rank(fb, 0);
                         if (leader) mbar_arrive_expect_tx(fb, tx);
@@ -1002,20 +1006,24 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     const uint32_t sB = sA + p.a_bytes;
                     // Descriptors of this stage; the K steps only move the start address by
                     // constant offsets (issue_kblock).  128-byte swizzle, 8-row groups 1 KB
-                    // apart; N-major B: 64-column chunks bk x 128 bytes apart.
+                    // apart; N-major B: 64-column chunks bk x 128 bytes apart, or (a share
+                    // that is an odd multiple of 32) 64-byte swizzle, 32-column chunks
+                    // bk x 64 bytes apart, 8-row groups 512 bytes apart.
                     // GEGLU: the gate chunks follow the value chunks (N-major: at the same
                     // chunk pitch; K-major: inside every 64-deep atom), one operand of 2 BN.
                     const uint64_t ad0 = smem_desc(sA, 16u, 1024u);
-                    const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * 128u;
-                    const uint64_t bd0 = smem_desc(sB, b_lbo, 1024u);
+                    const bool b64 = !p.b_kmajor && (p.BN / PAIR) % 64 != 0;  // 32-column boxes
+                    const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * (b64 ? 64u : 128u);
+                    const uint64_t bd0 = smem_desc(sB, b_lbo, b64 ? 512u : 1024u, b64 ? 4u : 2u);
+                    const uint32_t b_step16 = b64 ? 64u : 128u;
                     const uint32_t acc0 = kb > kb0 ? 1u : 0u;
                     const uint32_t batom16 = (p.b_atom_bytes * (uint32_t)n_b) >> 4;
                     if (p.b_kmajor) {
                         if (p.bk == 64) issue_kblock<PAIR, 4, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
                         else issue_kblock<PAIR, 8, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
                     } else {
-                        if (p.bk == 64) issue_kblock<PAIR, 4, 0>(d, ad0, bd0, p.idesc, acc0, 0u);
-                        else issue_kblock<PAIR, 8, 0>(d, ad0, bd0, p.idesc, acc0, 0u);
+                        if (p.bk == 64) issue_kblock<PAIR, 4, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16);
+                        else issue_kblock<PAIR, 8, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16);
                     }
                     issued_any = true;
                     // stage free (in both CTAs of a pair) once these MMAs completed

@@ -101,13 +101,18 @@ struct PlanChoice {
     GemmConfig one_up, one_down;  // the two GEMMs' configurations in that launch
 };
 
+// Columns of one box of an N-major ([K][N]) B tile: 64 (128-byte rows, 128-byte swizzle)
+// when the CTA's column share (BN, or BN/2 in a CTA pair; a multiple of 32) is a multiple
+// of 64, else 32 (64-byte rows, 64-byte swizzle), so that no column is loaded in vain.
+inline int b_box_cols(int BN, int pair) { return (BN / pair) % 64 == 0 ? 64 : 32; }
+
 // Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
-// 128 x 64) + n_b B tiles holding its share of the columns (BN, or BN/2 in a CTA
-// pair): in 64-column boxes of bk rows for a [K][N] weight (N-major, padded to 64
-// columns), or in bk/64 atoms of (share) rows x 64 for a [N][K] weight (K-major).
+// 128 x 64) + n_b B tiles holding its share of the columns: in b_box_cols-wide boxes of
+// bk rows for a [K][N] weight (N-major), or in bk/64 atoms of (share) rows x 64 for a
+// [N][K] weight (K-major).
 inline int b_tile_bytes(int BN, int pair, int bk, int b_kmajor) {
-    if (b_kmajor) return (BN / pair) * bk * 2;
-    return (BN / pair + 63) / 64 * 64 * bk * 2;
+    (void)b_kmajor;
+    return (BN / pair) * bk * 2;
 }
 inline int stage_bytes(int BN, int n_b, int pair, int bk, int b_kmajor = 0) {
     return kBM * bk * 2 + n_b * b_tile_bytes(BN, pair, bk, b_kmajor);

@@ -203,8 +203,9 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     if (!P->cache_valid || P->c_x != A_up || P->c_wu != t.W_up || P->c_h != H || P->c_wd != t.W_down ||
         P->c_y != t.Y) {
         // A operands: [rows][K] K-major, box 128 rows x 64 columns, 128-byte swizzle.
-        // B operands [K][N] (N-major): box bk rows (K) x 64 columns (N); [N][K] (K-major):
-        // box (BN / pair) rows (N) x 64 columns (K); 128-byte swizzle.
+        // B operands [K][N] (N-major): box bk rows (K) x 64 columns (N), 128-byte swizzle,
+        // or x 32 columns, 64-byte swizzle (b_box_cols); [N][K] (K-major): box (BN / pair)
+        // rows (N) x 64 columns (K), 128-byte swizzle.
         // Stores of H and Y: box 32 rows x 32 columns, 64-byte swizzle.
         const kt::GemmConfig& u = P->choice.up;
         const kt::GemmConfig& d = P->choice.down;
@@ -212,10 +213,12 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
         bool good =
             kt::encode_tmap(&P->tm_x, A_up, P->dtype, P->M, P->D, kt::kBM, kt::kAtomK, 128, &why) &&
             (km ? kt::encode_tmap(&P->tm_wu, t.W_up, P->dtype, P->F_up, P->D, u.BN / u.pair, 64, 128, &why)
-                : kt::encode_tmap(&P->tm_wu, t.W_up, P->dtype, P->D, P->F_up, u.bk, 64, 128, &why)) &&
+                : kt::encode_tmap(&P->tm_wu, t.W_up, P->dtype, P->D, P->F_up, u.bk, kt::b_box_cols(u.BN, u.pair),
+                                  2 * kt::b_box_cols(u.BN, u.pair), &why)) &&
             kt::encode_tmap(&P->tm_h, H, P->dtype, P->M, P->F, kt::kBM, kt::kAtomK, 128, &why) &&
             (km ? kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->D, P->F, d.BN / d.pair, 64, 128, &why)
-                : kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->F, P->D, d.bk, 64, 128, &why)) &&
+                : kt::encode_tmap(&P->tm_wd, t.W_down, P->dtype, P->F, P->D, d.bk, kt::b_box_cols(d.BN, d.pair),
+                                  2 * kt::b_box_cols(d.BN, d.pair), &why)) &&
             kt::encode_tmap(&P->tm_hs, H, P->dtype, P->M, P->F, 32, kt::kStoreCols, 64, &why) &&
             kt::encode_tmap(&P->tm_ys, t.Y, P->dtype, P->M, P->D, 32, kt::kStoreCols, 64, &why) &&
             (!P->choice.h_on_chip ||

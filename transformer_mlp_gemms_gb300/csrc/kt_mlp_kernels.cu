@@ -314,7 +314,7 @@ kt_status noalloc_down_proj(int64_t M, int64_t F, int64_t D, int dtype, const vo
     }
     alignas(64) CUtensorMap tmA, tmB, tmC;
     if (!encode_tmap(&tmA, H, dtype, M, F, kBM, kAtomK, 128, why) ||
-        !encode_tmap(&tmB, W_down, dtype, F, D, g.bk, 64, 128, why) ||
+        !encode_tmap(&tmB, W_down, dtype, F, D, g.bk, b_box_cols(g.BN, g.pair), 2 * b_box_cols(g.BN, g.pair), why) ||
         !encode_tmap(&tmC, Y, dtype, M, D, 32, kStoreCols, 64, why))
         return KT_ERR_CUDA;
     GemmParams q;
