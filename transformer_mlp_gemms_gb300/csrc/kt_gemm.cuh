@@ -8,8 +8,9 @@
 //   warp 0      producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
 //               A tile (128 x 64 K-major boxes, one per 64-deep atom of a BK = 64 or
 //               128 k-block) and the B tile(s) -- 64-column N-major boxes of an
-//               [in][out] weight, or (BN / PAIR)-row K-major boxes of an [out][in]
-//               weight -- into an S-stage shared-memory ring, one mbarrier pair
+//               [in][out] weight (32-column, 64-byte swizzle, for a CTA column share
+//               that is an odd multiple of 32), or (BN / PAIR)-row K-major boxes of
+//               an [out][in] weight -- into an S-stage shared-memory ring, one mbarrier pair
 //               (full / empty) per stage.  The down projection's producer first waits
 //               for the up projection's per-row-block counters of stored H tiles.
 //   warp 1      MMA issuer: one thread of the leader CTA issues tcgen05.mma kind::f16
