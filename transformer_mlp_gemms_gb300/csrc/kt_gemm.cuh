@@ -118,6 +118,20 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// Non-blocking test of the phase of parity `parity` (no suspension: the fast path of a
+// wait whose phase has usually completed already).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // As mbar_try_wait, acquiring at cluster scope: for barriers whose phase completes on
 // data written by other CTAs of the cluster (remote asynchronous stores).
 __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -994,37 +1008,42 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 if (tr && local == 1) trace_mark(tr, TR_S_MMA0);
                 const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
                 const int kb0 = c.kb0, kb1 = c.kb1;
+                // Descriptors of stage 0, computed once per tile: a stage's descriptors are
+                // those of stage 0 with the start address moved by the stage offset, and the
+                // K steps only move it by constant offsets (issue_kblock), so that the
+                // issuing thread's work between two k-blocks stays shorter than the MMAs the
+                // tensor pipe still has queued.  128-byte swizzle, 8-row groups 1 KB apart;
+                // N-major B: 64-column chunks bk x 128 bytes apart, or (a share that is an
+                // odd multiple of 32) 64-byte swizzle, 32-column chunks bk x 64 bytes apart,
+                // 8-row groups 512 bytes apart.  GEGLU: the gate chunks follow the value
+                // chunks (N-major: at the same chunk pitch; K-major: inside every 64-deep
+                // atom), one operand of 2 BN.
+                const bool b64 = !p.b_kmajor && (p.BN / PAIR) % 64 != 0;  // 32-column boxes
+                const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * (b64 ? 64u : 128u);
+                const uint64_t ad_s0 = smem_desc(base, 16u, 1024u);
+                const uint64_t bd_s0 = smem_desc(base + p.a_bytes, b_lbo, b64 ? 512u : 1024u, b64 ? 4u : 2u);
+                const uint32_t stage16 = p.stage_bytes >> 4;
+                const uint32_t b_step16 = b64 ? 64u : 128u;
+                const uint32_t batom16 = (p.b_atom_bytes * (uint32_t)n_b) >> 4;
+                const int variant = (p.b_kmajor ? 2 : 0) + (p.bk == 64 ? 0 : 1);
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(bar_full + 8u * stage, phase, abort_flag, p.error, DEV_TIMEOUT_MMA,
-                                    p.wait_limit_ns)) {
+                    const uint32_t fb = bar_full + 8u * stage;
+                    if (!mbar_test_wait(fb, phase) &&
+                        !wait_phase(fb, phase, abort_flag, p.error, DEV_TIMEOUT_MMA, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (tr && !issued_any) trace_mark(tr, TR_FIRST_FULL);
-                    const uint32_t sA = base + stage * p.stage_bytes;
-                    const uint32_t sB = sA + p.a_bytes;
-                    // Descriptors of this stage; the K steps only move the start address by
-                    // constant offsets (issue_kblock).  128-byte swizzle, 8-row groups 1 KB
-                    // apart; N-major B: 64-column chunks bk x 128 bytes apart, or (a share
-                    // that is an odd multiple of 32) 64-byte swizzle, 32-column chunks
-                    // bk x 64 bytes apart, 8-row groups 512 bytes apart.
-                    // GEGLU: the gate chunks follow the value chunks (N-major: at the same
-                    // chunk pitch; K-major: inside every 64-deep atom), one operand of 2 BN.
-                    const uint64_t ad0 = smem_desc(sA, 16u, 1024u);
-                    const bool b64 = !p.b_kmajor && (p.BN / PAIR) % 64 != 0;  // 32-column boxes
-                    const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * (b64 ? 64u : 128u);
-                    const uint64_t bd0 = smem_desc(sB, b_lbo, b64 ? 512u : 1024u, b64 ? 4u : 2u);
-                    const uint32_t b_step16 = b64 ? 64u : 128u;
+                    const uint64_t soff = (uint64_t)(stage * stage16);
+                    const uint64_t ad0 = ad_s0 + soff, bd0 = bd_s0 + soff;
                     const uint32_t acc0 = kb > kb0 ? 1u : 0u;
-                    const uint32_t batom16 = (p.b_atom_bytes * (uint32_t)n_b) >> 4;
-                    if (p.b_kmajor) {
-                        if (p.bk == 64) issue_kblock<PAIR, 4, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
-                        else issue_kblock<PAIR, 8, 1>(d, ad0, bd0, p.idesc, acc0, batom16);
-                    } else {
-                        if (p.bk == 64) issue_kblock<PAIR, 4, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16);
-                        else issue_kblock<PAIR, 8, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16);
+                    switch (variant) {
+                        case 0: issue_kblock<PAIR, 4, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16); break;
+                        case 1: issue_kblock<PAIR, 8, 0>(d, ad0, bd0, p.idesc, acc0, 0u, b_step16); break;
+                        case 2: issue_kblock<PAIR, 4, 1>(d, ad0, bd0, p.idesc, acc0, batom16); break;
+                        default: issue_kblock<PAIR, 8, 1>(d, ad0, bd0, p.idesc, acc0, batom16); break;
                     }
                     issued_any = true;
                     // stage free (in both CTAs of a pair) once these MMAs completed
