@@ -94,6 +94,11 @@ CASES = [
     ("tiny_everything", (5, 8, 8, wl.ACT_GELU_SIGMOID, wl.DT_F16, True), 1, 1, 1, None, None),
     ("geglu_pair_ln_bk128", (520, 264, 648, wl.ACT_GEGLU, wl.DT_BF16, True), 0, 1, 0, "128,2,128", None),
     ("wide_ln_reread", (40, 4096, 64, wl.ACT_GELU_ERF, wl.DT_BF16, False), 1, 1, 1, None, None),
+    # [in][out] weights whose CTA column share is an odd multiple of 32: 32-column weight
+    # boxes with 64-byte swizzle (single CTAs of 160 and 96 columns, a pair of 96 + 96)
+    ("tanh_inout_box32", (300, 352, 1000, wl.ACT_GELU_TANH, wl.DT_F16, True), 1, 0, 0, "160,1,64", "96,1,1,128"),
+    ("erf_inout_pair_box32", (520, 400, 776, wl.ACT_GELU_ERF, wl.DT_BF16, True), 0, 1, 0, "192,2,128",
+     "192,1,2,64"),
 ]
 
 
