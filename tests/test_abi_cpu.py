@@ -192,20 +192,46 @@ def test_planner_invariants_with_pytorch_order_weights(lib, name, act):
     assert info["weight_layout"] == kt_mlp.KT_W_OUT_IN
 
 
-def test_pytorch_order_weights_need_no_column_padding_in_shared_memory(lib, monkeypatch):
-    # a K-major B tile holds exactly BN / pair rows; the N-major one pads the columns
-    # of each CTA's share to whole 64-column boxes (the up projection's own ring: two launches)
+def _stage_check(g, n_b):
+    # one stage holds the CTA's 128 x BK A tile and n_b B tiles of exactly its column share
+    # (K-major: BN / pair rows; N-major: 64- or 32-column boxes, no column padded)
+    pair = g["BM"] // 128
+    share = g["BN"] // pair
+    stage = 128 * g["BK"] * 2 + n_b * share * g["BK"] * 2
+    reserve = 8 * 2048 + 512 + 2048 + 1024  # staging, barriers, bias, alignment
+    # (a second set of output staging buffers where it costs no stage)
+    assert g["smem_bytes"] - g["stages"] * stage in (reserve, reserve + 8 * 2048)
+
+
+def test_weight_tiles_need_no_column_padding_in_shared_memory(lib, monkeypatch):
+    # the planner's own choices in both weight orders (the up projection's own ring: two launches)
     monkeypatch.setenv("KT_FORCE_LAUNCHES", "2")
     for M, D, F, act in [(729, 1152, 4304, 1), (2048, 1280, 5120, 2), (8192, 640, 2560, 2)]:
         for layout in (0, 1):
             g = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, 0, False, weight_layout=layout), SMS)["up"]
-            pair = g["BM"] // 128
-            n_b = 2 if act == 2 else 1
-            share = g["BN"] // pair
-            b_cols = share if layout == 1 else -(-share // 64) * 64
-            stage = 128 * g["BK"] * 2 + n_b * b_cols * g["BK"] * 2
-            reserve = 8 * 2048 + 512 + 2048 + 1024  # staging, barriers, bias, alignment
-            assert g["smem_bytes"] == g["stages"] * stage + reserve
+            _stage_check(g, 2 if act == 2 else 1)
+
+
+@pytest.mark.parametrize("force", ["96,1,64", "160,1,128", "192,2,128", "64,2,64", "32,1,64"])
+def test_n_major_shares_of_odd_multiples_of_32_are_not_padded(lib, monkeypatch, force):
+    # column shares of 96, 160, 96, 32 and 32: 32-column boxes instead of padding to 64
+    monkeypatch.setenv("KT_FORCE_LAUNCHES", "2")
+    monkeypatch.setenv("KT_FORCE_UP", force)
+    g = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(1000, 1152, 4304, 1, 0, False), SMS)["up"]
+    assert (g["BN"], g["BM"] // 128, g["BK"]) == tuple(int(x) for x in force.split(","))
+    _stage_check(g, 1)
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+def test_one_launch_split_items_fit_one_round(lib, name):
+    # in one launch, a down projection split along K runs all its items in one round
+    w = wl.WORKLOADS[name]
+    info = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(w.M, w.D, w.F, w.act, w.dtype, w.bias,
+                                                     launches=kt_mlp.KT_LAUNCH_ONE), SMS)
+    assert info["one_launch"] == 1
+    d = info["down"]
+    if d["split_k"] > 1:
+        assert d["tiles_m"] * d["tiles_n"] * d["split_k"] <= SMS // (d["BM"] // 128)
 
 
 @pytest.mark.parametrize("M", [1, 33, 127, 128, 129, 729, 1000, 4097])
