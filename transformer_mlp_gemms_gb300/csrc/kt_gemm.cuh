@@ -1009,13 +1009,13 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 const uint32_t d = tmem_base + buf * (uint32_t)kAccSlot;
                 const int kb0 = c.kb0, kb1 = c.kb1;
                 // Descriptors of stage 0, computed once per tile: a stage's descriptors are
-                // those of stage 0 with the start address moved by the stage offset, and the
-                // K steps only move it by constant offsets (issue_kblock), so that the
-                // issuing thread's work between two k-blocks stays shorter than the MMAs the
-                // tensor pipe still has queued.  128-byte swizzle, 8-row groups 1 KB apart;
-                // N-major B: 64-column chunks bk x 128 bytes apart, or (a share that is an
-                // odd multiple of 32) 64-byte swizzle, 32-column chunks bk x 64 bytes apart,
-                // 8-row groups 512 bytes apart.  GEGLU: the gate chunks follow the value
+                // those of stage 0 with the start address moved by the stage offset (the
+                // 14-bit address field cannot carry: shared addresses stay below 256 KB), and
+                // the K steps only move it by constant offsets (issue_kblock), so that the
+                // issuing thread does little work between two k-blocks.  128-byte swizzle,
+                // 8-row groups 1 KB apart; N-major B: 64-column chunks bk x 128 bytes apart,
+                // or (a share that is an odd multiple of 32) 64-byte swizzle, 32-column
+                // chunks bk x 64 bytes apart, 8-row groups 512 bytes apart.  GEGLU: the gate chunks follow the value
                 // chunks (N-major: at the same chunk pitch; K-major: inside every 64-deep
                 // atom), one operand of 2 BN.
                 const bool b64 = !p.b_kmajor && (p.BN / PAIR) % 64 != 0;  // 32-column boxes
