@@ -29,6 +29,8 @@ CASES = [
     (SIGLIP, {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_ONE),   # one launch, down tiles split along K
     (SIGLIP, {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_TWO),   # two launches, cluster split-K
     ((2048, 1280, 5120, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_AUTO),  # pairs
+    # SDXL level 1: one launch of CTA pairs over many waves (the work counter reset by the last unit)
+    ((8192, 640, 2560, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_AUTO),
     ((300, 256, 1000, wl.ACT_SILU, wl.DT_F16, True), {"residual": True, "layernorm": True}, kt_mlp.KT_H_MEMORY,
      kt_mlp.KT_LAUNCH_AUTO),
     ((33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), {}, kt_mlp.KT_H_ON_CHIP, kt_mlp.KT_LAUNCH_AUTO),  # fused
@@ -36,7 +38,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("shape,opts,h_path,launches", CASES,
-                         ids=["siglip_one", "siglip_two", "sdxl_l2", "block", "h_on_chip"])
+                         ids=["siglip_one", "siglip_two", "sdxl_l2", "sdxl_l1_one", "block", "h_on_chip"])
 def test_graph_replay_matches_eager_runs(shape, opts, h_path, launches):
     M, D, F, act, dt, bias = shape
     res, ln = opts.get("residual", False), opts.get("layernorm", False)
