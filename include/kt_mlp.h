@@ -354,8 +354,11 @@ kt_status kt_debug_timestamp(void* dst, void* stream);
  * (cudaFree synchronises the whole device, cudaMalloc can block).
  *   H, W_down, Y : device pointers (16-byte aligned, row-major, dtype); the caller
  *                  owns them.  b_down: device pointer or NULL (no bias).
- * It runs the same kernel, with the same tile plan, as the down projection of
- * kt_mlp_run.  Instead of a plan's workspace, its split-K partials, tile counters and
+ * It runs the same kernel as the two-launch down projection of kt_mlp_run, with the
+ * tile plan the planner chooses without the cluster split-K reduction (its split-K
+ * partials go through global memory; for SigLIP's 729 x 4304 -> 1152 that plan can
+ * differ from kt_mlp_run's, which reduces inside clusters).  Instead of a plan's
+ * workspace, its split-K partials, tile counters and
  * error word live in one static device array of 16 MiB that the library holds on
  * every GPU that loads it, until the process exits.  A problem whose plan needs
  * more scratch than that is rejected with KT_ERR_UNSUPPORTED and a message giving

@@ -6,14 +6,16 @@ Tolerances, derived from the arithmetic (and stated once more in the design note
   the bar of the specification on the error of the computation, with RMS over the
   compared rows, plus the unavoidable final rounding of Y to the I/O dtype (half an
   ulp), which on its own exceeds 1e-2 * RMS for bf16 outputs beyond ~2.5 RMS.
-* H: within 1 ulp of the I/O dtype (ordered bit distance <= 1) for every element
-  whose pre-activation fp32 accumulation cannot move it further.  The GPU sums K
-  products in fp32; the classical bound |fl(sum) - sum| <= gamma_K * sum |x_k w_k|,
-  gamma_K = K u / (1 - K u), u = 2^-23 (one ulp: covers truncating adders), is
-  propagated through the activation (|gelu'| <= 1.15; GEGLU by the product rule),
-  plus 2^-20 relative for the fp32 activation itself.  An element passes if it is
-  within 1 ulp OR within ulp + that bound; and at least 99.5 % of elements must be
-  within 1 ulp outright.
+* H: within 1 ulp of the I/O dtype (ordered bit distance <= 1) wherever the GPU's
+  fp32 arithmetic cannot move the value by half an ulp, and within ``ulp + bound``
+  elsewhere.  The GPU sums K products in fp32; the classical bound
+  |fl(sum) - sum| <= gamma_K * sum |x_k w_k|, gamma_K = K u / (1 - K u), u = 2^-23
+  (one ulp: covers truncating adders), is propagated through the activation
+  (|gelu'| <= 1.15; GEGLU by the product rule), plus 2^-20 relative for the fp32
+  activation itself.  Where that bound is below half an ulp (of the spacing just below
+  |H|, the finer one at a power of two), the GPU's pre-rounding value lies within half
+  an ulp of the exact one, so the two roundings can differ by one step at most: there
+  the check is exact, with no relaxation and no tolerated fraction.
 """
 from __future__ import annotations
 
@@ -89,17 +91,28 @@ def h_bound(w, t_bits: dict, rows=None) -> np.ndarray:
 
 
 def check_h(H_gpu_bits: np.ndarray, H_oracle_bits: np.ndarray, bound: np.ndarray, dtype: int,
-            min_exact_frac: float = 0.995):
+            what: str = "H") -> dict:
+    """Check H element by element (rule above); return the distance statistics.
+
+    ``strict``: elements whose bound is below half an ulp (the rule allows them one
+    step at most); ``beyond_1ulp``: elements more than one step from the oracle
+    (each one in the relaxed region, within ulp + bound); ``max_dist``: the largest
+    ordered-bit distance.
+    """
     d = np.abs(ordered(H_gpu_bits) - ordered(H_oracle_bits))
-    within1 = d <= 1
-    frac = float(within1.mean())
     hg = oracle.decode(H_gpu_bits, dtype)
     ho = oracle.decode(H_oracle_bits, dtype)
     both_inf = np.isinf(hg) & np.isinf(ho) & (np.sign(hg) == np.sign(ho))
     err = np.where(both_inf, 0.0, np.abs(hg - ho))
-    ok = within1 | (err <= ulp(ho, dtype) + bound)
+    # spacing just below |H|: at a power of two the lower binade's (half as large)
+    fine = ulp(np.abs(ho) * (1.0 - 2.0 ** -12), dtype)
+    strict = bound < 0.5 * fine
+    within1 = d <= 1
+    ok = within1 | (~strict & (err <= ulp(ho, dtype) + bound))
     bad = np.argwhere(~ok)
-    assert bad.size == 0, (f"H: {bad.shape[0]} elements beyond 1 ulp + accumulation bound; first "
-                           f"{[(tuple(i), float(hg[tuple(i)]), float(ho[tuple(i)])) for i in bad[:5]]}")
-    assert frac >= min_exact_frac, f"H: only {frac:.5f} of elements within 1 ulp"
-    return frac
+    stats = {"elements": int(d.size), "strict": int(strict.sum()), "beyond_1ulp": int((~within1).sum()),
+             "max_dist": int(d.max()) if d.size else 0, "frac_within_1ulp": float(within1.mean()) if d.size else 1.0}
+    print(f"{what}: {stats}")
+    assert bad.size == 0, (f"{what}: {bad.shape[0]} elements beyond the rule ({stats}); first "
+                           f"{[(tuple(i), float(hg[tuple(i)]), float(ho[tuple(i)]), bool(strict[tuple(i)])) for i in bad[:5]]}")
+    return stats

@@ -3,8 +3,8 @@
 Each case draws a shape (M up to 4096, D and F multiples of 8 up to 1280 / 3000), an
 activation, a dtype, biases, the block options (LayerNorm, residual), the weight order
 and the H path (the planner's choice or H through memory), runs kt_mlp_plan_ex /
-kt_mlp_run_ex, and compares Y with the float64 oracle on sampled rows (every row for
-small M).  The planner picks its own tiles for each shape, so the cases reach tile
+kt_mlp_run_ex, and compares every element of Y, and of the rounded H where the plan
+writes H (H through memory), with the float64 oracle.  The planner picks its own tiles for each shape, so the cases reach tile
 modes (CTA pairs, BK, split-K kinds, the fused kernel) that no hand-written case pins.
 """
 import numpy as np
@@ -56,18 +56,23 @@ def test_random_problem(i):
     plan = kt_mlp.Plan(M, D, F, act, dt, bias, residual=res, layernorm=ln, weight_layout=layout, ln_eps=EPS,
                        h_path=h_path)
     Y = torch.full((M, D), float("nan"), dtype=wl.TORCH_DTYPES[dt], device="cuda")
+    h_mem = not plan.info()["h_on_chip"]
+    H = torch.full((M, F), float("nan"), dtype=wl.TORCH_DTYPES[dt], device="cuda") if h_mem else None
     plan.run_ex(d["X"], d["W_up"], d["W_down"], Y, d.get("b_up"), d.get("b_down"), d.get("R"),
-                d.get("ln_gamma"), d.get("ln_beta"))
+                d.get("ln_gamma"), d.get("ln_beta"), H_out=H)
     torch.cuda.synchronize()
     assert plan.status() == kt_mlp.KT_OK, kt_mlp.kt_last_error()
     desc = plan.describe()
     plan.close()
-    rows = None if M <= 64 else wl.sample_rows(M, 12, seed=i)
     b = {k: wl.bits(v) for k, v in t.items()}
     lnarg = (b["ln_gamma"], b["ln_beta"], EPS) if ln else None
-    _, Yx, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"), act=act, dtype=dt,
-                          rows=rows, R=b.get("R"), ln=lnarg)
-    yb = wl.bits(Y.cpu())
-    if rows is not None:
-        yb = yb[rows]
-    parity.check_y(yb, Yx, dt, what=f"Y ({desc})")
+    Ho, Yx, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"), act=act, dtype=dt,
+                           R=b.get("R"), ln=lnarg)
+    parity.check_y(wl.bits(Y.cpu()), Yx, dt, what=f"Y ({desc})")
+    if h_mem:
+        bb = dict(b)
+        if ln:  # the accumulation bound of H is that of the up projection of the normalised X
+            xn = oracle.layernorm(oracle.decode(b["X"], dt), oracle.decode(b["ln_gamma"], dt),
+                                  oracle.decode(b["ln_beta"], dt), EPS)
+            bb["X"] = oracle.encode(xn, dt)
+        parity.check_h(wl.bits(H.cpu()), Ho, parity.h_bound(w, bb), dt, what=f"H ({desc})")

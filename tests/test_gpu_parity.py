@@ -1,10 +1,11 @@
 """GPU parity: the CUDA path through the C ABI against the float64 oracle.
 
-Small shapes are compared element by element (Y and the rounded H); the full
-workload sizes, in the launch configuration the bench times, are compared on
-sampled rows (first, last, tile edges and random rows), which the oracle computes
-one by one.  Y buffers are poisoned with NaN before each run so that an
-unwritten tile cannot pass.
+Every comparison is element by element (Y and the rounded H), at small shapes and at
+the full workload sizes in the launch configuration the bench times: the oracle
+computes every row (a few seconds per workload on the host cores), so every row
+block of the one-launch work queue, of its readiness counters and of every split-K
+reduction is checked.  Y and H buffers are poisoned with NaN before each run so that
+an unwritten tile cannot pass.
 """
 import re
 
@@ -52,19 +53,19 @@ def _run(w, d, with_h=True, plan=None):
     return Y.cpu(), (H.cpu() if with_h else None)
 
 
-def _compare(w, t, Y, H, rows=None):
+def _compare(w, t, Y, H, rows=None, what=""):
     b = {k: wl.bits(v) for k, v in t.items()}
     Ho, Yx, _ = oracle.mlp(b["X"], b["W_up"], b["W_down"], b.get("b_up"), b.get("b_down"),
                            act=w.act, dtype=w.dtype, rows=rows)
     yb = wl.bits(Y)
     if rows is not None:
         yb = yb[rows]
-    parity.check_y(yb, Yx, w.dtype)
+    parity.check_y(yb, Yx, w.dtype, what=f"Y {what}")
     if H is not None:
         hb = wl.bits(H)
         if rows is not None:
             hb = hb[rows]
-        parity.check_h(hb, Ho, parity.h_bound(w, b, rows), w.dtype)
+        return parity.check_h(hb, Ho, parity.h_bound(w, b, rows), w.dtype, what=f"H {what}")
 
 
 # --------------------------------------------------------------------------
@@ -106,18 +107,34 @@ def test_shape_grid(M, D, F, act, dt, bias):
 
 
 # --------------------------------------------------------------------------
-# full workload sizes, sampled rows
+# full workload sizes, every element
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["siglip", "sdxl_l2", "sdxl_l1", "sweep_M256", "sweep_M1000", "sweep_M4096",
                                   "sweep_M16384"])
-def test_full_size_workload_sampled_rows(name):
+def test_full_size_workload_every_element(name):
     w = wl.WORKLOADS[name]
     t = wl.generate(w)
-    Y, H = _run(w, _to_dev(t))
-    rows = wl.sample_rows(w.M, 40, seed=w.seed)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    desc = plan.describe()
+    Y, H = _run(w, _to_dev(t), plan=plan)
+    plan.close()
     assert torch.isfinite(Y.float()).all(), "unwritten or non-finite Y"
-    _compare(w, t, Y, H, rows=rows)
+    stats = _compare(w, t, Y, H, what=name)
+    assert stats["elements"] == w.M * w.F, desc
+
+
+@pytest.mark.parametrize("name", ["siglip", "sweep_M256", "sweep_M1000"])
+@pytest.mark.parametrize("launches", [kt_mlp.KT_LAUNCH_ONE, kt_mlp.KT_LAUNCH_TWO])
+def test_full_size_both_launch_modes_every_element(name, launches):
+    # the small-M shapes in the launch mode the planner did not pick as well
+    w = wl.WORKLOADS[name]
+    t = wl.generate(w)
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias, launches=launches)
+    assert plan.info()["one_launch"] == (launches == kt_mlp.KT_LAUNCH_ONE)
+    Y, H = _run(w, _to_dev(t), plan=plan)
+    plan.close()
+    _compare(w, t, Y, H, what=f"{name} launches={launches}")
 
 
 # --------------------------------------------------------------------------
