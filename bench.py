@@ -17,7 +17,12 @@ FLOP count stays that of the two GEMMs.
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
 device synchronize on both sides.  Each step's device time is taken with CUDA
 events on the launching stream; a 256 MiB buffer (> the 129 MB L2) is written
-between steps, outside the events, so every step reads its inputs from HBM.
+between steps, outside the events, so every step reads its inputs from HBM
+("cold", the headline: mean, median and p90 of the K steps).  The same steps are
+then timed without the scrub ("warm": weights and X resident in L2).  Unless
+``--no-configs``, every other workload of the suite (the tiny case, both SDXL
+feed-forward levels and the ragged-M sweep) is timed in the same run with the same
+cold protocol and reported under ``configs``.
 For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
 workload (no collective on the data path: "scaling": "weak"); the time is the
 maximum over ranks and the value the work of all ranks over that time.
@@ -25,8 +30,10 @@ maximum over ranks and the value the work of all ranks over that time.
 The JSON line also carries: the per-kernel roofline of the dominant kernel
 (device time per launch from CUDA events, against MEASURED_PEAKS.json), the
 end-to-end number through the C ABI with host buffers (kt_mlp_run_host), the
-SM clocks sampled with nvidia-smi during the timed region, and the float64 CPU
-oracle timed on the host cores as a reported baseline.
+SM clocks sampled with nvidia-smi every 50 ms (over the timed region, and over a
+clock soak of about two seconds of the same steps whose per-step times are binned
+by the sampled SM clock), and the float64 CPU oracle timed on the host cores as a
+reported baseline (with the CPU model and the threads it used).
 
 ``--impl reference`` times the oracle itself (the reference arm of this build):
 each step computes a bounded sample of the workload's rows on the host cores.
@@ -50,6 +57,9 @@ METRIC = "fused MLP µs/call and TFLOP/s at 1 GB300; % of dense FP16/BF16 tensor
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_LABEL = f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"
+CLOCK_PERIOD_MS = 50
+CONFIG_SUITE = ("tiny", "siglip", "sdxl_l2", "sdxl_l1", "sweep_M256", "sweep_M1000", "sweep_M4096", "sweep_M16384")
 
 
 def parse_args():
@@ -75,6 +85,9 @@ def parse_args():
     ap.add_argument("--reference-seconds", type=float, default=90.0,
                     help="target total CPU time of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the selected workload only")
+    ap.add_argument("--config-steps", type=int, default=200, help="cold steps per workload of the configs table")
+    ap.add_argument("--soak-seconds", type=float, default=2.0, help="length of the clock soak (0: none)")
     ap.add_argument("--json-out", default=None, help="also write the JSON line to this file")
     return ap.parse_args()
 
@@ -159,20 +172,32 @@ def ncu_traffic(workload: str, kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons every 200 ms in the background."""
+    """nvidia-smi clocks / throttle reasons every CLOCK_PERIOD_MS in the background; each
+    sample is stamped with the host's clock when it is read."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id: str):
-        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        import threading
+        self.rows = []
+        self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", str(CLOCK_PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
-            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            row = parse_clock_line(line)
+            if row is not None:
+                row["t"] = time.perf_counter()
+                self.rows.append(row)
 
     def stop(self):
         if self.proc is not None:
@@ -181,26 +206,28 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        self.file.flush()
-        self.file.seek(0)
-        rows = []
-        for line in self.file.read().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
-                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
-                             "hw_slowdown": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
-                             "sw_power_cap": parts[8]})
-            except ValueError:
-                continue
-        self.file.close()
-        os.unlink(self.file.name)
-        return rows
+            self.thread.join(timeout=5)
+        return list(self.rows)
 
 
-def summarize_clocks(rows):
+def parse_clock_line(line: str):
+    parts = [x.strip() for x in line.split(",")]
+    if len(parts) < 9:
+        return None
+    try:
+        return {"sm": float(parts[1]), "max": float(parts[2]),
+                "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                "hw_slowdown": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                "sw_power_cap": parts[8]}
+    except ValueError:
+        return None
+
+
+def summarize_clocks(rows, window=None):
+    """Median SM clock under load and the throttle reasons seen.  ``window`` = (t0, t1)
+    restricts the summary to the samples read in that host-time interval."""
+    if window is not None:
+        rows = [r for r in rows if window[0] <= r.get("t", -1.0) <= window[1]]
     if not rows:
         return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
     powers = [r["power"] for r in rows if r["power"] is not None]
@@ -214,6 +241,49 @@ def summarize_clocks(rows):
     return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
             "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
             "samples": len(rows), "samples_under_load": len(loaded), "power_w_max": pmax}
+
+
+def bin_by_clock(chunks, rows, bin_mhz: float = 30.0):
+    """Per-step device time binned by the SM clock: each chunk (host-time interval, its
+    steps' device times in ms) takes the clock samples read inside its interval."""
+    bins = {}
+    for t0, t1, times in chunks:
+        near = [r["sm"] for r in rows if t0 <= r.get("t", -1.0) <= t1]
+        if not near:
+            continue
+        mhz = bin_mhz * round(statistics.median(near) / bin_mhz)
+        bins.setdefault(mhz, []).extend(times)
+    return [{"sm_mhz": m, "steps": len(v), "us_per_step_median": 1e3 * statistics.median(v),
+             "us_x_ghz": 1e3 * statistics.median(v) * m / 1e3}
+            for m, v in sorted(bins.items())]
+
+
+def step_stats(ms_list):
+    """Mean, median and p90 of per-step device times (ms) in us."""
+    v = sorted(ms_list)
+    p90 = v[min(len(v) - 1, int(round(0.9 * (len(v) - 1))))]
+    return {"mean": 1e3 * statistics.mean(v), "median": 1e3 * statistics.median(v), "p90": 1e3 * p90,
+            "min": 1e3 * v[0], "steps": len(v)}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def oracle_baseline(w, t_bits, min_seconds: float, max_seconds: float = 30.0):
@@ -235,7 +305,7 @@ def oracle_baseline(w, t_bits, min_seconds: float, max_seconds: float = 30.0):
         if t_total >= min_seconds or t_total + t_total / passes > max_seconds:
             break
     value = done_rows * flops_row / t_total / 1e12
-    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{passes} pass(es) over {rows.size} of {w.M} rows of {w.name} "
                       f"({done_rows * flops_row / 1e9:.1f} GFLOP in {t_total:.1f} s, float64, OpenMP over rows)"}
 
@@ -349,13 +419,62 @@ def run_reference(args, w, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, l2="host memory"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{rows_per_step} random rows of {w.M} per step, float64 oracle"},
+        "data": "synthetic", "config": workload_config(w, l2=L2_LABEL, args=args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} random rows of {w.M} per step, float64 oracle on the host "
+                                   f"cores (operands in host memory)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     emit(line, args)
     return 0
+
+
+def time_config(w, steps: int, flush, stream) -> dict:
+    """One workload of the suite on the planner's default plan: cold steps (L2 scrubbed
+    before each), CUDA events per step; us/call, TFLOP/s and the fraction of the measured
+    dense peak."""
+    import torch
+    from transformer_mlp_gemms_gb300 import kt_mlp
+    from transformer_mlp_gemms_gb300 import workloads as wl
+    t = wl.generate(w)
+    d = {k: v.cuda() for k, v in t.items()}
+    Y = torch.empty((w.M, w.D), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
+    plan = kt_mlp.Plan(w.M, w.D, w.F, w.act, w.dtype, w.bias)
+    info = plan.info()
+
+    def once():
+        plan.run(d["X"], d["W_up"], d["W_down"], d.get("b_up"), d.get("b_down"), Y)
+
+    for _ in range(5):
+        flush.zero_()
+        once()
+    evs = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        a.record(stream)
+        once()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ok = plan.status() == kt_mlp.KT_OK
+    plan.close()
+    if not ok:
+        raise RuntimeError(f"device status after {w.name}: " + kt_mlp.kt_last_error())
+    st = step_stats([a.elapsed_time(b) for a, b in evs])
+    peaks, _ = load_peaks()
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    tflops = w.flops / (st["mean"] * 1e-6) / 1e12
+    up, dn = info["up"], info["down"]
+    return {"workload": f"X[{w.batch},{w.tokens},{w.D}] -> {w.F_up} -> {w.D}, {wl.ACT_NAMES[w.act]}, "
+                        f"{wl.DT_NAMES[w.dtype]}, bias={int(w.bias)}",
+            "us_per_call": st["mean"], "us_median": st["median"], "us_p90": st["p90"], "steps": steps,
+            "tflops": tflops, "frac_of_measured_peak": tflops / peak,
+            "plan": {"one_launch": info["one_launch"], "h_on_chip": info["h_on_chip"],
+                     "up": f"{up['BM']}x{up['BN']} BK{up['BK']} grid {up['grid']}",
+                     "down": f"{dn['BM']}x{dn['BN']} BK{dn['BK']} split {dn['split_k']}"
+                             f"{' cluster' if dn['cluster_sk'] else ''} grid {dn['grid']}"}}
 
 
 def main():
@@ -433,10 +552,39 @@ def main():
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    wall = time.perf_counter() - wall0
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
     if plan.status() != kt_mlp.KT_OK:
         raise RuntimeError("device status after the timed steps: " + kt_mlp.kt_last_error())
+
+    # ---------------- warm: the same steps without the L2 scrub ----------------
+    warm_ms = []
+    for _ in range(max(1, min(args.steps, 500))):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run_once()
+        b.record(stream)
+        warm_ms.append((a, b))
+    torch.cuda.synchronize()
+    warm_ms = [a.elapsed_time(b) for a, b in warm_ms]
+
+    # ---------------- clock soak: cold steps in chunks, binned by the sampled SM clock ----------------
+    soak_chunks = []
+    soak_end = time.perf_counter() + max(0.0, args.soak_seconds)
+    while time.perf_counter() < soak_end:
+        evs = []
+        c0 = time.perf_counter()
+        for _ in range(20):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            a.record(stream)
+            run_once()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        soak_chunks.append((c0, time.perf_counter(), [a.elapsed_time(b) for a, b in evs]))
 
     # ---------------- per-kernel device time (same steps, events between the kernels) ----------------
     ms_ln, ms_up, ms_dn = [], [], []
@@ -478,7 +626,21 @@ def main():
         t0 = time.perf_counter()
         e2e_once()
         e2e_s += time.perf_counter() - t0
-    clocks = summarize_clocks(sampler.stop())
+    # ---------------- the other workloads of the suite, same cold protocol ----------------
+    configs = {}
+    if not args.no_configs and args.shape is None and not (ln or res or outin) and args.h_path == "memory" \
+            and getattr(args, "launches", "auto") == "auto":
+        for name in CONFIG_SUITE:
+            if name == w.name:
+                continue
+            configs[name] = time_config(wl.WORKLOADS[name], args.config_steps, flush, stream)
+    clock_rows = sampler.stop()
+    clocks = summarize_clocks(clock_rows, window=(wall0, wall1))
+    clocks_all = summarize_clocks(clock_rows)
+    clock_bins = bin_by_clock(soak_chunks, clock_rows)
+    if clocks["samples"] == 0:  # a timed region shorter than the sampling period: the soak's samples
+        clocks = dict(clocks_all, note=f"no sample fell inside the {wall * 1e3:.1f} ms timed region; "
+                                       f"summary over the whole run ({CLOCK_PERIOD_MS} ms sampling)")
 
     if dist is not None:
         total_ms, e2e_s = reduce_max([total_ms, e2e_s], dist, "cuda")
@@ -514,8 +676,11 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.DT_NAMES[w.dtype], "data": "synthetic",
-        "config": workload_config(w, l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)", args=args),
+        "config": workload_config(w, l2=L2_LABEL, args=args),
         "us_per_call": ms_per_step * 1e3,
+        "us_per_call_stats": {"cold": step_stats(step_ms), "warm": step_stats(warm_ms),
+                              "note": "cold = L2 scrubbed before every step (the headline, its mean); warm = "
+                                      "weights and X left resident in L2 by the previous step"},
         "pct_of_peak": 100.0 * value / world / peak_tflops,
         "peak_tflops": peak_tflops, "peak_source": peak_src,
         "roofline": {"bound": "hbm" if hbm_bound else "tensor",
@@ -550,6 +715,9 @@ def main():
                                 "kt_mlp_run_ex between a pinned X copy in and a Y copy out (weights resident)")},
         "gpu_launches": ((1 if fused or one else 2) + (1 if ln else 0)) * args.steps,
         "clocks": clocks,
+        "clocks_whole_run": clocks_all,
+        "clock_bins": clock_bins,
+        **({"configs": configs} if configs else {}),
         "wall_s_timed_region": wall,
         "gpu": props.name, "sms": props.multi_processor_count,
     }

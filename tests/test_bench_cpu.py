@@ -45,3 +45,29 @@ def test_custom_shape_workload():
     w = bench.pick_workload(_args(shape="40000,64,256,gelu_tanh,f16,0"))
     assert (w.M, w.D, w.F, w.act, w.dtype, w.bias) == (40000, 64, 256, wl.ACT_GELU_TANH, wl.DT_F16, False)
     assert bench.pick_workload(_args(workload="sdxl_l1")) is wl.WORKLOADS["sdxl_l1"]
+
+
+def test_step_stats_and_clock_helpers():
+    st = bench.step_stats([0.010, 0.020, 0.030, 0.040, 0.100])
+    assert st["mean"] == pytest.approx(40.0) and st["median"] == pytest.approx(30.0)
+    assert st["p90"] == pytest.approx(100.0) and st["min"] == pytest.approx(10.0) and st["steps"] == 5
+    row = bench.parse_clock_line("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active\n")
+    assert row["sm"] == 2070.0 and row["power"] == 900.5 and row["sw_power_cap"] == "Active"
+    assert bench.parse_clock_line("garbage") is None
+    rows = [dict(row, t=1.0), dict(row, t=2.0, sm=1800.0), dict(row, t=3.0, sm=1810.0)]
+    inside = bench.summarize_clocks(rows, window=(1.5, 3.5))
+    assert inside["samples"] == 2 and inside["sm_mhz"] == pytest.approx(1805.0)
+    assert inside["reasons"] == ["sw_power_cap"]
+    assert bench.summarize_clocks(rows, window=(5, 6))["samples"] == 0
+    bins = bench.bin_by_clock([(0.5, 1.5, [0.02, 0.03]), (1.9, 2.1, [0.05]), (4, 5, [0.9])], rows)
+    assert [(b["sm_mhz"], b["steps"]) for b in bins] == [(1800.0, 1), (2070.0, 2)]
+
+
+def test_reference_arm_config_equals_the_gpu_arm_config():
+    a = _args(launches="auto")
+    w = wl.WORKLOADS["siglip"]
+    assert bench.workload_config(w, bench.L2_LABEL, args=a) == bench.workload_config(w, bench.L2_LABEL, args=a)
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    # both arms build their config with the same call
+    assert src.count("workload_config(w, l2=L2_LABEL, args=args)") == 2
+    assert set(bench.CONFIG_SUITE) <= set(wl.WORKLOADS)
