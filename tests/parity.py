@@ -15,7 +15,8 @@ Tolerances, derived from the arithmetic (and stated once more in the design note
   activation itself.  Where that bound is below half an ulp (of the spacing just below
   |H|, the finer one at a power of two), the GPU's pre-rounding value lies within half
   an ulp of the exact one, so the two roundings can differ by one step at most: there
-  the check is exact, with no relaxation and no tolerated fraction.
+  the check is exact, with no relaxation.  Over all elements, at least MIN_WITHIN_1ULP
+  of them must be within one step (a floor set under the measured fractions).
 """
 from __future__ import annotations
 
@@ -62,8 +63,13 @@ def check_y(Y_gpu_bits: np.ndarray, Yx: np.ndarray, dtype: int, what: str = "Y")
     return float(err.max()) if err.size else 0.0, tol
 
 
-def h_bound(w, t_bits: dict, rows=None) -> np.ndarray:
-    """Per-element absolute bound of the fp32 accumulation error propagated to H."""
+def h_bound(w, t_bits: dict, rows=None, x_extra=None) -> np.ndarray:
+    """Per-element absolute bound of the fp32 accumulation error propagated to H.
+
+    ``x_extra`` (optional, [rows, D]): a per-element bound on how far the GPU's input of the
+    up projection may lie from the oracle's (the LayerNorm prologue's, ``ln_input_bound``);
+    its effect ``|x_extra| @ |W_up|`` joins the accumulation bound before the activation.
+    """
     x = oracle.decode(t_bits["X"], w.dtype)
     if rows is not None:
         x = x[rows]
@@ -74,6 +80,8 @@ def h_bound(w, t_bits: dict, rows=None) -> np.ndarray:
     K = w.D
     gamma = K * U32 / (1 - K * U32)
     E = gamma * S
+    if x_extra is not None:
+        E = E + oracle.linear(np.abs(x_extra), np.abs(wu))
     F = w.F
     if w.act == wl.ACT_GEGLU:
         v, g = P[:, :F], P[:, F:]
@@ -90,8 +98,45 @@ def h_bound(w, t_bits: dict, rows=None) -> np.ndarray:
     return bound + 2.0 ** -20 * np.abs(Hx)
 
 
+# The LayerNorm prologue's fp32 arithmetic: the GPU's normalised value before its one
+# rounding lies within LN_DELTA * (|gamma| (|n| + 1) + |beta|) of the exact one (n the
+# normalised value before gamma and beta): four times the fp32 error of the affine step's
+# operands, 2^-20 (|gamma| (|n| + 1) + |beta|).
+LN_DELTA = 2.0 ** -18
+
+
+def ln_input_bound(x_bits, gamma_bits, beta_bits, eps: float, dtype: int):
+    """The oracle's rounded LayerNorm output and a per-element bound on the GPU's distance
+    from it.  An element whose exact value lies farther than the GPU's fp32 error from a
+    rounding boundary rounds the same way on both sides (bound 0); one within that error of
+    a boundary ("ambiguous") may round to the neighbour: bound ulp + that error."""
+    x = oracle.decode(x_bits, dtype)
+    g, b = oracle.decode(gamma_bits, dtype), oracle.decode(beta_bits, dtype)
+    exact = oracle.layernorm(x, g, b, eps)
+    n = oracle.layernorm(x, np.ones_like(g), np.zeros_like(b), eps)
+    xn_bits = oracle.encode(exact, dtype)
+    r = oracle.decode(xn_bits, dtype)
+    delta = LN_DELTA * (np.abs(g) * (np.abs(n) + 1.0) + np.abs(b))
+    fine = ulp(np.abs(r) * (1.0 - 2.0 ** -12), dtype)  # the finer spacing at a power of two
+    to_boundary = 0.5 * fine - np.abs(exact - r)
+    ambiguous = to_boundary <= delta
+    return xn_bits, np.where(ambiguous, ulp(r, dtype) + delta, 0.0), ambiguous
+
+
+# The classical bound is a worst case (every rounding error of the K-term sum adding up);
+# at the workloads' K (1152-4304) it exceeds half an ulp of H for almost every element, so
+# it leaves most of them in the relaxed region.  Measured fractions of elements within one
+# step, every element of the full-size workloads: 0.99957 (SigLIP, f16) to 0.99975 (bf16
+# SDXL); with the LayerNorm prologue, whose fp32 statistics move a few normalised inputs by
+# one step, 0.99870 (SigLIP block, f16) to 0.99951 (bf16).  The floor keeps a margin under
+# the lowest; a handful of elements (MIN_WITHIN_1ULP_SLACK) is allowed on top, for problems
+# too small for a fraction to mean anything.
+MIN_WITHIN_1ULP = 0.998
+MIN_WITHIN_1ULP_SLACK = 4
+
+
 def check_h(H_gpu_bits: np.ndarray, H_oracle_bits: np.ndarray, bound: np.ndarray, dtype: int,
-            what: str = "H") -> dict:
+            what: str = "H", min_within_1ulp: float = MIN_WITHIN_1ULP) -> dict:
     """Check H element by element (rule above); return the distance statistics.
 
     ``strict``: elements whose bound is below half an ulp (the rule allows them one
@@ -115,4 +160,5 @@ def check_h(H_gpu_bits: np.ndarray, H_oracle_bits: np.ndarray, bound: np.ndarray
     print(f"{what}: {stats}")
     assert bad.size == 0, (f"{what}: {bad.shape[0]} elements beyond the rule ({stats}); first "
                            f"{[(tuple(i), float(hg[tuple(i)]), float(ho[tuple(i)]), bool(strict[tuple(i)])) for i in bad[:5]]}")
+    assert stats["beyond_1ulp"] <= (1.0 - min_within_1ulp) * d.size + MIN_WITHIN_1ULP_SLACK, f"{what}: {stats}"
     return stats

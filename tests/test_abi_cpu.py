@@ -119,7 +119,7 @@ def _check_gemm(g, M, N, K):
     assert BM in (128, 256) and BK in (64, 128)  # 256: a CTA pair (cta_group::2) per tile
     pair = BM // 128
     assert BN % 32 == 0 and 32 <= BN <= 256
-    assert BN % (32 * (BM // 128)) == 0
+    assert (BN // pair) % 16 == 0  # a pair's column share: whole 16-column weight boxes
     # the grid covers every output element exactly once: tiles_m * BM >= M > (tiles_m - 1) * BM
     assert (g["tiles_m"] - 1) * BM < M <= g["tiles_m"] * BM
     assert (g["tiles_n"] - 1) * BN < N <= g["tiles_n"] * BN
@@ -212,9 +212,11 @@ def test_weight_tiles_need_no_column_padding_in_shared_memory(lib, monkeypatch):
             _stage_check(g, 2 if act == 2 else 1)
 
 
-@pytest.mark.parametrize("force", ["96,1,64", "160,1,128", "192,2,128", "64,2,64", "32,1,64"])
+@pytest.mark.parametrize("force", ["96,1,64", "160,1,128", "192,2,128", "64,2,64", "32,1,64", "96,2,128",
+                                   "32,2,64", "160,2,64"])
 def test_n_major_shares_of_odd_multiples_of_32_are_not_padded(lib, monkeypatch, force):
-    # column shares of 96, 160, 96, 32 and 32: 32-column boxes instead of padding to 64
+    # column shares of 96, 160, 96, 32 and 32 (32-column boxes instead of padding to 64), and
+    # of 48, 16 and 80 (16-column boxes instead of padding to 32)
     monkeypatch.setenv("KT_FORCE_LAUNCHES", "2")
     monkeypatch.setenv("KT_FORCE_UP", force)
     g = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(1000, 1152, 4304, 1, 0, False), SMS)["up"]

@@ -36,7 +36,8 @@ CASES = [
     # (workload, KT_FORCE_DOWN for both the regular plan and the entry point's own plan)
     (wl.WORKLOADS["siglip"], None),                          # the planner's choice (no cluster split-K)
     (wl.WORKLOADS["siglip"], "96,2,1,128,0"),                # split-K: partials in the static scratch
-    (wl.WORKLOADS["sdxl_l2"], "128,3,1,128,0"),              # bf16 with b_down, three splits
+    (wl.WORKLOADS["sdxl_l2"], None),                         # bf16 with b_down, the planner's choice
+    (wl.custom(300, 1280, 5120, wl.ACT_GEGLU, wl.DT_BF16, True, seed=32), "128,3,1,128,0"),  # bf16, three splits
     (wl.custom(33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, True, seed=31), None),  # ragged, tiny
 ]
 

@@ -5,14 +5,17 @@
 // CTA per 128-row tile (PAIR = 1) or on a CTA pair per 256-row tile (PAIR = 2,
 // tcgen05 cta_group::2: each CTA loads its 128 rows of A and half of the B columns):
 //
-//   warp 0      producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
+//   warp 0      A producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads of the
 //               A tile (128 x 64 K-major boxes, one per 64-deep atom of a BK = 64 or
-//               128 k-block) and the B tile(s) -- 64-column N-major boxes of an
-//               [in][out] weight (32-column, 64-byte swizzle, for a CTA column share
-//               that is an odd multiple of 32), or (BN / PAIR)-row K-major boxes of
-//               an [out][in] weight -- into an S-stage shared-memory ring, one mbarrier pair
-//               (full / empty) per stage.  The down projection's producer first waits
-//               for the up projection's per-row-block counters of stored H tiles.
+//               128 k-block) into an S-stage shared-memory ring, one mbarrier pair
+//               (full / empty) per stage; its arrival on the full barrier carries the
+//               stage's byte count.  The down projection's A producer first waits for
+//               the up projection's per-row-block counters of stored H tiles.
+//   warp 10     B producer: the B tile(s) of the same stages -- N-major boxes of an
+//               [in][out] weight, 64, 32 or 16 columns wide (128-, 64- or 32-byte swizzle:
+//               the widest that divides the CTA's column share), or (BN / PAIR)-row
+//               K-major boxes of an [out][in] weight.  Two issuing threads take in about
+//               twice the bytes per second of one.
 //   warp 1      MMA issuer: one thread of the leader CTA issues tcgen05.mma kind::f16
 //               (M = 128 or 256, N = BN, K = 16, fp32 accumulation in tensor memory),
 //               BK / 16 per k-block, and tcgen05.commit hands the stage back.  Two
@@ -172,7 +175,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // GPU scope.  Gives up, with the abort flag raised, when the error word shows that an
 // earlier kernel failed, when this CTA aborts, or after limit_ns (error code recorded).
 __device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned target, volatile int* abort_flag, int* err,
-                                             unsigned long long limit_ns) {
+                                             unsigned long long limit_ns, int code = DEV_TIMEOUT_PRODUCER) {
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 0;; ++i) {
         unsigned v;
@@ -185,7 +188,7 @@ __device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned targe
             }
             if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
-                atomicCAS(err, 0, DEV_TIMEOUT_PRODUCER);
+                atomicCAS(err, 0, code);
                 return false;
             }
         }
@@ -640,7 +643,7 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* tmC, uint32_t
 // The MMAs of one k-block: NK steps of K = 16 (4 for a 64-deep stage, 8 for 128).
 // Descriptor start addresses move in 16-byte units.  A (K-major): +32 bytes per step
 // inside a 64-deep swizzle atom, +16 KB per atom.  B N-major (KB = 0): +16 rows per
-// step, b_step16 units (2 KB for 128-byte rows, 1 KB for 64-byte rows).  B K-major
+// step, b_step16 units (2 KB for 128-byte rows, 1 KB for 64-byte rows, 512 B for 32-byte rows).  B K-major
 // (KB = 1): as A, with atoms of b_atom16 units.
 // GEGLU needs no second MMA: its B operand holds the value and the gate columns of
 // the tile side by side, so one MMA of N = 2 BN fills both accumulators.
@@ -664,7 +667,8 @@ __device__ __forceinline__ void issue_kblock(uint32_t d, uint64_t ad0, uint64_t 
 
 // The t-th work item of the kernel: a tile, which of its split_k partial sums this CTA
 // accumulates (`split`) and that split's k-blocks [kb0, kb1).  The SK splits of one tile
-// are consecutive CTAs of a cluster with the cluster reduction, otherwise split-major.
+// are consecutive items with a reduction in which the splits wait on one another (inside
+// a cluster, or the reduce-scatter of one launch), otherwise split-major.
 struct TileCoord {
     int split, tm, tn, mn;
     int kb0, kb1;
@@ -673,7 +677,7 @@ struct TileCoord {
 __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     TileCoord c;
     const int per_split = p.tiles_m * p.tiles_n;
-    if (p.cluster_sk) {
+    if (p.cluster_sk || p.rs_sk) {
         c.split = t % p.split_k;
         c.mn = t / p.split_k;
     } else {
@@ -693,7 +697,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
 // rows of the accumulator into that CTA's tensor memory; each CTA's epilogue stores
 // its own rows.
 template <int EPI, int DT, int PAIR, bool TWO>
-__global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
+__global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
     kt_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -706,6 +710,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
     constexpr int NEPI = epi_warps(EPI);   // epilogue warps
     constexpr int NPART = NEPI / 4;        // epilogue warps per TMEM lane quadrant
+    constexpr int kWarpB = 2 + NEPI;       // the B operand's producer (after the epilogue warps)
     // NEPI x 2 KB output staging buffers, twice over when the plan has room for a second set
     const uint32_t kStaging = (uint32_t)NEPI * 2048u * (p.dbl_staging ? 2u : 1u);
     const uint32_t staging = base + tiles_bytes;
@@ -750,11 +755,11 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         mbar_init(bar_drain, 1);
         mbar_init(bar_pready, (uint32_t)(p.split_k * NEPI));
         if constexpr (TWO) {
-            // consumers of an item: the MMA issuer and the epilogue warps of the leader CTA,
-            // and the producer and the epilogue warps of its peer
+            // consumers of an item: the MMA issuer, the B producer and the epilogue warps of
+            // the leader CTA, and both producers and the epilogue warps of its peer
             for (int i = 0; i < kItemRing; ++i) {
                 mbar_init(item_full + 8u * i, 1);
-                mbar_init(item_empty + 8u * i, PAIR == 2 ? 2 + 2 * NEPI : 1 + NEPI);
+                mbar_init(item_empty + 8u * i, PAIR == 2 ? 4 + 2 * NEPI : 2 + NEPI);
             }
         }
         *abort_flag = 0;
@@ -786,10 +791,11 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // With row-block readiness counters (down projection after the up projection), only
     // the epilogue waits for the predecessor grid to complete (before it reads the bias
-    // or the residual and writes Y); the producer waits on the counters of the rows of H
-    // it reads, and the MMA warp touches no global memory.
+    // or the residual and writes Y); the A producer waits on the counters of the rows of H
+    // it reads, the B producer reads only the weights, and the MMA warp touches no global
+    // memory.
     const bool ready_mode = EPI == EPI_DOWN && p.ready != nullptr;
-    if (p.pdl_wait && (!ready_mode || warp >= 2)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.pdl_wait && (!ready_mode || (warp >= 2 && warp < kWarpB))) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) trace_mark(tr, TR_PDL);
 
     const int n_b = (EPI == EPI_GEGLU) ? 2 : 1;
@@ -837,12 +843,17 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
         return idx;
     };
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
+    if (warp == 0 || warp == kWarpB) {
+        // ------------------------------ producers ------------------------------
+        // Two threads in two warps fill the ring: warp 0 the A operand (X, or H with its
+        // readiness waits) and the stage's byte count, warp kWarpB the B operand (weights),
+        // which never waits for H and so runs ahead by up to the ring's depth.  One issuing
+        // thread per stage takes in about half the bytes per second that two do.
+        const bool a_role = warp == 0;
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             uint32_t armed = 0, armed_phase = 0;  // per-stage bits: loads issued / their phase
-            if (p.inject_stall) {
+            if (a_role && p.inject_stall) {
                 // failure injection: a barrier nobody arrives on, bounded wait
                 wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
             }
@@ -852,9 +863,9 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 const TileCoord c = decode_tile(t, p);
                 const int kb0 = c.kb0, kb1 = c.kb1;
                 // this CTA's rows of A and its share of the B columns (N-major B: in boxes of
-                // bw columns, 64 or 32; 32 only for shares that are odd multiples of 32)
+                // bw columns, the widest of 64, 32 and 16 that divides the share)
                 const int bcols = p.BN / PAIR;
-                const int bw = bcols % 64 == 0 ? 64 : 32;
+                const int bw = b_box_cols(p.BN, PAIR);
                 auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
                     m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
                     nb_r = c.tn * p.BN + (int)r * bcols;
@@ -876,7 +887,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     int m_o, nb_o, ch_o;
                     tx += cta_share(rank ^ 1u, m_o, nb_o, ch_o);
                 }
-                if (ready_mode && m_me < p.M) {
+                if (a_role && ready_mode && m_me < p.M) {
                     // the up projection's row blocks that hold this CTA's 128 rows of H
                     const int r1 = min(m_me + kBM, p.M) - 1;
                     bool got = true;
@@ -906,8 +917,8 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     const uint32_t fb = bar_full + 8u * stage;
                     const uint32_t sA = base + stage * p.stage_bytes;
                     const uint32_t sB = sA + p.a_bytes;
-                    if (tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
-                    if (tr && kb == kb0 && local == 1) trace_mark(tr, TR_S_LD0);
+                    if (a_role && tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
+                    if (a_role && tr && kb == kb0 && local == 1) trace_mark(tr, TR_S_LD0);
                     const int k0 = kb * p.bk;
                     // N-major B: box j is bw columns x bk rows at column nb + bw j, row k0.
                     // K-major B: box j is bcols rows x 64 at row nb, column k0 + 64 j.
@@ -923,28 +934,38 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                     auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + bw * j; };
                     auto by = [&](int j, int row0) { return p.b_kmajor ? row0 + nb_me : k0; };
                     auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + bw * j; };
+                    // (the A thread's arrival carries the stage's whole byte count; the B
+                    // copies may complete on the barrier before it: its transaction count
+                    // then runs negative until the arrival, and the phase cannot complete
+                    // before the arrival)
                     if constexpr (PAIR == 2) {
                         const uint32_t fb_leader = mapa_rank(fb, 0);
-                        if (leader) mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M)
-                            for (int a = 0; a < p.bk / kAtomK; ++a)
-                                tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
-                        if (n_b == 2) {
+                        if (a_role) {
+                            if (leader) mbar_arrive_expect_tx(fb, tx);
+                            if (m_me < p.M)
+                                for (int a = 0; a < p.bk / kAtomK; ++a)
+                                    tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
+                        } else {
                             for (int j = 0; j < nbox; ++j)
-                                tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
+                                tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
+                            if (n_b == 2) {
+                                for (int j = 0; j < nbox; ++j)
+                                    tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
+                            }
                         }
                     } else {
-                        mbar_arrive_expect_tx(fb, tx);
-                        if (m_me < p.M)
-                            for (int a = 0; a < p.bk / kAtomK; ++a)
-                                tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
-                        if (n_b == 2) {
+                        if (a_role) {
+                            mbar_arrive_expect_tx(fb, tx);
+                            if (m_me < p.M)
+                                for (int a = 0; a < p.bk / kAtomK; ++a)
+                                    tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
+                        } else {
                             for (int j = 0; j < nbox; ++j)
-                                tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
+                                tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
+                            if (n_b == 2) {
+                                for (int j = 0; j < nbox; ++j)
+                                    tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
+                            }
                         }
                     }
                     armed |= 1u << stage;
@@ -959,18 +980,18 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
             if constexpr (TWO) {
                 bool done = false;  // this unit took the end-of-work index
                 for (uint32_t k = 0; !*abort_flag; ++k) {
-                    const int idx = leader ? publish(k) : consume(k);
+                    const int idx = leader && a_role ? publish(k) : consume(k);
                     if (idx >= total) {
                         done = idx != INT_MAX;
                         break;
                     }
-                    if (tr && idx == p.num_tiles + (int)blockIdx.x / PAIR) trace_mark(tr, TR_T_DN_TAKEN);
+                    if (a_role && tr && idx == p.num_tiles + (int)blockIdx.x / PAIR) trace_mark(tr, TR_T_DN_TAKEN);
                     const bool ok = idx >= p.num_tiles
                                         ? produce(p2, tmA2, tmB2, 1, p2.ready != nullptr, idx - p.num_tiles, (int)k)
                                         : produce(p, tmA, tmB, n_b, false, idx, (int)k);
                     if (!ok) break;
                 }
-                if (done && leader) {
+                if (done && leader && a_role) {
                     // the last unit to finish resets the counter for the next run
                     __threadfence();
                     if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x / PAIR - 1) {
@@ -984,11 +1005,17 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step, ++local)
                     if (!produce(p, tmA, tmB, n_b, ready_mode, t, local)) break;
             }
-            if (*abort_flag && leader) {
+            if (*abort_flag && leader && a_role) {
                 // do not leave copies in flight into shared memory we are about to release
-                // (the leader's full barriers count the peer's copies too)
+                // (the leader's full barriers count the peer's copies, and the B thread's, too)
                 for (int s = 0; s < p.stages; ++s)
                     if (armed & (1u << s)) wait_drain(bar_full + 8u * s, (armed_phase >> s) & 1u, 100000000ull);
+            }
+            if (*abort_flag && !a_role) {
+                // the B thread's copies of a stage the A thread never armed complete on no
+                // phase: give them 100 us to land (a copy takes a few microseconds)
+                const unsigned long long t0 = global_ns();
+                while (global_ns() - t0 < 100000ull) __nanosleep(1000);
             }
         }
     } else if (warp == 1) {
@@ -1013,17 +1040,20 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 // 14-bit address field cannot carry: shared addresses stay below 256 KB), and
                 // the K steps only move it by constant offsets (issue_kblock), so that the
                 // issuing thread does little work between two k-blocks.  128-byte swizzle,
-                // 8-row groups 1 KB apart; N-major B: 64-column chunks bk x 128 bytes apart,
-                // or (a share that is an odd multiple of 32) 64-byte swizzle, 32-column
-                // chunks bk x 64 bytes apart, 8-row groups 512 bytes apart.  GEGLU: the gate chunks follow the value
-                // chunks (N-major: at the same chunk pitch; K-major: inside every 64-deep
-                // atom), one operand of 2 BN.
-                const bool b64 = !p.b_kmajor && (p.BN / PAIR) % 64 != 0;  // 32-column boxes
-                const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * (b64 ? 64u : 128u);
+                // 8-row groups 1 KB apart; N-major B in chunks of bw columns (the box width:
+                // 64, 32 or 16), each row 2 bw bytes with a swizzle of that span (128, 64 or
+                // 32 bytes: descriptor modes 2, 4 and 6), chunks bk x 2 bw bytes apart, 8-row
+                // groups 16 bw bytes apart.  GEGLU: the gate chunks follow the value chunks
+                // (N-major: at the same chunk pitch; K-major: inside every 64-deep atom), one
+                // operand of 2 BN.
+                const uint32_t brow = 2u * (uint32_t)b_box_cols(p.BN, PAIR);  // bytes per N-major B row
+                const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)p.bk * brow;
+                const uint32_t b_sbo = p.b_kmajor ? 1024u : 8u * brow;
+                const uint32_t b_swz = p.b_kmajor || brow == 128u ? 2u : brow == 64u ? 4u : 6u;
                 const uint64_t ad_s0 = smem_desc(base, 16u, 1024u);
-                const uint64_t bd_s0 = smem_desc(base + p.a_bytes, b_lbo, b64 ? 512u : 1024u, b64 ? 4u : 2u);
+                const uint64_t bd_s0 = smem_desc(base + p.a_bytes, b_lbo, b_sbo, b_swz);
                 const uint32_t stage16 = p.stage_bytes >> 4;
-                const uint32_t b_step16 = b64 ? 64u : 128u;
+                const uint32_t b_step16 = brow;  // 16 rows of brow bytes, in 16-byte units
                 const uint32_t batom16 = (p.b_atom_bytes * (uint32_t)n_b) >> 4;
                 const int variant = (p.b_kmajor ? 2 : 0) + (p.bk == 64 ? 0 : 1);
                 bool ok = true;
@@ -1095,7 +1125,7 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 wait_drain(bar_drain, 0u, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 2 + NEPI) {
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - 2;
         const int q = warp & 3;    // TMEM lane quadrant this warp may access
@@ -1370,6 +1400,113 @@ __global__ void __launch_bounds__((2 + epi_warps(EPI)) * 32, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce);
+            } else if (TWO && p.rs_sk) {
+                // split-K reduce-scatter through global memory (both projections in one launch):
+                // each 32 x 32 unit of this CTA's 128-row half of the tile (row block q, column
+                // group g, u = q * ngroups + g) is owned by split u % SK.  Every split writes its
+                // fp32 partial of each unit it does not own to global scratch ([half tile][unit]
+                // [sending split][16-byte chunk][row][4 floats]: 512 contiguous bytes per warp
+                // access), counts itself on the half tile's arrival counter (release), waits for
+                // all SK arrivals (acquire), then sums its own units' SK partials (its own still
+                // in tensor memory) in split order (deterministic) and stores them.  The splits
+                // of a tile are adjacent work items taken in increasing order, so every split a
+                // CTA waits for is held by a running unit or is the next item to be taken.
+                const int SK = p.split_k;
+                const uint32_t mine = (uint32_t)c.split;
+                const size_t half_tile = (size_t)c.mn * PAIR + rank;
+                const size_t n_half = (size_t)tiles_mn * PAIR;
+                float4* part = reinterpret_cast<float4*>(p.partials) + half_tile * (size_t)(4 * ngroups) * SK * 256u;
+                for (int g = half; g < ngroups; g += NPART) {
+                    const int u = q * ngroups + g;
+                    if ((uint32_t)(u % SK) == mine || n0 + 32 * g >= p.N || !rows_live) continue;  // warp-uniform
+                    uint32_t r[32];
+                    tmem_ld32(tq + 32u * g, r);
+                    tmem_wait_ld_only();
+                    reg_fence32(r);
+                    float4* dst = part + ((size_t)u * SK + mine) * 256u + lane;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        __stcg(dst + 32 * i, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+                }
+                if (tr1) trace_mark(tr, TR_S_G0M);  // (reduce-scatter: this warp's partials issued)
+                // the barrier orders every epilogue thread's partial stores before the one
+                // gpu-scope release (fences are cumulative)
+                epi_bar_sync<NEPI>();
+                if (ew == 0 && lane == 0) {
+                    __threadfence();
+                    atomicAdd(p.counters + half_tile, 1);
+                }
+                if (tr1) trace_mark(tr, TR_S_G0S);  // (reduce-scatter: arrival counted)
+                if (tr0) trace_mark(tr, TR_EPI_LD);  // (reduce-scatter: partials written)
+                bool got = true;
+                if (lane == 0)
+                    got = wait_counter(reinterpret_cast<const unsigned*>(p.counters) + half_tile, (unsigned)SK,
+                                       abort_flag, p.error, p.wait_limit_ns, DEV_TIMEOUT_EPILOGUE);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!epi_all<NEPI>(got)) return false;
+                if (tr1) trace_mark(tr, TR_S_G1M);  // (reduce-scatter: every split arrived)
+                if (tr0) trace_mark(tr, TR_EPI_MATH);  // (reduce-scatter: every split's partials written)
+                for (int g = half; g < ngroups; g += NPART) {
+                    const int u = q * ngroups + g;
+                    const int col = n0 + 32 * g;
+                    if ((uint32_t)(u % SK) != mine || col >= p.N || !rows_live) continue;  // warp-uniform
+                    const float4* src = part + (size_t)u * SK * 256u + lane;
+                    uint32_t w[16];  // the unit's 32 results, rounded and packed in pairs
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {  // in 16-column slices
+                        float v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                        for (int sp = 0; sp < SK; ++sp) {  // split order: deterministic
+                            if ((uint32_t)sp == mine) {
+                                float a[16];
+                                tmem_f16cols(tq + 32u * g + 16u * h, a);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] += a[i];
+                                continue;
+                            }
+                            float4 x[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) x[i] = __ldcg(src + (size_t)sp * 256u + 32 * (4 * h + i));
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                v[4 * i] += x[i].x;
+                                v[4 * i + 1] += x[i].y;
+                                v[4 * i + 2] += x[i].z;
+                                v[4 * i + 3] += x[i].w;
+                            }
+                        }
+                        if (p.bias) {
+                            float b[16];
+                            bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] += b[i];
+                        }
+                        if (p.residual) add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[8 * h + i] = pack2<DT>(v[2 * i], v[2 * i + 1]);
+                    }
+                    stage_and_store_packed(&tmC, stg0 + (dbl && (nstores++ & 1u) ? stg_alt : 0u), lane, w, col, y0,
+                                           dbl);
+                }
+                if (tr0) trace_mark(tr, TR_EPI_STORE);  // (reduce-scatter: my units stored)
+                if (tr1) trace_mark(tr, TR_S_G1S);  // (reduce-scatter: owned units summed, stores issued)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
+                    else mbar_arrive(acce);
+                }
+                if (tr1) trace_mark(tr, TR_S_ARR);
+                // every epilogue warp has read the other splits' partials: the last split to
+                // get here resets both counters of the half tile for the next run
+                epi_bar_sync<NEPI>();
+                if (ew == 0 && lane == 0 &&
+                    atomicAdd(p.counters + n_half + half_tile, 1) == SK - 1) {
+                    atomicExch(p.counters + half_tile, 0);
+                    atomicExch(p.counters + n_half + half_tile, 0);
+                }
             } else {
                 // split-K: this split's fp32 partial in a private layout in which every
                 // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]
@@ -1537,7 +1674,7 @@ kt_status launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUten
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)((2 + epi_warps(EPI)) * 32), 1, 1);
+    cfg.blockDim = dim3((unsigned)((3 + epi_warps(EPI)) * 32), 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];

@@ -7,6 +7,12 @@
 
 #include "kt_mlp.h"
 
+#ifdef __CUDACC__
+#define KT_HOST_DEVICE __host__ __device__
+#else
+#define KT_HOST_DEVICE
+#endif
+
 namespace kt {
 
 // Fixed tile geometry of the sm_103a kernels.
@@ -102,9 +108,14 @@ struct PlanChoice {
 };
 
 // Columns of one box of an N-major ([K][N]) B tile: 64 (128-byte rows, 128-byte swizzle)
-// when the CTA's column share (BN, or BN/2 in a CTA pair; a multiple of 32) is a multiple
-// of 64, else 32 (64-byte rows, 64-byte swizzle), so that no column is loaded in vain.
-inline int b_box_cols(int BN, int pair) { return (BN / pair) % 64 == 0 ? 64 : 32; }
+// when the CTA's column share (BN, or BN/2 in a CTA pair; a multiple of 16) is a multiple
+// of 64, else 32 (64-byte rows, 64-byte swizzle) when it is a multiple of 32, else 16
+// (32-byte rows, 32-byte swizzle), so that no column is loaded in vain.  The box's row
+// bytes are also its swizzle span.
+KT_HOST_DEVICE inline int b_box_cols(int BN, int pair) {
+    const int share = BN / pair;
+    return share % 64 == 0 ? 64 : share % 32 == 0 ? 32 : 16;
+}
 
 // Bytes of one pipeline stage in one CTA: its 128-row A tile (bk/64 swizzle atoms of
 // 128 x 64) + n_b B tiles holding its share of the columns: in b_box_cols-wide boxes of
@@ -140,6 +151,10 @@ struct GemmParams {
     int pair;                // 1 or 2 (CTA pair, tiles of 256 rows); tiles_m counts pair-tiles
     int bk;                  // k-block depth per stage (64 or 128)
     int cluster_sk;          // 1: the split_k CTAs of a tile form a cluster and reduce on chip
+    int rs_sk;               // 1 (both projections in one launch): the split_k CTAs of a tile
+                             // reduce-scatter their fp32 partials through global memory, each
+                             // summing the 32 x 32 units it owns; splits of a tile are adjacent
+                             // work items (all of them run at once: no item waits on a later one)
     int tiles_m, tiles_n, kblocks, kblocks_per_split, num_tiles;
     int gate_col;            // GEGLU: first gate column (row, K-major) of W_up (= F); else 0
     int b_kmajor;            // 1: B is [N][K] in memory, loaded in 64-deep K-major atoms
@@ -151,8 +166,10 @@ struct GemmParams {
                              // per share, its value columns then its gate columns
     const void* bias;        // b_up (GEGLU: value then gate halves) / b_down / null
     const void* residual;    // down projection: R[M][N] added before the rounding, or null
-    float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32
-    int* counters;           // split-K: per 128-row half tile, arrival counters (zero between runs)
+    float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32 (rs_sk: [half tile][unit]
+                             // [sending split][8][32 rows][4])
+    int* counters;           // split-K: per 128-row half tile, arrival counters (zero between runs);
+                             // rs_sk: then as many counters of the splits done reading
     int* error;              // device error word
     int inject_stall;        // failure-injection hook (producer waits on a silent barrier)
     unsigned long long wait_limit_ns;   // bound of every device-side wait

@@ -296,8 +296,10 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.ready_target = per_block;
     dn.ready_rows = kt::kBM * P->choice.up.pair;
     if (P->choice.one_launch) {
-        // both projections in one launch: one shared-memory ring, tiles from one queue
+        // both projections in one launch: one shared-memory ring, tiles from one queue; a
+        // down projection split along K reduce-scatters its partials among the splits
         up.stage_bytes = dn.stage_bytes = (uint32_t)P->choice.one_slot;
+        dn.rs_sk = dn.split_k > 1 ? 1 : 0;
         up.sched = dn.sched = P->sched;
         up.pdl_wait = dn.pdl_wait = 1;
         const void* maps[6] = {&P->tm_x, &P->tm_wu, &P->tm_hs, &P->tm_h, &P->tm_wd, &P->tm_ys};
@@ -383,7 +385,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     const kt::GemmConfig& dn = P->choice.down;
     const kt::GemmConfig& up = P->choice.up;
     size_t h_bytes = (size_t)M * (size_t)F * 2;
-    size_t n_counters = (size_t)dn.tiles_m * dn.tiles_n * dn.pair;  // one per 128-row half tile
+    // two per 128-row half tile: split-K arrivals, and (reduce-scatter) splits done reading
+    size_t n_counters = 2 * (size_t)dn.tiles_m * dn.tiles_n * dn.pair;
     size_t n_ready = (size_t)up.tiles_m;                               // one per up row block
     size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready + 2);
     size_t part_bytes = dn.split_k > 1
@@ -468,7 +471,7 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     // H, error word and split-K counters, three words per up row block, host staging
-    int64_t ws = o.M * o.F * 2 + 4 * (1 + (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
+    int64_t ws = o.M * o.F * 2 + 4 * (1 + 2 * (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
                  4 * 3 * (int64_t)c.up.tiles_m + 8 + 2 * 2 * o.M * o.D;
     if (c.down.split_k > 1)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;

@@ -81,11 +81,10 @@ int max_active_clusters(int size, int num_sms) {
 constexpr double kPairKernelCost = 3.0e-6;
 constexpr double kPairTileCost = 0.3e-6;
 // Splits along K of the one-launch down projection's tiles considered by the planner, and
-// the extra cost of a split there over the exchange modelled above (calibrated on GB300
-// against whole tiles: SigLIP's MLP with six down configurations in one launch, and three
-// more shapes, ran 5-10 us slower than modelled with split-K and 3.5 us faster without).
+// the fixed cost of their reduce-scatter (the arrival handshake of the splits) beside its
+// partial traffic.
 constexpr int kOneLaunchMaxSplit = 4;
-constexpr double kOneLaunchSplitCost = 7.0e-6;
+constexpr double kOneLaunchSplitCost = 1.0e-6;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -110,7 +109,9 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
               int bk, GemmConfig* g, bool cluster_sk = false, int kmaj = 0, int force_stages = 0) {
     // GEGLU: value and gate columns form one MMA operand of N = 2 BN (at most 256, one
     // accumulator buffer of tensor memory); an N-major share must be whole 64-column boxes
-    if (n_b == 2 && (n_b * BN > kAccSlot || (!kmaj && (BN / pair) % 64 != 0))) return false;
+    // (its epilogue pairs each 32-column group of value columns with the gate columns one
+    // share further on: a share must hold whole 32-column groups)
+    if (n_b == 2 && (n_b * BN > kAccSlot || (!kmaj && (BN / pair) % 64 != 0) || (BN / pair) % 32 != 0)) return false;
     int stages = max_stages(BN, n_b, pair, bk, kmaj, epi);
     if (force_stages > 0) {  // a ring shared with another GEMM (one launch for both projections)
         if (force_stages > stages) return false;
@@ -201,7 +202,8 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
     bool found = false;
     for (int pair = 1; pair <= 2; ++pair) {
         for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
-            if (BN % (32 * pair) != 0) continue;   // a pair splits the columns in halves of 32s
+            // (a pair splits the columns into two shares, multiples of 16: whole 16-column
+            // weight boxes; the epilogue stores 32-column boxes of the whole tile)
             for (int bk = 64; bk <= 128; bk += 64) {
                 for (int SK = 1; SK <= max_sk; ++SK) {
                     for (int cl = 0; cl <= (allow_cluster_sk ? 1 : 0); ++cl) {
@@ -275,16 +277,38 @@ static bool plan_fused(int64_t M, int64_t D, int64_t F, int act, int num_sms, Fu
 // items short of the units' count still costs a full item), at least the total work spread
 // over the units, plus the last epilogue (with the split-K exchange) and the launch.
 static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sms, int kmaj, PlanChoice* out,
-                            const GemmConfig* forced_down) {
+                            const GemmConfig* forced_up, const GemmConfig* forced_down) {
     out->one_launch = 0;
     out->one_est_us = 0.0;
-    const GemmConfig& u0 = out->up;
-    const int pair = u0.pair;
     const int epi_up = up_epilogue(act);
     const int n_b = act == KT_ACT_GEGLU ? 2 : 1;
-    const int units = num_sms / pair;
+    // the up projection's candidates: the forced one, or the best tile of each CTA pairing
+    // (the down projection runs with the same pairing in one launch)
+    GemmConfig ups[2];
+    int n_ups = 0;
+    if (forced_up) {
+        ups[n_ups++] = *forced_up;
+    } else {
+        for (int pair = 1; pair <= 2; ++pair) {
+            bool got = false;
+            for (int BN = 32; BN <= 256; BN += 32)
+                for (int bk = 64; bk <= 128; bk += 64) {
+                    GemmConfig g;
+                    if (!evaluate(M, F, D, BN, 1, n_b, epi_up, num_sms, pair, bk, &g, false, kmaj)) continue;
+                    if (!got || better(g, ups[n_ups])) {
+                        ups[n_ups] = g;
+                        got = true;
+                    }
+                }
+            if (got) ++n_ups;
+        }
+    }
     bool found = false;
-    for (int BN = 32 * pair; BN <= 256; BN += 32 * pair)
+    for (int iu = 0; iu < n_ups; ++iu) {
+    const GemmConfig& u0 = ups[iu];
+    const int pair = u0.pair;
+    const int units = num_sms / pair;
+    for (int BN = 32; BN <= 256; BN += 32)
       for (int bk = 64; bk <= 128; bk += 64)
         for (int SK = 1; SK <= kOneLaunchMaxSplit; ++SK) {
             if (forced_down && (forced_down->BN != BN || forced_down->bk != bk || forced_down->pair != pair ||
@@ -306,9 +330,14 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
             const double n = grid / pair;
             const double work = (up_tiles * u.t_tile_us + dn_items * d.t_tile_us) / n;
             const double rounds = up_tiles * u.t_tile_us / n + std::ceil(dn_items / n) * d.t_tile_us;
-            const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us + d.t_x_us) +
-                             kKernelOverhead * 1e6 + (pair == 2 ? kPairKernelCost * 1e6 : 0.0) +
-                             (SK > 1 ? kOneLaunchSplitCost * 1e6 : 0.0);
+            // the splits of a tile reduce-scatter their partials: each writes the (SK - 1) / SK
+            // of its fp32 partial that other splits own and reads as much back
+            const double part = kBM * BN * 4.0;
+            const double t_x = SK > 1 ? ((SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate) +
+                                         kOneLaunchSplitCost) * 1e6
+                                      : 0.0;
+            const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us + t_x) +
+                             kKernelOverhead * 1e6 + (pair == 2 ? kPairKernelCost * 1e6 : 0.0);
             if (!found || t < out->one_est_us) {
                 found = true;
                 out->one_est_us = t;
@@ -321,10 +350,12 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
                 u.dbl_staging = d.dbl_staging = out->one_dbl;
                 u.stages = d.stages = stages;
                 u.smem_bytes = d.smem_bytes = out->one_smem;
+                d.t_x_us = t_x;
                 out->one_up = u;
                 out->one_down = d;
             }
         }
+    }
     if (found) out->one_launch = 1;
 }
 
@@ -368,9 +399,9 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         int bn = 0, pr = 1, bk = 64;
         GemmConfig g;
         int nf = std::sscanf(e, "%d,%d,%d", &bn, &pr, &bk);
-        if (nf < 1 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
+        if (nf < 1 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % 32 != 0 || bn < 32 ||
             bn > 256 || !evaluate(M, F, D, bn, 1, n_b, epi_up, num_sms, pr, bk, &g, false, kmaj)) {
-            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32, 64 for a pair; BK 64 or "
+            *why = "KT_FORCE_UP must be a feasible \"BN[,PAIR[,BK]]\" (BN a multiple of 32; BK 64 or "
                    "128; GEGLU: BN <= 128, and BN / PAIR a multiple of 64 for [in][out] weights)";
             return KT_ERR_INVALID;
         }
@@ -380,7 +411,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         int bn = 0, sk = 0, pr = 1, bk = 64, cl = 0;
         GemmConfig g;
         int nf = std::sscanf(e, "%d,%d,%d,%d,%d", &bn, &sk, &pr, &bk, &cl);
-        if (nf < 2 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % (32 * pr) != 0 || bn < 32 ||
+        if (nf < 2 || (pr != 1 && pr != 2) || (bk != 64 && bk != 128) || bn % 32 != 0 || bn < 32 ||
             bn > 256 || sk < 1 || sk > 64 || (cl && !allow_cluster_sk) ||
             !evaluate(M, D, F, bn, sk, 1, EPI_DOWN, num_sms, pr, bk, &g, cl != 0, kmaj)) {
             *why = "KT_FORCE_DOWN must be a feasible \"BN,SK[,PAIR[,BK[,CLUSTER]]]\" (no empty split)";
@@ -435,7 +466,8 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
     if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
         const double t_two = out->up.est_us + out->down.est_us;
-        plan_one_launch(M, D, F, act, num_sms, kmaj, out, forced_dn ? &out->down : nullptr);
+        plan_one_launch(M, D, F, act, num_sms, kmaj, out, std::getenv("KT_FORCE_UP") ? &out->up : nullptr,
+                        forced_dn ? &out->down : nullptr);
         if (force_launches == 0 && out->one_launch && out->one_est_us >= t_two) out->one_launch = 0;
         if (out->one_launch) {  // the configurations that launch runs
             out->up = out->one_up;
