@@ -126,12 +126,15 @@ def ln_input_bound(x_bits, gamma_bits, beta_bits, eps: float, dtype: int):
 # The classical bound is a worst case (every rounding error of the K-term sum adding up);
 # at the workloads' K (1152-4304) it exceeds half an ulp of H for almost every element, so
 # it leaves most of them in the relaxed region.  Measured fractions of elements within one
-# step, every element of the full-size workloads: 0.99957 (SigLIP, f16) to 0.99975 (bf16
-# SDXL); with the LayerNorm prologue, whose fp32 statistics move a few normalised inputs by
-# one step, 0.99870 (SigLIP block, f16) to 0.99951 (bf16).  The floor keeps a margin under
-# the lowest; a handful of elements (MIN_WITHIN_1ULP_SLACK) is allowed on top, for problems
-# too small for a fraction to mean anything.
-MIN_WITHIN_1ULP = 0.998
+# step, every element of the full-size workloads and the random problems: at least 0.99957
+# (SigLIP, f16) without LayerNorm; with the LayerNorm prologue, whose fp32 statistics move a
+# few normalised inputs by one step, down to 0.99870 (SigLIP block, f16) and 0.9970 (small
+# f16 GEGLU blocks, where the product of two activations doubles the effect).  The floors
+# keep a margin under the lowest of each kind; a handful of elements
+# (MIN_WITHIN_1ULP_SLACK) is allowed on top, for problems too small for a fraction to mean
+# anything.
+MIN_WITHIN_1ULP = 0.999
+MIN_WITHIN_1ULP_LN = 0.995
 MIN_WITHIN_1ULP_SLACK = 4
 
 

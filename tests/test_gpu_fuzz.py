@@ -74,4 +74,5 @@ def test_random_problem(i):
         extra = None
         if ln:  # the up projection reads the normalised X (elements near a rounding boundary may differ)
             bb["X"], extra, _ = parity.ln_input_bound(b["X"], b["ln_gamma"], b["ln_beta"], EPS, dt)
-        parity.check_h(wl.bits(H.cpu()), Ho, parity.h_bound(w, bb, x_extra=extra), dt, what=f"H ({desc})")
+        parity.check_h(wl.bits(H.cpu()), Ho, parity.h_bound(w, bb, x_extra=extra), dt, what=f"H ({desc})",
+                       min_within_1ulp=parity.MIN_WITHIN_1ULP_LN if ln else parity.MIN_WITHIN_1ULP)

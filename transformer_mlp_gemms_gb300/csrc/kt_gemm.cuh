@@ -95,6 +95,10 @@ __device__ __forceinline__ uint32_t sm_id() {
 __device__ __forceinline__ void trace_mark(unsigned long long* tr, int slot) {
     if (tr) tr[(size_t)blockIdx.x * kTraceSlots + slot] = global_ns();
 }
+// As trace_mark, keeping the latest of several threads' marks.
+__device__ __forceinline__ void trace_max(unsigned long long* tr, int slot) {
+    if (tr) atomicMax(tr + (size_t)blockIdx.x * kTraceSlots + slot, global_ns());
+}
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -189,6 +193,30 @@ __device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned targe
             if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(err, 0, code);
+                return false;
+            }
+        }
+        __nanosleep(32);
+    }
+}
+
+// As wait_counter, on a 64-bit counter that only grows (no wrap-around within a run's
+// reach): waits until it reaches `target`; a time-out records DEV_TIMEOUT_EPILOGUE.
+__device__ __forceinline__ bool wait_counter64(const unsigned long long* ctr, unsigned long long target,
+                                               volatile int* abort_flag, int* err, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_flag || *reinterpret_cast<volatile int*>(err) != 0) {
+                *abort_flag = 1;
+                return false;
+            }
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, DEV_TIMEOUT_EPILOGUE);
                 return false;
             }
         }
@@ -462,6 +490,28 @@ __device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approxi
     return y;
 }
 
+// 1/d for d >= 1 on the FMA pipe instead of the MUFU unit, whose 16 results per clock and
+// SM bound the activation epilogues (two MUFU operations per element): a bit-level seed,
+// K - bits(d) read as a float, with K = 0x7EF311C0 chosen by a search over [1, 2) for the
+// smallest largest relative error (5.1e-2), then three Newton steps r <- r + r (1 - d r),
+// each squaring the relative error (2.6e-3, 6.5e-6, then below fp32 rounding).  Beyond
+// 2^126 the result is 0, as rcp.approx.ftz flushes its subnormal results there (NaN stays
+// NaN through the caller's product).
+__device__ __forceinline__ float rcp_newton(float d) {
+    float r = __int_as_float(0x7EF311C0 - __float_as_int(d));
+    r = fmaf(r, fmaf(-d, r, 1.0f), r);
+    r = fmaf(r, fmaf(-d, r, 1.0f), r);
+    r = fmaf(r, fmaf(-d, r, 1.0f), r);
+    return d < 0x1p126f ? r : 0.0f;
+}
+// The reciprocal of the activations: MUFU, or (NT) the FMA-pipe Newton form.  The epilogues
+// take the Newton form for three columns in four, which balances the two pipes.
+template <bool NT>
+__device__ __forceinline__ float rcp_act(float d) {
+    if constexpr (NT) return rcp_newton(d);
+    else return rcp_approx(d);
+}
+
 // gelu_erf(z) = z * Phi(z), and Phi(-|z|) = erfc(a) / 2 with a = |z| / sqrt 2.
 // erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
 // 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), P of degree 9,
@@ -481,10 +531,11 @@ constexpr float kU = 0.84932180028801907f;  // sqrt(log2(e) / 2): u = |z| kU
 constexpr float kA = 0.83255461115769776f;  // 1 / sqrt(log2 e):  a = u kA
 }  // namespace erfc_fit
 
+template <bool NT = false>
 __device__ __forceinline__ float gelu_erf_f(float z) {
     using namespace erfc_fit;
     const float u = fabsf(z) * kU;
-    const float tp = rcp_approx(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
+    const float tp = rcp_act<NT>(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
     float q = fmaf(kQ9, tp, kQ8);
     q = fmaf(q, tp, kQ7);
     q = fmaf(q, tp, kQ6);
@@ -501,27 +552,30 @@ __device__ __forceinline__ float gelu_erf_f(float z) {
 
 // gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
 // exp(-2u) = 2^(z (c1 + c2 z^2)), c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1.
+template <bool NT = false>
 __device__ __forceinline__ float gelu_tanh_f(float z) {
     const float x = z * fmaf(-0.1029432395800235f, z * z, -2.302208198144325f);
-    return z * rcp_approx(1.0f + ex2_approx(x));
+    return z * rcp_act<NT>(1.0f + ex2_approx(x));
 }
 
 // z * sigmoid(a z) = z / (1 + exp(-a z)) = z / (1 + 2^(c z)),  c = -a log2(e):
 // a = 1.702 for the sigmoid form of GELU, a = 1 for SiLU.  For z -> -inf the power
 // overflows to +inf and the reciprocal to 0, so the result goes to -0 (no NaN).
+template <bool NT = false>
 __device__ __forceinline__ float gelu_sigmoid_f(float z) {
-    return z * rcp_approx(1.0f + ex2_approx(z * -2.4554669595930157f));
+    return z * rcp_act<NT>(1.0f + ex2_approx(z * -2.4554669595930157f));
 }
+template <bool NT = false>
 __device__ __forceinline__ float silu_f(float z) {
-    return z * rcp_approx(1.0f + ex2_approx(z * -1.4426950408889634f));
+    return z * rcp_act<NT>(1.0f + ex2_approx(z * -1.4426950408889634f));
 }
 
-template <int EPI>
+template <int EPI, bool NT = false>
 __device__ __forceinline__ float act_f(float z) {
-    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f(z);
-    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f(z);
-    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f(z);
-    else if constexpr (EPI == EPI_SILU) return silu_f(z);
+    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f<NT>(z);
+    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f<NT>(z);
+    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f<NT>(z);
+    else if constexpr (EPI == EPI_SILU) return silu_f<NT>(z);
     else return z;
 }
 
@@ -708,6 +762,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
 
     const uint32_t tiles_bytes = (uint32_t)p.stages * p.stage_bytes;
+    constexpr int EPI_UP = EPI;            // the up projection's epilogue (epi_item's EPI is per item)
     constexpr int NEPI = epi_warps(EPI);   // epilogue warps
     constexpr int NPART = NEPI / 4;        // epilogue warps per TMEM lane quadrant
     constexpr int kWarpB = 2 + NEPI;       // the B operand's producer (after the epilogue warps)
@@ -727,6 +782,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
     uint32_t* tmem_slot = slots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(slots + 2);
+    // reduce-scatter split-K: the run's arrival target, shared by the epilogue warps
+    volatile unsigned long long* rs_target = reinterpret_cast<volatile unsigned long long*>(slots + 4);
     // TWO (both projections in one launch): the work-item ring, kItemRing deep: item
     // indices and their full / empty barriers (in the barrier area, past the slots)
     const uint32_t item_idx = staging + kStaging + 256u;
@@ -1246,10 +1303,12 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                 }
 #pragma unroll
                                 for (int i = 0; i < 16; i += 2) {
+                                    // (MUFU reciprocal for one column in four, Newton for the rest)
+                                    const float g0 = __uint_as_float(rg[i]) + bg[i];
+                                    const float g1 = __uint_as_float(rg[i + 1]) + bg[i + 1];
                                     const float y0v = (__uint_as_float(rv[i]) + bv[i]) *
-                                                      gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
-                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) *
-                                                      gelu_erf_f(__uint_as_float(rg[i + 1]) + bg[i + 1]);
+                                                      ((i & 3) == 0 ? gelu_erf_f<false>(g0) : gelu_erf_f<true>(g0));
+                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) * gelu_erf_f<true>(g1);
                                     w[8 * h + i / 2] = pack2<DT>(y0v, y1v);
                                 }
                             }
@@ -1281,7 +1340,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                     for (int i = 0; i < 16; ++i) v[i] += b[i];
                                 }
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] = act_f<EPI>(v[i]);
+                                for (int i = 0; i < 16; ++i)  // (MUFU reciprocal for one column in four)
+                                    v[i] = (i & 3) == 0 ? act_f<EPI, false>(v[i]) : act_f<EPI, true>(v[i]);
                                 if constexpr (EPI == EPI_DOWN)
                                     if (p.residual)
                                         add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
@@ -1400,21 +1460,26 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce);
-            } else if (TWO && p.rs_sk) {
+            } else if (TWO && EPI_UP != EPI_GEGLU && p.rs_sk) {
+                // (not compiled into the GEGLU kernels, whose epilogue leaves no registers for
+                // it: their one-launch splits are summed by the last CTA to arrive, below)
                 // split-K reduce-scatter through global memory (both projections in one launch):
                 // each 32 x 32 unit of this CTA's 128-row half of the tile (row block q, column
                 // group g, u = q * ngroups + g) is owned by split u % SK.  Every split writes its
                 // fp32 partial of each unit it does not own to global scratch ([half tile][unit]
                 // [sending split][16-byte chunk][row][4 floats]: 512 contiguous bytes per warp
-                // access), counts itself on the half tile's arrival counter (release), waits for
-                // all SK arrivals (acquire), then sums its own units' SK partials (its own still
-                // in tensor memory) in split order (deterministic) and stores them.  The splits
-                // of a tile are adjacent work items taken in increasing order, so every split a
-                // CTA waits for is held by a running unit or is the next item to be taken.
+                // access), counts itself on the half tile's 64-bit arrival counter (release),
+                // waits for all SK arrivals of its run (acquire), then sums its own units' SK
+                // partials (its own still in tensor memory) in split order (deterministic) and
+                // stores them.  The counter only grows, by SK per run: the value an arrival
+                // returns tells its run (old / SK), so nothing resets it (a reset would put
+                // atomic round trips on every CTA's path to its exit), and at 64 bits it never
+                // wraps.  The splits of a tile are adjacent work items taken in increasing
+                // order, so every split a CTA waits for is held by a running unit or is the
+                // next item to be taken.
                 const int SK = p.split_k;
                 const uint32_t mine = (uint32_t)c.split;
                 const size_t half_tile = (size_t)c.mn * PAIR + rank;
-                const size_t n_half = (size_t)tiles_mn * PAIR;
                 float4* part = reinterpret_cast<float4*>(p.partials) + half_tile * (size_t)(4 * ngroups) * SK * 256u;
                 for (int g = half; g < ngroups; g += NPART) {
                     const int u = q * ngroups + g;
@@ -1431,21 +1496,23 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 }
                 if (tr1) trace_mark(tr, TR_S_G0M);  // (reduce-scatter: this warp's partials issued)
                 // the barrier orders every epilogue thread's partial stores before the one
-                // gpu-scope release (fences are cumulative)
+                // gpu-scope release (fences are cumulative); the arrival's return value, the
+                // run's target, goes to every epilogue warp through shared memory
+                unsigned long long* arrivals = reinterpret_cast<unsigned long long*>(p.counters) + half_tile;
                 epi_bar_sync<NEPI>();
                 if (ew == 0 && lane == 0) {
                     __threadfence();
-                    atomicAdd(p.counters + half_tile, 1);
+                    const unsigned long long old = atomicAdd(arrivals, 1ull);
+                    rs_target[0] = (old / (unsigned long long)SK + 1ull) * (unsigned long long)SK;
                 }
+                epi_bar_sync<NEPI>();
                 if (tr1) trace_mark(tr, TR_S_G0S);  // (reduce-scatter: arrival counted)
                 if (tr0) trace_mark(tr, TR_EPI_LD);  // (reduce-scatter: partials written)
                 bool got = true;
-                if (lane == 0)
-                    got = wait_counter(reinterpret_cast<const unsigned*>(p.counters) + half_tile, (unsigned)SK,
-                                       abort_flag, p.error, p.wait_limit_ns, DEV_TIMEOUT_EPILOGUE);
+                if (lane == 0) got = wait_counter64(arrivals, rs_target[0], abort_flag, p.error, p.wait_limit_ns);
                 got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                 if (!epi_all<NEPI>(got)) return false;
-                if (tr1) trace_mark(tr, TR_S_G1M);  // (reduce-scatter: every split arrived)
+                if (tr && local == 1 && lane == 0) trace_max(tr, TR_S_G1M);  // (every split arrived: latest warp)
                 if (tr0) trace_mark(tr, TR_EPI_MATH);  // (reduce-scatter: every split's partials written)
                 for (int g = half; g < ngroups; g += NPART) {
                     const int u = q * ngroups + g;
@@ -1458,24 +1525,52 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                         float v[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-                        for (int sp = 0; sp < SK; ++sp) {  // split order: deterministic
-                            if ((uint32_t)sp == mine) {
-                                float a[16];
-                                tmem_f16cols(tq + 32u * g + 16u * h, a);
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] += a[i];
-                                continue;
+                        for (int e = 0; e < 2; ++e) {  // in 8-column eighths of the unit
+                            // every other split's 8 columns of this row in flight at once (one
+                            // memory round trip per eighth, not one per split; the k-th other
+                            // split is k + (k >= mine), so the array index stays a compile-time
+                            // constant and x lives in registers), then the sum in split order
+                            float4 x[kRsMaxSplit - 1][2];
+#pragma unroll
+                            for (int k = 0; k < kRsMaxSplit - 1; ++k) {
+                                if (k >= SK - 1) continue;
+                                const int sp = k + (k >= (int)mine ? 1 : 0);
+#pragma unroll
+                                for (int i = 0; i < 2; ++i)
+                                    x[k][i] = __ldcg(src + (size_t)sp * 256u + 32 * (4 * h + 2 * e + i));
                             }
-                            float4 x[4];
+                            float* ve = v + 8 * e;
+                            // this split's own partial, from tensor memory at its place in split
+                            // order (warp-uniform condition)
+                            auto add_own = [&]() {
+                                uint32_t r[8];
+                                asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                                               "=r"(r[6]), "=r"(r[7])
+                                             : "r"(tq + 32u * g + 16u * h + 8u * e)
+                                             : "memory");
+                                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                                             : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                                               "+r"(r[6]), "+r"(r[7])
+                                             :
+                                             : "memory");
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) x[i] = __ldcg(src + (size_t)sp * 256u + 32 * (4 * h + i));
+                                for (int i = 0; i < 8; ++i) ve[i] += __uint_as_float(r[i]);
+                            };
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                v[4 * i] += x[i].x;
-                                v[4 * i + 1] += x[i].y;
-                                v[4 * i + 2] += x[i].z;
-                                v[4 * i + 3] += x[i].w;
+                            for (int k = 0; k < kRsMaxSplit - 1; ++k) {  // split order: deterministic
+                                if (k >= SK - 1) continue;
+                                if (k == (int)mine) add_own();  // this split comes before the k-th other one
+#pragma unroll
+                                for (int i = 0; i < 2; ++i) {
+                                    ve[4 * i] += x[k][i].x;
+                                    ve[4 * i + 1] += x[k][i].y;
+                                    ve[4 * i + 2] += x[k][i].z;
+                                    ve[4 * i + 3] += x[k][i].w;
+                                }
                             }
+                            if ((int)mine == SK - 1) add_own();  // the last split
                         }
                         if (p.bias) {
                             float b[16];
@@ -1491,7 +1586,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                            dbl);
                 }
                 if (tr0) trace_mark(tr, TR_EPI_STORE);  // (reduce-scatter: my units stored)
-                if (tr1) trace_mark(tr, TR_S_G1S);  // (reduce-scatter: owned units summed, stores issued)
+                // (reduce-scatter: owned units summed and their stores issued, the latest warp)
+                if (tr && local == 1 && lane == 0) trace_max(tr, TR_S_G1S);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -1499,14 +1595,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                     else mbar_arrive(acce);
                 }
                 if (tr1) trace_mark(tr, TR_S_ARR);
-                // every epilogue warp has read the other splits' partials: the last split to
-                // get here resets both counters of the half tile for the next run
-                epi_bar_sync<NEPI>();
-                if (ew == 0 && lane == 0 &&
-                    atomicAdd(p.counters + n_half + half_tile, 1) == SK - 1) {
-                    atomicExch(p.counters + half_tile, 0);
-                    atomicExch(p.counters + n_half + half_tile, 0);
-                }
+                // rs_target is rewritten by the next split-K item only after every warp has
+                // passed this item's barriers: the next item's first barrier orders it
             } else {
                 // split-K: this split's fp32 partial in a private layout in which every
                 // warp access is 512 contiguous bytes: [16-column chunk][quarter][row][4]

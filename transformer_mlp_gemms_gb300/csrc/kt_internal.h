@@ -42,6 +42,7 @@ constexpr int smem_reserve(int epi) {
 }
 constexpr int kMaxStages = 8;
 constexpr int kItemRing = 4;  // work items published ahead when both projections run in one launch
+constexpr int kRsMaxSplit = 4;  // largest split along K of the one-launch down projection (reduce-scatter)
 
 // Epilogue kinds (one kernel instantiation each, times two dtypes).
 enum Epi : int {
@@ -169,7 +170,8 @@ struct GemmParams {
     float* partials;         // split-K: [split_k][tiles_m*BM][tiles_n*BN] fp32 (rs_sk: [half tile][unit]
                              // [sending split][8][32 rows][4])
     int* counters;           // split-K: per 128-row half tile, arrival counters (zero between runs);
-                             // rs_sk: then as many counters of the splits done reading
+                             // rs_sk: one 64-bit arrival counter per half tile (8-byte aligned),
+                             // growing by split_k per run
     int* error;              // device error word
     int inject_stall;        // failure-injection hook (producer waits on a silent barrier)
     unsigned long long wait_limit_ns;   // bound of every device-side wait

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -99,7 +100,7 @@ struct kt_mlp_plan_s {
     // device workspace (one allocation each)
     void* H = nullptr;          // [M][F]
     float* partials = nullptr;  // [SK][tiles_m*128][tiles_n*BN] when the down GEMM splits K
-    int* flags = nullptr;       // [0] error word, [1..] split-K tile counters, then row-block counters
+    int* flags = nullptr;       // [0] error word, [2..] split-K tile counters, then row-block counters
     unsigned* ready = nullptr;  // per up-projection row block: CTA tiles of H stored (inside flags)
     unsigned* readers = nullptr;  // per row block: the down projection's waits done this run (inside flags)
     unsigned* ready_expect = nullptr;  // per row block: the down projection's waits per run (own allocation)
@@ -287,7 +288,7 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.bias = P->bias ? t.b_down : nullptr;
     dn.residual = t.R;
     dn.partials = P->partials;
-    dn.counters = P->flags + 1;
+    dn.counters = P->flags + 2;  // 8-byte aligned: the reduce-scatter's counters are 64-bit
     dn.pdl_wait = 1;
     dn.trace = P->trace_down;
     dn.ready = P->ready;
@@ -297,9 +298,10 @@ kt_status run_impl(kt_mlp_plan_t P, const kt_mlp_tensors& t, void* H, void* stre
     dn.ready_rows = kt::kBM * P->choice.up.pair;
     if (P->choice.one_launch) {
         // both projections in one launch: one shared-memory ring, tiles from one queue; a
-        // down projection split along K reduce-scatters its partials among the splits
+        // down projection split along K reduce-scatters its partials among the splits (GEGLU:
+        // the last split to arrive sums them)
         up.stage_bytes = dn.stage_bytes = (uint32_t)P->choice.one_slot;
-        dn.rs_sk = dn.split_k > 1 ? 1 : 0;
+        dn.rs_sk = dn.split_k > 1 && P->act != KT_ACT_GEGLU ? 1 : 0;
         up.sched = dn.sched = P->sched;
         up.pdl_wait = dn.pdl_wait = 1;
         const void* maps[6] = {&P->tm_x, &P->tm_wu, &P->tm_hs, &P->tm_h, &P->tm_wd, &P->tm_ys};
@@ -388,7 +390,8 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
     // two per 128-row half tile: split-K arrivals, and (reduce-scatter) splits done reading
     size_t n_counters = 2 * (size_t)dn.tiles_m * dn.tiles_n * dn.pair;
     size_t n_ready = (size_t)up.tiles_m;                               // one per up row block
-    size_t flag_bytes = 4 * (1 + n_counters + 2 * n_ready + 2);
+    // [0] error word, [1] padding, [2 ..) split-K counters, readiness counters, work counters
+    size_t flag_bytes = 4 * (2 + n_counters + 2 * n_ready + 2);
     size_t part_bytes = dn.split_k > 1
                             ? (size_t)dn.split_k * dn.tiles_m * dn.pair * kt::kBM * (size_t)dn.tiles_n * dn.BN * 4
                             : 0;
@@ -408,9 +411,9 @@ kt_status create_plan(const kt_mlp_options& o, kt_mlp_plan_t* out) {
         free_plan(P);
         return cuda_fail("cudaMemset", e);
     }
-    P->ready = reinterpret_cast<unsigned*>(P->flags + 1 + n_counters);
+    P->ready = reinterpret_cast<unsigned*>(P->flags + 2 + n_counters);
     P->readers = P->ready + n_ready;
-    P->sched = P->flags + 1 + n_counters + 2 * n_ready;
+    P->sched = P->flags + 2 + n_counters + 2 * n_ready;
     P->flag_bytes = flag_bytes;
     {
         // how many times this plan's down projection waits on each up row block per run:
@@ -471,7 +474,7 @@ kt_status info_impl(const kt_mlp_options& o, int num_sms, kt_plan_info* out) {
     kt::plan_fill_info(c.up, &out->up);
     kt::plan_fill_info(c.down, &out->down);
     // H, error word and split-K counters, three words per up row block, host staging
-    int64_t ws = o.M * o.F * 2 + 4 * (1 + 2 * (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
+    int64_t ws = o.M * o.F * 2 + 4 * (2 + 2 * (int64_t)c.down.tiles_m * c.down.tiles_n * c.down.pair) +
                  4 * 3 * (int64_t)c.up.tiles_m + 8 + 2 * 2 * o.M * o.D;
     if (c.down.split_k > 1)
         ws += (int64_t)c.down.split_k * c.down.tiles_m * c.down.pair * kt::kBM * (int64_t)c.down.tiles_n * c.down.BN * 4;

@@ -83,8 +83,11 @@ constexpr double kPairTileCost = 0.3e-6;
 // Splits along K of the one-launch down projection's tiles considered by the planner, and
 // the fixed cost of their reduce-scatter (the arrival handshake of the splits) beside its
 // partial traffic.
-constexpr int kOneLaunchMaxSplit = 4;
+constexpr int kOneLaunchMaxSplit = kRsMaxSplit;
 constexpr double kOneLaunchSplitCost = 1.0e-6;
+// GEGLU's one-launch splits are summed by the last split to arrive (all partials through
+// global memory, read back by one CTA): calibrated on GB300 at 7 us over the modelled exchange.
+constexpr double kOneLaunchLastArriverCost = 7.0e-6;
 
 double epi_cost_per_elem(int epi) {      // seconds per output element per SM (model)
     switch (epi) {
@@ -333,9 +336,11 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
             // the splits of a tile reduce-scatter their partials: each writes the (SK - 1) / SK
             // of its fp32 partial that other splits own and reads as much back
             const double part = kBM * BN * 4.0;
-            const double t_x = SK > 1 ? ((SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate) +
-                                         kOneLaunchSplitCost) * 1e6
-                                      : 0.0;
+            const double t_x = SK == 1 ? 0.0
+                               : act == KT_ACT_GEGLU
+                                   ? d.t_x_us + kOneLaunchLastArriverCost * 1e6
+                                   : ((SK - 1.0) / SK * part * (1.0 / kSmStoreRate + 1.0 / kSmReadRate) +
+                                      kOneLaunchSplitCost) * 1e6;
             const double t = std::max(work, rounds) + std::max(u.t_epi_us, d.t_epi_us + t_x) +
                              kKernelOverhead * 1e6 + (pair == 2 ? kPairKernelCost * 1e6 : 0.0);
             if (!found || t < out->one_est_us) {
