@@ -490,28 +490,6 @@ __device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approxi
     return y;
 }
 
-// 1/d for d >= 1 on the FMA pipe instead of the MUFU unit, whose 16 results per clock and
-// SM bound the activation epilogues (two MUFU operations per element): a bit-level seed,
-// K - bits(d) read as a float, with K = 0x7EF311C0 chosen by a search over [1, 2) for the
-// smallest largest relative error (5.1e-2), then three Newton steps r <- r + r (1 - d r),
-// each squaring the relative error (2.6e-3, 6.5e-6, then below fp32 rounding).  Beyond
-// 2^126 the result is 0, as rcp.approx.ftz flushes its subnormal results there (NaN stays
-// NaN through the caller's product).
-__device__ __forceinline__ float rcp_newton(float d) {
-    float r = __int_as_float(0x7EF311C0 - __float_as_int(d));
-    r = fmaf(r, fmaf(-d, r, 1.0f), r);
-    r = fmaf(r, fmaf(-d, r, 1.0f), r);
-    r = fmaf(r, fmaf(-d, r, 1.0f), r);
-    return d < 0x1p126f ? r : 0.0f;
-}
-// The reciprocal of the activations: MUFU, or (NT) the FMA-pipe Newton form.  The epilogues
-// take the Newton form for three columns in four, which balances the two pipes.
-template <bool NT>
-__device__ __forceinline__ float rcp_act(float d) {
-    if constexpr (NT) return rcp_newton(d);
-    else return rcp_approx(d);
-}
-
 // gelu_erf(z) = z * Phi(z), and Phi(-|z|) = erfc(a) / 2 with a = |z| / sqrt 2.
 // erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
 // 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), P of degree 9,
@@ -531,11 +509,10 @@ constexpr float kU = 0.84932180028801907f;  // sqrt(log2(e) / 2): u = |z| kU
 constexpr float kA = 0.83255461115769776f;  // 1 / sqrt(log2 e):  a = u kA
 }  // namespace erfc_fit
 
-template <bool NT = false>
 __device__ __forceinline__ float gelu_erf_f(float z) {
     using namespace erfc_fit;
     const float u = fabsf(z) * kU;
-    const float tp = rcp_act<NT>(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
+    const float tp = rcp_approx(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
     float q = fmaf(kQ9, tp, kQ8);
     q = fmaf(q, tp, kQ7);
     q = fmaf(q, tp, kQ6);
@@ -552,30 +529,27 @@ __device__ __forceinline__ float gelu_erf_f(float z) {
 
 // gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
 // exp(-2u) = 2^(z (c1 + c2 z^2)), c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1.
-template <bool NT = false>
 __device__ __forceinline__ float gelu_tanh_f(float z) {
     const float x = z * fmaf(-0.1029432395800235f, z * z, -2.302208198144325f);
-    return z * rcp_act<NT>(1.0f + ex2_approx(x));
+    return z * rcp_approx(1.0f + ex2_approx(x));
 }
 
 // z * sigmoid(a z) = z / (1 + exp(-a z)) = z / (1 + 2^(c z)),  c = -a log2(e):
 // a = 1.702 for the sigmoid form of GELU, a = 1 for SiLU.  For z -> -inf the power
 // overflows to +inf and the reciprocal to 0, so the result goes to -0 (no NaN).
-template <bool NT = false>
 __device__ __forceinline__ float gelu_sigmoid_f(float z) {
-    return z * rcp_act<NT>(1.0f + ex2_approx(z * -2.4554669595930157f));
+    return z * rcp_approx(1.0f + ex2_approx(z * -2.4554669595930157f));
 }
-template <bool NT = false>
 __device__ __forceinline__ float silu_f(float z) {
-    return z * rcp_act<NT>(1.0f + ex2_approx(z * -1.4426950408889634f));
+    return z * rcp_approx(1.0f + ex2_approx(z * -1.4426950408889634f));
 }
 
-template <int EPI, bool NT = false>
+template <int EPI>
 __device__ __forceinline__ float act_f(float z) {
-    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f<NT>(z);
-    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f<NT>(z);
-    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f<NT>(z);
-    else if constexpr (EPI == EPI_SILU) return silu_f<NT>(z);
+    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f(z);
+    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f(z);
+    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f(z);
+    else if constexpr (EPI == EPI_SILU) return silu_f(z);
     else return z;
 }
 
@@ -1303,12 +1277,10 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                 }
 #pragma unroll
                                 for (int i = 0; i < 16; i += 2) {
-                                    // (MUFU reciprocal for one column in four, Newton for the rest)
-                                    const float g0 = __uint_as_float(rg[i]) + bg[i];
-                                    const float g1 = __uint_as_float(rg[i + 1]) + bg[i + 1];
                                     const float y0v = (__uint_as_float(rv[i]) + bv[i]) *
-                                                      ((i & 3) == 0 ? gelu_erf_f<false>(g0) : gelu_erf_f<true>(g0));
-                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) * gelu_erf_f<true>(g1);
+                                                      gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
+                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) *
+                                                      gelu_erf_f(__uint_as_float(rg[i + 1]) + bg[i + 1]);
                                     w[8 * h + i / 2] = pack2<DT>(y0v, y1v);
                                 }
                             }
@@ -1340,8 +1312,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                     for (int i = 0; i < 16; ++i) v[i] += b[i];
                                 }
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)  // (MUFU reciprocal for one column in four)
-                                    v[i] = (i & 3) == 0 ? act_f<EPI, false>(v[i]) : act_f<EPI, true>(v[i]);
+                                for (int i = 0; i < 16; ++i) v[i] = act_f<EPI>(v[i]);
                                 if constexpr (EPI == EPI_DOWN)
                                     if (p.residual)
                                         add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);
@@ -1465,7 +1436,9 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 // it: their one-launch splits are summed by the last CTA to arrive, below)
                 // split-K reduce-scatter through global memory (both projections in one launch):
                 // each 32 x 32 unit of this CTA's 128-row half of the tile (row block q, column
-                // group g, u = q * ngroups + g) is owned by split u % SK.  Every split writes its
+                // group g, u = q * ngroups + g) is owned by split (g / NPART + q + half) % SK: the
+                // groups one warp handles (g = half, half + NPART, ...) go to different splits, so
+                // that no warp sums more units than the others (up to SK groups per warp).  Every split writes its
                 // fp32 partial of each unit it does not own to global scratch ([half tile][unit]
                 // [sending split][16-byte chunk][row][4 floats]: 512 contiguous bytes per warp
                 // access), counts itself on the half tile's 64-bit arrival counter (release),
@@ -1480,10 +1453,11 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 const int SK = p.split_k;
                 const uint32_t mine = (uint32_t)c.split;
                 const size_t half_tile = (size_t)c.mn * PAIR + rank;
+                auto rs_owner = [&](int g) { return (uint32_t)((g / NPART + q + half) % SK); };
                 float4* part = reinterpret_cast<float4*>(p.partials) + half_tile * (size_t)(4 * ngroups) * SK * 256u;
                 for (int g = half; g < ngroups; g += NPART) {
                     const int u = q * ngroups + g;
-                    if ((uint32_t)(u % SK) == mine || n0 + 32 * g >= p.N || !rows_live) continue;  // warp-uniform
+                    if (rs_owner(g) == mine || n0 + 32 * g >= p.N || !rows_live) continue;  // warp-uniform
                     uint32_t r[32];
                     tmem_ld32(tq + 32u * g, r);
                     tmem_wait_ld_only();
@@ -1517,7 +1491,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 for (int g = half; g < ngroups; g += NPART) {
                     const int u = q * ngroups + g;
                     const int col = n0 + 32 * g;
-                    if ((uint32_t)(u % SK) != mine || col >= p.N || !rows_live) continue;  // warp-uniform
+                    if (rs_owner(g) != mine || col >= p.N || !rows_live) continue;  // warp-uniform
                     const float4* src = part + (size_t)u * SK * 256u + lane;
                     uint32_t w[16];  // the unit's 32 results, rounded and packed in pairs
 #pragma unroll

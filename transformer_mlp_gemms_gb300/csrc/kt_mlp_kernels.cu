@@ -32,22 +32,20 @@ __global__ void __launch_bounds__(256) kt_copy16_kernel(const uint4* __restrict_
     for (; i < n16; i += stride) dst[i] = src[i];
 }
 
-// Elementwise evaluation of the epilogue's fp32 activations (test hook): element i takes
-// the MUFU reciprocal when i % 4 == 0 and the FMA-pipe Newton reciprocal otherwise, as the
-// epilogues do per column, so that a test over a grid covers both forms.
-template <bool NT>
-__device__ __forceinline__ float activation_at(int act, float x, const float* __restrict__ g, int64_t i) {
-    if (act == KT_ACT_GELU_ERF) return gelu_erf_f<NT>(x);
-    if (act == KT_ACT_GELU_TANH) return gelu_tanh_f<NT>(x);
-    if (act == KT_ACT_GEGLU) return x * gelu_erf_f<NT>(g[i]);
-    if (act == KT_ACT_GELU_SIGMOID) return gelu_sigmoid_f<NT>(x);
-    if (act == KT_ACT_SILU) return silu_f<NT>(x);
-    return x;
-}
+// Elementwise evaluation of the epilogue's fp32 activations (test hook).
 __global__ void kt_activation_kernel(int act, const float* __restrict__ z, const float* __restrict__ g,
                                      float* __restrict__ out, int64_t n) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        out[i] = (i & 3) == 0 ? activation_at<false>(act, z[i], g, i) : activation_at<true>(act, z[i], g, i);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float x = z[i];
+        float y;
+        if (act == KT_ACT_GELU_ERF) y = gelu_erf_f(x);
+        else if (act == KT_ACT_GELU_TANH) y = gelu_tanh_f(x);
+        else if (act == KT_ACT_GEGLU) y = x * gelu_erf_f(g[i]);
+        else if (act == KT_ACT_GELU_SIGMOID) y = gelu_sigmoid_f(x);
+        else if (act == KT_ACT_SILU) y = silu_f(x);
+        else y = x;
+        out[i] = y;
+    }
 }
 
 // LayerNorm prologue ("SDXL as a requirements inventory", section 1.3: the block's

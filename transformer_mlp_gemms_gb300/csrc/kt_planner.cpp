@@ -190,6 +190,13 @@ bool evaluate(int64_t M, int64_t N, int64_t K, int BN, int SK, int n_b, int epi,
     return true;
 }
 
+// N-major weight boxes of 16 columns (a CTA share that is an odd multiple of 16) move 32-byte
+// rows: four times the L2 requests per byte of 64-column boxes.  Measured on GB300 they lose
+// (SDXL level 2's down projection as 256 x 160 pair tiles, 16-column boxes: 75.8 us; as
+// 256 x 192, 32-column boxes: 73.7 us), so the planner's own search leaves them out; a
+// forced plan (KT_FORCE_UP / KT_FORCE_DOWN) may still use them.
+bool narrow_boxes(int BN, int pair, int kmaj) { return !kmaj && b_box_cols(BN, pair) < 32; }
+
 bool better(const GemmConfig& a, const GemmConfig& b) {
     // a strictly better than b?
     if (a.est_us < b.est_us * (1.0 - 1e-9)) return true;
@@ -207,6 +214,7 @@ bool choose(int64_t M, int64_t N, int64_t K, int n_b, int epi, int max_sk, int n
         for (int BN = 32; BN <= 256; BN += 32) {  // whole 32-column store boxes
             // (a pair splits the columns into two shares, multiples of 16: whole 16-column
             // weight boxes; the epilogue stores 32-column boxes of the whole tile)
+            if (narrow_boxes(BN, pair, kmaj)) continue;
             for (int bk = 64; bk <= 128; bk += 64) {
                 for (int SK = 1; SK <= max_sk; ++SK) {
                     for (int cl = 0; cl <= (allow_cluster_sk ? 1 : 0); ++cl) {
@@ -296,6 +304,7 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
             bool got = false;
             for (int BN = 32; BN <= 256; BN += 32)
                 for (int bk = 64; bk <= 128; bk += 64) {
+                    if (narrow_boxes(BN, pair, kmaj)) continue;
                     GemmConfig g;
                     if (!evaluate(M, F, D, BN, 1, n_b, epi_up, num_sms, pair, bk, &g, false, kmaj)) continue;
                     if (!got || better(g, ups[n_ups])) {
@@ -317,6 +326,7 @@ static void plan_one_launch(int64_t M, int64_t D, int64_t F, int act, int num_sm
             if (forced_down && (forced_down->BN != BN || forced_down->bk != bk || forced_down->pair != pair ||
                                 forced_down->split_k != SK || forced_down->cluster_sk))
                 continue;
+            if (!forced_down && narrow_boxes(BN, pair, kmaj)) continue;
             GemmConfig d0;
             if (!evaluate(M, D, F, BN, SK, 1, EPI_DOWN, num_sms, pair, bk, &d0, false, kmaj)) continue;
             const int slot = std::max(stage_bytes(u0.BN, n_b, pair, u0.bk, kmaj), stage_bytes(BN, 1, pair, bk, kmaj));
