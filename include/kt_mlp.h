@@ -76,12 +76,16 @@ typedef enum { KT_H_AUTO = 0, KT_H_MEMORY = 1, KT_H_ON_CHIP = 2 } kt_h_path;
 
 /* How the two projections are launched when H goes through memory.  KT_LAUNCH_TWO: two
  * persistent kernels, the down projection's CTAs starting as the up projection's finish
- * (programmatic dependent launch) and loading rows of H as they are stored.  KT_LAUNCH_ONE:
- * one persistent kernel that takes up tiles, then down tiles, from one work queue (a down
- * tile once its rows of H are stored); no split-K for the down projection.  KT_LAUNCH_AUTO
- * is the planner's choice: one launch when the up projection is a single wave, the
- * two-launch down projection would split K and the model prefers one launch (SigLIP's
- * 729 tokens), two launches otherwise. */
+ * (programmatic dependent launch) and loading rows of H as they are stored; a down
+ * projection split along K reduces inside clusters or through global memory.
+ * KT_LAUNCH_ONE: one persistent kernel that takes up tiles, then down items, from one work
+ * queue (a down item once its rows of H are stored); down items may be K splits of a tile,
+ * reduce-scattered among the splits through global memory (GEGLU: summed by the last split
+ * to arrive).  KT_LAUNCH_AUTO is the planner's choice: one launch where the model prefers
+ * it and either (a) the up projection is a single wave of single-CTA tiles and the
+ * two-launch down projection would split K (SigLIP's 729 tokens, M = 256), or (b) the
+ * two-launch down projection takes two waves of whole tiles (SDXL level 1, M = 4096); two
+ * launches otherwise. */
 typedef enum { KT_LAUNCH_AUTO = 0, KT_LAUNCH_ONE = 1, KT_LAUNCH_TWO = 2 } kt_launches;
 
 /* Memory order of W_up and W_down. */
@@ -201,9 +205,10 @@ kt_status kt_mlp_plan(int64_t M, int64_t D, int64_t F, kt_act act, kt_dtype dtyp
 
 /*
  * kt_mlp_run -- enqueue the MLP on `stream` (a cudaStream_t; NULL = legacy default
- * stream).  Two kernel launches: the up GEMM with the fused bias/activation/rounding
- * epilogue writing H into the plan's workspace, then the down GEMM (programmatic
- * dependent launch) writing Y.  All pointers are device pointers owned by the
+ * stream).  The plan's launch schedule (kt_plan_info.one_launch): either one persistent
+ * kernel running both projections, or two -- the up GEMM with the fused
+ * bias/activation/rounding epilogue writing H into the plan's workspace, then the down GEMM
+ * (programmatic dependent launch) writing Y.  All pointers are device pointers owned by the
  * caller, 16-byte aligned, laid out as described at the top of this file.  b_up /
  * b_down must be non-NULL iff the plan has bias = 1.  Asynchronous: returns after
  * enqueueing.  A plan must not run concurrently on two streams (one workspace).
