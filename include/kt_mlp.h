@@ -338,8 +338,13 @@ kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_dow
  * (GEGLU) / z[i] (none) / gelu_sigmoid(z[i]) / silu(z[i]), for i < n, enqueued on
  * `stream`.  The same device
  * functions as the fused epilogue; exposed so that their accuracy can be tested
- * against the oracle on their own.  gate is read only for GEGLU.
+ * against the oracle on their own.  gate is read only for GEGLU.  The epilogues
+ * evaluate the activations on pairs of values with the paired fp32 instructions
+ * (add / mul / fma .rn.f32x2); `act` alone selects that form, `act |
+ * KT_ACTIVATION_SCALAR_FORM` the same steps as two scalar instructions each, which
+ * must give the same bits.  Any other flag: KT_ERR_INVALID.
  */
+#define KT_ACTIVATION_SCALAR_FORM 0x100
 kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, float* out, int64_t n,
                               void* stream);
 

@@ -237,15 +237,19 @@ def test_plan_reports_its_choice():
     assert re.search(r"up: (128|256)x\d+", desc) and re.search(r"down: (128|256)x\d+", desc)
 
 
-@pytest.mark.parametrize("act", [wl.ACT_GELU_ERF, wl.ACT_GELU_TANH, wl.ACT_GEGLU, wl.ACT_GELU_SIGMOID, wl.ACT_SILU])
-def test_device_activation_accuracy(act):
+ACTS = [wl.ACT_GELU_ERF, wl.ACT_GELU_TANH, wl.ACT_GEGLU, wl.ACT_GELU_SIGMOID, wl.ACT_SILU]
+
+
+@pytest.mark.parametrize("form", [0, kt_mlp.KT_ACTIVATION_SCALAR_FORM], ids=["paired", "scalar"])
+@pytest.mark.parametrize("act", ACTS)
+def test_device_activation_accuracy(act, form):
     # the epilogue's fp32 activations against the float64 oracle on a dense grid:
     # relative error <= 2e-5, over 10x below half an fp16 ulp (2.4e-4)
     z = torch.linspace(-9.0, 9.0, 400001, dtype=torch.float32)
     g = torch.flip(z, [0]).contiguous()
     zd, gd = z.cuda(), g.cuda()
     out = torch.empty_like(zd)
-    kt_mlp.kt_debug_activation(act, zd, gd, out, z.numel())
+    kt_mlp.kt_debug_activation(act | form, zd, gd, out, z.numel())
     torch.cuda.synchronize()
     got = out.cpu().double().numpy()
     zz = z.double().numpy()
@@ -259,3 +263,31 @@ def test_device_activation_accuracy(act):
     rel = np.abs(got[big] - ref[big]) / np.abs(ref[big])
     assert rel.max() <= 2e-5, (float(rel.max()), float(zz[big][np.argmax(rel)]))
     assert np.all(np.abs(got[~big]) <= 1e-29)
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_paired_and_scalar_forms_agree_bit_for_bit(act):
+    # the epilogues' paired fp32 instructions against the same steps as scalar
+    # instructions, each rounded once either way: the bits must agree everywhere,
+    # signed zeros, tiny, huge and odd-length tails included (an odd count leaves the
+    # last element paired with itself)
+    z = torch.cat([torch.linspace(-40.0, 40.0, 1000001, dtype=torch.float32),
+                   torch.tensor([0.0, -0.0, 1e-30, -1e-30, 1e-40, -1e-40, 88.0, -88.0, 1e30, -1e30],
+                                dtype=torch.float32)])
+    g = torch.flip(z, [0]).contiguous()
+    zd, gd = z.cuda(), g.cuda()
+    outs = []
+    for form in (0, kt_mlp.KT_ACTIVATION_SCALAR_FORM):
+        out = torch.empty_like(zd)
+        kt_mlp.kt_debug_activation(act | form, zd, gd, out, z.numel())
+        outs.append(out.cpu().view(torch.int32))
+    torch.cuda.synchronize()
+    differ = (outs[0] != outs[1]).nonzero().flatten()
+    assert differ.numel() == 0, (differ[:5].tolist(), z[differ[:5]].tolist())
+
+
+def test_activation_rejects_unknown_form():
+    z = torch.zeros(4, device="cuda")
+    with pytest.raises(kt_mlp.KtError) as e:
+        kt_mlp.kt_debug_activation(wl.ACT_GELU_TANH | 0x200, z, z, z, 4)
+    assert e.value.status == kt_mlp.KT_ERR_INVALID

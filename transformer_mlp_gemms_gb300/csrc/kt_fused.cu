@@ -280,8 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) bv[i] = bg[i] = 0.0f;
                     }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = (__uint_as_float(r[i]) + bv[i]) * gelu_erf_f(__uint_as_float(gr[i]) + bg[i]);
+                    for (int i = 0; i < 32; i += 2)
+                        f2_split(geglu_f2<true>(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), f2(bv[i], bv[i + 1]),
+                                          f2(__uint_as_float(gr[i]), __uint_as_float(gr[i + 1])), f2(bg[i], bg[i + 1])),
+                                 v[i], v[i + 1]);
                 } else {
                     tmem_wait_ld_only();
                     reg_fence32(r);
@@ -293,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) bb[i] = 0.0f;
                     }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = act_f<EPI>(__uint_as_float(r[i]) + bb[i]);
+                    for (int i = 0; i < 32; i += 2)
+                        f2_split(act_f2<EPI, true>(f2_add<true>(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                                    f2(bb[i], bb[i + 1]))),
+                                 v[i], v[i + 1]);
                 }
                 // hidden columns past F meet zero rows of W_down; keep them exactly zero
 #pragma unroll

@@ -490,6 +490,57 @@ __device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approxi
     return y;
 }
 
+// Pairs of fp32 values, and their arithmetic in two forms: P = true issues the
+// sm_100-family paired instructions (add / sub / mul / fma .rn.f32x2 on the two values
+// as one 64-bit register pair), P = false two scalar .rn instructions.  Both round each
+// lane exactly as one scalar .rn instruction does (and neither form is contracted
+// into a different fma), so the two forms give the same bits; the paired one issues
+// about half the instructions.  The hardware approximations (ex2, rcp) and the sign
+// selects are per lane in both.  The epilogues use the paired form; the scalar one
+// serves the test hook, which checks that the two agree bit for bit.
+struct f32x2 {
+    float x, y;
+};
+__device__ __forceinline__ f32x2 f2(float a, float b) { return f32x2{a, b}; }
+__device__ __forceinline__ f32x2 f2(float a) { return f32x2{a, a}; }
+__device__ __forceinline__ void f2_split(f32x2 v, float& a, float& b) {
+    a = v.x;
+    b = v.y;
+}
+#define KT_F2_BINARY(name, op, scalar)                                                                  \
+    template <bool P>                                                                                 \
+    __device__ __forceinline__ f32x2 name(f32x2 a, f32x2 b) {                                         \
+        if constexpr (P) {                                                                            \
+            f32x2 o;                                                                                  \
+            asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" op      \
+                ".rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"                                   \
+                : "=f"(o.x), "=f"(o.y)                                                                \
+                : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                            \
+            return o;                                                                                 \
+        } else {                                                                                      \
+            return f32x2{scalar(a.x, b.x), scalar(a.y, b.y)};                                         \
+        }                                                                                             \
+    }
+KT_F2_BINARY(f2_add, "add", __fadd_rn)
+KT_F2_BINARY(f2_sub, "sub", __fsub_rn)
+KT_F2_BINARY(f2_mul, "mul", __fmul_rn)
+#undef KT_F2_BINARY
+template <bool P>
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    if constexpr (P) {
+        f32x2 o;
+        asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+            "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+            : "=f"(o.x), "=f"(o.y)
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+        return o;
+    } else {
+        return f32x2{__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y)};
+    }
+}
+__device__ __forceinline__ f32x2 f2_ex2(f32x2 v) { return f32x2{ex2_approx(v.x), ex2_approx(v.y)}; }
+__device__ __forceinline__ f32x2 f2_rcp(f32x2 v) { return f32x2{rcp_approx(v.x), rcp_approx(v.y)}; }
+
 // gelu_erf(z) = z * Phi(z), and Phi(-|z|) = erfc(a) / 2 with a = |z| / sqrt 2.
 // erfc(a), a >= 0, by the Chebyshev fit of Numerical Recipes in C (2nd ed., section
 // 6.2, "erfcc"): erfc(a) = t * exp(-a^2 + P(t)), t = 1 / (1 + a/2), P of degree 9,
@@ -509,48 +560,59 @@ constexpr float kU = 0.84932180028801907f;  // sqrt(log2(e) / 2): u = |z| kU
 constexpr float kA = 0.83255461115769776f;  // 1 / sqrt(log2 e):  a = u kA
 }  // namespace erfc_fit
 
-__device__ __forceinline__ float gelu_erf_f(float z) {
+template <bool P>
+__device__ __forceinline__ f32x2 gelu_erf_f2(f32x2 z) {
     using namespace erfc_fit;
-    const float u = fabsf(z) * kU;
-    const float tp = rcp_approx(fmaf(u, kA, 2.0f));  // t' = 1 / (2 + a)
-    float q = fmaf(kQ9, tp, kQ8);
-    q = fmaf(q, tp, kQ7);
-    q = fmaf(q, tp, kQ6);
-    q = fmaf(q, tp, kQ5);
-    q = fmaf(q, tp, kQ4);
-    q = fmaf(q, tp, kQ3);
-    q = fmaf(q, tp, kQ2);
-    q = fmaf(q, tp, kQ1);
-    q = fmaf(q, tp, kQ0);
-    const float h = tp * ex2_approx(fmaf(-u, u, q));  // Phi(-|z|)
-    const float zh = z * h;
-    return z >= 0.0f ? z - zh : zh;
+    const f32x2 az = f2(fabsf(z.x), fabsf(z.y));
+    const f32x2 u = f2_mul<P>(az, f2(kU)), nu = f2_mul<P>(az, f2(-kU));  // u and -u, both exact
+    const f32x2 tp = f2_rcp(f2_fma<P>(u, f2(kA), f2(2.0f)));             // t' = 1 / (2 + a)
+    f32x2 q = f2_fma<P>(f2(kQ9), tp, f2(kQ8));
+    q = f2_fma<P>(q, tp, f2(kQ7));
+    q = f2_fma<P>(q, tp, f2(kQ6));
+    q = f2_fma<P>(q, tp, f2(kQ5));
+    q = f2_fma<P>(q, tp, f2(kQ4));
+    q = f2_fma<P>(q, tp, f2(kQ3));
+    q = f2_fma<P>(q, tp, f2(kQ2));
+    q = f2_fma<P>(q, tp, f2(kQ1));
+    q = f2_fma<P>(q, tp, f2(kQ0));
+    const f32x2 zh = f2_mul<P>(z, f2_mul<P>(tp, f2_ex2(f2_fma<P>(nu, u, q))));  // z Phi(-|z|)
+    const f32x2 r = f2_sub<P>(z, zh);
+    return f2(z.x >= 0.0f ? r.x : zh.x, z.y >= 0.0f ? r.y : zh.y);
 }
 
 // gelu_tanh(z) = 0.5 z (1 + tanh(u)) = z / (1 + exp(-2u)),  u = sqrt(2/pi)(z + 0.044715 z^3);
 // exp(-2u) = 2^(z (c1 + c2 z^2)), c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1.
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-    const float x = z * fmaf(-0.1029432395800235f, z * z, -2.302208198144325f);
-    return z * rcp_approx(1.0f + ex2_approx(x));
+template <bool P>
+__device__ __forceinline__ f32x2 gelu_tanh_f2(f32x2 z) {
+    const f32x2 x = f2_mul<P>(z, f2_fma<P>(f2(-0.1029432395800235f), f2_mul<P>(z, z), f2(-2.302208198144325f)));
+    return f2_mul<P>(z, f2_rcp(f2_add<P>(f2(1.0f), f2_ex2(x))));
 }
 
 // z * sigmoid(a z) = z / (1 + exp(-a z)) = z / (1 + 2^(c z)),  c = -a log2(e):
 // a = 1.702 for the sigmoid form of GELU, a = 1 for SiLU.  For z -> -inf the power
 // overflows to +inf and the reciprocal to 0, so the result goes to -0 (no NaN).
-__device__ __forceinline__ float gelu_sigmoid_f(float z) {
-    return z * rcp_approx(1.0f + ex2_approx(z * -2.4554669595930157f));
+template <bool P>
+__device__ __forceinline__ f32x2 gelu_sigmoid_f2(f32x2 z) {
+    return f2_mul<P>(z, f2_rcp(f2_add<P>(f2(1.0f), f2_ex2(f2_mul<P>(z, f2(-2.4554669595930157f))))));
 }
-__device__ __forceinline__ float silu_f(float z) {
-    return z * rcp_approx(1.0f + ex2_approx(z * -1.4426950408889634f));
+template <bool P>
+__device__ __forceinline__ f32x2 silu_f2(f32x2 z) {
+    return f2_mul<P>(z, f2_rcp(f2_add<P>(f2(1.0f), f2_ex2(f2_mul<P>(z, f2(-1.4426950408889634f))))));
 }
 
-template <int EPI>
-__device__ __forceinline__ float act_f(float z) {
-    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f(z);
-    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f(z);
-    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f(z);
-    else if constexpr (EPI == EPI_SILU) return silu_f(z);
+template <int EPI, bool P>
+__device__ __forceinline__ f32x2 act_f2(f32x2 z) {
+    if constexpr (EPI == EPI_GELU_ERF) return gelu_erf_f2<P>(z);
+    else if constexpr (EPI == EPI_GELU_TANH) return gelu_tanh_f2<P>(z);
+    else if constexpr (EPI == EPI_GELU_SIGMOID) return gelu_sigmoid_f2<P>(z);
+    else if constexpr (EPI == EPI_SILU) return silu_f2<P>(z);
     else return z;
+}
+
+// GEGLU on a pair: (value + b_value) * gelu_erf(gate + b_gate).
+template <bool P>
+__device__ __forceinline__ f32x2 geglu_f2(f32x2 v, f32x2 bv, f32x2 g, f32x2 bg) {
+    return f2_mul<P>(f2_add<P>(v, bv), gelu_erf_f2<P>(f2_add<P>(g, bg)));
 }
 
 template <int DT>
@@ -1277,10 +1339,12 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                 }
 #pragma unroll
                                 for (int i = 0; i < 16; i += 2) {
-                                    const float y0v = (__uint_as_float(rv[i]) + bv[i]) *
-                                                      gelu_erf_f(__uint_as_float(rg[i]) + bg[i]);
-                                    const float y1v = (__uint_as_float(rv[i + 1]) + bv[i + 1]) *
-                                                      gelu_erf_f(__uint_as_float(rg[i + 1]) + bg[i + 1]);
+                                    float y0v, y1v;
+                                    f2_split(geglu_f2<true>(f2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1])),
+                                                      f2(bv[i], bv[i + 1]),
+                                                      f2(__uint_as_float(rg[i]), __uint_as_float(rg[i + 1])),
+                                                      f2(bg[i], bg[i + 1])),
+                                             y0v, y1v);
                                     w[8 * h + i / 2] = pack2<DT>(y0v, y1v);
                                 }
                             }
@@ -1305,14 +1369,15 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                 float v[16];
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[16 * h + i]);
-                                if (p.bias) {
-                                    float b[16];
-                                    bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
+                                const bool has_bias = p.bias != nullptr;
+                                float b[16];
+                                if (has_bias) bias_from_smem<16>(bsm + 128u * (uint32_t)g + 64u * (uint32_t)h, b);
 #pragma unroll
-                                    for (int i = 0; i < 16; ++i) v[i] += b[i];
+                                for (int i = 0; i < 16; i += 2) {
+                                    f32x2 z = f2(v[i], v[i + 1]);
+                                    if (has_bias) z = f2_add<true>(z, f2(b[i], b[i + 1]));
+                                    f2_split(act_f2<EPI, true>(z), v[i], v[i + 1]);
                                 }
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] = act_f<EPI>(v[i]);
                                 if constexpr (EPI == EPI_DOWN)
                                     if (p.residual)
                                         add_residual32<DT, 16>(p.residual, y0 + lane, p.M, col + 16 * h, p.N, v);

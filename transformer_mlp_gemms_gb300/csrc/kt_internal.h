@@ -259,8 +259,8 @@ kt_status launch_layernorm(int dtype, const void* X, const void* gamma, const vo
                            int64_t M, int64_t D, void* stream, const char** why);
 
 // Elementwise activation test kernel (kt_mlp_kernels.cu).
-kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
-                            const char** why);
+kt_status launch_activation(int act, bool paired, const float* z, const float* g, float* out, int64_t n,
+                            void* stream, const char** why);
 
 // One-thread kernel writing %globaltimer to dst (kt_mlp_kernels.cu).
 kt_status launch_timestamp(void* dst, void* stream, const char** why);

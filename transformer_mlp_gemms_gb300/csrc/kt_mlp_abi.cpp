@@ -697,13 +697,16 @@ kt_status kt_mlp_debug_trace(kt_mlp_plan_t plan, void* trace_up, void* trace_dow
     return ok();
 }
 
-kt_status kt_debug_activation(kt_act act, const float* z, const float* gate, float* out, int64_t n,
+kt_status kt_debug_activation(kt_act act_and_form, const float* z, const float* gate, float* out, int64_t n,
                               void* stream) {
+    const int form = (int)act_and_form & ~0xff;
+    const int act = (int)act_and_form & 0xff;
+    if (form != 0 && form != KT_ACTIVATION_SCALAR_FORM) return fail(KT_ERR_INVALID, "unknown activation form");
     if (act < KT_ACT_GELU_ERF || act > KT_ACT_SILU) return fail(KT_ERR_INVALID, "unknown activation");
     if (n < 0 || (n > 0 && (!z || !out || (act == KT_ACT_GEGLU && !gate))))
         return fail(KT_ERR_INVALID, "z and out (and gate for GEGLU) must be non-NULL, n >= 0");
     const char* why = "";
-    kt_status s = kt::launch_activation(act, z, gate, out, n, stream, &why);
+    kt_status s = kt::launch_activation(act, form == 0, z, gate, out, n, stream, &why);
     if (s != KT_OK) return fail(s, why);
     return ok();
 }

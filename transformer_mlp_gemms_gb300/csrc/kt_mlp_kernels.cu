@@ -32,19 +32,29 @@ __global__ void __launch_bounds__(256) kt_copy16_kernel(const uint4* __restrict_
     for (; i < n16; i += stride) dst[i] = src[i];
 }
 
-// Elementwise evaluation of the epilogue's fp32 activations (test hook).
-__global__ void kt_activation_kernel(int act, const float* __restrict__ z, const float* __restrict__ g,
-                                     float* __restrict__ out, int64_t n) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const float x = z[i];
-        float y;
-        if (act == KT_ACT_GELU_ERF) y = gelu_erf_f(x);
-        else if (act == KT_ACT_GELU_TANH) y = gelu_tanh_f(x);
-        else if (act == KT_ACT_GEGLU) y = x * gelu_erf_f(g[i]);
-        else if (act == KT_ACT_GELU_SIGMOID) y = gelu_sigmoid_f(x);
-        else if (act == KT_ACT_SILU) y = silu_f(x);
-        else y = x;
-        out[i] = y;
+// Elementwise evaluation of the epilogue's fp32 activations (test hook), through the
+// same pair functions the epilogues call, in the paired-instruction form (P) or the
+// scalar one: elements 2j and 2j + 1 form one pair (an odd last element is paired with
+// itself).  GEGLU adds -0 as both biases, which keeps every value's bits.
+template <bool P>
+__device__ __forceinline__ f32x2 activation_pair(int act, f32x2 x, f32x2 gate) {
+    if (act == KT_ACT_GELU_ERF) return gelu_erf_f2<P>(x);
+    if (act == KT_ACT_GELU_TANH) return gelu_tanh_f2<P>(x);
+    if (act == KT_ACT_GEGLU) return geglu_f2<P>(x, f2(-0.0f), gate, f2(-0.0f));
+    if (act == KT_ACT_GELU_SIGMOID) return gelu_sigmoid_f2<P>(x);
+    if (act == KT_ACT_SILU) return silu_f2<P>(x);
+    return x;
+}
+__global__ void kt_activation_kernel(int act, bool paired, const float* __restrict__ z,
+                                     const float* __restrict__ g, float* __restrict__ out, int64_t n) {
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < pairs; j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = 2 * j, i1 = 2 * j + 1 < n ? 2 * j + 1 : 2 * j;
+        const f32x2 x = f2(z[i0], z[i1]);
+        const f32x2 gate = act == KT_ACT_GEGLU ? f2(g[i0], g[i1]) : f2(0.0f);
+        const f32x2 y = paired ? activation_pair<true>(act, x, gate) : activation_pair<false>(act, x, gate);
+        out[i0] = y.x;
+        if (i1 != i0) out[i1] = y.y;
     }
 }
 
@@ -412,11 +422,11 @@ kt_status launch_layernorm(int dtype, const void* X, const void* gamma, const vo
     return KT_OK;
 }
 
-kt_status launch_activation(int act, const float* z, const float* g, float* out, int64_t n, void* stream,
-                            const char** why) {
+kt_status launch_activation(int act, bool paired, const float* z, const float* g, float* out, int64_t n,
+                            void* stream, const char** why) {
     const int64_t blocks = n == 0 ? 0 : std::min<int64_t>((n + 255) / 256, 4096);
     if (blocks > 0)
-        kt_activation_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(act, z, g, out, n);
+        kt_activation_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(act, paired, z, g, out, n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

@@ -21,6 +21,7 @@ KT_F16, KT_BF16 = 0, 1
 KT_W_IN_OUT, KT_W_OUT_IN = 0, 1
 KT_H_AUTO, KT_H_MEMORY, KT_H_ON_CHIP = 0, 1, 2
 KT_LAUNCH_AUTO, KT_LAUNCH_ONE, KT_LAUNCH_TWO = 0, 1, 2
+KT_ACTIVATION_SCALAR_FORM = 0x100  # kt_debug_activation: the scalar instruction form
 KT_OK, KT_ERR_INVALID, KT_ERR_UNSUPPORTED, KT_ERR_CUDA, KT_ERR_TIMEOUT, KT_ERR_NOMEM = range(6)
 STATUS_NAMES = {0: "KT_OK", 1: "KT_ERR_INVALID", 2: "KT_ERR_UNSUPPORTED", 3: "KT_ERR_CUDA",
                 4: "KT_ERR_TIMEOUT", 5: "KT_ERR_NOMEM"}
