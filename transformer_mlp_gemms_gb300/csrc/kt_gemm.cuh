@@ -781,6 +781,80 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p) {
     return c;
 }
 
+// This CTA's part of a tile's operands (CTA r of the pair): its first row of A (m_r),
+// its first B column (nb_r) and how many B boxes it loads per k-block (chunks_r; N-major
+// B: boxes of bw columns, the widest of 64, 32 and 16 that divides the share; K-major:
+// one box of the share's rows per 64-deep atom).  Boxes entirely past the tensor are not
+// loaded: they would only feed accumulator rows / columns that are never stored.
+// Returns the bytes this CTA's copies of one k-block bring in.
+template <int PAIR>
+__device__ __forceinline__ uint32_t cta_share(const GemmParams& p, const TileCoord& c, uint32_t r, int n_b, int& m_r,
+                                              int& nb_r, int& chunks_r) {
+    const int bcols = p.BN / PAIR;
+    const int bw = b_box_cols(p.BN, PAIR);
+    m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
+    nb_r = c.tn * p.BN + (int)r * bcols;
+    const uint32_t a_b = m_r < p.M ? p.a_bytes : 0u;
+    if (p.b_kmajor) {
+        chunks_r = nb_r < p.N ? 1 : 0;
+        return a_b + (uint32_t)(n_b * chunks_r) * p.b_bytes;
+    }
+    chunks_r = 0;  // boxes of the share that start inside [0, N)
+    for (int ch = 0; ch * bw < bcols; ++ch)
+        if (nb_r + bw * ch < p.N) chunks_r = ch + 1;
+    return a_b + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * (uint32_t)bw * 2u);
+}
+
+// The copies of one k-block (starting at K = k0) into the stage at sA with full barrier
+// fb.  A role: the stage's byte count (tx; with CTA pairs, both CTAs' bytes, counted on
+// the leader's barrier) and the A boxes; B role: the B boxes.  The B copies may complete
+// on the barrier before the A thread's arrival: its transaction count then runs negative
+// until the arrival, and the phase cannot complete before it.
+template <int PAIR>
+__device__ __forceinline__ void issue_kblock_copies(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                                    int n_b, bool a_role, bool leader, uint32_t fb, uint32_t sA,
+                                                    int k0, int m_me, int nb_me, int chunks, uint32_t tx) {
+    const uint32_t sB = sA + p.a_bytes;
+    const int bw = b_box_cols(p.BN, PAIR);
+    // N-major B: box j is bw columns x bk rows at column nb + bw j, row k0.
+    // K-major B: box j is bcols rows x 64 at row nb, column k0 + 64 j.
+    const uint32_t box_bytes = p.b_kmajor ? p.b_atom_bytes : (uint32_t)p.bk * (uint32_t)bw * 2u;
+    const int nbox = p.b_kmajor ? (chunks ? p.bk / kAtomK : 0) : chunks;
+    // shared-memory slots of value box j and gate box j: N-major, the gate chunks follow
+    // all value chunks at the same pitch; K-major, each 64-deep atom holds this CTA's
+    // value rows, then its gate rows
+    auto vslot = [&](int j) { return sB + box_bytes * (uint32_t)(p.b_kmajor ? n_b * j : j); };
+    auto gslot = [&](int j) {
+        return p.b_kmajor ? sB + box_bytes * (uint32_t)(2 * j + 1) : sB + p.b_bytes + box_bytes * (uint32_t)j;
+    };
+    auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + bw * j; };
+    auto by = [&](int j, int row0) { return p.b_kmajor ? row0 + nb_me : k0; };
+    auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + bw * j; };
+    if constexpr (PAIR == 2) {
+        const uint32_t fb_leader = mapa_rank(fb, 0);
+        if (a_role) {
+            if (leader) mbar_arrive_expect_tx(fb, tx);
+            if (m_me < p.M)
+                for (int a = 0; a < p.bk / kAtomK; ++a)
+                    tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
+        } else {
+            for (int j = 0; j < nbox; ++j) tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
+            if (n_b == 2)
+                for (int j = 0; j < nbox; ++j) tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
+        }
+    } else {
+        if (a_role) {
+            mbar_arrive_expect_tx(fb, tx);
+            if (m_me < p.M)
+                for (int a = 0; a < p.bk / kAtomK; ++a) tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
+        } else {
+            for (int j = 0; j < nbox; ++j) tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
+            if (n_b == 2)
+                for (int j = 0; j < nbox; ++j) tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
+        }
+    }
+}
+
 // PAIR = 1: one CTA per 128 x BN tile (cta_group::1).  PAIR = 2: a cluster pair per
 // 256 x BN tile (cta_group::2): each CTA loads its 128 rows of A and half of the B
 // columns; the even CTA (the leader) issues the MMAs, which write each CTA's 128
@@ -908,12 +982,15 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
     // ahead (the counter's round trip then overlaps the previous item's loads); down tiles
     // are taken on demand, so that none waits on a unit still busy with an earlier tile.
     int next_idx = -1;
-    auto publish = [&](uint32_t k) -> int {  // leader CTA's producer
-        const uint32_t slot = k % kItemRing, par = (k / kItemRing) & 1u;
+    // Item k >= 1 goes through ring slot (k - 1) % kItemRing; item 0 is unit0 for every
+    // role and never enters the ring, so that no role waits for another before its first
+    // item (at a kernel's start that wait would be the publisher's whole first code path).
+    auto publish = [&](uint32_t k) -> int {  // leader CTA's producer, k >= 1
+        const uint32_t r = k - 1u, slot = r % kItemRing, par = (r / kItemRing) & 1u;
         if (!wait_phase(item_empty + 8u * slot, par ^ 1u, abort_flag, p.error, DEV_TIMEOUT_PRODUCER,
                         p.wait_limit_ns))
             return INT_MAX;
-        const int idx = k == 0 ? unit0 : next_idx >= 0 ? next_idx : unit_step + atomicAdd(p.sched, 1);
+        const int idx = next_idx >= 0 ? next_idx : unit_step + atomicAdd(p.sched, 1);
         next_idx = idx + 2 * unit_step < p.num_tiles ? unit_step + atomicAdd(p.sched, 1) : -1;
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(item_idx + 4u * slot), "r"(idx) : "memory");
         if constexpr (PAIR == 2) {
@@ -924,8 +1001,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
         mbar_arrive(item_full + 8u * slot);
         return idx;
     };
-    auto consume = [&](uint32_t k) -> int {  // one thread per consuming warp
-        const uint32_t slot = k % kItemRing, par = (k / kItemRing) & 1u;
+    auto consume = [&](uint32_t k) -> int {  // one thread per consuming warp, k >= 1
+        const uint32_t r = k - 1u, slot = r % kItemRing, par = (r / kItemRing) & 1u;
         if (!wait_phase<PAIR == 2>(item_full + 8u * slot, par, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
                                    p.wait_limit_ns))
             return INT_MAX;
@@ -934,6 +1011,15 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
         if constexpr (PAIR == 2) mbar_arrive_cluster(mapa_rank(item_empty + 8u * slot, 0));
         else mbar_arrive(item_empty + 8u * slot);
         return idx;
+    };
+    // item k for a role: the static first item, else the ring's
+    auto item_of = [&](uint32_t k, bool publisher) -> int {
+        if (k == 0) {
+            if (publisher)  // one index taken ahead while up tiles remain for every unit
+                next_idx = unit0 + 2 * unit_step < p.num_tiles ? unit_step + atomicAdd(p.sched, 1) : -1;
+            return unit0 < total ? unit0 : total;
+        }
+        return publisher ? publish(k) : consume(k);
     };
 
     if (warp == 0 || warp == kWarpB) {
@@ -950,35 +1036,17 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 // failure injection: a barrier nobody arrives on, bounded wait
                 wait_phase(bar_stall, 0, abort_flag, p.error, DEV_INJECTED_STALL, p.stall_limit_ns);
             }
-            // one work item of one projection (p: its parameters, tmA / tmB: its operands)
+            // one work item of one projection (p: its parameters, tmA / tmB: its operands);
+            // its first `skip` k-blocks were issued already (the early copies below)
             auto produce = [&](const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, const int n_b,
-                               const bool ready_mode, const int t, const int local) -> bool {
+                               const bool ready_mode, const int t, const int local, const int skip) -> bool {
                 const TileCoord c = decode_tile(t, p);
                 const int kb0 = c.kb0, kb1 = c.kb1;
-                // this CTA's rows of A and its share of the B columns (N-major B: in boxes of
-                // bw columns, the widest of 64, 32 and 16 that divides the share)
-                const int bcols = p.BN / PAIR;
-                const int bw = b_box_cols(p.BN, PAIR);
-                auto cta_share = [&](uint32_t r, int& m_r, int& nb_r, int& chunks_r) -> uint32_t {
-                    m_r = c.tm * (kBM * PAIR) + (int)r * kBM;
-                    nb_r = c.tn * p.BN + (int)r * bcols;
-                    // boxes entirely past the tensor are not loaded: they would only feed
-                    // accumulator rows / columns that are never stored
-                    const uint32_t a_b = m_r < p.M ? p.a_bytes : 0u;
-                    if (p.b_kmajor) {  // one box of bcols rows x 64 per atom, or none
-                        chunks_r = nb_r < p.N ? 1 : 0;
-                        return a_b + (uint32_t)(n_b * chunks_r) * p.b_bytes;
-                    }
-                    chunks_r = 0;  // boxes of the share that start inside [0, N)
-                    for (int ch = 0; ch * bw < bcols; ++ch)
-                        if (nb_r + bw * ch < p.N) chunks_r = ch + 1;
-                    return a_b + (uint32_t)(n_b * chunks_r) * ((uint32_t)p.bk * (uint32_t)bw * 2u);
-                };
                 int m_me, nb_me, chunks;
-                uint32_t tx = cta_share(rank, m_me, nb_me, chunks);
+                uint32_t tx = cta_share<PAIR>(p, c, rank, n_b, m_me, nb_me, chunks);
                 if (PAIR == 2) {  // the leader's full barrier counts the bytes of both CTAs
                     int m_o, nb_o, ch_o;
-                    tx += cta_share(rank ^ 1u, m_o, nb_o, ch_o);
+                    tx += cta_share<PAIR>(p, c, rank ^ 1u, n_b, m_o, nb_o, ch_o);
                 }
                 if (a_role && ready_mode && m_me < p.M) {
                     // the up projection's row blocks that hold this CTA's 128 rows of H
@@ -1001,66 +1069,16 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                         trace_mark(tr, TR_T_DN_READY);
                 }
                 bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0 + skip; kb < kb1; ++kb) {
                     if (!wait_phase(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.error,
                                     DEV_TIMEOUT_PRODUCER, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar_full + 8u * stage;
-                    const uint32_t sA = base + stage * p.stage_bytes;
-                    const uint32_t sB = sA + p.a_bytes;
                     if (a_role && tr && armed == 0) trace_mark(tr, TR_FIRST_TMA);
                     if (a_role && tr && kb == kb0 && local == 1) trace_mark(tr, TR_S_LD0);
-                    const int k0 = kb * p.bk;
-                    // N-major B: box j is bw columns x bk rows at column nb + bw j, row k0.
-                    // K-major B: box j is bcols rows x 64 at row nb, column k0 + 64 j.
-                    const uint32_t box_bytes = p.b_kmajor ? p.b_atom_bytes : (uint32_t)p.bk * (uint32_t)bw * 2u;
-                    const int nbox = p.b_kmajor ? (chunks ? p.bk / kAtomK : 0) : chunks;
-                    // shared-memory slots of value box j and gate box j: N-major, the gate
-                    // chunks follow all value chunks at the same pitch; K-major, each 64-deep
-                    // atom holds this CTA's value rows, then its gate rows
-                    auto vslot = [&](int j) { return sB + box_bytes * (uint32_t)(p.b_kmajor ? n_b * j : j); };
-                    auto gslot = [&](int j) {
-                        return p.b_kmajor ? sB + box_bytes * (uint32_t)(2 * j + 1) : sB + p.b_bytes + box_bytes * (uint32_t)j;
-                    };
-                    auto bx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : nb_me + bw * j; };
-                    auto by = [&](int j, int row0) { return p.b_kmajor ? row0 + nb_me : k0; };
-                    auto gx = [&](int j) { return p.b_kmajor ? k0 + kAtomK * j : p.gate_col + nb_me + bw * j; };
-                    // (the A thread's arrival carries the stage's whole byte count; the B
-                    // copies may complete on the barrier before it: its transaction count
-                    // then runs negative until the arrival, and the phase cannot complete
-                    // before the arrival)
-                    if constexpr (PAIR == 2) {
-                        const uint32_t fb_leader = mapa_rank(fb, 0);
-                        if (a_role) {
-                            if (leader) mbar_arrive_expect_tx(fb, tx);
-                            if (m_me < p.M)
-                                for (int a = 0; a < p.bk / kAtomK; ++a)
-                                    tma_load_2d_pair(sA + 16384u * a, &tmA, fb_leader, k0 + kAtomK * a, m_me);
-                        } else {
-                            for (int j = 0; j < nbox; ++j)
-                                tma_load_2d_pair(vslot(j), &tmB, fb_leader, bx(j), by(j, 0));
-                            if (n_b == 2) {
-                                for (int j = 0; j < nbox; ++j)
-                                    tma_load_2d_pair(gslot(j), &tmB, fb_leader, gx(j), by(j, p.gate_col));
-                            }
-                        }
-                    } else {
-                        if (a_role) {
-                            mbar_arrive_expect_tx(fb, tx);
-                            if (m_me < p.M)
-                                for (int a = 0; a < p.bk / kAtomK; ++a)
-                                    tma_load_2d(sA + 16384u * a, &tmA, fb, k0 + kAtomK * a, m_me);
-                        } else {
-                            for (int j = 0; j < nbox; ++j)
-                                tma_load_2d(vslot(j), &tmB, fb, bx(j), by(j, 0));
-                            if (n_b == 2) {
-                                for (int j = 0; j < nbox; ++j)
-                                    tma_load_2d(gslot(j), &tmB, fb, gx(j), by(j, p.gate_col));
-                            }
-                        }
-                    }
+                    issue_kblock_copies<PAIR>(p, tmA, tmB, n_b, a_role, leader, bar_full + 8u * stage,
+                                              base + stage * p.stage_bytes, kb * p.bk, m_me, nb_me, chunks, tx);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == (uint32_t)p.stages) {
@@ -1070,18 +1088,44 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 }
                 return ok;
             };
+            // Early copies: the first item of a unit is static (item unit0).  When it waits on
+            // nothing (an up-projection tile, or a tile of a projection without readiness
+            // counters), its first k-blocks go out here, one per stage of the fresh ring, before
+            // the item ring and the general path: at a kernel's start every code region runs
+            // for the first time and waits for its instruction fetch, and the general path's
+            // regions (item ring, tile decode, ring waits) put ~1.5 us before the first copy.
+            int pre = 0;  // k-blocks of the first item issued here
+            const bool first_free = TWO ? unit0 < p.num_tiles : (unit0 < p.num_tiles && !ready_mode);
+            if (first_free && !p.inject_stall) {
+                const TileCoord c = decode_tile(unit0, p);
+                int m_me, nb_me, chunks;
+                uint32_t tx = cta_share<PAIR>(p, c, rank, n_b, m_me, nb_me, chunks);
+                if (PAIR == 2) {
+                    int m_o, nb_o, ch_o;
+                    tx += cta_share<PAIR>(p, c, rank ^ 1u, n_b, m_o, nb_o, ch_o);
+                }
+                pre = min(p.stages, c.kb1 - c.kb0);
+                if (a_role && tr) trace_mark(tr, TR_FIRST_TMA);
+                for (int s = 0; s < pre; ++s)
+                    issue_kblock_copies<PAIR>(p, tmA, tmB, n_b, a_role, leader, bar_full + 8u * s,
+                                              base + (uint32_t)s * p.stage_bytes, (c.kb0 + s) * p.bk, m_me, nb_me,
+                                              chunks, tx);
+                armed = (pre >= 32 ? 0xffffffffu : (1u << pre) - 1u);
+                stage = (uint32_t)(pre % p.stages);
+                phase = pre == p.stages ? 1u : 0u;
+            }
             if constexpr (TWO) {
                 bool done = false;  // this unit took the end-of-work index
                 for (uint32_t k = 0; !*abort_flag; ++k) {
-                    const int idx = leader && a_role ? publish(k) : consume(k);
+                    const int idx = item_of(k, leader && a_role);
                     if (idx >= total) {
                         done = idx != INT_MAX;
                         break;
                     }
                     if (a_role && tr && idx == p.num_tiles + (int)blockIdx.x / PAIR) trace_mark(tr, TR_T_DN_TAKEN);
                     const bool ok = idx >= p.num_tiles
-                                        ? produce(p2, tmA2, tmB2, 1, p2.ready != nullptr, idx - p.num_tiles, (int)k)
-                                        : produce(p, tmA, tmB, n_b, false, idx, (int)k);
+                                        ? produce(p2, tmA2, tmB2, 1, p2.ready != nullptr, idx - p.num_tiles, (int)k, 0)
+                                        : produce(p, tmA, tmB, n_b, false, idx, (int)k, k == 0 ? pre : 0);
                     if (!ok) break;
                 }
                 if (done && leader && a_role) {
@@ -1096,7 +1140,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
             } else {
                 int local = 0;
                 for (int t = unit0; t < p.num_tiles && !*abort_flag; t += unit_step, ++local)
-                    if (!produce(p, tmA, tmB, n_b, ready_mode, t, local)) break;
+                    if (!produce(p, tmA, tmB, n_b, ready_mode, t, local, local == 0 ? pre : 0)) break;
             }
             if (*abort_flag && leader && a_role) {
                 // do not leave copies in flight into shared memory we are about to release
@@ -1192,7 +1236,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
             if constexpr (TWO) {
                 unsigned long long n_up = 0, n_dn = 0;
                 for (uint32_t k = 0;; ++k) {
-                    const int idx = consume(k);
+                    const int idx = item_of(k, false);
                     if (idx >= total) break;
                     const bool dn = idx >= p.num_tiles;
                     const bool ok = dn ? mma_item(p2, 1, idx - p.num_tiles, (int)k) : mma_item(p, n_b, idx, (int)k);
@@ -1740,7 +1784,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
         if constexpr (TWO) {
             for (uint32_t k = 0;; ++k) {
                 int idx = 0;
-                if (lane == 0) idx = consume(k);
+                if (lane == 0) idx = item_of(k, false);
                 idx = __shfl_sync(0xffffffffu, idx, 0);
                 // every epilogue warp took the same item, unless the kernel is aborting
                 if (!epi_all<NEPI>(idx < total)) break;
