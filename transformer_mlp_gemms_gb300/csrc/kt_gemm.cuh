@@ -1602,6 +1602,13 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                     const int col = n0 + 32 * g;
                     if (rs_owner(g) != mine || col >= p.N || !rows_live) continue;  // warp-uniform
                     const float4* src = part + (size_t)u * SK * 256u + lane;
+                    // this split's own partial of the unit, from tensor memory, first: no
+                    // tensor-memory access (an ordering point for the compiler) sits between
+                    // the other splits' loads below, so they can all be in flight together
+                    uint32_t own[32];
+                    tmem_ld32(tq + 32u * g, own);
+                    tmem_wait_ld_only();
+                    reg_fence32(own);
                     uint32_t w[16];  // the unit's 32 results, rounded and packed in pairs
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {  // in 16-column slices
@@ -1610,9 +1617,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {  // in 8-column eighths of the unit
-                            // every other split's 8 columns of this row in flight at once (one
-                            // memory round trip per eighth, not one per split; the k-th other
-                            // split is k + (k >= mine), so the array index stays a compile-time
+                            // every other split's 8 columns of this row (the k-th other split
+                            // is k + (k >= mine), so the array index stays a compile-time
                             // constant and x lives in registers), then the sum in split order
                             float4 x[kRsMaxSplit - 1][2];
 #pragma unroll
@@ -1624,22 +1630,10 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                                     x[k][i] = __ldcg(src + (size_t)sp * 256u + 32 * (4 * h + 2 * e + i));
                             }
                             float* ve = v + 8 * e;
-                            // this split's own partial, from tensor memory at its place in split
-                            // order (warp-uniform condition)
-                            auto add_own = [&]() {
-                                uint32_t r[8];
-                                asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                                             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                                               "=r"(r[6]), "=r"(r[7])
-                                             : "r"(tq + 32u * g + 16u * h + 8u * e)
-                                             : "memory");
-                                asm volatile("tcgen05.wait::ld.sync.aligned;"
-                                             : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                                               "+r"(r[6]), "+r"(r[7])
-                                             :
-                                             : "memory");
+                            const uint32_t* oe = own + 16 * h + 8 * e;
+                            auto add_own = [&]() {  // this split, at its place in split order
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) ve[i] += __uint_as_float(r[i]);
+                                for (int i = 0; i < 8; ++i) ve[i] += __uint_as_float(oe[i]);
                             };
 #pragma unroll
                             for (int k = 0; k < kRsMaxSplit - 1; ++k) {  // split order: deterministic
