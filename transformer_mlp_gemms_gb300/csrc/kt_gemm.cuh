@@ -1592,7 +1592,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 if (tr1) trace_mark(tr, TR_S_G0S);  // (reduce-scatter: arrival counted)
                 if (tr0) trace_mark(tr, TR_EPI_LD);  // (reduce-scatter: partials written)
                 bool got = true;
-                if (lane == 0) got = wait_counter64(arrivals, rs_target[0], abort_flag, p.error, p.wait_limit_ns);
+                // one poller per CTA (the barrier below hands its outcome to every warp)
+                if (ew == 0 && lane == 0) got = wait_counter64(arrivals, rs_target[0], abort_flag, p.error, p.wait_limit_ns);
                 got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                 if (!epi_all<NEPI>(got)) return false;
                 if (tr && local == 1 && lane == 0) trace_max(tr, TR_S_G1M);  // (every split arrived: latest warp)
