@@ -447,18 +447,19 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     }
     // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory.  The
     // planner's own choice (KT_LAUNCH_AUTO), where the model also prefers one launch:
-    //  - the up projection is a single wave of single-CTA tiles (all of H is stored at about
-    //    the same time, so the second kernel's launch and set-up sit on the critical path)
-    //    and the two-launch down projection would split K (its cluster exchange sits there
-    //    too); or
+    //  - the up projection is a single wave (of single CTAs or of CTA pairs: all of H is
+    //    stored at about the same time, so the second kernel's launch and set-up sit on the
+    //    critical path) and the two-launch down projection would split K (its cluster
+    //    exchange sits there too); or
     //  - the two-launch down projection takes two waves of whole tiles (in one launch its
     //    tiles fill the units as they leave the up projection, instead of a partial second
     //    wave);
-    // otherwise two.  This rule reproduces the measured winner on all nine benchmark shapes
-    // (one launch: SigLIP 36.8 against 40.0 us, M = 256 26.3 against 28.9, SDXL level 1
-    // 82.7 against 84.3, M = 4096 78.1 against 79.6; two launches: the tiny case, M = 1000
-    // 39.2 against 41.0, SDXL level 2 75.6 against 78.0 (a one-wave down projection), and
-    // M = 16384 229.4 against 243.1 (five down waves)).  Override: KT_FORCE_LAUNCHES=1|2.
+    // otherwise two.  This rule reproduces the measured winner on the benchmark shapes
+    // (GB300, CUDA events, 256 MiB scrub between calls; one launch against two: SigLIP 32.2
+    // against 37.7 us, M = 256 24.7 against 29.6, M = 1000 36.7 against 38.2, M = 4096
+    // 74.3 against 77.6, SDXL level 1 83.5 against 83.2 (a tie); two launches: SDXL level 2
+    // 70.7 against 73.4 (a one-wave down projection), M = 16384 229.5 against 242.9 (five
+    // down waves); the tiny case keeps H on chip).  Override: KT_FORCE_LAUNCHES=1|2.
     out->one_launch = 0;
     if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
         *why = "unknown launches option";
@@ -476,7 +477,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     const bool forced_dn = std::getenv("KT_FORCE_DOWN") != nullptr;
     const bool auto_one =
         launches == KT_LAUNCH_AUTO && !forced_dn &&
-        ((out->up.waves == 1 && out->up.pair == 1 && out->down.split_k > 1) ||
+        ((out->up.waves == 1 && out->down.split_k > 1) ||
          (out->down.split_k == 1 && out->down.waves == 2));
     const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
     if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
