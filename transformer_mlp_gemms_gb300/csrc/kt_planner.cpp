@@ -453,13 +453,15 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     //    exchange sits there too); or
     //  - the two-launch down projection takes two waves of whole tiles (in one launch its
     //    tiles fill the units as they leave the up projection, instead of a partial second
-    //    wave);
+    //    wave), unless the activation is GEGLU (its one-launch kernel carries the
+    //    last-arriver split path beside the GEGLU epilogue and spills a few bytes);
     // otherwise two.  This rule reproduces the measured winner on the benchmark shapes
     // (GB300, CUDA events, 256 MiB scrub between calls; one launch against two: SigLIP 32.2
     // against 37.7 us, M = 256 24.7 against 29.6, M = 1000 36.7 against 38.2, M = 4096
-    // 74.3 against 77.6, SDXL level 1 83.5 against 83.2 (a tie); two launches: SDXL level 2
-    // 70.7 against 73.4 (a one-wave down projection), M = 16384 229.5 against 242.9 (five
-    // down waves); the tiny case keeps H on chip).  Override: KT_FORCE_LAUNCHES=1|2.
+    // 74.3 against 77.6; two launches: SDXL level 1 83.4 against 85.0 (83.2 against 83.5
+    // on another box), SDXL level 2 70.7 against 73.4 (a one-wave down projection), M =
+    // 16384 229.5 against 242.9 (five down waves); the tiny case keeps H on chip).
+    // Override: KT_FORCE_LAUNCHES=1|2.
     out->one_launch = 0;
     if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
         *why = "unknown launches option";
@@ -478,7 +480,7 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
     const bool auto_one =
         launches == KT_LAUNCH_AUTO && !forced_dn &&
         ((out->up.waves == 1 && out->down.split_k > 1) ||
-         (out->down.split_k == 1 && out->down.waves == 2));
+         (out->down.split_k == 1 && out->down.waves == 2 && act != KT_ACT_GEGLU));
     const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
     if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
         const double t_two = out->up.est_us + out->down.est_us;
