@@ -30,7 +30,7 @@ CASES = [
     (SIGLIP, {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_TWO),   # two launches, cluster split-K
     ((2048, 1280, 5120, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_AUTO),  # pairs
     # SDXL level 1: one launch of CTA pairs over many waves (the work counter reset by the last unit)
-    ((8192, 640, 2560, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_AUTO),
+    ((8192, 640, 2560, wl.ACT_GEGLU, wl.DT_BF16, True), {}, kt_mlp.KT_H_MEMORY, kt_mlp.KT_LAUNCH_ONE),
     ((300, 256, 1000, wl.ACT_SILU, wl.DT_F16, True), {"residual": True, "layernorm": True}, kt_mlp.KT_H_MEMORY,
      kt_mlp.KT_LAUNCH_AUTO),
     ((33, 64, 176, wl.ACT_GELU_ERF, wl.DT_F16, False), {}, kt_mlp.KT_H_ON_CHIP, kt_mlp.KT_LAUNCH_AUTO),  # fused
