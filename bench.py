@@ -30,7 +30,7 @@ maximum over ranks and the value the work of all ranks over that time.
 The JSON line also carries: the per-kernel roofline of the dominant kernel
 (device time per launch from CUDA events, against MEASURED_PEAKS.json), the
 end-to-end number through the C ABI with host buffers (kt_mlp_run_host), the
-SM clocks sampled with nvidia-smi every 50 ms (over the timed region, and over a
+SM clocks sampled with nvidia-smi every 20 ms (over the timed region, and over a
 clock soak of about two seconds of the same steps whose per-step times are binned
 by the sampled SM clock), and the float64 CPU oracle timed on the host cores as a
 reported baseline (with the CPU model and the threads it used).
@@ -58,14 +58,14 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_LABEL = f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"
-CLOCK_PERIOD_MS = 50
+CLOCK_PERIOD_MS = 20
 CONFIG_SUITE = ("tiny", "siglip", "sdxl_l2", "sdxl_l1", "sweep_M256", "sweep_M1000", "sweep_M4096", "sweep_M16384")
 
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="siglip")
     ap.add_argument("--block", default="", help="comma list of block options: ln (LayerNorm prologue), "
