@@ -70,3 +70,43 @@ def test_check_y_tolerance(dtype):
     nan[0, 0] = 0x7E00  # a NaN pattern in both formats' quiet-NaN range
     with pytest.raises(AssertionError):
         parity.check_y(nan, Yx, dtype)
+
+
+@pytest.mark.parametrize("dtype,spacing", [(wl.DT_F16, 2.0 ** -24), (wl.DT_BF16, 2.0 ** -133)])
+def test_ulp_at_zero_is_the_subnormal_spacing(dtype, spacing):
+    # the dtype's spacing at zero (and throughout the subnormal range), not the spacing at 1
+    u = parity.ulp(np.array([0.0, -0.0, spacing, 3 * spacing, 1.0]), dtype)
+    assert list(u[:4]) == [spacing] * 4
+    assert u[4] == (2.0 ** -10 if dtype == wl.DT_F16 else 2.0 ** -7)
+
+
+def test_check_h_near_zero_uses_the_subnormal_ulp():
+    # an oracle zero: a few subnormal steps off is within ulp + bound where the bound is an
+    # accumulation error many subnormal steps wide, and rejected where the bound is tiny
+    ho = np.zeros((4, 4), dtype=np.uint16)
+    hg = ho.copy()
+    hg[1, 2] = _step(hg[1, 2], -14)  # -14 subnormal steps (f16: -8.3e-7)
+    stats = parity.check_h(hg, ho, np.full(ho.shape, 2e-4), wl.DT_F16)
+    assert stats["beyond_1ulp"] == 1 and stats["max_dist"] == 14 and stats["counted"] == 0
+    with pytest.raises(AssertionError):
+        parity.check_h(hg, ho, np.full(ho.shape, 1e-9), wl.DT_F16)
+
+
+def test_fraction_floor_counts_elements_away_from_zero_only():
+    w, b, Ho, _, _ = _case(wl.DT_F16)
+    o = oracle.decode(Ho, wl.DT_F16)
+    u = parity.ulp(o, wl.DT_F16)
+    # half the elements with a bound of 4 ulps, the other half of 100 ulps (near zero)
+    bound = np.where(np.arange(Ho.size).reshape(Ho.shape) % 2 == 0, 4 * u, 100 * u)
+    near_zero = np.argwhere(bound > parity.FRACTION_BOUND_ULPS * u)
+    counted = np.argwhere(bound < parity.FRACTION_BOUND_ULPS * u)
+    many = Ho.copy()
+    for ij in near_zero[: Ho.size // 10]:  # 10 % of all elements three steps off, all near zero
+        many[tuple(ij)] = _step(many[tuple(ij)], 3)
+    stats = parity.check_h(many, Ho, bound, wl.DT_F16)
+    assert stats["beyond_1ulp"] == Ho.size // 10 and stats["counted_beyond_1ulp"] == 0
+    bad = Ho.copy()
+    for ij in counted[: Ho.size // 20]:  # 10 % of the counted elements two steps off, each within ulp + bound
+        bad[tuple(ij)] = _step(bad[tuple(ij)], 2)
+    with pytest.raises(AssertionError, match="counted_beyond_1ulp"):
+        parity.check_h(bad, Ho, bound, wl.DT_F16)
