@@ -48,13 +48,34 @@ def _case(i):
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_problem(i):
+    _run_case(i, None)
+
+
+# more seeds, H through memory, each problem in both launch modes (one persistent kernel
+# for both projections, and two kernels): the work queue, the item ring, the early first
+# copies and the split-K exchanges of both schedules on shapes no hand-written case has
+N_CASES_BOTH = 64
+
+
+@pytest.mark.parametrize("launches", [kt_mlp.KT_LAUNCH_ONE, kt_mlp.KT_LAUNCH_TWO], ids=["one", "two"])
+@pytest.mark.parametrize("i", range(N_CASES, N_CASES + N_CASES_BOTH))
+def test_random_problem_both_launch_modes(i, launches):
+    _run_case(i, launches)
+
+
+def _run_case(i, launches):
     M, D, F, act, dt, bias, res, ln, layout, h_path = _case(i)
+    if launches is not None:
+        h_path = kt_mlp.KT_H_MEMORY
     w = wl.custom(M, D, F, act, dt, bias, seed=9000 + i)
     t = wl.generate(w, residual=res, layernorm=ln)
     dev = wl.torch_order(t) if layout else t
     d = {k: v.cuda() for k, v in dev.items()}
+    opts = {} if launches is None else {"launches": launches}
     plan = kt_mlp.Plan(M, D, F, act, dt, bias, residual=res, layernorm=ln, weight_layout=layout, ln_eps=EPS,
-                       h_path=h_path)
+                       h_path=h_path, **opts)
+    if launches is not None:
+        assert plan.info()["one_launch"] == (launches == kt_mlp.KT_LAUNCH_ONE)
     Y = torch.full((M, D), float("nan"), dtype=wl.TORCH_DTYPES[dt], device="cuda")
     h_mem = not plan.info()["h_on_chip"]
     H = torch.full((M, F), float("nan"), dtype=wl.TORCH_DTYPES[dt], device="cuda") if h_mem else None
