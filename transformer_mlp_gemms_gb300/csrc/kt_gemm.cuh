@@ -300,6 +300,27 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrivals without release ordering (a release-ordered arrival costs its thread several
+// tenths of a microsecond): for a thread whose only earlier access the waiter depends on
+// is a load that an acquire already orders before the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Hand a 32-bit value to the waiters of a cluster peer's barrier (both addresses in the
+// peer's shared memory): the arrival announces 4 bytes, and an asynchronous store of the
+// value completes them, so the phase completes only once the value is in place.
+__device__ __forceinline__ void post_index(uint32_t slot_cluster, uint32_t bar_cluster, int value) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], 4;" ::"r"(bar_cluster)
+                 : "memory");
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(slot_cluster),
+                 "r"(value), "r"(bar_cluster)
+                 : "memory");
+}
+
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int x,
                                                  int y) {
@@ -992,12 +1013,10 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
             return INT_MAX;
         const int idx = next_idx >= 0 ? next_idx : unit_step + atomicAdd(p.sched, 1);
         next_idx = idx + 2 * unit_step < p.num_tiles ? unit_step + atomicAdd(p.sched, 1) : -1;
+        // the pair's peer gets the index by an asynchronous store that completes on its slot's
+        // full barrier, as copies do (no cluster-scope release-ordered arrival)
+        if constexpr (PAIR == 2) post_index(mapa_rank(item_idx + 4u * slot, 1), mapa_rank(item_full + 8u * slot, 1), idx);
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(item_idx + 4u * slot), "r"(idx) : "memory");
-        if constexpr (PAIR == 2) {
-            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa_rank(item_idx + 4u * slot, 1)), "r"(idx)
-                         : "memory");
-            mbar_arrive_cluster(mapa_rank(item_full + 8u * slot, 1));
-        }
         mbar_arrive(item_full + 8u * slot);
         return idx;
     };
@@ -1006,10 +1025,12 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
         if (!wait_phase<PAIR == 2>(item_full + 8u * slot, par, abort_flag, p.error, DEV_TIMEOUT_EPILOGUE,
                                    p.wait_limit_ns))
             return INT_MAX;
+        // the slot is free for the publisher's next index once this read is done: the
+        // acquire orders the arrival after it, so the arrival itself need not release
         int idx;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(idx) : "r"(item_idx + 4u * slot) : "memory");
-        if constexpr (PAIR == 2) mbar_arrive_cluster(mapa_rank(item_empty + 8u * slot, 0));
-        else mbar_arrive(item_empty + 8u * slot);
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(idx) : "r"(item_idx + 4u * slot) : "memory");
+        if constexpr (PAIR == 2) mbar_arrive_cluster_relaxed(mapa_rank(item_empty + 8u * slot, 0));
+        else mbar_arrive_relaxed(item_empty + 8u * slot);
         return idx;
     };
     // item k for a role: the static first item, else the ring's
