@@ -81,11 +81,8 @@ typedef enum { KT_H_AUTO = 0, KT_H_MEMORY = 1, KT_H_ON_CHIP = 2 } kt_h_path;
  * KT_LAUNCH_ONE: one persistent kernel that takes up tiles, then down items, from one work
  * queue (a down item once its rows of H are stored); down items may be K splits of a tile,
  * reduce-scattered among the splits through global memory (GEGLU: summed by the last split
- * to arrive).  KT_LAUNCH_AUTO is the planner's choice: one launch where the model prefers
- * it and either (a) the up projection is a single wave (of single CTAs or CTA pairs) and
- * the two-launch down projection would split K (SigLIP's 729 tokens, M = 256, M = 1000),
- * or (b) the two-launch down projection takes two waves of whole tiles and the activation
- * is not GEGLU (M = 4096); two launches otherwise (SDXL levels 1 and 2, M = 16384). */
+ * to arrive).  KT_LAUNCH_AUTO is the planner's choice: one launch wherever a one-launch
+ * plan exists (measured faster on every benchmark shape), else two. */
 typedef enum { KT_LAUNCH_AUTO = 0, KT_LAUNCH_ONE = 1, KT_LAUNCH_TWO = 2 } kt_launches;
 
 /* Memory order of W_up and W_down. */

@@ -446,21 +446,14 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
             out->h_on_chip = 1;
     }
     // Both projections in one launch (KT_LAUNCH_ONE), where H goes through memory.  The
-    // planner's own choice (KT_LAUNCH_AUTO), where the model also prefers one launch:
-    //  - the up projection is a single wave (of single CTAs or of CTA pairs: all of H is
-    //    stored at about the same time, so the second kernel's launch and set-up sit on the
-    //    critical path) and the two-launch down projection would split K (its cluster
-    //    exchange sits there too); or
-    //  - the two-launch down projection takes two waves of whole tiles (in one launch its
-    //    tiles fill the units as they leave the up projection, instead of a partial second
-    //    wave), unless the activation is GEGLU (its one-launch kernel carries the
-    //    last-arriver split path beside the GEGLU epilogue and spills a few bytes);
-    // otherwise two.  This rule reproduces the measured winner on the benchmark shapes
-    // (GB300, CUDA events, 256 MiB scrub between calls; one launch against two: SigLIP 32.2
-    // against 37.7 us, M = 256 24.7 against 29.6, M = 1000 36.7 against 38.2, M = 4096
-    // 74.3 against 77.6; two launches: SDXL level 1 83.4 against 85.0 (83.2 against 83.5
-    // on another box), SDXL level 2 70.7 against 73.4 (a one-wave down projection), M =
-    // 16384 229.5 against 242.9 (five down waves); the tiny case keeps H on chip).
+    // planner's own choice (KT_LAUNCH_AUTO) is one launch wherever a one-launch plan exists:
+    // the second kernel's launch, its CTAs' set-up and the partial waves at the boundary
+    // between the projections cost more than one launch's work queue now that the queue
+    // hands items on without cluster-scope release-ordered arrivals (GB300, CUDA events,
+    // 256 MiB scrub between calls; one launch against two: SigLIP 32.3 against 37.7 us,
+    // M = 256 24.6 against 29.6, M = 1000 35.1 against 38.2, M = 4096 69.7 against 77.6,
+    // SDXL level 2 69.2 against 70.7, SDXL level 1 81.5 against 84.0, M = 16384 227.6
+    // against 229.6 us); the tiny case keeps H on chip.
     // Override: KT_FORCE_LAUNCHES=1|2.
     out->one_launch = 0;
     if (launches != KT_LAUNCH_AUTO && launches != KT_LAUNCH_ONE && launches != KT_LAUNCH_TWO) {
@@ -477,16 +470,11 @@ kt_status plan_choose(int64_t M, int64_t D, int64_t F, int act, int num_sms, Pla
         launches = v == 1 ? KT_LAUNCH_ONE : KT_LAUNCH_TWO;
     }
     const bool forced_dn = std::getenv("KT_FORCE_DOWN") != nullptr;
-    const bool auto_one =
-        launches == KT_LAUNCH_AUTO && !forced_dn &&
-        ((out->up.waves == 1 && out->down.split_k > 1) ||
-         (out->down.split_k == 1 && out->down.waves == 2 && act != KT_ACT_GEGLU));
+    const bool auto_one = launches == KT_LAUNCH_AUTO && !forced_dn;
     const int force_launches = launches == KT_LAUNCH_ONE ? 1 : auto_one ? 0 : 2;
     if (allow_one_launch && !out->h_on_chip && force_launches != 2) {
-        const double t_two = out->up.est_us + out->down.est_us;
         plan_one_launch(M, D, F, act, num_sms, kmaj, out, std::getenv("KT_FORCE_UP") ? &out->up : nullptr,
                         forced_dn ? &out->down : nullptr);
-        if (force_launches == 0 && out->one_launch && out->one_est_us >= t_two) out->one_launch = 0;
         if (out->one_launch) {  // the configurations that launch runs
             out->up = out->one_up;
             out->down = out->one_down;
