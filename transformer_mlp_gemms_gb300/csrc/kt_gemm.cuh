@@ -301,8 +301,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 // Arrivals without release ordering (a release-ordered arrival costs its thread several
-// tenths of a microsecond): for a thread whose only earlier access the waiter depends on
-// is a load that an acquire already orders before the arrival.
+// tenths of a microsecond): for a thread whose earlier accesses the waiter depends on are
+// complete by other means: a load that an acquire orders before the arrival (the work
+// queue's slots), or tensor-memory loads that tcgen05.wait::ld has completed (an epilogue
+// handing its accumulator back to the MMA issuer).
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -1462,8 +1464,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
-                    else mbar_arrive(acce);
+                    if constexpr (PAIR == 2) mbar_arrive_cluster_relaxed(acce);
+                    else mbar_arrive_relaxed(acce);
                 }
                 if (tr1) trace_mark(tr, TR_S_ARR);
                 if (EPI != EPI_DOWN && p.ready != nullptr) pending_rows = c.tm;  // counted later
@@ -1560,7 +1562,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 if (tr0) trace_mark(tr, TR_EPI_STORE);  // (cluster split-K: my units stored)
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce);
+                if (lane == 0) mbar_arrive_relaxed(acce);
             } else if (TWO && EPI_UP != EPI_GEGLU && p.rs_sk) {
                 // (not compiled into the GEGLU kernels, whose epilogue leaves no registers for
                 // it: their one-launch splits are summed by the last CTA to arrive, below)
@@ -1690,8 +1692,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
-                    else mbar_arrive(acce);
+                    if constexpr (PAIR == 2) mbar_arrive_cluster_relaxed(acce);
+                    else mbar_arrive_relaxed(acce);
                 }
                 if (tr1) trace_mark(tr, TR_S_ARR);
                 // rs_target is rewritten by the next split-K item only after every warp has
@@ -1720,8 +1722,8 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if constexpr (PAIR == 2) mbar_arrive_cluster(acce);
-                    else mbar_arrive(acce);
+                    if constexpr (PAIR == 2) mbar_arrive_cluster_relaxed(acce);
+                    else mbar_arrive_relaxed(acce);
                 }
                 // the barrier orders every epilogue thread's partial stores before the
                 // arrival thread's gpu-scope release (fences are cumulative)
