@@ -288,6 +288,13 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same rendezvous without release ordering, for the kernel's start: what the peers
+// must see of this CTA's set-up (its barriers' initialisation) is already published by
+// fence.mbarrier_init.release.cluster.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address, in the cluster shared window, of the same shared variable in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;
@@ -970,7 +977,7 @@ __global__ void __launch_bounds__((3 + epi_warps(EPI)) * 32, 1)
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
-    if (PAIR == 2 || p.cluster_sk) cluster_sync_all();  // peers' barriers initialised before any remote signal
+    if (PAIR == 2 || p.cluster_sk) cluster_sync_relaxed();  // peers' barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) trace_mark(tr, TR_SETUP);
