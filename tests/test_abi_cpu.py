@@ -223,6 +223,25 @@ def test_n_major_shares_of_odd_multiples_of_32_are_not_padded(lib, monkeypatch, 
     _stage_check(g, 1)
 
 
+@pytest.mark.parametrize("act,dtype,bias", [(1, 0, False), (0, 0, True), (2, 1, True)])
+@pytest.mark.parametrize("M", [1, 77, 256, 729, 1024, 4096])
+def test_auto_launches_once_wherever_one_launch_applies(lib, M, act, dtype, bias):
+    # the planner's own choice is one launch exactly when the one-launch planner has a plan
+    # (H through memory), and then the same plan as KT_LAUNCH_ONE
+    D, F = (1280, 5120) if act == 2 else (1152, 4304)
+    auto = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, dtype, bias, h_path=kt_mlp.KT_H_MEMORY), SMS)
+    try:
+        one = kt_mlp.kt_mlp_plan_info_ex(kt_mlp.options(M, D, F, act, dtype, bias, h_path=kt_mlp.KT_H_MEMORY,
+                                                        launches=kt_mlp.KT_LAUNCH_ONE), SMS)
+    except kt_mlp.KtError:
+        one = None
+    assert auto["one_launch"] == (1 if one is not None and one["one_launch"] else 0)
+    if auto["one_launch"]:
+        for k in ("up", "down"):
+            assert auto[k] == one[k]
+        assert auto["one_launch_grid"] == one["one_launch_grid"]
+
+
 @pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
 def test_one_launch_split_items_fit_one_round(lib, name):
     # in one launch, a down projection split along K runs all its items in one round
